@@ -1,0 +1,331 @@
+"""Benchmark of the batch-invariant MoE prefill path on GB300.
+
+One step = one pass of the whole path over one prefill batch of M = 4096
+tokens (16 requests of 256) through 40 layers; each layer runs, in stream
+order:
+  bi_router_topk      F32 router, H=2048, E=256, top-8 (logits, ids,
+                      weights, margins)
+  bi_shared_gate      the shared-expert gate dot and sigmoid
+  bi_route_trace_hash per-request FNV-1a hashes, chained over the layers
+  bi_gemm_bf16        the M-invariant bf16 projection, K = N = 4096
+Every layer has its own weights and its own hidden states, so a step
+streams about 4 GB (inputs larger than the 129 MB L2; no flush needed).
+
+value: tokens/s of whole steps (all ranks).  Per-part device times come from
+CUDA events recorded around each call inside the timed steps; the roofline
+object describes the dominant kernel.
+
+--impl reference times the CPU oracle (the plain C reference the tests
+check against) on a bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+LAYERS, M, H, E, K_TOP = 40, 4096, 2048, 256, 8
+G_N = G_K = 4096
+N_REQ = 16
+METRIC = "router+top-k tokens/s & M-invariant bf16 GEMM TFLOP/s, % of roofline"
+WORKLOAD = ("moe-prefill block prologue: 40 layers x (F32 router H2048 E256 top8 + shared gate + "
+            "route hash + bf16 projection K=N=4096), M=4096 tokens (16 requests x 256)")
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs", 6781.4), d.get("bf16_tflops", 1897.4), d.get("bf16_tflops_sustained", 1683.3), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# FP32 FMA peak from unit counts and clock: 152 SMs x 128 FP32 lanes x 2 flop x 2070 MHz
+FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
+
+
+class Clocks:
+    """nvidia-smi sampled every 200 ms during the timed region."""
+
+    def __init__(self, gpu_index: int):
+        q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={q}",
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        out, _ = self.p.communicate(timeout=10)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    from serving_numerics_gb300 import binding as bi
+    from serving_numerics_gb300 import synth
+
+    ws, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    bi.load()
+    dev = torch.device("cuda", local)
+    seed = 1000 + rank
+
+    # resident weights and inputs (seeded, drawn on the device)
+    Wg = [synth.device_normal((E, H), seed * 100 + l, 0.02, torch.float32, dev) for l in range(LAYERS)]
+    Wsg = [synth.device_normal((H,), seed * 100 + 50 + l, 0.02, torch.float32, dev) for l in range(LAYERS)]
+    Bw = [synth.device_normal((G_N, G_K), seed * 100 + 100 + l, 1 / 64, torch.bfloat16, dev) for l in range(LAYERS)]
+    X = [synth.device_normal((M, H), seed * 100 + 200 + l, 1.0, torch.float32, dev) for l in range(LAYERS)]
+    A = [synth.device_normal((M, G_K), seed * 100 + 300 + l, 1 / 64, torch.bfloat16, dev) for l in range(LAYERS)]
+    logits = torch.empty((LAYERS, M, E), dtype=torch.float32, device=dev)
+    ids = torch.empty((LAYERS, M, K_TOP), dtype=torch.int32, device=dev)
+    wts = torch.empty((LAYERS, M, K_TOP), dtype=torch.float32, device=dev)
+    mg = torch.empty((LAYERS, M), dtype=torch.float32, device=dev)
+    mu = torch.empty((LAYERS, M), dtype=torch.int32, device=dev)
+    gdot = torch.empty((LAYERS, M), dtype=torch.float32, device=dev)
+    gsig = torch.empty((LAYERS, M), dtype=torch.float32, device=dev)
+    Cout = torch.empty((M, G_N), dtype=torch.bfloat16, device=dev)
+    hashes = torch.empty((N_REQ,), dtype=torch.int64, device=dev)
+    offs = [i * (M // N_REQ) for i in range(N_REQ + 1)]
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    launches_per_layer = 5   # router projection + selection, gate, hash, GEMM
+
+    def layer(l, ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        bi.bi_router_topk(X[l], Wg[l], bi.BI_F32, bi.BI_F32, M, H, E, K_TOP, logits[l], ids[l], wts[l],
+                          mg[l], mu[l], stream=sh)
+        if ev is not None:
+            ev[1].record(stream)
+        bi.bi_shared_gate(X[l], Wsg[l], M, H, gdot[l], gsig[l], stream=sh)
+        bi.bi_route_trace_hash(ids[l], M, K_TOP, offs, None if l == 0 else hashes, hashes, stream=sh)
+        if ev is not None:
+            ev[2].record(stream)
+        bi.bi_gemm_bf16(A[l], Bw[l], Cout, M, G_N, G_K, G_K, G_K, G_N, stream=sh)
+        if ev is not None:
+            ev[3].record(stream)
+
+    def step(evs=None):
+        for l in range(LAYERS):
+            layer(l, None if evs is None else evs[l])
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert bi.bi_get_last_device_error() == 0
+
+    # --- timed region: K steps, per-call events inside, clocks sampled
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(LAYERS)]
+           for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = Clocks(local)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for s in range(args.steps):
+        step(evs[s])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    ck = clocks.stop()
+    ms = t0.elapsed_time(t1)
+    if ws > 1:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    router_ms = [evs[s][l][0].elapsed_time(evs[s][l][1]) for s in range(args.steps) for l in range(LAYERS)]
+    gemm_ms = [evs[s][l][2].elapsed_time(evs[s][l][3]) for s in range(args.steps) for l in range(LAYERS)]
+    assert bi.bi_get_last_device_error() == 0
+
+    # --- end to end: inputs from pinned host memory, results back to host
+    pin_X = [torch.empty((M, H), dtype=torch.float32, pin_memory=True) for _ in range(LAYERS)]
+    pin_A = [torch.empty((M, G_K), dtype=torch.bfloat16, pin_memory=True) for _ in range(LAYERS)]
+    for l in range(LAYERS):
+        pin_X[l].copy_(X[l])
+        pin_A[l].copy_(A[l])
+    res_ids = torch.empty((M, K_TOP), dtype=torch.int32, pin_memory=True)
+    res_w = torch.empty((M, K_TOP), dtype=torch.float32, pin_memory=True)
+    res_h = torch.empty((N_REQ,), dtype=torch.int64, pin_memory=True)
+    e2e_steps = max(1, min(args.steps, 5))
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    w0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        for l in range(LAYERS):
+            X[l].copy_(pin_X[l], non_blocking=True)
+            A[l].copy_(pin_A[l], non_blocking=True)
+            layer(l)
+        res_ids.copy_(ids[LAYERS - 1], non_blocking=True)
+        res_w.copy_(wts[LAYERS - 1], non_blocking=True)
+        res_h.copy_(hashes, non_blocking=True)
+        torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - w0
+    if ws > 1:
+        tt = torch.tensor([e2e_s], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_s = float(tt.item())
+    h2d = LAYERS * (M * H * 4 + M * G_K * 2)
+    d2h = M * K_TOP * 8 + N_REQ * 8
+
+    hbm, bf16_burst, bf16_sus, src = peaks()
+    tokens = M * ws * args.steps
+    value = tokens / (ms / 1e3)
+    g_avg = statistics.mean(gemm_ms) / 1e3
+    r_avg = statistics.mean(router_ms) / 1e3
+    g_flop = 2.0 * M * G_N * G_K
+    r_flop = 2.0 * M * E * H
+    r_bytes = 4 * E * H + 4 * M * H + 4 * M * E + 8 * M * K_TOP + 8 * M
+    g_bytes = 2 * (M * G_K + G_N * G_K + M * G_N)
+    out = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32 router / bf16 GEMM (f32 accumulate)",
+        "data": "synthetic (seeded normal draws, shapes of the pages' workloads)",
+        "config": {"workload": WORKLOAD, "tokens_per_step_per_gpu": M, "layers": LAYERS,
+                   "parallelism": f"replicas x{ws} (tokens sharded, no collective)",
+                   "l2": "inputs larger than L2 (about 4 GB streamed per step)"},
+        "parts": {
+            "router_topk_tokens_per_s": M / r_avg, "router_call_us": r_avg * 1e6,
+            "router_tflops": r_flop / r_avg / 1e12,
+            "gemm_tflops": g_flop / g_avg / 1e12, "gemm_call_us": g_avg * 1e6,
+            "gemm_frac_of_bf16_sustained": g_flop / g_avg / 1e12 / bf16_sus,
+        },
+        "roofline": {"bound": "tensor", "achieved": g_flop / g_avg / 1e12, "peak": bf16_sus,
+                     "unit": "TFLOP/s", "frac": g_flop / g_avg / 1e12 / bf16_sus, "traffic": None,
+                     "kernel": "gemm_bf16_kernel",
+                     "peak_source": f"{src} bf16 sustained (kernel timed inside a long step)",
+                     "algorithmic_bytes": g_bytes},
+        "roofline_router": {"bound": "alu", "achieved": r_flop / r_avg / 1e12, "peak": FP32_PEAK_TFLOPS,
+                            "unit": "TFLOP/s", "frac": r_flop / r_avg / 1e12 / FP32_PEAK_TFLOPS,
+                            "traffic": None, "algorithmic_bytes": r_bytes,
+                            "hbm_time_frac": (r_bytes / (hbm * 1e9)) / r_avg,
+                            "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 x 2070 MHz"},
+        "e2e": {"value": M * ws * e2e_steps / e2e_s, "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_layer * LAYERS * args.steps,
+        "clocks": ck,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+def cpu_baseline(budget_s: float = 15.0):
+    """The oracle, as it stands, on the host: one layer of the step for a
+    growing number of tokens until about budget_s of CPU time, scaled to
+    the 40-layer step.  Single-threaded (the oracle has no threading)."""
+    import numpy as np
+
+    from oracle import oracle as orc
+    from serving_numerics_gb300 import synth
+    orc.build()
+    W = synth.router_weights(7, 0, E, H)
+    wsg = synth.shared_gate_weights(7, 0, H)
+    B = synth.gemm_b(7, G_N, G_K)
+    n, spent, t_tok = 0, 0.0, 0.0
+    while spent < budget_s:
+        X = synth.tokens(7, 0, n, 1, H)
+        Ar = synth.gemm_a(7, 1, G_K, layer=n)
+        t = time.perf_counter()
+        r = orc.router_full(X, W, K_TOP, "f32")
+        orc.shared_gate(X, wsg)
+        orc.route_hash(r["ids"])
+        orc.gemm_bf16(Ar, B)
+        dt = time.perf_counter() - t
+        spent += dt
+        n += 1
+    per_token_layer = spent / n
+    return {"value": 1.0 / (per_token_layer * LAYERS), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} tokens through 1 of the 40 layers (router+gate+hash+GEMM row), "
+                      f"{spent:.1f} s single-threaded, scaled to 40 layers"}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    budget = max(5.0, min(30.0, 60.0 / max(1, args.steps)))
+    vals = []
+    for _ in range(args.warmup):
+        cpu_baseline(budget_s=1.0)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        vals.append(cpu_baseline(budget_s=budget))
+    total = time.perf_counter() - t
+    v = statistics.mean(x["value"] for x in vals)
+    out = {"metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)", "impl": "reference",
+           "data": "synthetic (seeded normal draws)",
+           "config": {"workload": WORKLOAD, "tokens_per_step_per_gpu": M, "layers": LAYERS},
+           "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                            "sample": vals[-1]["sample"]},
+           "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,203 @@
+/*
+ * bi.h -- C ABI of libbi, a batch-invariant (M-invariant) MoE prefill
+ * numerics library for one NVIDIA GB300 (sm_103a).
+ *
+ * Every result row computed here is a function of that row's inputs and of
+ * the problem's fixed sizes (H, E, k, N, K) only: never of the total token
+ * count M, of the row's position in the batch, or of what else shares the
+ * call.  That is the property the source pages turn on:
+ *
+ *  [P1] "batch changed the model's mind" (blog): "m-scan: the staircase"
+ *       (a router GEMV whose library picks its reduction order by M moves a
+ *       request's logits when co-arrivals change M), "16% of routing
+ *       decisions" (top-k turns that drift into different expert sets),
+ *       "The fix: m-invariant twins" (one fixed per-row reduction order,
+ *       independent of how many rows share the launch).
+ *  [P3] "The Illusion of Determinism in Disaggregated Inference": "The
+ *       engineering cost of determinism" (cache hit vs miss runs the GEMM at
+ *       another M), "The low-level math of tile shapes" (tile shape chosen by
+ *       M changes the K-reduction tree), "The arithmetic cost of
+ *       batch-invariant kernels" (a static reduction tree for every shape).
+ *  [P4] "diag(MODEL-MM-QWEN4-EXP): the MoE expert selections DIFFER, and a
+ *       third of the boundaries are exact bf16 ties": intro (lowest-index
+ *       tie-break), "Why a value tap could never have said this" (sorted ids,
+ *       margin in ULPs under the sign-magnitude order, FNV-1a per call),
+ *       "Why it is not a defect" (bf16 gate, f32 widening inside top-k).
+ *
+ * Conventions for every call
+ *  - All pointers are DEVICE pointers of the current CUDA device unless a
+ *    parameter says otherwise.  The caller owns every buffer.
+ *  - Calls are asynchronous on stream `s` (NULL = the legacy default
+ *    stream) and never synchronise the host.
+ *  - Arguments are validated on the host before anything is launched; an
+ *    invalid call returns an error and leaves every output untouched.
+ *  - A launch failure reported by the runtime returns BI_ERR_CUDA.  Faults
+ *    detected on the device (a bounded wait that ran out) set a sticky
+ *    device word read by bi_get_last_device_error().
+ *  - There is no CPU fallback: an unsupported shape is an error.
+ *  - Data-pointer alignment: 16 bytes.  Layouts are row-major.
+ *  - bf16 means IEEE binary32 with the low 16 bits dropped (bfloat16).
+ */
+#ifndef BI_H
+#define BI_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define BI_API __attribute__((visibility("default")))
+#else
+#define BI_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    BI_OK = 0,
+    BI_ERR_INVALID_ARG = 1,       /* null pointer, negative size, k >= E ... */
+    BI_ERR_UNSUPPORTED_SHAPE = 2, /* a size outside the limits below */
+    BI_ERR_MISALIGNED = 3,        /* a pointer or stride breaks the 16-byte rule */
+    BI_ERR_CUDA = 4,              /* the CUDA runtime reported an error */
+    BI_ERR_TIMEOUT = 5            /* a device-side bounded wait ran out */
+} bi_status;
+
+typedef enum { BI_F32 = 0, BI_BF16 = 1 } bi_dtype;
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *bi_stream;
+
+/* Limits checked by every call. */
+#define BI_MAX_E 1024          /* experts per router call */
+#define BI_MAX_K 32            /* experts selected per token */
+#define BI_MAX_H 32768         /* router hidden size */
+#define BI_MAX_HASH_RANGES 256 /* row ranges per route-hash call */
+
+/*
+ * bi_router_topk -- MoE router for one prefill call: projection, top-k,
+ * softmax over the selected, routing margin.
+ *
+ * Defined by [P1] "m-scan: the staircase" (logits = X . W_gate^T, then
+ * top_k(8 of 256)), [P1] "16% of routing decisions" (the selected set and
+ * its ranking), [P4] intro and "Why it is not a defect" (bf16-logit gate,
+ * lowest-index tie-break), [P4] "Why a value tap could never have said
+ * this" (margin = smallest selected minus largest rejected logit, also in
+ * ULPs of the logit dtype under the sign-magnitude total order).
+ *
+ *   x           [M, H]  in_dtype   token hidden states
+ *   w_gate      [E, H]  in_dtype   router weight (one row per expert)
+ *   in_dtype    BI_F32 or BI_BF16
+ *   logit_dtype BI_F32, or BI_BF16: the f32 dot is rounded to bf16
+ *               (nearest, ties to even) and selection runs on those values
+ *   logits_out  [M, E]  logit_dtype  required
+ *   ids_out     [M, k]  int32    required; rank order: value descending,
+ *               exact ties by ascending expert index
+ *   weights_out [M, k]  f32      optional (NULL): w_j = exp(l_j - l_0) /
+ *               sum_{i<k} exp(l_i - l_0), summed in rank order
+ *   margin_out  [M]     f32      optional: l_(k-1) - l_(k), the smallest
+ *               selected minus the largest rejected logit (>= 0)
+ *   margin_ulps_out [M] int32    optional: the same gap counted in ULPs of
+ *               the logit dtype under the sign-magnitude order (+0 == -0),
+ *               saturated at INT32_MAX; 0 means an exact tie at the boundary
+ *
+ * Reduction order (the invariance contract): h is cut into slabs of 128;
+ * each slab into 16 blocks of 8.  Partition q (0..15) takes block q of every
+ * slab and runs ONE fused multiply-add chain in f32 from +0 over the h < H
+ * it owns, in increasing order.  The 16 partial sums are added by a fixed
+ * pairwise tree: (0+1),(2+3),... then pairs of those, four levels.  This
+ * order depends on H alone.
+ *
+ * Limits: 1 <= H <= BI_MAX_H, H % 8 == 0; 32 <= E <= BI_MAX_E, E % 32 == 0;
+ * 1 <= k <= BI_MAX_K, k < E; M >= 0 (M == 0 returns BI_OK and does nothing).
+ * Logits must be finite for the weights and margins to be meaningful (a
+ * NaN ranks above every number and ties other NaNs by index).
+ *
+ * Scratch: when M is small the partitions are spread over several thread
+ * blocks whose partial sums meet in a library-owned device buffer
+ * (allocated once per device on the first call that needs it, never freed
+ * before exit).  Make a first call before capturing a CUDA graph.
+ */
+BI_API bi_status bi_router_topk(const void *x, const void *w_gate, bi_dtype in_dtype,
+                         bi_dtype logit_dtype, int32_t M, int32_t H, int32_t E, int32_t k,
+                         void *logits_out, int32_t *ids_out, float *weights_out,
+                         float *margin_out, int32_t *margin_ulps_out, bi_stream s);
+
+/*
+ * bi_shared_gate -- the one-output shared-expert gate: dot = X[m,:] . w_sg,
+ * gate = 1 / (1 + exp(-dot)).
+ *
+ * Defined by [P1] "m-scan: the staircase" (the shared-expert gate dot, one
+ * output per token) and [P1] "The fix: m-invariant twins" (sigmoid_dot_rows
+ * with a fixed per-row order).  Same reduction order as bi_router_topk.
+ *
+ *   x            [M, H] f32;  w_sg [H] f32
+ *   dot_out      [M] f32 required;  sigmoid_out [M] f32 optional (NULL)
+ * Limits: 1 <= H <= BI_MAX_H, H % 8 == 0; M >= 0.
+ */
+BI_API bi_status bi_shared_gate(const float *x, const float *w_sg, int32_t M, int32_t H,
+                         float *dot_out, float *sigmoid_out, bi_stream s);
+
+/*
+ * bi_gemm_bf16 -- M-invariant projection C = A . B^T on the tensor cores.
+ *
+ * Defined by [P3] "The low-level math of tile shapes" (bf16 GEMM with FP32
+ * accumulation stored as BF16; a K-reduction tree chosen by M is what makes
+ * rows differ) and [P3] "The arithmetic cost of batch-invariant kernels"
+ * (one static reduction tree for every M, small batches padded to the fixed
+ * tile, no shape heuristics, no split-K).
+ *
+ *   A [M, K] bf16, row stride lda (elements)
+ *   B [N, K] bf16, row stride ldb: the [out, in] weight of a linear layer
+ *   C [M, N] bf16, row stride ldc; C = round_bf16(sum_k A[m,k] B[n,k]),
+ *     f32 accumulation in a fixed K order (blocks of 64 in order, 16 per
+ *     tensor-core step), one tile shape (128 x 256) for every M.
+ * Limits: M >= 0 (0 is a no-op), 1 <= N, N % 16 == 0, 64 <= K, K % 64 == 0,
+ * lda >= K, ldb >= K, ldc >= N, each a multiple of 8; M, N <= 2^31 - 1.
+ */
+BI_API bi_status bi_gemm_bf16(const void *A, const void *B, void *C, int32_t M, int32_t N, int32_t K,
+                       int64_t lda, int64_t ldb, int64_t ldc, bi_stream s);
+
+/*
+ * bi_route_trace_hash -- per-request route hash: 64-bit FNV-1a over the
+ * selected expert SETS of a range of token rows.
+ *
+ * Defined by [P4] "Why a value tap could never have said this": per call, an
+ * FNV-1a hash of every token's sorted id list, so that comparing two arms is
+ * one comparison (the combine over the k slots is order-invariant, so the
+ * set, not the ranking, is what is compared).
+ *
+ *   ids          [M, k] int32 (device), as written by bi_router_topk
+ *   row_offsets  HOST array [n_ranges + 1], non-decreasing, 0 <= . <= M:
+ *                range r covers rows [row_offsets[r], row_offsets[r+1])
+ *   basis        device [n_ranges] start values, or NULL for the FNV-1a
+ *                64 offset basis 0xcbf29ce484222325 (pass the previous
+ *                layer's hashes to chain layers; may alias hash_out)
+ *   hash_out     device [n_ranges]
+ * For each row of a range: its k ids sorted ascending, serialised as
+ * little-endian int32 bytes, rows in order, no separator; each byte is
+ * xor-ed into the hash, which is then multiplied by 0x100000001b3 mod 2^64.
+ * Ranges are hashed in parallel; an empty range returns its basis.
+ * Limits: 1 <= k <= BI_MAX_K; 1 <= n_ranges <= BI_MAX_HASH_RANGES.
+ */
+BI_API bi_status bi_route_trace_hash(const int32_t *ids, int32_t M, int32_t k,
+                              const int32_t *row_offsets, int32_t n_ranges,
+                              const uint64_t *basis, uint64_t *hash_out, bi_stream s);
+
+/* Human-readable name of a status code (static string). */
+BI_API const char *bi_status_string(bi_status st);
+
+/*
+ * Reads and clears the sticky device-side error word of the current device
+ * (BI_OK if no kernel reported a fault).  Synchronises the device.
+ */
+BI_API bi_status bi_get_last_device_error(void);
+
+/* ABI version of this header: bumps on any incompatible change. */
+#define BI_ABI_VERSION 1
+BI_API int32_t bi_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* BI_H */

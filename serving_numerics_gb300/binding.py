@@ -1,0 +1,179 @@
+"""Thin ctypes binding of libbi.so (include/bi.h).
+
+Argument marshalling only: every step of the path runs in the library's
+CUDA kernels.  Tensors are torch CUDA tensors (PyTorch provides device memory
+and streams); their data pointers are passed through unchanged.  If the
+library has not been built, `load()` raises: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libbi.so")
+
+BI_OK, BI_ERR_INVALID_ARG, BI_ERR_UNSUPPORTED_SHAPE, BI_ERR_MISALIGNED, BI_ERR_CUDA, BI_ERR_TIMEOUT = range(6)
+BI_F32, BI_BF16 = 0, 1
+BI_MAX_E, BI_MAX_K, BI_MAX_H, BI_MAX_HASH_RANGES = 1024, 32, 32768, 256
+FNV64_BASIS = 0xCBF29CE484222325
+
+# name -> (restype, argtypes), mirroring include/bi.h
+_P, _I32, _I64 = C.c_void_p, C.c_int32, C.c_int64
+SIGNATURES = {
+    "bi_router_topk": (C.c_int, [_P, _P, C.c_int, C.c_int, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P]),
+    "bi_shared_gate": (C.c_int, [_P, _P, _I32, _I32, _P, _P, _P]),
+    "bi_gemm_bf16": (C.c_int, [_P, _P, _P, _I32, _I32, _I32, _I64, _I64, _I64, _P]),
+    "bi_route_trace_hash": (C.c_int, [_P, _I32, _I32, _P, _I32, _P, _P, _P]),
+    "bi_status_string": (C.c_char_p, [C.c_int]),
+    "bi_get_last_device_error": (C.c_int, []),
+    "bi_abi_version": (C.c_int32, []),
+}
+
+_lib = None
+
+
+class BiError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)}")
+
+
+def load(path: str = LIB_PATH):
+    """Load libbi.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it first "
+                               "(python -c 'import __graft_entry__ as g; g.build()')")
+        lib = C.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def status_string(st: int) -> str:
+    return load().bi_status_string(st).decode()
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(st: int, where: str):
+    if st != BI_OK:
+        raise BiError(st, where)
+
+
+# ------------------------------------------------------------- raw ABI calls
+def bi_router_topk(x, w_gate, in_dtype, logit_dtype, M, H, E, k, logits_out, ids_out,
+                   weights_out=None, margin_out=None, margin_ulps_out=None, stream=None, check=True):
+    st = load().bi_router_topk(_ptr(x), _ptr(w_gate), in_dtype, logit_dtype, M, H, E, k,
+                               _ptr(logits_out), _ptr(ids_out), _ptr(weights_out), _ptr(margin_out),
+                               _ptr(margin_ulps_out), _stream(stream))
+    if check:
+        _check(st, "bi_router_topk")
+    return st
+
+
+def bi_shared_gate(x, w_sg, M, H, dot_out, sigmoid_out=None, stream=None, check=True):
+    st = load().bi_shared_gate(_ptr(x), _ptr(w_sg), M, H, _ptr(dot_out), _ptr(sigmoid_out), _stream(stream))
+    if check:
+        _check(st, "bi_shared_gate")
+    return st
+
+
+def bi_gemm_bf16(A, B, Cout, M, N, K, lda, ldb, ldc, stream=None, check=True):
+    st = load().bi_gemm_bf16(_ptr(A), _ptr(B), _ptr(Cout), M, N, K, lda, ldb, ldc, _stream(stream))
+    if check:
+        _check(st, "bi_gemm_bf16")
+    return st
+
+
+def bi_route_trace_hash(ids, M, k, row_offsets, basis, hash_out, stream=None, check=True):
+    """row_offsets: a host sequence of n_ranges + 1 ints."""
+    n = len(row_offsets) - 1
+    arr = (C.c_int32 * max(1, n + 1))(*[int(v) for v in row_offsets])
+    st = load().bi_route_trace_hash(_ptr(ids), M, k, C.cast(arr, C.c_void_p), n, _ptr(basis),
+                                    _ptr(hash_out), _stream(stream))
+    if check:
+        _check(st, "bi_route_trace_hash")
+    return st
+
+
+def bi_get_last_device_error() -> int:
+    return load().bi_get_last_device_error()
+
+
+def bi_abi_version() -> int:
+    return load().bi_abi_version()
+
+
+# ------------------------------------------------------------- tensor helpers
+def router_topk(x, w_gate, k: int, logit_dtype: str = "f32", stream=None, out=None):
+    """Allocate the outputs with torch and run bi_router_topk.
+
+    x [M,H], w_gate [E,H]: both float32 or both bfloat16 CUDA tensors.
+    Returns dict(logits, ids, weights, margin, margin_ulps)."""
+    import torch
+    M, H = x.shape
+    E = w_gate.shape[0]
+    ind = BI_F32 if x.dtype == torch.float32 else BI_BF16
+    ld = BI_F32 if logit_dtype == "f32" else BI_BF16
+    if out is None:
+        dev = x.device
+        out = {
+            "logits": torch.empty((M, E), dtype=torch.float32 if ld == BI_F32 else torch.bfloat16, device=dev),
+            "ids": torch.empty((M, k), dtype=torch.int32, device=dev),
+            "weights": torch.empty((M, k), dtype=torch.float32, device=dev),
+            "margin": torch.empty((M,), dtype=torch.float32, device=dev),
+            "margin_ulps": torch.empty((M,), dtype=torch.int32, device=dev),
+        }
+    bi_router_topk(x, w_gate, ind, ld, M, H, E, k, out["logits"], out["ids"], out.get("weights"),
+                   out.get("margin"), out.get("margin_ulps"), stream=stream)
+    return out
+
+
+def shared_gate(x, w_sg, stream=None):
+    import torch
+    M, H = x.shape
+    dot = torch.empty((M,), dtype=torch.float32, device=x.device)
+    sig = torch.empty((M,), dtype=torch.float32, device=x.device)
+    bi_shared_gate(x, w_sg, M, H, dot, sig, stream=stream)
+    return dot, sig
+
+
+def gemm_bf16(A, B, stream=None, out=None):
+    import torch
+    M, K = A.shape
+    N = B.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    bi_gemm_bf16(A, B, out, M, N, K, A.stride(0), B.stride(0), out.stride(0), stream=stream)
+    return out
+
+
+def route_hash(ids, row_offsets, basis=None, stream=None):
+    """Per-range FNV-1a hashes (torch int64 tensor viewed as uint64 bits)."""
+    import torch
+    M, k = ids.shape
+    n = len(row_offsets) - 1
+    out = torch.empty((n,), dtype=torch.int64, device=ids.device)
+    bi_route_trace_hash(ids, M, k, row_offsets, basis, out, stream=stream)
+    return out

@@ -1,0 +1,79 @@
+// bi_internal.h -- host-side state shared by the translation units of libbi.
+// Not part of the public ABI (include/bi.h is).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <stdint.h>
+
+#include "bi.h"
+
+namespace bi {
+
+// Per-device state, created on the first call made with that device current.
+struct Device {
+    int ordinal = -1;
+    int sm_count = 0;
+    unsigned int *err = nullptr;   // device address of the sticky error word
+    void *scratch = nullptr;       // router partial sums (see router.cu)
+    size_t scratch_bytes = 0;
+    uint64_t attr_done = 0;        // kernels whose smem attribute is set (bit per kernel id)
+};
+
+// The state of the current device (never NULL on BI_OK).
+bi_status current_device(Device **out);
+
+// Grow-only device scratch owned by the library (allocated at most a few
+// times per device over the process lifetime, never per call).
+bi_status device_scratch(Device *d, size_t bytes, void **out);
+
+// cuTensorMapEncodeTiled, resolved once through the runtime.
+bi_status encode_tiled(CUtensorMap *map, CUtensorMapDataType dt, uint32_t rank,
+                       const void *gaddr, const uint64_t *dims, const uint64_t *strides_bytes,
+                       const uint32_t *box, CUtensorMapSwizzle swizzle);
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline bi_status from_cuda(cudaError_t e) { return e == cudaSuccess ? BI_OK : BI_ERR_CUDA; }
+
+// Launch with programmatic dependent launch enabled: the kernel may start
+// while the previous kernel in the stream drains; every kernel of this
+// library waits (griddepcontrol.wait) before touching global memory.
+template <typename... KArgs, typename... Args>
+bi_status launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                     cudaStream_t s, Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+    return from_cuda(e);
+}
+
+// Set the dynamic shared memory limit of `kernel` once per device.
+template <typename K>
+bi_status set_smem_once(Device *d, int kernel_id, K kernel, size_t bytes)
+{
+    uint64_t bit = 1ull << kernel_id;
+    if (d->attr_done & bit) return BI_OK;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)bytes);
+    if (e != cudaSuccess) return BI_ERR_CUDA;
+    d->attr_done |= bit;
+    return BI_OK;
+}
+
+// kernel ids for set_smem_once (one bit each)
+enum : int {
+    KID_ROUTER_PROJ = 0,   // 10 instantiations: 0..9
+    KID_GEMM = 16,
+};
+
+}  // namespace bi

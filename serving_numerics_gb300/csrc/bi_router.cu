@@ -1,0 +1,481 @@
+// bi_router.cu -- bi_router_topk: M-invariant MoE router projection on CUDA
+// cores (f32 FMA, never TF32), then top-k with the lowest-index tie-break,
+// softmax over the selected and the routing margin.
+//
+// Source pages: "batch changed the model's mind" ("m-scan: the staircase",
+// "The fix: m-invariant twins"); "diag(MODEL-MM-QWEN4-EXP): the MoE expert
+// selections DIFFER ..." (intro, "Why a value tap could never have said
+// this", "Why it is not a defect").
+//
+// Reduction contract (depends on H only).  h is cut into slabs of 128 and
+// each slab into 16 blocks of 8.  Partition q in 0..15 owns block q of every
+// slab; its partial sum is ONE f32 fused multiply-add chain from +0 over the
+// h < H it owns, in increasing h.  The 16 partials are added by the pairwise
+// tree (0+1),(2+3),...,(14+15), then (01+23),..., four levels.
+//
+// Work decomposition (free to depend on M, since it never changes the
+// order): a work tile is 32 tokens x 32 experts.  Its 16 partitions are
+// split over C thread blocks (C = 1, 2, 4, 8 or 16; 16/C warps each, one
+// warp per partition).  A block adds its partitions with the lower levels of
+// the tree; with C > 1 the C group sums meet in library scratch and the
+// selection kernel adds them with the remaining upper levels.  C grows only
+// when there are too few tiles to fill the GPU (small M).
+//
+// Data path: each partition's [32 rows x 8] block of X and of W_gate is
+// staged by its own TMA box into shared memory (f32: 32-byte swizzle, which
+// makes the lane access pattern below bank-conflict free), a ring of stages
+// deep.  Lane (tg, eg) of a warp owns tokens tg+8j (j<4) and experts eg+4i
+// (i<8): 32 accumulators.
+#include <cuda_bf16.h>
+#include <limits.h>
+
+#include "bi_device.cuh"
+#include "bi_internal.h"
+
+namespace bi {
+namespace {
+
+constexpr int kTileM = 32, kTileE = 32, kSlab = 128, kBlk = 8, kParts = 16;
+
+template <typename InT, int C>
+struct ProjCfg {
+    static constexpr int NPL = kParts / C;                      // partitions (= warps) per block
+    static constexpr int THREADS = 32 * NPL;
+    static constexpr int PART_BYTES = kTileM * kBlk * (int)sizeof(InT);   // one TMA box
+    static constexpr int OP_BYTES = PART_BYTES * NPL;           // X (or W) part of a stage
+    static constexpr int STAGE_BYTES = 2 * OP_BYTES;
+    static constexpr int NST_RAW = (96 * 1024) / STAGE_BYTES;
+    static constexpr int NST = NST_RAW > 16 ? 16 : (NST_RAW < 2 ? 2 : NST_RAW);
+    static constexpr int TREE_BYTES = (NPL / 2) * 1024 * 4;
+    static constexpr int OUT_BYTES = kTileM * (kTileE + 1) * 4;
+    static constexpr int BODY0 = NST * STAGE_BYTES;
+    static constexpr int BODY1 = TREE_BYTES > OUT_BYTES ? TREE_BYTES : OUT_BYTES;
+    static constexpr int BODY = BODY0 > BODY1 ? BODY0 : BODY1;
+    static constexpr int SMEM = BODY + 1024;                     // + alignment slack
+};
+
+// One 8-wide block of the chain for a 4x8 register tile, f32 inputs.
+// Box layout: row r (32 bytes) at 32*r, its 16-byte half c stored at half
+// c ^ bit2(r) (TMA 32-byte swizzle: address bit 4 ^= address bit 7).
+__device__ __forceinline__ void block_f32(float (&acc)[4][8], const uint8_t *xs, const uint8_t *ws,
+                                          int tg, int eg)
+{
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+        float4 xv[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int r = tg + 8 * j;
+            xv[j] = *reinterpret_cast<const float4 *>(xs + 32 * r + 16 * (c ^ ((r >> 2) & 1)));
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int r = eg + 4 * i;
+            const float4 wv =
+                *reinterpret_cast<const float4 *>(ws + 32 * r + 16 * (c ^ ((r >> 2) & 1)));
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float a = acc[j][i];
+                a = __fmaf_rn(xv[j].x, wv.x, a);
+                a = __fmaf_rn(xv[j].y, wv.y, a);
+                a = __fmaf_rn(xv[j].z, wv.z, a);
+                a = __fmaf_rn(xv[j].w, wv.w, a);
+                acc[j][i] = a;
+            }
+        }
+    }
+}
+
+// The same for bf16 inputs (box rows of 16 bytes, no swizzle).  Products
+// of two bf16 values are exact in f32, so each step rounds once, as in f32.
+__device__ __forceinline__ void block_bf16(float (&acc)[4][8], const uint8_t *xs, const uint8_t *ws,
+                                           int tg, int eg)
+{
+    uint4 xr[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) xr[j] = *reinterpret_cast<const uint4 *>(xs + 16 * (tg + 8 * j));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint4 wr = *reinterpret_cast<const uint4 *>(ws + 16 * (eg + 4 * i));
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            float a = acc[j][i];
+            a = __fmaf_rn(bf16lo(xr[j].x), bf16lo(wr.x), a);
+            a = __fmaf_rn(bf16hi(xr[j].x), bf16hi(wr.x), a);
+            a = __fmaf_rn(bf16lo(xr[j].y), bf16lo(wr.y), a);
+            a = __fmaf_rn(bf16hi(xr[j].y), bf16hi(wr.y), a);
+            a = __fmaf_rn(bf16lo(xr[j].z), bf16lo(wr.z), a);
+            a = __fmaf_rn(bf16hi(xr[j].z), bf16hi(wr.z), a);
+            a = __fmaf_rn(bf16lo(xr[j].w), bf16lo(wr.w), a);
+            a = __fmaf_rn(bf16hi(xr[j].w), bf16hi(wr.w), a);
+            acc[j][i] = a;
+        }
+    }
+}
+
+enum OutMode : int { OUT_F32 = 0, OUT_BF16 = 1, OUT_PARTIAL = 2 };
+
+template <typename InT, int C>
+__global__ void __launch_bounds__(ProjCfg<InT, C>::THREADS)
+router_proj_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
+                   int M, int E, int H, int out_mode, void *__restrict__ out, unsigned int *err)
+{
+    using Cfg = ProjCfg<InT, C>;
+    constexpr int NPL = Cfg::NPL, NST = Cfg::NST;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t full_bar[NST];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~uintptr_t(1023));
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int e_tile = blockIdx.x / C, g = blockIdx.x % C;
+    const int m0 = blockIdx.y * kTileM, e0 = e_tile * kTileE, q0 = g * NPL;
+    const int ns = (H + kSlab - 1) / kSlab;
+    const int tg = lane & 7, eg = lane >> 3;
+
+    if (tid == 0) {
+        prefetch_tmap(&tmx);
+        prefetch_tmap(&tmw);
+#pragma unroll
+        for (int s = 0; s < NST; ++s) mbar_init(&full_bar[s], 1);
+        mbar_init_fence();
+    }
+    __syncthreads();
+    pdl_wait();       // inputs may come from the previous kernel in the stream
+    pdl_trigger();
+
+    // producer: thread 0 stages slab s into ring slot `slot` (valid blocks only)
+    auto issue = [&](int s, int slot) {
+        uint8_t *st = smem + slot * Cfg::STAGE_BYTES;
+        int nvalid = 0;
+#pragma unroll
+        for (int w = 0; w < NPL; ++w) nvalid += (kSlab * s + kBlk * (q0 + w) < H) ? 1 : 0;
+        mbar_arrive_expect_tx(&full_bar[slot], (uint32_t)(nvalid * 2 * Cfg::PART_BYTES));
+#pragma unroll
+        for (int w = 0; w < NPL; ++w) {
+            const int h0 = kSlab * s + kBlk * (q0 + w);
+            if (h0 < H) {
+                tma_load_2d(st + w * Cfg::PART_BYTES, &tmx, &full_bar[slot], h0, m0);
+                tma_load_2d(st + Cfg::OP_BYTES + w * Cfg::PART_BYTES, &tmw, &full_bar[slot], h0, e0);
+            }
+        }
+    };
+
+    const int nst = ns < NST ? ns : NST;
+    if (tid == 0)
+        for (int s = 0; s < nst; ++s) issue(s, s);
+
+    float acc[4][8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[j][i] = 0.0f;
+
+    for (int s = 0; s < ns; ++s) {
+        const int slot = s % NST;
+        mbar_wait(&full_bar[slot], (uint32_t)((s / NST) & 1), err, 0x11);
+        if (kSlab * s + kBlk * (q0 + warp) < H) {      // warp-uniform
+            const uint8_t *st = smem + slot * Cfg::STAGE_BYTES;
+            if constexpr (sizeof(InT) == 4)
+                block_f32(acc, st + warp * Cfg::PART_BYTES, st + Cfg::OP_BYTES + warp * Cfg::PART_BYTES, tg, eg);
+            else
+                block_bf16(acc, st + warp * Cfg::PART_BYTES, st + Cfg::OP_BYTES + warp * Cfg::PART_BYTES, tg, eg);
+        }
+        __syncthreads();                                   // slot free again
+        if (tid == 0 && s + NST < ns) issue(s + NST, slot);
+    }
+
+    // lower levels of the pairwise tree, over this block's NPL partitions
+    float *tree = reinterpret_cast<float *>(smem);
+#pragma unroll
+    for (int d = 1; d < NPL; d *= 2) {
+        const int p = warp / (2 * d);
+        if ((warp % (2 * d)) == d) {
+            float *dst = tree + p * 1024;
+#pragma unroll
+            for (int v = 0; v < 32; ++v) dst[v * 32 + lane] = acc[v >> 3][v & 7];
+        }
+        __syncthreads();
+        if ((warp % (2 * d)) == 0) {
+            const float *src = tree + p * 1024;
+#pragma unroll
+            for (int v = 0; v < 32; ++v) acc[v >> 3][v & 7] = acc[v >> 3][v & 7] + src[v * 32 + lane];
+        }
+        __syncthreads();
+    }
+
+    // stage the 32x32 result and write it row-coalesced
+    float *tile = reinterpret_cast<float *>(smem);
+    if (warp == 0) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) tile[(tg + 8 * j) * (kTileE + 1) + eg + 4 * i] = acc[j][i];
+    }
+    __syncthreads();
+    for (int idx = tid; idx < kTileM * kTileE; idx += Cfg::THREADS) {
+        const int t = idx >> 5, e = idx & 31, m = m0 + t;
+        if (m < M) {
+            const float v = tile[t * (kTileE + 1) + e];
+            const size_t o = (size_t)m * E + e0 + e;
+            if (out_mode == OUT_F32)
+                static_cast<float *>(out)[o] = v;
+            else if (out_mode == OUT_BF16)
+                static_cast<__nv_bfloat16 *>(out)[o] = __float2bfloat16_rn(v);
+            else
+                static_cast<float *>(out)[(size_t)g * M * E + o] = v;
+        }
+    }
+}
+
+// Order key of an f32 value: larger key = ranks higher.  NaN ranks above
+// everything; -0 is folded onto +0 so the two compare equal.  Key 0 is below
+// every real value (the smallest, -inf, maps to 0x007FFFFF) and marks a
+// taken expert.
+__device__ __forceinline__ uint32_t rank_key(float x)
+{
+    uint32_t u = __float_as_uint(x);
+    if ((u & 0x7FFFFFFFu) > 0x7F800000u) return 0xFFFFFFFFu;
+    if (u == 0x80000000u) u = 0u;
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Sign-magnitude ordinal of a logit-dtype pattern (+0 and -0 both 0).
+__device__ __forceinline__ long long sm_ord(float x, int bf16)
+{
+    uint32_t u = __float_as_uint(x);
+    if (bf16) {
+        const uint32_t b = u >> 16;
+        return (b & 0x8000u) ? -(long long)(b & 0x7FFFu) : (long long)b;
+    }
+    return (u & 0x80000000u) ? -(long long)(u & 0x7FFFFFFFu) : (long long)u;
+}
+
+constexpr int kSelWarps = 8;
+
+// One warp per token: finish the tree (C > 1), round to the logit dtype,
+// then k+1 rounds of warp arg-max (value desc, index asc).  Round k yields
+// the largest rejected logit for the margin.
+template <int EPLM>
+__global__ void __launch_bounds__(32 * kSelWarps)
+router_select_kernel(const float *__restrict__ part, int C, void *logits, int logit_bf16, int M,
+                     int E, int k, int32_t *__restrict__ ids, float *__restrict__ weights,
+                     float *__restrict__ margin, int32_t *__restrict__ ulps)
+{
+    pdl_wait();
+    pdl_trigger();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m = blockIdx.x * kSelWarps + warp;
+    if (m >= M) return;
+    const int epl = E >> 5;
+
+    float v[EPLM];
+    uint32_t key[EPLM];
+#pragma unroll
+    for (int i = 0; i < EPLM; ++i) {
+        v[i] = 0.0f;
+        key[i] = 0u;
+        if (i < epl) {
+            const size_t o = (size_t)m * E + lane + 32 * i;
+            float x;
+            if (C == 1) {
+                x = logit_bf16 ? __bfloat162float(static_cast<const __nv_bfloat16 *>(logits)[o])
+                               : static_cast<const float *>(logits)[o];
+            } else {
+                float p[16];
+#pragma unroll
+                for (int q = 0; q < 16; ++q) p[q] = (q < C) ? part[(size_t)q * M * E + o] : 0.0f;
+#pragma unroll
+                for (int d = 1; d < 16; d *= 2)
+                    if (d < C) {
+#pragma unroll
+                        for (int q = 0; q + d < 16; q += 2 * d) p[q] = p[q] + p[q + d];
+                    }
+                x = p[0];
+                if (logit_bf16) {
+                    const __nv_bfloat16 b = __float2bfloat16_rn(x);
+                    static_cast<__nv_bfloat16 *>(logits)[o] = b;
+                    x = __bfloat162float(b);
+                } else {
+                    static_cast<float *>(logits)[o] = x;
+                }
+            }
+            v[i] = x;
+            key[i] = rank_key(x);
+        }
+    }
+
+    uint32_t bk = 0u;
+    uint32_t bidx = 0xFFFFFFFFu;
+    float bv = 0.0f;
+    auto rescan = [&]() {
+        bk = 0u;
+        bidx = 0xFFFFFFFFu;
+#pragma unroll
+        for (int i = 0; i < EPLM; ++i)
+            if (key[i] > bk) {              // ascending i: first maximum = lowest index
+                bk = key[i];
+                bidx = (uint32_t)(lane + 32 * i);
+                bv = v[i];
+            }
+    };
+    rescan();
+
+    float l0 = 0.0f, den = 0.0f, my_e = 0.0f, v_sel_min = 0.0f, v_rej_max = 0.0f;
+    int my_id = 0;
+    for (int r = 0; r <= k; ++r) {
+        const uint32_t mk = __reduce_max_sync(0xFFFFFFFFu, bk);
+        const uint32_t win = __reduce_min_sync(0xFFFFFFFFu, bk == mk ? bidx : 0xFFFFFFFFu);
+        const float wv = __shfl_sync(0xFFFFFFFFu, bv, (int)(win & 31u));
+        if (r == k) {
+            v_rej_max = wv;
+            break;
+        }
+        if (r == 0) l0 = wv;
+        const float ex = expf(wv - l0);
+        den += ex;                           // rank order
+        if (lane == r) {
+            my_e = ex;
+            my_id = (int)win;
+        }
+        v_sel_min = wv;
+        if ((int)(win & 31u) == lane) {
+#pragma unroll
+            for (int i = 0; i < EPLM; ++i)
+                if ((uint32_t)(lane + 32 * i) == win) key[i] = 0u;
+            rescan();
+        }
+    }
+    if (lane < k) {
+        ids[(size_t)m * k + lane] = my_id;
+        if (weights) weights[(size_t)m * k + lane] = my_e / den;
+    }
+    if (lane == 0) {
+        if (margin) margin[m] = v_sel_min - v_rej_max;
+        if (ulps) {
+            long long d = sm_ord(v_sel_min, logit_bf16) - sm_ord(v_rej_max, logit_bf16);
+            if (d > INT_MAX) d = INT_MAX;
+            if (d < INT_MIN) d = INT_MIN;
+            ulps[m] = (int32_t)d;
+        }
+    }
+}
+
+template <typename InT, int C>
+bi_status launch_proj(Device *d, const CUtensorMap &tmx, const CUtensorMap &tmw, int M, int E,
+                      int H, int out_mode, void *out, cudaStream_t s, int kid)
+{
+    using Cfg = ProjCfg<InT, C>;
+    auto kern = router_proj_kernel<InT, C>;
+    bi_status st = set_smem_once(d, kid, kern, Cfg::SMEM);
+    if (st != BI_OK) return st;
+    dim3 grid((E / kTileE) * C, (M + kTileM - 1) / kTileM);
+    return launch_pdl(kern, grid, dim3(Cfg::THREADS), (size_t)Cfg::SMEM, s, tmx, tmw, M, E, H,
+                      out_mode, out, d->err);
+}
+
+template <typename InT>
+bi_status launch_proj_c(Device *d, int C, const CUtensorMap &tmx, const CUtensorMap &tmw, int M,
+                        int E, int H, int out_mode, void *out, cudaStream_t s)
+{
+    const int base = KID_ROUTER_PROJ + (sizeof(InT) == 4 ? 0 : 5);
+    switch (C) {
+    case 1: return launch_proj<InT, 1>(d, tmx, tmw, M, E, H, out_mode, out, s, base + 0);
+    case 2: return launch_proj<InT, 2>(d, tmx, tmw, M, E, H, out_mode, out, s, base + 1);
+    case 4: return launch_proj<InT, 4>(d, tmx, tmw, M, E, H, out_mode, out, s, base + 2);
+    case 8: return launch_proj<InT, 8>(d, tmx, tmw, M, E, H, out_mode, out, s, base + 3);
+    default: return launch_proj<InT, 16>(d, tmx, tmw, M, E, H, out_mode, out, s, base + 4);
+    }
+}
+
+// How many blocks share one tile's 16 partitions: the smallest power of two
+// that gives at least one block per SM, capped at 16 and by the scratch
+// bound.  Any choice gives the same bits; this only trades parallelism for
+// scratch traffic.
+int choose_split(int M, int E, int sms)
+{
+    const long long tiles = (long long)((M + kTileM - 1) / kTileM) * (E / kTileE);
+    int C = 1;
+    while (C < 16 && tiles * C < sms) C *= 2;
+    while (C > 1 && (long long)C * M * E * 4 > (16ll << 20)) C /= 2;
+    return C;
+}
+
+}  // namespace
+}  // namespace bi
+
+using namespace bi;
+
+extern "C" bi_status bi_router_topk(const void *x, const void *w_gate, bi_dtype in_dtype,
+                                    bi_dtype logit_dtype, int32_t M, int32_t H, int32_t E, int32_t k,
+                                    void *logits_out, int32_t *ids_out, float *weights_out,
+                                    float *margin_out, int32_t *margin_ulps_out, bi_stream s)
+{
+    if ((in_dtype != BI_F32 && in_dtype != BI_BF16) || (logit_dtype != BI_F32 && logit_dtype != BI_BF16))
+        return BI_ERR_INVALID_ARG;
+    if (M < 0 || H <= 0 || E <= 0 || k <= 0 || k >= E) return BI_ERR_INVALID_ARG;
+    if (H > BI_MAX_H || (H % 8) != 0 || E < 32 || E > BI_MAX_E || (E % 32) != 0 || k > BI_MAX_K)
+        return BI_ERR_UNSUPPORTED_SHAPE;
+    if (M > (1 << 21)) return BI_ERR_UNSUPPORTED_SHAPE;
+    if (M == 0) return BI_OK;
+    if (!x || !w_gate || !logits_out || !ids_out) return BI_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w_gate)) return BI_ERR_MISALIGNED;
+    const uintptr_t lal = logit_dtype == BI_F32 ? 3u : 1u;
+    if ((reinterpret_cast<uintptr_t>(logits_out) & lal) || (reinterpret_cast<uintptr_t>(ids_out) & 3u) ||
+        (reinterpret_cast<uintptr_t>(weights_out) & 3u) || (reinterpret_cast<uintptr_t>(margin_out) & 3u) ||
+        (reinterpret_cast<uintptr_t>(margin_ulps_out) & 3u))
+        return BI_ERR_MISALIGNED;
+
+    Device *d = nullptr;
+    bi_status st = current_device(&d);
+    if (st != BI_OK) return st;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(s);
+
+    const int C = choose_split(M, E, d->sm_count);
+    void *part = nullptr;
+    if (C > 1) {
+        st = device_scratch(d, (size_t)C * M * E * sizeof(float), &part);
+        if (st != BI_OK) return st;
+    }
+
+    const bool f32in = in_dtype == BI_F32;
+    const uint64_t es = f32in ? 4 : 2;
+    const CUtensorMapDataType dt = f32in ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const CUtensorMapSwizzle sw = f32in ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_NONE;
+    const uint32_t box[2] = {(uint32_t)kBlk, (uint32_t)kTileM};
+    alignas(64) CUtensorMap tmx, tmw;
+    {
+        const uint64_t dims[2] = {(uint64_t)H, (uint64_t)M};
+        const uint64_t strides[1] = {(uint64_t)H * es};
+        if ((st = encode_tiled(&tmx, dt, 2, x, dims, strides, box, sw)) != BI_OK) return st;
+    }
+    {
+        const uint64_t dims[2] = {(uint64_t)H, (uint64_t)E};
+        const uint64_t strides[1] = {(uint64_t)H * es};
+        if ((st = encode_tiled(&tmw, dt, 2, w_gate, dims, strides, box, sw)) != BI_OK) return st;
+    }
+
+    const int lbf = logit_dtype == BI_BF16 ? 1 : 0;
+    const int out_mode = C > 1 ? OUT_PARTIAL : (lbf ? OUT_BF16 : OUT_F32);
+    void *out = C > 1 ? part : logits_out;
+    st = f32in ? launch_proj_c<float>(d, C, tmx, tmw, M, E, H, out_mode, out, cs)
+               : launch_proj_c<__nv_bfloat16>(d, C, tmx, tmw, M, E, H, out_mode, out, cs);
+    if (st != BI_OK) return st;
+
+    const int epl = E / 32;
+    dim3 grid((M + kSelWarps - 1) / kSelWarps), block(32 * kSelWarps);
+    const float *pp = static_cast<const float *>(part);
+    if (epl <= 4)
+        st = launch_pdl(router_select_kernel<4>, grid, block, 0, cs, pp, C, logits_out, lbf, M, E, k,
+                        ids_out, weights_out, margin_out, margin_ulps_out);
+    else if (epl <= 8)
+        st = launch_pdl(router_select_kernel<8>, grid, block, 0, cs, pp, C, logits_out, lbf, M, E, k,
+                        ids_out, weights_out, margin_out, margin_ulps_out);
+    else if (epl <= 16)
+        st = launch_pdl(router_select_kernel<16>, grid, block, 0, cs, pp, C, logits_out, lbf, M, E, k,
+                        ids_out, weights_out, margin_out, margin_ulps_out);
+    else
+        st = launch_pdl(router_select_kernel<32>, grid, block, 0, cs, pp, C, logits_out, lbf, M, E, k,
+                        ids_out, weights_out, margin_out, margin_ulps_out);
+    return st;
+}

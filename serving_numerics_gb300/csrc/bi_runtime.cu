@@ -1,0 +1,111 @@
+// bi_runtime.cu -- per-device state, the sticky device error word, tensor-map
+// encoding and the small ABI utilities (status strings, version).
+#include <mutex>
+
+#include "bi_internal.h"
+
+namespace bi {
+
+// Sticky error word: a kernel that gives up a bounded wait records
+// (status | where << 8) here; bi_get_last_device_error() reads and clears it.
+__device__ unsigned int g_device_error;
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+Device g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+}  // namespace
+
+bi_status current_device(Device **out)
+{
+    int ord = -1;
+    if (cudaGetDevice(&ord) != cudaSuccess || ord < 0 || ord >= kMaxDevices) return BI_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    Device &d = g_dev[ord];
+    if (d.ordinal < 0) {
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, ord) != cudaSuccess)
+            return BI_ERR_CUDA;
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return BI_ERR_CUDA;
+        d.sm_count = sms;
+        d.err = static_cast<unsigned int *>(p);
+        d.ordinal = ord;
+    }
+    *out = &d;
+    return BI_OK;
+}
+
+bi_status device_scratch(Device *d, size_t bytes, void **out)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (d->scratch_bytes < bytes) {
+        // grow-only; the old buffer may still be in use by queued kernels, so
+        // it is kept (leaked) rather than freed under their feet
+        size_t want = bytes < (size_t(2) << 20) ? (size_t(2) << 20) : bytes;
+        void *p = nullptr;
+        if (cudaMalloc(&p, want) != cudaSuccess) return BI_ERR_CUDA;
+        d->scratch = p;
+        d->scratch_bytes = want;
+    }
+    *out = d->scratch;
+    return BI_OK;
+}
+
+bi_status encode_tiled(CUtensorMap *map, CUtensorMapDataType dt, uint32_t rank,
+                       const void *gaddr, const uint64_t *dims, const uint64_t *strides_bytes,
+                       const uint32_t *box, CUtensorMapSwizzle swizzle)
+{
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!g_encode) {
+            void *fn = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                 cudaEnableDefault, &q) != cudaSuccess ||
+                q != cudaDriverEntryPointSuccess || !fn)
+                return BI_ERR_CUDA;
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+    }
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = g_encode(map, dt, rank, const_cast<void *>(gaddr),
+                          reinterpret_cast<const cuuint64_t *>(dims),
+                          reinterpret_cast<const cuuint64_t *>(strides_bytes),
+                          reinterpret_cast<const cuuint32_t *>(box), estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? BI_OK : BI_ERR_CUDA;
+}
+
+}  // namespace bi
+
+extern "C" {
+
+const char *bi_status_string(bi_status st)
+{
+    switch (st) {
+    case BI_OK: return "BI_OK";
+    case BI_ERR_INVALID_ARG: return "BI_ERR_INVALID_ARG: a pointer is NULL or a size is negative or inconsistent";
+    case BI_ERR_UNSUPPORTED_SHAPE: return "BI_ERR_UNSUPPORTED_SHAPE: a size is outside the library's limits";
+    case BI_ERR_MISALIGNED: return "BI_ERR_MISALIGNED: a pointer or stride is not 16-byte aligned";
+    case BI_ERR_CUDA: return "BI_ERR_CUDA: the CUDA runtime reported an error";
+    case BI_ERR_TIMEOUT: return "BI_ERR_TIMEOUT: a device-side bounded wait ran out";
+    }
+    return "unknown bi_status";
+}
+
+bi_status bi_get_last_device_error(void)
+{
+    unsigned int v = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess) return BI_ERR_CUDA;
+    if (cudaMemcpyFromSymbol(&v, bi::g_device_error, sizeof v) != cudaSuccess) return BI_ERR_CUDA;
+    unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(bi::g_device_error, &zero, sizeof zero) != cudaSuccess) return BI_ERR_CUDA;
+    return static_cast<bi_status>(v & 0xFFu);
+}
+
+int32_t bi_abi_version(void) { return BI_ABI_VERSION; }
+
+}  // extern "C"

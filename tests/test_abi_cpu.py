@@ -1,0 +1,117 @@
+"""The C ABI without a GPU: the library loads, exports every symbol the
+header declares, and rejects invalid arguments on the host before any CUDA
+call (so these calls are safe on a machine with no GPU)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "bi.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from serving_numerics_gb300 import binding, build
+    build.build()
+    return binding.load()
+
+
+def declared_symbols():
+    txt = open(HEADER).read()
+    return sorted(set(re.findall(r"BI_API\s+[\w\s\*]+?\b(bi_\w+)\s*\(", txt)))
+
+
+def test_header_declares_the_abi():
+    names = declared_symbols()
+    for want in ("bi_router_topk", "bi_shared_gate", "bi_gemm_bf16", "bi_route_trace_hash",
+                 "bi_status_string", "bi_get_last_device_error", "bi_abi_version"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from serving_numerics_gb300 import binding
+    for name in declared_symbols():
+        assert hasattr(lib, name), f"libbi.so does not export {name}"
+        assert name in binding.SIGNATURES, f"binding lacks {name}"
+    assert lib.bi_abi_version() == 1
+
+
+def test_status_strings(lib):
+    from serving_numerics_gb300 import binding as b
+    for st in range(6):
+        assert b.status_string(st).startswith("BI_")
+
+
+FAKE = 0x10000          # never dereferenced: every call below fails validation first
+MIS = FAKE + 4          # not 16-byte aligned
+
+
+def _router(lib, **kw):
+    a = dict(x=FAKE, w=FAKE, ind=0, ld=0, M=4, H=256, E=64, k=4, logits=FAKE, ids=FAKE,
+             weights=None, margin=None, ulps=None)
+    a.update(kw)
+    return lib.bi_router_topk(a["x"], a["w"], a["ind"], a["ld"], a["M"], a["H"], a["E"], a["k"],
+                              a["logits"], a["ids"], a["weights"], a["margin"], a["ulps"], None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(M=-1), 1), (dict(k=0), 1), (dict(k=64), 1), (dict(H=0), 1), (dict(E=0), 1),
+    (dict(ind=2), 1), (dict(ld=7), 1),
+    (dict(H=260), 2), (dict(E=48), 2), (dict(E=2048), 2), (dict(k=33, E=64), 2), (dict(H=40000), 2),
+    (dict(x=None), 1), (dict(ids=None), 1), (dict(logits=None), 1),
+    (dict(x=MIS), 3), (dict(w=MIS), 3), (dict(ids=FAKE + 2), 3),
+])
+def test_router_validation(lib, kw, want):
+    assert _router(lib, **kw) == want
+
+
+def test_router_m0_is_noop(lib):
+    assert _router(lib, M=0, x=None, w=None, logits=None, ids=None) == 0
+
+
+@pytest.mark.parametrize("args,want", [
+    ((FAKE, FAKE, -1, 256, FAKE, None), 1), ((FAKE, FAKE, 4, 0, FAKE, None), 1),
+    ((FAKE, FAKE, 4, 12, FAKE, None), 2), ((None, FAKE, 4, 256, FAKE, None), 1),
+    ((MIS, FAKE, 4, 256, FAKE, None), 3), ((FAKE, FAKE, 4, 256, None, None), 1),
+    ((None, None, 0, 256, None, None), 0),
+])
+def test_gate_validation(lib, args, want):
+    assert lib.bi_shared_gate(*args, None) == want
+
+
+@pytest.mark.parametrize("args,want", [
+    ((FAKE, FAKE, FAKE, -1, 256, 64, 64, 64, 256), 1),
+    ((FAKE, FAKE, FAKE, 4, 256, 96, 96, 96, 256), 2),      # K % 64
+    ((FAKE, FAKE, FAKE, 4, 250, 64, 64, 64, 250), 2),      # N % 16
+    ((FAKE, FAKE, FAKE, 4, 256, 64, 32, 64, 256), 1),      # lda < K
+    ((FAKE, FAKE, FAKE, 4, 256, 64, 68, 64, 256), 3),      # lda % 8
+    ((MIS, FAKE, FAKE, 4, 256, 64, 64, 64, 256), 3),
+    ((None, FAKE, FAKE, 4, 256, 64, 64, 64, 256), 1),
+    ((None, None, None, 0, 256, 64, 64, 64, 256), 0),
+])
+def test_gemm_validation(lib, args, want):
+    assert lib.bi_gemm_bf16(*args, None) == want
+
+
+def _offs(v):
+    arr = (C.c_int32 * len(v))(*v)
+    return C.cast(arr, C.c_void_p), arr
+
+
+@pytest.mark.parametrize("offs,M,k,n,want", [
+    ([0, 3, 2], 5, 4, 2, 1),      # decreasing
+    ([0, 6], 5, 4, 1, 1),         # past M
+    ([0, 5], 5, 0, 1, 1),         # k = 0
+    ([0, 5], 5, 33, 1, 2),        # k > max
+    ([0, 5], 5, 4, 0, 1),         # no ranges
+])
+def test_hash_validation(lib, offs, M, k, n, want):
+    p, keep = _offs(offs)
+    assert lib.bi_route_trace_hash(FAKE, M, k, p, n, None, FAKE, None) == want
+
+
+def test_hash_too_many_ranges(lib):
+    p, keep = _offs([0] * 300)
+    assert lib.bi_route_trace_hash(FAKE, 5, 4, p, 299, None, FAKE, None) == 2
