@@ -320,7 +320,10 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--layers", type=int, default=LAYERS,
+                    help="fewer layers for a small profiling case (the benchmark uses 40)")
     args = ap.parse_args()
+    globals()["LAYERS"] = args.layers
     if args.impl == "reference":
         run_reference(args)
     else:
