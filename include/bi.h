@@ -184,6 +184,40 @@ BI_API bi_status bi_route_trace_hash(const int32_t *ids, int32_t M, int32_t k,
                               const int32_t *row_offsets, int32_t n_ranges,
                               const uint64_t *basis, uint64_t *hash_out, bi_stream s);
 
+/*
+ * bi_router_topk_noalloc -- bi_router_topk for callers that must not
+ * allocate device memory, with the same arguments and bit-identical results.
+ *
+ * No counterpart on the source pages: it exists for the caller, not for the
+ * method.  bi_router_topk allocates its partial-sum scratch lazily with
+ * cudaMalloc the first time a small batch needs it.  Some callers cannot let
+ * a library do that: a serving engine that owns all device memory through
+ * its own pool and forbids allocations outside it, or code that records the
+ * router into a CUDA graph, where a first-time cudaMalloc inside the capture
+ * is not allowed.  This entry point instead uses a fixed device array of
+ * BI_NOALLOC_SCRATCH_BYTES compiled into the library (held by every GPU that
+ * loads the library until the process exits) and never calls cudaMalloc,
+ * cudaFree or any allocating routine.
+ *
+ * It always spreads each 32x32 tile's 16 partitions over 16 thread blocks
+ * (the small-batch decomposition), needing 16*M*E*4 bytes of scratch, so it
+ * serves M*E <= BI_NOALLOC_SCRATCH_BYTES / 64 (M <= 64 at E = 256, M <= 32
+ * at E = 512, M <= 16 at E = 1024); larger problems return
+ * BI_ERR_UNSUPPORTED_SHAPE.  The first call on each device looks up the
+ * array's device address (cudaGetSymbolAddress, with that device current):
+ * make that first call before any stream capture.  Every call shares the one
+ * array, whose contents persist between calls; each call overwrites all of
+ * the scratch it reads before reading it, so nothing needs clearing.  Calls
+ * that overlap on the GPU (on different streams, or from different host
+ * threads) race on the array and must be serialised by the caller.
+ */
+#define BI_NOALLOC_SCRATCH_BYTES (1u << 20)
+BI_API bi_status bi_router_topk_noalloc(const void *x, const void *w_gate, bi_dtype in_dtype,
+                                        bi_dtype logit_dtype, int32_t M, int32_t H, int32_t E,
+                                        int32_t k, void *logits_out, int32_t *ids_out,
+                                        float *weights_out, float *margin_out,
+                                        int32_t *margin_ulps_out, bi_stream s);
+
 /* Human-readable name of a status code (static string). */
 BI_API const char *bi_status_string(bi_status st);
 

@@ -16,12 +16,14 @@ LIB_PATH = os.path.join(PKG, "libbi.so")
 BI_OK, BI_ERR_INVALID_ARG, BI_ERR_UNSUPPORTED_SHAPE, BI_ERR_MISALIGNED, BI_ERR_CUDA, BI_ERR_TIMEOUT = range(6)
 BI_F32, BI_BF16 = 0, 1
 BI_MAX_E, BI_MAX_K, BI_MAX_H, BI_MAX_HASH_RANGES = 1024, 32, 32768, 256
+BI_NOALLOC_SCRATCH_BYTES = 1 << 20
 FNV64_BASIS = 0xCBF29CE484222325
 
 # name -> (restype, argtypes), mirroring include/bi.h
 _P, _I32, _I64 = C.c_void_p, C.c_int32, C.c_int64
 SIGNATURES = {
     "bi_router_topk": (C.c_int, [_P, _P, C.c_int, C.c_int, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P]),
+    "bi_router_topk_noalloc": (C.c_int, [_P, _P, C.c_int, C.c_int, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P]),
     "bi_shared_gate": (C.c_int, [_P, _P, _I32, _I32, _P, _P, _P]),
     "bi_gemm_bf16": (C.c_int, [_P, _P, _P, _I32, _I32, _I32, _I64, _I64, _I64, _P]),
     "bi_route_trace_hash": (C.c_int, [_P, _I32, _I32, _P, _I32, _P, _P, _P]),
@@ -89,6 +91,17 @@ def bi_router_topk(x, w_gate, in_dtype, logit_dtype, M, H, E, k, logits_out, ids
                                _ptr(margin_ulps_out), _stream(stream))
     if check:
         _check(st, "bi_router_topk")
+    return st
+
+
+def bi_router_topk_noalloc(x, w_gate, in_dtype, logit_dtype, M, H, E, k, logits_out, ids_out,
+                           weights_out=None, margin_out=None, margin_ulps_out=None, stream=None,
+                           check=True):
+    st = load().bi_router_topk_noalloc(_ptr(x), _ptr(w_gate), in_dtype, logit_dtype, M, H, E, k,
+                                       _ptr(logits_out), _ptr(ids_out), _ptr(weights_out),
+                                       _ptr(margin_out), _ptr(margin_ulps_out), _stream(stream))
+    if check:
+        _check(st, "bi_router_topk_noalloc")
     return st
 
 

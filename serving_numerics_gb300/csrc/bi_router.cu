@@ -479,3 +479,104 @@ extern "C" bi_status bi_router_topk(const void *x, const void *w_gate, bi_dtype 
                         ids_out, weights_out, margin_out, margin_ulps_out);
     return st;
 }
+
+// ---------------------------------------------------------------------------
+// bi_router_topk_noalloc: the same router for callers that cannot allocate
+// device memory (an engine whose memory all comes from its own pool, or code
+// recording the router into a CUDA graph).  The partial sums of the 16
+// partition groups live in a fixed array compiled into the library instead
+// of the lazily allocated scratch of bi_router_topk.  Host code must not pass
+// the array's name to a kernel (that is a host-side stand-in); its device
+// address is looked up once per device with cudaGetSymbolAddress.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+static __device__ __align__(256) float g_noalloc_partials[BI_NOALLOC_SCRATCH_BYTES / sizeof(float)];
+
+namespace bi {
+namespace {
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[64];
+
+// Device address of g_noalloc_partials on the current device (looked up on
+// the first call per device).
+bi_status noalloc_scratch(const Device *d, void **out)
+{
+    if (d->ordinal < 0 || d->ordinal >= 64) return BI_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[d->ordinal]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_partials) != cudaSuccess || !p) return BI_ERR_CUDA;
+        g_noalloc_ptr[d->ordinal] = p;
+    }
+    *out = g_noalloc_ptr[d->ordinal];
+    return BI_OK;
+}
+}  // namespace
+}  // namespace bi
+
+extern "C" bi_status bi_router_topk_noalloc(const void *x, const void *w_gate, bi_dtype in_dtype,
+                                            bi_dtype logit_dtype, int32_t M, int32_t H, int32_t E,
+                                            int32_t k, void *logits_out, int32_t *ids_out,
+                                            float *weights_out, float *margin_out,
+                                            int32_t *margin_ulps_out, bi_stream s)
+{
+    if ((in_dtype != BI_F32 && in_dtype != BI_BF16) || (logit_dtype != BI_F32 && logit_dtype != BI_BF16))
+        return BI_ERR_INVALID_ARG;
+    if (M < 0 || H <= 0 || E <= 0 || k <= 0 || k >= E) return BI_ERR_INVALID_ARG;
+    if (H > BI_MAX_H || (H % 8) != 0 || E < 32 || E > BI_MAX_E || (E % 32) != 0 || k > BI_MAX_K)
+        return BI_ERR_UNSUPPORTED_SHAPE;
+    constexpr int C = 16;                                   // always the 16-way split
+    if ((size_t)C * (size_t)M * (size_t)E * sizeof(float) > (size_t)BI_NOALLOC_SCRATCH_BYTES)
+        return BI_ERR_UNSUPPORTED_SHAPE;                    // beyond the fixed array
+    if (M == 0) return BI_OK;
+    if (!x || !w_gate || !logits_out || !ids_out) return BI_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w_gate)) return BI_ERR_MISALIGNED;
+    const uintptr_t lal = logit_dtype == BI_F32 ? 3u : 1u;
+    if ((reinterpret_cast<uintptr_t>(logits_out) & lal) || (reinterpret_cast<uintptr_t>(ids_out) & 3u) ||
+        (reinterpret_cast<uintptr_t>(weights_out) & 3u) || (reinterpret_cast<uintptr_t>(margin_out) & 3u) ||
+        (reinterpret_cast<uintptr_t>(margin_ulps_out) & 3u))
+        return BI_ERR_MISALIGNED;
+
+    Device *d = nullptr;
+    bi_status st = current_device(&d);
+    if (st != BI_OK) return st;
+    void *part = nullptr;
+    if ((st = noalloc_scratch(d, &part)) != BI_OK) return st;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(s);
+
+    const bool f32in = in_dtype == BI_F32;
+    const uint64_t es = f32in ? 4 : 2;
+    const CUtensorMapDataType dt = f32in ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const CUtensorMapSwizzle sw = f32in ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_NONE;
+    const uint32_t box[2] = {(uint32_t)kBlk, (uint32_t)kTileM};
+    alignas(64) CUtensorMap tmx, tmw;
+    {
+        const uint64_t dims[2] = {(uint64_t)H, (uint64_t)M};
+        const uint64_t strides[1] = {(uint64_t)H * es};
+        if ((st = encode_tiled(&tmx, dt, 2, x, dims, strides, box, sw)) != BI_OK) return st;
+    }
+    {
+        const uint64_t dims[2] = {(uint64_t)H, (uint64_t)E};
+        const uint64_t strides[1] = {(uint64_t)H * es};
+        if ((st = encode_tiled(&tmw, dt, 2, w_gate, dims, strides, box, sw)) != BI_OK) return st;
+    }
+    const int lbf = logit_dtype == BI_BF16 ? 1 : 0;
+    st = f32in ? launch_proj_c<float>(d, C, tmx, tmw, M, E, H, OUT_PARTIAL, part, cs)
+               : launch_proj_c<__nv_bfloat16>(d, C, tmx, tmw, M, E, H, OUT_PARTIAL, part, cs);
+    if (st != BI_OK) return st;
+    const int epl = E / 32;
+    dim3 grid((M + kSelWarps - 1) / kSelWarps), block(32 * kSelWarps);
+    const float *pp = static_cast<const float *>(part);
+    if (epl <= 4)
+        return launch_pdl(router_select_kernel<4>, grid, block, 0, cs, pp, C, logits_out, lbf, M, E, k,
+                          ids_out, weights_out, margin_out, margin_ulps_out);
+    if (epl <= 8)
+        return launch_pdl(router_select_kernel<8>, grid, block, 0, cs, pp, C, logits_out, lbf, M, E, k,
+                          ids_out, weights_out, margin_out, margin_ulps_out);
+    if (epl <= 16)
+        return launch_pdl(router_select_kernel<16>, grid, block, 0, cs, pp, C, logits_out, lbf, M, E, k,
+                          ids_out, weights_out, margin_out, margin_ulps_out);
+    return launch_pdl(router_select_kernel<32>, grid, block, 0, cs, pp, C, logits_out, lbf, M, E, k,
+                      ids_out, weights_out, margin_out, margin_ulps_out);
+}
