@@ -1,12 +1,12 @@
 """Benchmark of the batch-invariant MoE prefill path on GB300.
 
 One step = one pass of the whole path over one prefill batch of M = 4096
-tokens (16 requests of 256) through 40 layers; each layer runs, in stream
-order:
+tokens (16 requests of 256) through 40 layers; each layer runs:
   bi_router_topk      F32 router, H=2048, E=256, top-8 (logits, ids,
                       weights, margins)
   bi_shared_gate      the shared-expert gate dot and sigmoid
-  bi_route_trace_hash per-request FNV-1a hashes, chained over the layers
+  bi_route_trace_hash per-request FNV-1a hashes, chained over the layers (on
+                      a side stream: it only reads that layer's ids)
   bi_gemm_bf16        the M-invariant bf16 projection, K = N = 4096
 Every layer has its own weights and its own hidden states, so a step
 streams about 4 GB (inputs larger than the 129 MB L2; no flush needed).
@@ -130,6 +130,10 @@ def run_ours(args):
     offs = [i * (M // N_REQ) for i in range(N_REQ + 1)]
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
+    # the route hash only reads each layer's ids: it runs on a side stream,
+    # ordered after that layer's router by an event, chained layer to layer
+    side = torch.cuda.Stream(dev)
+    ids_ready = [torch.cuda.Event() for _ in range(LAYERS)]
     launches_per_layer = 5   # router projection + selection, gate, hash, GEMM
 
     def layer(l, ev=None):
@@ -137,10 +141,13 @@ def run_ours(args):
             ev[0].record(stream)
         bi.bi_router_topk(X[l], Wg[l], bi.BI_F32, bi.BI_F32, M, H, E, K_TOP, logits[l], ids[l], wts[l],
                           mg[l], mu[l], stream=sh)
+        ids_ready[l].record(stream)
         if ev is not None:
             ev[1].record(stream)
+        side.wait_event(ids_ready[l])
+        bi.bi_route_trace_hash(ids[l], M, K_TOP, offs, None if l == 0 else hashes, hashes,
+                               stream=side.cuda_stream)
         bi.bi_shared_gate(X[l], Wsg[l], M, H, gdot[l], gsig[l], stream=sh)
-        bi.bi_route_trace_hash(ids[l], M, K_TOP, offs, None if l == 0 else hashes, hashes, stream=sh)
         if ev is not None:
             ev[2].record(stream)
         bi.bi_gemm_bf16(A[l], Bw[l], Cout, M, G_N, G_K, G_K, G_K, G_N, stream=sh)
@@ -150,6 +157,7 @@ def run_ours(args):
     def step(evs=None):
         for l in range(LAYERS):
             layer(l, None if evs is None else evs[l])
+        stream.wait_stream(side)      # the step ends when every hash is done
 
     for _ in range(args.warmup):
         step()
@@ -202,6 +210,7 @@ def run_ours(args):
             layer(l)
         res_ids.copy_(ids[LAYERS - 1], non_blocking=True)
         res_w.copy_(wts[LAYERS - 1], non_blocking=True)
+        stream.wait_stream(side)
         res_h.copy_(hashes, non_blocking=True)
         torch.cuda.synchronize()
     e2e_s = time.perf_counter() - w0
@@ -250,12 +259,64 @@ def run_ours(args):
         "gpu_launches": launches_per_layer * LAYERS * args.steps,
         "clocks": ck,
     }
+    if not args.no_sweep:
+        out["router_sweep"] = router_sweep(bi, synth, torch, dev, hbm)
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_seconds)
     if rank == 0:
         print(json.dumps(out), flush=True)
     if ws > 1:
         dist.destroy_process_group()
+
+
+def router_sweep(bi, synth, torch, dev, hbm_gbs):
+    """bi_router_topk alone (F32, H=2048, E=256, top-8, all outputs) at
+    several M: back-to-back calls cycling through 96 gate matrices (192 MiB,
+    more than L2) so every call reads its weights from HBM, captured in a
+    CUDA graph and replayed (the calls keep their programmatic-dependent
+    launch edges); the per-call time is against the binding roofline
+    max(bytes / HBM, flops / FP32)."""
+    pool = 96
+    Ws = [synth.device_normal((E, H), 77000 + i, 0.02, torch.float32, dev) for i in range(pool)]
+    res = []
+    stream = torch.cuda.current_stream(dev)
+    for Mi in (1, 4, 16, 64, 256, 1024, 4096):
+        xs = [synth.device_normal((Mi, H), 78000 + i, 1.0, torch.float32, dev) for i in range(8)]
+        lg = torch.empty((Mi, E), dtype=torch.float32, device=dev)
+        ids = torch.empty((Mi, K_TOP), dtype=torch.int32, device=dev)
+        w = torch.empty((Mi, K_TOP), dtype=torch.float32, device=dev)
+        mg = torch.empty((Mi,), dtype=torch.float32, device=dev)
+        mu = torch.empty((Mi,), dtype=torch.int32, device=dev)
+
+        def calls(n):
+            for i in range(n):
+                bi.bi_router_topk(xs[i % 8], Ws[i % pool], bi.BI_F32, bi.BI_F32, Mi, H, E, K_TOP, lg, ids, w,
+                                  mg, mu, stream=None)
+        calls(pool)                       # warm-up (also sizes the library's scratch)
+        n = pool if Mi <= 1024 else pool // 2
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()        # replayed, so host launch cost is not timed
+        with torch.cuda.graph(g):
+            calls(n)
+        g.replay()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(3):
+            g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        t = a.elapsed_time(b) / 1e3 / (3 * n)
+        del g
+        byt = 4 * E * H + 4 * Mi * H + 4 * Mi * E + 8 * Mi * K_TOP + 8 * Mi
+        flop = 2.0 * Mi * E * H
+        t_hbm, t_alu = byt / (hbm_gbs * 1e9), flop / (FP32_PEAK_TFLOPS * 1e12)
+        res.append({"M": Mi, "us_per_call": t * 1e6, "GBps": byt / t / 1e9, "TFLOPs": flop / t / 1e12,
+                    "bound": "hbm" if t_hbm >= t_alu else "alu",
+                    "frac_of_binding_roofline": max(t_hbm, t_alu) / t,
+                    "frac_of_hbm": (byt / t / 1e9) / hbm_gbs})
+    del Ws
+    return res
 
 
 def cpu_baseline(budget_s: float = 15.0):
@@ -319,6 +380,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the router-only M sweep")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--layers", type=int, default=LAYERS,
                     help="fewer layers for a small profiling case (the benchmark uses 40)")

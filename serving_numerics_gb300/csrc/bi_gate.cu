@@ -97,6 +97,7 @@ extern "C" bi_status bi_shared_gate(const float *x, const float *w_sg, int32_t M
     Device *d = nullptr;
     bi_status st = current_device(&d);
     if (st != BI_OK) return st;
+    if ((st = set_smem_once(d, KID_GATE, shared_gate_kernel, 0)) != BI_OK) return st;
     const int tokens_per_block = 2 * kGateWarps;
     dim3 grid((M + tokens_per_block - 1) / tokens_per_block);
     return launch_pdl(shared_gate_kernel, grid, dim3(32 * kGateWarps), 0,

@@ -57,15 +57,23 @@ bi_status launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
     return from_cuda(e);
 }
 
-// Set the dynamic shared memory limit of `kernel` once per device.
+// Once per device and kernel: the dynamic shared memory limit, and the
+// largest shared-memory carveout.  Every kernel of the library asks for the
+// same carveout, so a small kernel resident on an SM never leaves it
+// configured for less shared memory than the next large-tile block needs
+// (an SM changes its carveout only when it is empty, so a mismatch would
+// make the large block wait for the small one to finish).
 template <typename K>
 bi_status set_smem_once(Device *d, int kernel_id, K kernel, size_t bytes)
 {
     uint64_t bit = 1ull << kernel_id;
     if (d->attr_done & bit) return BI_OK;
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)bytes);
-    if (e != cudaSuccess) return BI_ERR_CUDA;
+    if (bytes > 0 &&
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess)
+        return BI_ERR_CUDA;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+        return BI_ERR_CUDA;
     d->attr_done |= bit;
     return BI_OK;
 }
@@ -74,6 +82,9 @@ bi_status set_smem_once(Device *d, int kernel_id, K kernel, size_t bytes)
 enum : int {
     KID_ROUTER_PROJ = 0,   // 10 instantiations: 0..9
     KID_GEMM = 16,
+    KID_SELECT = 20,       // 4 instantiations: 20..23
+    KID_GATE = 24,
+    KID_HASH = 25,         // 4 instantiations: 25..28
 };
 
 }  // namespace bi

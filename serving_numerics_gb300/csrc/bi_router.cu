@@ -14,18 +14,21 @@
 // tree (0+1),(2+3),...,(14+15), then (01+23),..., four levels.
 //
 // Work decomposition (free to depend on M, since it never changes the
-// order): a work tile is 32 tokens x 32 experts.  Its 16 partitions are
-// split over C thread blocks (C = 1, 2, 4, 8 or 16; 16/C warps each, one
-// warp per partition).  A block adds its partitions with the lower levels of
-// the tree; with C > 1 the C group sums meet in library scratch and the
-// selection kernel adds them with the remaining upper levels.  C grows only
-// when there are too few tiles to fill the GPU (small M).
+// order): one tile shape for every M, 32 tokens x 64 experts.  A tile's 16
+// partitions are split over C thread blocks (C = 1, 2, 4, 8 or 16; 16/C
+// warps each, one warp per partition).  A block adds its partitions with the
+// lower levels of the tree; with C > 1 the C group sums meet in library
+// scratch and the selection kernel adds them with the remaining upper
+// levels.  C grows only when there are too few tiles to fill the GPU.
 //
-// Data path: each partition's [32 rows x 8] block of X and of W_gate is
-// staged by its own TMA box into shared memory (f32: 32-byte swizzle, which
-// makes the lane access pattern below bank-conflict free), a ring of stages
-// deep.  Lane (tg, eg) of a warp owns tokens tg+8j (j<4) and experts eg+4i
-// (i<8): 32 accumulators.
+// Data path: each partition's [32 rows x 8] block of X and [64 rows x 8]
+// block of W_gate are staged by TMA into shared memory (f32: 32-byte
+// swizzle), a ring of stages deep.  Lane (tg, eg) of a warp owns tokens
+// tg + 4j and experts eg + 8i (j, i < 8): 64 accumulators.  A 128-bit
+// shared load moves 512 bytes whatever the lanes share, so the shared-memory
+// path delivers 32 lane-floats per clock against 128 FMAs per clock; an
+// 8 x 8 thread tile (64 FMAs per 16 floats loaded) is the smallest that
+// keeps the FMA pipe, not the shared-memory pipe, the limit.
 #include <cuda_bf16.h>
 #include <limits.h>
 
@@ -35,46 +38,60 @@
 namespace bi {
 namespace {
 
-constexpr int kTileM = 32, kTileE = 32, kSlab = 128, kBlk = 8, kParts = 16;
+constexpr int kTileM = 32, kTileE = 64, kSlab = 128, kBlk = 8, kParts = 16;
 
 template <typename InT, int C>
 struct ProjCfg {
-    static constexpr int NPL = kParts / C;                      // partitions (= warps) per block
+    static constexpr int ES = (int)sizeof(InT);
+    static constexpr int NPL = kParts / C;                       // partitions (= warps) per block
     static constexpr int THREADS = 32 * NPL;
-    static constexpr int PART_BYTES = kTileM * kBlk * (int)sizeof(InT);   // one TMA box
-    static constexpr int OP_BYTES = PART_BYTES * NPL;           // X (or W) part of a stage
-    static constexpr int STAGE_BYTES = 2 * OP_BYTES;
-    static constexpr int NST_RAW = (96 * 1024) / STAGE_BYTES;
+    // one TMA box covers PB adjacent partition blocks of a slab: rows of
+    // P = PB * 8 * ES bytes (at most 128), swizzled over their whole width
+    static constexpr int PB0 = 128 / (kBlk * ES);
+    static constexpr int PB = NPL < PB0 ? NPL : PB0;
+    static constexpr int P = PB * kBlk * ES;
+    static constexpr int NB = NPL / PB;                          // boxes per operand per stage
+    static constexpr int XBOX = kTileM * P, WBOX = kTileE * P;
+    static constexpr int XOP = XBOX * NB, WOP = WBOX * NB;       // per stage
+    static constexpr int STAGE_BYTES = XOP + WOP;
+    static constexpr int NST_RAW = (192 * 1024) / STAGE_BYTES;
     static constexpr int NST = NST_RAW > 16 ? 16 : (NST_RAW < 2 ? 2 : NST_RAW);
-    static constexpr int TREE_BYTES = (NPL / 2) * 1024 * 4;
+    static constexpr int TREE_BYTES = (NPL / 2) * 64 * 32 * 4;    // 64 values x 32 lanes per slot
     static constexpr int OUT_BYTES = kTileM * (kTileE + 1) * 4;
     static constexpr int BODY0 = NST * STAGE_BYTES;
     static constexpr int BODY1 = TREE_BYTES > OUT_BYTES ? TREE_BYTES : OUT_BYTES;
     static constexpr int BODY = BODY0 > BODY1 ? BODY0 : BODY1;
-    static constexpr int SMEM = BODY + 1024;                     // + alignment slack
+    static constexpr int SMEM = BODY + 1024;                      // + alignment slack
+    static_assert(P == 16 || P == 32 || P == 64 || P == 128, "TMA swizzle span");
 };
 
-// One 8-wide block of the chain for a 4x8 register tile, f32 inputs.
-// Box layout: row r (32 bytes) at 32*r, its 16-byte half c stored at half
-// c ^ bit2(r) (TMA 32-byte swizzle: address bit 4 ^= address bit 7).
-__device__ __forceinline__ void block_f32(float (&acc)[4][8], const uint8_t *xs, const uint8_t *ws,
-                                          int tg, int eg)
+// Byte offset of 16-byte chunk `ch` of row r in a box with P-byte rows and
+// the P-byte TMA swizzle: address bits [4, 4+log2(P/16)) are xor-ed with
+// bits [7, 7+log2(P/16)) (every box starts 1024-byte aligned); P = 16 is
+// the unswizzled case.
+template <int P>
+__device__ __forceinline__ int swz(int r, int ch)
 {
-#pragma unroll
+    return r * P + 16 * (ch ^ ((r * P >> 7) & (P / 16 - 1)));
+}
+
+// One 8-wide block of the chain for the 8x8 thread tile, f32 inputs.  The
+// block is chunks 2*pc and 2*pc+1 of each row of its box.
+template <int P>
+__device__ __forceinline__ void block_f32(float (&acc)[8][8], const uint8_t *xs, const uint8_t *ws,
+                                          int pc, int tg, int eg)
+{
+#pragma unroll 1
     for (int c = 0; c < 2; ++c) {
-        float4 xv[4];
+        float4 xv[8];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int r = tg + 8 * j;
-            xv[j] = *reinterpret_cast<const float4 *>(xs + 32 * r + 16 * (c ^ ((r >> 2) & 1)));
-        }
+        for (int j = 0; j < 8; ++j)
+            xv[j] = *reinterpret_cast<const float4 *>(xs + swz<P>(tg + 4 * j, 2 * pc + c));
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const int r = eg + 4 * i;
-            const float4 wv =
-                *reinterpret_cast<const float4 *>(ws + 32 * r + 16 * (c ^ ((r >> 2) & 1)));
+            const float4 wv = *reinterpret_cast<const float4 *>(ws + swz<P>(eg + 8 * i, 2 * pc + c));
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < 8; ++j) {
                 float a = acc[j][i];
                 a = __fmaf_rn(xv[j].x, wv.x, a);
                 a = __fmaf_rn(xv[j].y, wv.y, a);
@@ -86,29 +103,31 @@ __device__ __forceinline__ void block_f32(float (&acc)[4][8], const uint8_t *xs,
     }
 }
 
-// The same for bf16 inputs (box rows of 16 bytes, no swizzle).  Products
-// of two bf16 values are exact in f32, so each step rounds once, as in f32.
-__device__ __forceinline__ void block_bf16(float (&acc)[4][8], const uint8_t *xs, const uint8_t *ws,
-                                           int tg, int eg)
+// The same for bf16 inputs: the block is chunk pc of each row; it is used
+// in two halves of four values (8-byte loads).  Products of two bf16 values
+// are exact in f32, so each step rounds once, as in f32.
+template <int P>
+__device__ __forceinline__ void block_bf16(float (&acc)[8][8], const uint8_t *xs, const uint8_t *ws,
+                                           int pc, int tg, int eg)
 {
-    uint4 xr[4];
+#pragma unroll 1
+    for (int c = 0; c < 2; ++c) {
+        uint2 xr[8];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) xr[j] = *reinterpret_cast<const uint4 *>(xs + 16 * (tg + 8 * j));
+        for (int j = 0; j < 8; ++j)
+            xr[j] = *reinterpret_cast<const uint2 *>(xs + swz<P>(tg + 4 * j, pc) + 8 * c);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const uint4 wr = *reinterpret_cast<const uint4 *>(ws + 16 * (eg + 4 * i));
+        for (int i = 0; i < 8; ++i) {
+            const uint2 wr = *reinterpret_cast<const uint2 *>(ws + swz<P>(eg + 8 * i, pc) + 8 * c);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            float a = acc[j][i];
-            a = __fmaf_rn(bf16lo(xr[j].x), bf16lo(wr.x), a);
-            a = __fmaf_rn(bf16hi(xr[j].x), bf16hi(wr.x), a);
-            a = __fmaf_rn(bf16lo(xr[j].y), bf16lo(wr.y), a);
-            a = __fmaf_rn(bf16hi(xr[j].y), bf16hi(wr.y), a);
-            a = __fmaf_rn(bf16lo(xr[j].z), bf16lo(wr.z), a);
-            a = __fmaf_rn(bf16hi(xr[j].z), bf16hi(wr.z), a);
-            a = __fmaf_rn(bf16lo(xr[j].w), bf16lo(wr.w), a);
-            a = __fmaf_rn(bf16hi(xr[j].w), bf16hi(wr.w), a);
-            acc[j][i] = a;
+            for (int j = 0; j < 8; ++j) {
+                float a = acc[j][i];
+                a = __fmaf_rn(bf16lo(xr[j].x), bf16lo(wr.x), a);
+                a = __fmaf_rn(bf16hi(xr[j].x), bf16hi(wr.x), a);
+                a = __fmaf_rn(bf16lo(xr[j].y), bf16lo(wr.y), a);
+                a = __fmaf_rn(bf16hi(xr[j].y), bf16hi(wr.y), a);
+                acc[j][i] = a;
+            }
         }
     }
 }
@@ -116,7 +135,7 @@ __device__ __forceinline__ void block_bf16(float (&acc)[4][8], const uint8_t *xs
 enum OutMode : int { OUT_F32 = 0, OUT_BF16 = 1, OUT_PARTIAL = 2 };
 
 template <typename InT, int C>
-__global__ void __launch_bounds__(ProjCfg<InT, C>::THREADS)
+__global__ void __launch_bounds__(ProjCfg<InT, C>::THREADS, 1)
 router_proj_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
                    int M, int E, int H, int out_mode, void *__restrict__ out, unsigned int *err)
 {
@@ -124,6 +143,7 @@ router_proj_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
     constexpr int NPL = Cfg::NPL, NST = Cfg::NST;
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[NST];
+    __shared__ int released[NST];          // warps done with the slot's current slab
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~uintptr_t(1023));
 
@@ -131,32 +151,37 @@ router_proj_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
     const int e_tile = blockIdx.x / C, g = blockIdx.x % C;
     const int m0 = blockIdx.y * kTileM, e0 = e_tile * kTileE, q0 = g * NPL;
     const int ns = (H + kSlab - 1) / kSlab;
-    const int tg = lane & 7, eg = lane >> 3;
+    const int tg = lane & 3, eg = lane >> 2;
 
     if (tid == 0) {
         prefetch_tmap(&tmx);
         prefetch_tmap(&tmw);
 #pragma unroll
-        for (int s = 0; s < NST; ++s) mbar_init(&full_bar[s], 1);
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(&full_bar[s], 1);
+            released[s] = 0;
+        }
         mbar_init_fence();
     }
     __syncthreads();
     pdl_wait();       // inputs may come from the previous kernel in the stream
     pdl_trigger();
 
-    // producer: thread 0 stages slab s into ring slot `slot` (valid blocks only)
+    // producer step: stage slab s into ring slot `slot` (valid blocks only);
+    // thread 0 fills the ring, then whichever warp releases a slot last
+    // refills it
     auto issue = [&](int s, int slot) {
         uint8_t *st = smem + slot * Cfg::STAGE_BYTES;
-        int nvalid = 0;
+        int nvalid = 0;        // boxes starting before H (a box may run past H: TMA fills zeros)
 #pragma unroll
-        for (int w = 0; w < NPL; ++w) nvalid += (kSlab * s + kBlk * (q0 + w) < H) ? 1 : 0;
-        mbar_arrive_expect_tx(&full_bar[slot], (uint32_t)(nvalid * 2 * Cfg::PART_BYTES));
+        for (int bx = 0; bx < Cfg::NB; ++bx) nvalid += (kSlab * s + kBlk * (q0 + bx * Cfg::PB) < H) ? 1 : 0;
+        mbar_arrive_expect_tx(&full_bar[slot], (uint32_t)(nvalid * (Cfg::XBOX + Cfg::WBOX)));
 #pragma unroll
-        for (int w = 0; w < NPL; ++w) {
-            const int h0 = kSlab * s + kBlk * (q0 + w);
+        for (int bx = 0; bx < Cfg::NB; ++bx) {
+            const int h0 = kSlab * s + kBlk * (q0 + bx * Cfg::PB);
             if (h0 < H) {
-                tma_load_2d(st + w * Cfg::PART_BYTES, &tmx, &full_bar[slot], h0, m0);
-                tma_load_2d(st + Cfg::OP_BYTES + w * Cfg::PART_BYTES, &tmw, &full_bar[slot], h0, e0);
+                tma_load_2d(st + bx * Cfg::XBOX, &tmx, &full_bar[slot], h0, m0);
+                tma_load_2d(st + Cfg::XOP + bx * Cfg::WBOX, &tmw, &full_bar[slot], h0, e0);
             }
         }
     };
@@ -164,26 +189,48 @@ router_proj_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
     const int nst = ns < NST ? ns : NST;
     if (tid == 0)
         for (int s = 0; s < nst; ++s) issue(s, s);
+    __syncthreads();
 
-    float acc[4][8];
+    float acc[8][8];
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
+    for (int j = 0; j < 8; ++j)
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[j][i] = 0.0f;
 
+    // a warp whose four token rows are all past M has nothing to compute
+    const bool live = tg < M - m0;
+    int slot = 0;
+    uint32_t phase = 0;
     for (int s = 0; s < ns; ++s) {
-        const int slot = s % NST;
-        mbar_wait(&full_bar[slot], (uint32_t)((s / NST) & 1), err, 0x11);
-        if (kSlab * s + kBlk * (q0 + warp) < H) {      // warp-uniform
+        mbar_wait(&full_bar[slot], phase, err, 0x11);
+        if (live && kSlab * s + kBlk * (q0 + warp) < H) {
             const uint8_t *st = smem + slot * Cfg::STAGE_BYTES;
+            const int bx = warp / Cfg::PB, pc = warp % Cfg::PB;
+            const uint8_t *xs = st + bx * Cfg::XBOX, *ws = st + Cfg::XOP + bx * Cfg::WBOX;
             if constexpr (sizeof(InT) == 4)
-                block_f32(acc, st + warp * Cfg::PART_BYTES, st + Cfg::OP_BYTES + warp * Cfg::PART_BYTES, tg, eg);
+                block_f32<Cfg::P>(acc, xs, ws, pc, tg, eg);
             else
-                block_bf16(acc, st + warp * Cfg::PART_BYTES, st + Cfg::OP_BYTES + warp * Cfg::PART_BYTES, tg, eg);
+                block_bf16<Cfg::P>(acc, xs, ws, pc, tg, eg);
         }
-        __syncthreads();                                   // slot free again
-        if (tid == 0 && s + NST < ns) issue(s + NST, slot);
+        // release the slot without a block-wide barrier: the last warp to
+        // finish with it stages slab s + NST into it
+        __syncwarp();
+        if (lane == 0) {
+            __threadfence_block();
+            if (atomicAdd(&released[slot], 1) == NPL - 1) {
+                released[slot] = 0;
+                if (s + NST < ns) {
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    issue(s + NST, slot);
+                }
+            }
+        }
+        if (++slot == NST) {
+            slot = 0;
+            phase ^= 1u;
+        }
     }
+    __syncthreads();                                       // every warp is done with the ring
 
     // lower levels of the pairwise tree, over this block's NPL partitions
     float *tree = reinterpret_cast<float *>(smem);
@@ -191,31 +238,31 @@ router_proj_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
     for (int d = 1; d < NPL; d *= 2) {
         const int p = warp / (2 * d);
         if ((warp % (2 * d)) == d) {
-            float *dst = tree + p * 1024;
+            float *dst = tree + p * 2048;
 #pragma unroll
-            for (int v = 0; v < 32; ++v) dst[v * 32 + lane] = acc[v >> 3][v & 7];
+            for (int v = 0; v < 64; ++v) dst[v * 32 + lane] = acc[v >> 3][v & 7];
         }
         __syncthreads();
         if ((warp % (2 * d)) == 0) {
-            const float *src = tree + p * 1024;
+            const float *src = tree + p * 2048;
 #pragma unroll
-            for (int v = 0; v < 32; ++v) acc[v >> 3][v & 7] = acc[v >> 3][v & 7] + src[v * 32 + lane];
+            for (int v = 0; v < 64; ++v) acc[v >> 3][v & 7] = acc[v >> 3][v & 7] + src[v * 32 + lane];
         }
         __syncthreads();
     }
 
-    // stage the 32x32 result and write it row-coalesced
+    // stage the 32x64 result and write it row-coalesced
     float *tile = reinterpret_cast<float *>(smem);
     if (warp == 0) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
+        for (int j = 0; j < 8; ++j)
 #pragma unroll
-            for (int i = 0; i < 8; ++i) tile[(tg + 8 * j) * (kTileE + 1) + eg + 4 * i] = acc[j][i];
+            for (int i = 0; i < 8; ++i) tile[(tg + 4 * j) * (kTileE + 1) + eg + 8 * i] = acc[j][i];
     }
     __syncthreads();
     for (int idx = tid; idx < kTileM * kTileE; idx += Cfg::THREADS) {
-        const int t = idx >> 5, e = idx & 31, m = m0 + t;
-        if (m < M) {
+        const int t = idx >> 6, e = idx & 63, m = m0 + t;
+        if (m < M && e0 + e < E) {
             const float v = tile[t * (kTileE + 1) + e];
             const size_t o = (size_t)m * E + e0 + e;
             if (out_mode == OUT_F32)
@@ -362,30 +409,67 @@ router_select_kernel(const float *__restrict__ part, int C, void *logits, int lo
 }
 
 template <typename InT, int C>
-bi_status launch_proj(Device *d, const CUtensorMap &tmx, const CUtensorMap &tmw, int M, int E,
-                      int H, int out_mode, void *out, cudaStream_t s, int kid)
+bi_status launch_proj(Device *d, const void *x, const void *w, int M, int E, int H, int out_mode, void *out,
+                      cudaStream_t s, int kid)
 {
     using Cfg = ProjCfg<InT, C>;
     auto kern = router_proj_kernel<InT, C>;
     bi_status st = set_smem_once(d, kid, kern, Cfg::SMEM);
     if (st != BI_OK) return st;
-    dim3 grid((E / kTileE) * C, (M + kTileM - 1) / kTileM);
+    const CUtensorMapDataType dt = sizeof(InT) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const CUtensorMapSwizzle sw = Cfg::P == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : Cfg::P == 64  ? CU_TENSOR_MAP_SWIZZLE_64B
+                                : Cfg::P == 32  ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_NONE;
+    const uint64_t strides[1] = {(uint64_t)H * sizeof(InT)};
+    alignas(64) CUtensorMap tmx, tmw;
+    {
+        const uint64_t dims[2] = {(uint64_t)H, (uint64_t)M};
+        const uint32_t box[2] = {(uint32_t)(Cfg::PB * kBlk), (uint32_t)kTileM};
+        if ((st = encode_tiled(&tmx, dt, 2, x, dims, strides, box, sw)) != BI_OK) return st;
+    }
+    {
+        const uint64_t dims[2] = {(uint64_t)H, (uint64_t)E};
+        const uint32_t box[2] = {(uint32_t)(Cfg::PB * kBlk), (uint32_t)kTileE};
+        if ((st = encode_tiled(&tmw, dt, 2, w, dims, strides, box, sw)) != BI_OK) return st;
+    }
+    dim3 grid(((E + kTileE - 1) / kTileE) * C, (M + kTileM - 1) / kTileM);
     return launch_pdl(kern, grid, dim3(Cfg::THREADS), (size_t)Cfg::SMEM, s, tmx, tmw, M, E, H,
                       out_mode, out, d->err);
 }
 
 template <typename InT>
-bi_status launch_proj_c(Device *d, int C, const CUtensorMap &tmx, const CUtensorMap &tmw, int M,
-                        int E, int H, int out_mode, void *out, cudaStream_t s)
+bi_status launch_proj_c(Device *d, int C, const void *x, const void *w, int M, int E, int H, int out_mode,
+                        void *out, cudaStream_t s)
 {
     const int base = KID_ROUTER_PROJ + (sizeof(InT) == 4 ? 0 : 5);
     switch (C) {
-    case 1: return launch_proj<InT, 1>(d, tmx, tmw, M, E, H, out_mode, out, s, base + 0);
-    case 2: return launch_proj<InT, 2>(d, tmx, tmw, M, E, H, out_mode, out, s, base + 1);
-    case 4: return launch_proj<InT, 4>(d, tmx, tmw, M, E, H, out_mode, out, s, base + 2);
-    case 8: return launch_proj<InT, 8>(d, tmx, tmw, M, E, H, out_mode, out, s, base + 3);
-    default: return launch_proj<InT, 16>(d, tmx, tmw, M, E, H, out_mode, out, s, base + 4);
+    case 1: return launch_proj<InT, 1>(d, x, w, M, E, H, out_mode, out, s, base + 0);
+    case 2: return launch_proj<InT, 2>(d, x, w, M, E, H, out_mode, out, s, base + 1);
+    case 4: return launch_proj<InT, 4>(d, x, w, M, E, H, out_mode, out, s, base + 2);
+    case 8: return launch_proj<InT, 8>(d, x, w, M, E, H, out_mode, out, s, base + 3);
+    default: return launch_proj<InT, 16>(d, x, w, M, E, H, out_mode, out, s, base + 4);
     }
+}
+
+template <int EPLM>
+bi_status launch_select1(Device *d, dim3 grid, dim3 block, cudaStream_t cs, const float *pp, int C,
+                         void *logits, int lbf, int M, int E, int k, int32_t *ids, float *w, float *mg,
+                         int32_t *mu)
+{
+    const int kid = KID_SELECT + (EPLM == 4 ? 0 : EPLM == 8 ? 1 : EPLM == 16 ? 2 : 3);
+    bi_status st = set_smem_once(d, kid, router_select_kernel<EPLM>, 0);
+    if (st != BI_OK) return st;
+    return launch_pdl(router_select_kernel<EPLM>, grid, block, 0, cs, pp, C, logits, lbf, M, E, k, ids, w, mg, mu);
+}
+
+bi_status launch_select(Device *d, int epl, dim3 grid, dim3 block, cudaStream_t cs, const float *pp, int C,
+                        void *logits, int lbf, int M, int E, int k, int32_t *ids, float *w, float *mg,
+                        int32_t *mu)
+{
+    if (epl <= 4) return launch_select1<4>(d, grid, block, cs, pp, C, logits, lbf, M, E, k, ids, w, mg, mu);
+    if (epl <= 8) return launch_select1<8>(d, grid, block, cs, pp, C, logits, lbf, M, E, k, ids, w, mg, mu);
+    if (epl <= 16) return launch_select1<16>(d, grid, block, cs, pp, C, logits, lbf, M, E, k, ids, w, mg, mu);
+    return launch_select1<32>(d, grid, block, cs, pp, C, logits, lbf, M, E, k, ids, w, mg, mu);
 }
 
 // How many blocks share one tile's 16 partitions: the smallest power of two
@@ -394,7 +478,7 @@ bi_status launch_proj_c(Device *d, int C, const CUtensorMap &tmx, const CUtensor
 // scratch traffic.
 int choose_split(int M, int E, int sms)
 {
-    const long long tiles = (long long)((M + kTileM - 1) / kTileM) * (E / kTileE);
+    const long long tiles = (long long)((M + kTileM - 1) / kTileM) * ((E + kTileE - 1) / kTileE);
     int C = 1;
     while (C < 16 && tiles * C < sms) C *= 2;
     while (C > 1 && (long long)C * M * E * 4 > (16ll << 20)) C /= 2;
@@ -439,45 +523,19 @@ extern "C" bi_status bi_router_topk(const void *x, const void *w_gate, bi_dtype 
     }
 
     const bool f32in = in_dtype == BI_F32;
-    const uint64_t es = f32in ? 4 : 2;
-    const CUtensorMapDataType dt = f32in ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    const CUtensorMapSwizzle sw = f32in ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_NONE;
-    const uint32_t box[2] = {(uint32_t)kBlk, (uint32_t)kTileM};
-    alignas(64) CUtensorMap tmx, tmw;
-    {
-        const uint64_t dims[2] = {(uint64_t)H, (uint64_t)M};
-        const uint64_t strides[1] = {(uint64_t)H * es};
-        if ((st = encode_tiled(&tmx, dt, 2, x, dims, strides, box, sw)) != BI_OK) return st;
-    }
-    {
-        const uint64_t dims[2] = {(uint64_t)H, (uint64_t)E};
-        const uint64_t strides[1] = {(uint64_t)H * es};
-        if ((st = encode_tiled(&tmw, dt, 2, w_gate, dims, strides, box, sw)) != BI_OK) return st;
-    }
 
     const int lbf = logit_dtype == BI_BF16 ? 1 : 0;
     const int out_mode = C > 1 ? OUT_PARTIAL : (lbf ? OUT_BF16 : OUT_F32);
     void *out = C > 1 ? part : logits_out;
-    st = f32in ? launch_proj_c<float>(d, C, tmx, tmw, M, E, H, out_mode, out, cs)
-               : launch_proj_c<__nv_bfloat16>(d, C, tmx, tmw, M, E, H, out_mode, out, cs);
+    st = f32in ? launch_proj_c<float>(d, C, x, w_gate, M, E, H, out_mode, out, cs)
+               : launch_proj_c<__nv_bfloat16>(d, C, x, w_gate, M, E, H, out_mode, out, cs);
     if (st != BI_OK) return st;
 
     const int epl = E / 32;
     dim3 grid((M + kSelWarps - 1) / kSelWarps), block(32 * kSelWarps);
     const float *pp = static_cast<const float *>(part);
-    if (epl <= 4)
-        st = launch_pdl(router_select_kernel<4>, grid, block, 0, cs, pp, C, logits_out, lbf, M, E, k,
-                        ids_out, weights_out, margin_out, margin_ulps_out);
-    else if (epl <= 8)
-        st = launch_pdl(router_select_kernel<8>, grid, block, 0, cs, pp, C, logits_out, lbf, M, E, k,
-                        ids_out, weights_out, margin_out, margin_ulps_out);
-    else if (epl <= 16)
-        st = launch_pdl(router_select_kernel<16>, grid, block, 0, cs, pp, C, logits_out, lbf, M, E, k,
-                        ids_out, weights_out, margin_out, margin_ulps_out);
-    else
-        st = launch_pdl(router_select_kernel<32>, grid, block, 0, cs, pp, C, logits_out, lbf, M, E, k,
-                        ids_out, weights_out, margin_out, margin_ulps_out);
-    return st;
+    return launch_select(d, epl, grid, block, cs, pp, C, logits_out, lbf, M, E, k, ids_out, weights_out,
+                         margin_out, margin_ulps_out);
 }
 
 // ---------------------------------------------------------------------------
@@ -546,37 +604,13 @@ extern "C" bi_status bi_router_topk_noalloc(const void *x, const void *w_gate, b
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(s);
 
     const bool f32in = in_dtype == BI_F32;
-    const uint64_t es = f32in ? 4 : 2;
-    const CUtensorMapDataType dt = f32in ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    const CUtensorMapSwizzle sw = f32in ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_NONE;
-    const uint32_t box[2] = {(uint32_t)kBlk, (uint32_t)kTileM};
-    alignas(64) CUtensorMap tmx, tmw;
-    {
-        const uint64_t dims[2] = {(uint64_t)H, (uint64_t)M};
-        const uint64_t strides[1] = {(uint64_t)H * es};
-        if ((st = encode_tiled(&tmx, dt, 2, x, dims, strides, box, sw)) != BI_OK) return st;
-    }
-    {
-        const uint64_t dims[2] = {(uint64_t)H, (uint64_t)E};
-        const uint64_t strides[1] = {(uint64_t)H * es};
-        if ((st = encode_tiled(&tmw, dt, 2, w_gate, dims, strides, box, sw)) != BI_OK) return st;
-    }
     const int lbf = logit_dtype == BI_BF16 ? 1 : 0;
-    st = f32in ? launch_proj_c<float>(d, C, tmx, tmw, M, E, H, OUT_PARTIAL, part, cs)
-               : launch_proj_c<__nv_bfloat16>(d, C, tmx, tmw, M, E, H, OUT_PARTIAL, part, cs);
+    st = f32in ? launch_proj_c<float>(d, C, x, w_gate, M, E, H, OUT_PARTIAL, part, cs)
+               : launch_proj_c<__nv_bfloat16>(d, C, x, w_gate, M, E, H, OUT_PARTIAL, part, cs);
     if (st != BI_OK) return st;
     const int epl = E / 32;
     dim3 grid((M + kSelWarps - 1) / kSelWarps), block(32 * kSelWarps);
     const float *pp = static_cast<const float *>(part);
-    if (epl <= 4)
-        return launch_pdl(router_select_kernel<4>, grid, block, 0, cs, pp, C, logits_out, lbf, M, E, k,
-                          ids_out, weights_out, margin_out, margin_ulps_out);
-    if (epl <= 8)
-        return launch_pdl(router_select_kernel<8>, grid, block, 0, cs, pp, C, logits_out, lbf, M, E, k,
-                          ids_out, weights_out, margin_out, margin_ulps_out);
-    if (epl <= 16)
-        return launch_pdl(router_select_kernel<16>, grid, block, 0, cs, pp, C, logits_out, lbf, M, E, k,
-                          ids_out, weights_out, margin_out, margin_ulps_out);
-    return launch_pdl(router_select_kernel<32>, grid, block, 0, cs, pp, C, logits_out, lbf, M, E, k,
-                      ids_out, weights_out, margin_out, margin_ulps_out);
+    return launch_select(d, epl, grid, block, cs, pp, C, logits_out, lbf, M, E, k, ids_out, weights_out,
+                         margin_out, margin_ulps_out);
 }

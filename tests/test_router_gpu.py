@@ -1,5 +1,10 @@
 """Router parity: bi_router_topk on the GPU against the CPU oracle.
 
+The library splits each 32x64 tile's 16 partitions over 1, 2, 4, 8 or 16
+thread blocks depending on M; the cases below cover every split in every
+input/logit dtype, including E that is not a multiple of the 64-expert
+tile.
+
 Logits within the stated tolerance of the exact dot; ids bit-exact wherever
 the oracle's margin exceeds twice that tolerance; the oracle's top-k applied
 to the GPU's OWN logits bit-exact against the GPU ids for every token;
@@ -48,8 +53,8 @@ CASES_F32 = [
     # (M, H, E, k)
     (1, 256, 64, 4), (19, 256, 64, 4), (37, 256, 64, 4), (96, 256, 64, 4),
     (1, 2048, 256, 8), (7, 2048, 256, 8), (75, 2048, 256, 8), (300, 2048, 256, 8),
-    (1100, 2048, 256, 8),
-    (33, 264, 96, 5), (5, 8, 32, 1), (70, 136, 1024, 32),
+    (1100, 2048, 256, 8), (520, 200, 128, 6), (3000, 136, 1024, 32),
+    (33, 264, 96, 5), (5, 8, 32, 1), (70, 136, 1024, 32), (600, 264, 96, 5),
 ]
 
 
@@ -69,7 +74,7 @@ def test_router_f32_parity(bi, orc, M, H, E, k):
     assert safe.mean() > 0.5
 
 
-@pytest.mark.parametrize("M", [1, 5, 64, 200])
+@pytest.mark.parametrize("M", [1, 5, 64, 200, 700])
 def test_router_bf16_logits_tie_grid(bi, orc, M):
     """Tie-heavy grid inputs: f32 sums are exact in any order, so the bf16
     logits, ids, ties and margins must equal the oracle bit for bit."""
@@ -105,8 +110,9 @@ def test_tie_heavy_workload_counts(bi, orc):
     assert gpu_ties == orc_ties == 78
 
 
-def test_router_bf16_in_f32_logits(bi, orc):
-    X = synth.to_bf16_bits(synth.tokens(2, 0, 0, 40, 512))
+@pytest.mark.parametrize("M", [40, 900])
+def test_router_bf16_in_f32_logits(bi, orc, M):
+    X = synth.to_bf16_bits(synth.tokens(2, 0, 0, M, 512))
     W = synth.to_bf16_bits(synth.router_weights(2, 0, 128, 512))
     g = run_router(bi, X, W, 6, "f32")
     exact = orc.router_logits(X, W)
@@ -115,13 +121,14 @@ def test_router_bf16_in_f32_logits(bi, orc):
     check_selection_on_own_logits(orc, g, 6)
 
 
-def test_router_f32_in_bf16_logits(bi, orc):
+@pytest.mark.parametrize("M", [50, 1000])
+def test_router_f32_in_bf16_logits(bi, orc, M):
     """General f32 inputs, bf16 logits.  The GPU rounds its f32 sum (itself
     within the f32 tolerance of the exact dot) to bf16, so it lies within
     one bf16 ULP plus the f32 tolerance of the exact logit; one ULP alone
     cannot hold for logits near zero, where the f32 error exceeds a bf16
     ULP.  Away from zero the ordinal distance is at most one."""
-    X = synth.tokens(3, 0, 0, 50, 2048)
+    X = synth.tokens(3, 0, 0, M, 2048)
     W = synth.router_weights(3, 0, 512, 2048)
     g = run_router(bi, X, W, 10, "bf16")
     ref = orc.router_full(X, W, 10, "bf16")
@@ -161,3 +168,19 @@ def test_router_nan_and_zero_rules(bi, orc):
     assert np.all(g["ids"][:, 0] == 40)
     sel = orc.selection_from_logits(g["logits"], k)
     assert np.array_equal(g["ids"], sel["ids"])
+
+
+@pytest.mark.parametrize("E", [64, 256, 1024])
+def test_router_splits_bit_identical(bi, E):
+    """The same tokens under different partition splits: rows 0..299
+    computed in a 300-token batch and inside a 2000-token batch (fewer
+    blocks per tile) give identical bytes in every output."""
+    import torch
+    H, k = 2048, 8
+    X = synth.tokens(6, 0, 0, 2000, H)
+    w = gu.dev_f32(synth.router_weights(6, 0, E, H))
+    small = bi.router_topk(gu.dev_f32(X[:300]), w, k, "f32")
+    big = bi.router_topk(gu.dev_f32(X), w, k, "f32")
+    torch.cuda.synchronize()
+    for f in ("logits", "ids", "weights", "margin", "margin_ulps"):
+        assert small[f].cpu().numpy().tobytes() == big[f][:300].cpu().numpy().tobytes(), f
