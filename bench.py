@@ -280,7 +280,7 @@ def router_sweep(bi, synth, torch, dev, hbm_gbs):
     Ws = [synth.device_normal((E, H), 77000 + i, 0.02, torch.float32, dev) for i in range(pool)]
     res = []
     stream = torch.cuda.current_stream(dev)
-    for Mi in (1, 4, 16, 64, 256, 1024, 4096):
+    for Mi in (1, 4, 16, 64, 128, 256, 1024, 4096):
         xs = [synth.device_normal((Mi, H), 78000 + i, 1.0, torch.float32, dev) for i in range(8)]
         lg = torch.empty((Mi, E), dtype=torch.float32, device=dev)
         ids = torch.empty((Mi, K_TOP), dtype=torch.int32, device=dev)

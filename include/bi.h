@@ -113,10 +113,17 @@ typedef struct CUstream_st *bi_stream;
  * Logits must be finite for the weights and margins to be meaningful (a
  * NaN ranks above every number and ties other NaNs by index).
  *
- * Scratch: when M is small the partitions are spread over several thread
- * blocks whose partial sums meet in a library-owned device buffer
- * (allocated once per device on the first call that needs it, never freed
- * before exit).  Make a first call before capturing a CUDA graph.
+ * Scratch: for mid-size batches the partitions of a tile are spread over
+ * several thread blocks whose partial sums meet in a library-owned device
+ * buffer (allocated once per device on the first call that needs it, never
+ * freed before exit).  Make a first call before capturing a CUDA graph.
+ *
+ * Ordering: the kernels start streaming w_gate before they wait for the
+ * preceding kernel in the stream (programmatic dependent launch); x is read
+ * only after that wait.  So w_gate must not be written by a kernel on `s`
+ * that releases its dependents early (griddepcontrol.launch_dependents) and
+ * may still be running; ordinary kernels, copies and this library's own
+ * kernels are safe.
  */
 BI_API bi_status bi_router_topk(const void *x, const void *w_gate, bi_dtype in_dtype,
                          bi_dtype logit_dtype, int32_t M, int32_t H, int32_t E, int32_t k,

@@ -85,6 +85,7 @@ enum : int {
     KID_SELECT = 20,       // 4 instantiations: 20..23
     KID_GATE = 24,
     KID_HASH = 25,         // 4 instantiations: 25..28
+    KID_ROUTER_GEMV = 30,  // 4 instantiations: 30..33
 };
 
 }  // namespace bi

@@ -164,12 +164,9 @@ router_proj_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
         mbar_init_fence();
     }
     __syncthreads();
-    pdl_wait();       // inputs may come from the previous kernel in the stream
-    pdl_trigger();
 
     // producer step: stage slab s into ring slot `slot` (valid blocks only);
-    // thread 0 fills the ring, then whichever warp releases a slot last
-    // refills it
+    // after the prologue, whichever warp releases a slot last refills it
     auto issue = [&](int s, int slot) {
         uint8_t *st = smem + slot * Cfg::STAGE_BYTES;
         int nvalid = 0;        // boxes starting before H (a box may run past H: TMA fills zeros)
@@ -186,10 +183,36 @@ router_proj_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
         }
     };
 
+    // prologue: the gate boxes of the first stages are weights, not the
+    // preceding kernel's output, so they stream before the dependency wait;
+    // the X boxes follow it
     const int nst = ns < NST ? ns : NST;
-    if (tid == 0)
-        for (int s = 0; s < nst; ++s) issue(s, s);
-    __syncthreads();
+    if (tid == 0) {
+        for (int s = 0; s < nst; ++s) {
+            uint8_t *st = smem + s * Cfg::STAGE_BYTES;
+            int nvalid = 0;
+#pragma unroll
+            for (int bx = 0; bx < Cfg::NB; ++bx) nvalid += (kSlab * s + kBlk * (q0 + bx * Cfg::PB) < H) ? 1 : 0;
+            mbar_arrive_expect_tx(&full_bar[s], (uint32_t)(nvalid * (Cfg::XBOX + Cfg::WBOX)));
+#pragma unroll
+            for (int bx = 0; bx < Cfg::NB; ++bx) {
+                const int h0 = kSlab * s + kBlk * (q0 + bx * Cfg::PB);
+                if (h0 < H) tma_load_2d(st + Cfg::XOP + bx * Cfg::WBOX, &tmw, &full_bar[s], h0, e0);
+            }
+        }
+    }
+    pdl_wait();       // X may be the preceding kernel's output
+    pdl_trigger();
+    if (tid == 0) {
+        for (int s = 0; s < nst; ++s) {
+            uint8_t *st = smem + s * Cfg::STAGE_BYTES;
+#pragma unroll
+            for (int bx = 0; bx < Cfg::NB; ++bx) {
+                const int h0 = kSlab * s + kBlk * (q0 + bx * Cfg::PB);
+                if (h0 < H) tma_load_2d(st + bx * Cfg::XBOX, &tmx, &full_bar[s], h0, m0);
+            }
+        }
+    }
 
     float acc[8][8];
 #pragma unroll
@@ -408,6 +431,194 @@ router_select_kernel(const float *__restrict__ part, int C, void *logits, int lo
     }
 }
 
+// ---------------------------------------------------------------------------
+// Small-batch twin: the same reduction contract shaped like a matrix-vector
+// product, for batches too small to fill 32-token tiles.  One warp owns two
+// experts; lane 16*x + q runs partition q's chain for expert x over up to 8
+// tokens (8 accumulators), reading whole 128-wide slabs of X ([8 rows x 128])
+// and of the two gate rows ([2 rows x 128]) that TMA stages in a ring.  The
+// 16 partials of a (token, expert) sit in 16 lanes of one half-warp and are
+// added by butterfly shuffles with offsets 1, 2, 4, 8: lanes q and q^d hold
+// the same sum after each level (fp addition is commutative), and the
+// levels pair exactly the partitions the pairwise tree pairs.  No scratch,
+// and every gate row is read by one warp of its own, so even M = 1 spreads
+// W_gate over E/2 thread blocks.
+// ---------------------------------------------------------------------------
+constexpr int kGemvT = 8;       // tokens per block
+
+// WPB warps per block share one staged X tile; each warp owns 2 experts.
+template <typename InT, int WPB>
+struct GemvCfg {
+    static constexpr int NST = WPB == 1 ? 16 : 8;                    // ring depth (slabs)
+    static constexpr int XBOX = kGemvT * kSlab * (int)sizeof(InT);   // [8 rows x 128]
+    static constexpr int WBOX = 2 * WPB * kSlab * (int)sizeof(InT);  // [2*WPB rows x 128]
+    static constexpr int STAGE_BYTES = XBOX + WBOX;
+    static constexpr int SMEM = NST * STAGE_BYTES + 1024;
+};
+
+template <typename InT, int WPB>
+__global__ void __launch_bounds__(32 * WPB)
+router_gemv_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
+                   int M, int E, int H, int logit_bf16, void *__restrict__ out, unsigned int *err)
+{
+    using Cfg = GemvCfg<InT, WPB>;
+    constexpr int NST = Cfg::NST;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t full_bar[NST];
+    __shared__ int released[NST];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~uintptr_t(1023));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, q = lane & 15;
+    const int x = 2 * warp + (lane >> 4);               // expert within the block
+    const int e0 = blockIdx.x * 2 * WPB, m0 = blockIdx.y * kGemvT;
+    const int ns = (H + kSlab - 1) / kSlab;
+    const int nt = min(kGemvT, M - m0);
+    const int nst = ns < NST ? ns : NST;
+
+    if (tid == 0) {
+        prefetch_tmap(&tmx);
+        prefetch_tmap(&tmw);
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(&full_bar[s], 1);
+            released[s] = 0;
+        }
+        mbar_init_fence();
+        // the gate rows are weights, not produced by the preceding kernel:
+        // start streaming them before waiting for it
+        for (int s = 0; s < nst; ++s) {
+            uint8_t *st = smem + s * Cfg::STAGE_BYTES;
+            mbar_arrive_expect_tx(&full_bar[s], (uint32_t)Cfg::STAGE_BYTES);
+            tma_load_2d(st + Cfg::XBOX, &tmw, &full_bar[s], kSlab * s, e0);
+        }
+    }
+    pdl_wait();                  // X may be the preceding kernel's output
+    pdl_trigger();
+    if (tid == 0)
+        for (int s = 0; s < nst; ++s)
+            tma_load_2d(smem + s * Cfg::STAGE_BYTES, &tmx, &full_bar[s], kSlab * s, m0);
+    __syncthreads();
+
+    auto refill = [&](int s, int slot) {
+        uint8_t *st = smem + slot * Cfg::STAGE_BYTES;
+        mbar_arrive_expect_tx(&full_bar[slot], (uint32_t)Cfg::STAGE_BYTES);
+        tma_load_2d(st + Cfg::XBOX, &tmw, &full_bar[slot], kSlab * s, e0);
+        tma_load_2d(st, &tmx, &full_bar[slot], kSlab * s, m0);
+    };
+
+    float acc[kGemvT];
+#pragma unroll
+    for (int t = 0; t < kGemvT; ++t) acc[t] = 0.0f;
+    int slot = 0;
+    uint32_t phase = 0;
+    for (int s = 0; s < ns; ++s) {
+        mbar_wait(&full_bar[slot], phase, err, 0x18);
+        const uint8_t *st = smem + slot * Cfg::STAGE_BYTES;
+        if (kSlab * s + kBlk * q < H) {
+            if constexpr (sizeof(InT) == 4) {
+                const float *ws = reinterpret_cast<const float *>(st + Cfg::XBOX) + x * kSlab + kBlk * q;
+                const float4 w0 = *reinterpret_cast<const float4 *>(ws);
+                const float4 w1 = *reinterpret_cast<const float4 *>(ws + 4);
+#pragma unroll
+                for (int t = 0; t < kGemvT; ++t) {
+                    if (t < nt) {
+                        const float *xs = reinterpret_cast<const float *>(st) + t * kSlab + kBlk * q;
+                        const float4 a0 = *reinterpret_cast<const float4 *>(xs);
+                        const float4 a1 = *reinterpret_cast<const float4 *>(xs + 4);
+                        float a = acc[t];
+                        a = __fmaf_rn(a0.x, w0.x, a);
+                        a = __fmaf_rn(a0.y, w0.y, a);
+                        a = __fmaf_rn(a0.z, w0.z, a);
+                        a = __fmaf_rn(a0.w, w0.w, a);
+                        a = __fmaf_rn(a1.x, w1.x, a);
+                        a = __fmaf_rn(a1.y, w1.y, a);
+                        a = __fmaf_rn(a1.z, w1.z, a);
+                        a = __fmaf_rn(a1.w, w1.w, a);
+                        acc[t] = a;
+                    }
+                }
+            } else {
+                const uint4 wr = *reinterpret_cast<const uint4 *>(st + Cfg::XBOX + 2 * (x * kSlab + kBlk * q));
+#pragma unroll
+                for (int t = 0; t < kGemvT; ++t) {
+                    if (t < nt) {
+                        const uint4 xr = *reinterpret_cast<const uint4 *>(st + 2 * (t * kSlab + kBlk * q));
+                        float a = acc[t];
+                        a = __fmaf_rn(bf16lo(xr.x), bf16lo(wr.x), a);
+                        a = __fmaf_rn(bf16hi(xr.x), bf16hi(wr.x), a);
+                        a = __fmaf_rn(bf16lo(xr.y), bf16lo(wr.y), a);
+                        a = __fmaf_rn(bf16hi(xr.y), bf16hi(wr.y), a);
+                        a = __fmaf_rn(bf16lo(xr.z), bf16lo(wr.z), a);
+                        a = __fmaf_rn(bf16hi(xr.z), bf16hi(wr.z), a);
+                        a = __fmaf_rn(bf16lo(xr.w), bf16lo(wr.w), a);
+                        a = __fmaf_rn(bf16hi(xr.w), bf16hi(wr.w), a);
+                        acc[t] = a;
+                    }
+                }
+            }
+        }
+        // the last warp done with the slot refills it with slab s + NST
+        __syncwarp();
+        if (lane == 0) {
+            __threadfence_block();
+            if (atomicAdd(&released[slot], 1) == WPB - 1) {
+                released[slot] = 0;
+                if (s + NST < ns) {
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    refill(s + NST, slot);
+                }
+            }
+        }
+        if (++slot == NST) {
+            slot = 0;
+            phase ^= 1u;
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < kGemvT; ++t) {
+#pragma unroll
+        for (int d = 1; d < 16; d *= 2) acc[t] = acc[t] + __shfl_xor_sync(0xFFFFFFFFu, acc[t], d);
+    }
+    const int e = e0 + x;
+    if (q == 0 && e < E) {
+#pragma unroll
+        for (int t = 0; t < kGemvT; ++t) {
+            if (t < nt) {
+                const size_t o = (size_t)(m0 + t) * E + e;
+                if (logit_bf16)
+                    static_cast<__nv_bfloat16 *>(out)[o] = __float2bfloat16_rn(acc[t]);
+                else
+                    static_cast<float *>(out)[o] = acc[t];
+            }
+        }
+    }
+}
+
+template <typename InT, int WPB>
+bi_status launch_gemv(Device *d, const void *x, const void *w, int M, int E, int H, int logit_bf16, void *out,
+                      cudaStream_t s)
+{
+    using Cfg = GemvCfg<InT, WPB>;
+    auto kern = router_gemv_kernel<InT, WPB>;
+    bi_status st = set_smem_once(d, KID_ROUTER_GEMV + (sizeof(InT) == 4 ? 0 : 2) + (WPB == 1 ? 0 : 1), kern,
+                                 Cfg::SMEM);
+    if (st != BI_OK) return st;
+    const CUtensorMapDataType dt = sizeof(InT) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const uint64_t strides[1] = {(uint64_t)H * sizeof(InT)};
+    alignas(64) CUtensorMap tmx, tmw;
+    {
+        const uint64_t dims[2] = {(uint64_t)H, (uint64_t)M};
+        const uint32_t box[2] = {(uint32_t)kSlab, (uint32_t)kGemvT};
+        if ((st = encode_tiled(&tmx, dt, 2, x, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE)) != BI_OK) return st;
+    }
+    {
+        const uint64_t dims[2] = {(uint64_t)H, (uint64_t)E};
+        const uint32_t box[2] = {(uint32_t)kSlab, (uint32_t)(2 * WPB)};
+        if ((st = encode_tiled(&tmw, dt, 2, w, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE)) != BI_OK) return st;
+    }
+    dim3 grid((E + 2 * WPB - 1) / (2 * WPB), (M + kGemvT - 1) / kGemvT);
+    return launch_pdl(kern, grid, dim3(32 * WPB), (size_t)Cfg::SMEM, s, tmx, tmw, M, E, H, logit_bf16, out, d->err);
+}
+
 template <typename InT, int C>
 bi_status launch_proj(Device *d, const void *x, const void *w, int M, int E, int H, int out_mode, void *out,
                       cudaStream_t s, int kid)
@@ -472,6 +683,9 @@ bi_status launch_select(Device *d, int epl, dim3 grid, dim3 block, cudaStream_t 
     return launch_select1<32>(d, grid, block, cs, pp, C, logits, lbf, M, E, k, ids, w, mg, mu);
 }
 
+// Batches up to this many tokens take the matrix-vector twin.
+constexpr int kGemvMaxM = 64;
+
 // How many blocks share one tile's 16 partitions: the smallest power of two
 // that gives at least one block per SM, capped at 16 and by the scratch
 // bound.  Any choice gives the same bits; this only trades parallelism for
@@ -515,7 +729,8 @@ extern "C" bi_status bi_router_topk(const void *x, const void *w_gate, bi_dtype 
     if (st != BI_OK) return st;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(s);
 
-    const int C = choose_split(M, E, d->sm_count);
+    const bool small = M <= kGemvMaxM;
+    const int C = small ? 1 : choose_split(M, E, d->sm_count);
     void *part = nullptr;
     if (C > 1) {
         st = device_scratch(d, (size_t)C * M * E * sizeof(float), &part);
@@ -527,8 +742,15 @@ extern "C" bi_status bi_router_topk(const void *x, const void *w_gate, bi_dtype 
     const int lbf = logit_dtype == BI_BF16 ? 1 : 0;
     const int out_mode = C > 1 ? OUT_PARTIAL : (lbf ? OUT_BF16 : OUT_F32);
     void *out = C > 1 ? part : logits_out;
-    st = f32in ? launch_proj_c<float>(d, C, x, w_gate, M, E, H, out_mode, out, cs)
-               : launch_proj_c<__nv_bfloat16>(d, C, x, w_gate, M, E, H, out_mode, out, cs);
+    if (small && M <= kGemvT)
+        st = f32in ? launch_gemv<float, 1>(d, x, w_gate, M, E, H, lbf, logits_out, cs)
+                   : launch_gemv<__nv_bfloat16, 1>(d, x, w_gate, M, E, H, lbf, logits_out, cs);
+    else if (small)
+        st = f32in ? launch_gemv<float, 4>(d, x, w_gate, M, E, H, lbf, logits_out, cs)
+                   : launch_gemv<__nv_bfloat16, 4>(d, x, w_gate, M, E, H, lbf, logits_out, cs);
+    else
+        st = f32in ? launch_proj_c<float>(d, C, x, w_gate, M, E, H, out_mode, out, cs)
+                   : launch_proj_c<__nv_bfloat16>(d, C, x, w_gate, M, E, H, out_mode, out, cs);
     if (st != BI_OK) return st;
 
     const int epl = E / 32;
