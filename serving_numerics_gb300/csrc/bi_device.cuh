@@ -17,6 +17,15 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p)
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// The first 1024-byte aligned byte of a dynamic shared-memory array.  The
+// offset is added to the __shared__ pointer itself (never through an
+// integer round trip), so the compiler still knows the result is shared
+// memory and emits shared loads for it rather than generic ones.
+__device__ __forceinline__ uint8_t *smem_align1024(uint8_t *smem_raw)
+{
+    return smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+}
+
 __device__ __forceinline__ uint64_t global_ns()
 {
     uint64_t t;
@@ -24,6 +33,10 @@ __device__ __forceinline__ uint64_t global_ns()
     return t;
 }
 
+// Programmatic dependent launch.  Every kernel of the library triggers its
+// dependents at entry (so the next kernel in the stream can be resident and
+// stream its weights early) and calls pdl_wait() before it reads anything a
+// preceding kernel may have written or writes anything it may still read.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 

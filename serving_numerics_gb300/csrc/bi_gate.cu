@@ -21,8 +21,8 @@ __global__ void __launch_bounds__(32 * kGateWarps)
 shared_gate_kernel(const float *__restrict__ x, const float *__restrict__ w, int M, int H,
                    float *__restrict__ dot, float *__restrict__ sig)
 {
+    pdl_trigger();   // dependents may launch now; each waits before reading our outputs
     pdl_wait();
-    pdl_trigger();
     const int lane = threadIdx.x & 31, q = lane & 15;
     const int m = (blockIdx.x * kGateWarps + (threadIdx.x >> 5)) * 2 + (lane >> 4);
     const bool active = m < M;

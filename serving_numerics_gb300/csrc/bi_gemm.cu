@@ -123,11 +123,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 gemm_bf16_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__ CUtensorMap tmb,
                  __nv_bfloat16 *__restrict__ C, int M, int N, int K, long long ldc, unsigned int *err)
 {
+    pdl_trigger();   // dependents may launch now; each waits before reading our outputs
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[STAGES], empty_bar[STAGES], tfull_bar[2], tempty_bar[2];
     __shared__ uint32_t tmem_base_sh;
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                ~uintptr_t(1023));
+    uint8_t *smem = smem_align1024(smem_raw);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m_tiles = (M + BM - 1) / BM, n_tiles = (N + BN - 1) / BN;
@@ -153,7 +153,6 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant_
     const uint32_t tmem_base = tmem_base_sh;
 
     pdl_wait();
-    pdl_trigger();
 
     if (warp == 0) {
         if (lane == 0) {   // TMA producer

@@ -44,8 +44,8 @@ __global__ void __launch_bounds__(32 * kHashWarps)
 route_hash_kernel(const int32_t *__restrict__ ids, int k, HashRanges rr, int n_ranges,
                   const uint64_t *basis, uint64_t *out)
 {
+    pdl_trigger();   // dependents may launch now; each waits before reading our outputs
     pdl_wait();
-    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int r = blockIdx.x * kHashWarps + (threadIdx.x >> 5);
     if (r >= n_ranges) return;                        // warp-uniform

@@ -87,9 +87,11 @@ __device__ __forceinline__ void block_f32(float (&acc)[8][8], const uint8_t *xs,
 #pragma unroll
         for (int j = 0; j < 8; ++j)
             xv[j] = *reinterpret_cast<const float4 *>(xs + swz<P>(tg + 4 * j, 2 * pc + c));
+        float4 wn = *reinterpret_cast<const float4 *>(ws + swz<P>(eg, 2 * pc + c));
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const float4 wv = *reinterpret_cast<const float4 *>(ws + swz<P>(eg + 8 * i, 2 * pc + c));
+            const float4 wv = wn;       // this expert's four values; the next one loads meanwhile
+            if (i + 1 < 8) wn = *reinterpret_cast<const float4 *>(ws + swz<P>(eg + 8 * (i + 1), 2 * pc + c));
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 float a = acc[j][i];
@@ -139,13 +141,13 @@ __global__ void __launch_bounds__(ProjCfg<InT, C>::THREADS, 1)
 router_proj_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
                    int M, int E, int H, int out_mode, void *__restrict__ out, unsigned int *err)
 {
+    pdl_trigger();   // dependents may launch now; each waits before reading our outputs
     using Cfg = ProjCfg<InT, C>;
     constexpr int NPL = Cfg::NPL, NST = Cfg::NST;
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[NST];
     __shared__ int released[NST];          // warps done with the slot's current slab
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                ~uintptr_t(1023));
+    uint8_t *smem = smem_align1024(smem_raw);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int e_tile = blockIdx.x / C, g = blockIdx.x % C;
@@ -202,7 +204,6 @@ router_proj_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
         }
     }
     pdl_wait();       // X may be the preceding kernel's output
-    pdl_trigger();
     if (tid == 0) {
         for (int s = 0; s < nst; ++s) {
             uint8_t *st = smem + s * Cfg::STAGE_BYTES;
@@ -332,71 +333,100 @@ router_select_kernel(const float *__restrict__ part, int C, void *logits, int lo
                      int E, int k, int32_t *__restrict__ ids, float *__restrict__ weights,
                      float *__restrict__ margin, int32_t *__restrict__ ulps)
 {
+    pdl_trigger();   // dependents may launch now; each waits before reading our outputs
     pdl_wait();
-    pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m = blockIdx.x * kSelWarps + warp;
     if (m >= M) return;
     const int epl = E >> 5;
 
+    // gather this lane's logits (experts lane + 32 i), all loads issued first
     float v[EPLM];
-    uint32_t key[EPLM];
+    const size_t row = (size_t)m * E + lane;
+    if (C == 1) {
+        if (logit_bf16) {
+            const __nv_bfloat16 *lp = static_cast<const __nv_bfloat16 *>(logits) + row;
 #pragma unroll
-    for (int i = 0; i < EPLM; ++i) {
-        v[i] = 0.0f;
-        key[i] = 0u;
-        if (i < epl) {
-            const size_t o = (size_t)m * E + lane + 32 * i;
-            float x;
-            if (C == 1) {
-                x = logit_bf16 ? __bfloat162float(static_cast<const __nv_bfloat16 *>(logits)[o])
-                               : static_cast<const float *>(logits)[o];
-            } else {
-                float p[16];
+            for (int i = 0; i < EPLM; ++i) v[i] = i < epl ? __bfloat162float(lp[32 * i]) : 0.0f;
+        } else {
+            const float *lp = static_cast<const float *>(logits) + row;
 #pragma unroll
-                for (int q = 0; q < 16; ++q) p[q] = (q < C) ? part[(size_t)q * M * E + o] : 0.0f;
+            for (int i = 0; i < EPLM; ++i) v[i] = i < epl ? lp[32 * i] : 0.0f;
+        }
+    } else {
+        // finish the pairwise tree over the C group sums, then round to the
+        // logit dtype and store the logits
+        const size_t gs = (size_t)M * E;
 #pragma unroll
-                for (int d = 1; d < 16; d *= 2)
-                    if (d < C) {
+        for (int i = 0; i < EPLM; ++i) {
+            float p[16];
 #pragma unroll
-                        for (int q = 0; q + d < 16; q += 2 * d) p[q] = p[q] + p[q + d];
-                    }
-                x = p[0];
+            for (int q = 0; q < 16; ++q) p[q] = (i < epl && q < C) ? part[(size_t)q * gs + row + 32 * i] : 0.0f;
+#pragma unroll
+            for (int d = 1; d < 16; d *= 2)
+                if (d < C) {
+#pragma unroll
+                    for (int q = 0; q + d < 16; q += 2 * d) p[q] = p[q] + p[q + d];
+                }
+            v[i] = p[0];
+        }
+#pragma unroll
+        for (int i = 0; i < EPLM; ++i) {
+            if (i < epl) {
                 if (logit_bf16) {
-                    const __nv_bfloat16 b = __float2bfloat16_rn(x);
-                    static_cast<__nv_bfloat16 *>(logits)[o] = b;
-                    x = __bfloat162float(b);
+                    const __nv_bfloat16 b = __float2bfloat16_rn(v[i]);
+                    static_cast<__nv_bfloat16 *>(logits)[row + 32 * i] = b;
+                    v[i] = __bfloat162float(b);
                 } else {
-                    static_cast<float *>(logits)[o] = x;
+                    static_cast<float *>(logits)[row + 32 * i] = v[i];
                 }
             }
-            v[i] = x;
-            key[i] = rank_key(x);
         }
     }
 
-    uint32_t bk = 0u;
-    uint32_t bidx = 0xFFFFFFFFu;
-    float bv = 0.0f;
-    auto rescan = [&]() {
-        bk = 0u;
-        bidx = 0xFFFFFFFFu;
+    // each lane sorts its (key, index) pairs once, best first (ascending
+    // index among equal keys); a round then only compares lane heads
+    uint32_t key[EPLM];
+    int idx[EPLM];
 #pragma unroll
-        for (int i = 0; i < EPLM; ++i)
-            if (key[i] > bk) {              // ascending i: first maximum = lowest index
-                bk = key[i];
-                bidx = (uint32_t)(lane + 32 * i);
-                bv = v[i];
-            }
-    };
-    rescan();
+    for (int i = 0; i < EPLM; ++i) {
+        key[i] = i < epl ? rank_key(v[i]) : 0u;
+        idx[i] = lane + 32 * i;
+    }
+#pragma unroll
+    for (int a = 0; a < EPLM; ++a) {            // odd-even transposition network
+#pragma unroll
+        for (int i = a & 1; i + 1 < EPLM; i += 2) {
+            const bool sw = key[i + 1] > key[i];    // equal keys keep the lower index first
+            const uint32_t k0 = sw ? key[i + 1] : key[i], k1 = sw ? key[i] : key[i + 1];
+            const int i0 = sw ? idx[i + 1] : idx[i], i1 = sw ? idx[i] : idx[i + 1];
+            const float v0 = sw ? v[i + 1] : v[i], v1 = sw ? v[i] : v[i + 1];
+            key[i] = k0; key[i + 1] = k1; idx[i] = i0; idx[i + 1] = i1; v[i] = v0; v[i + 1] = v1;
+        }
+    }
 
     float l0 = 0.0f, den = 0.0f, my_e = 0.0f, v_sel_min = 0.0f, v_rej_max = 0.0f;
     int my_id = 0;
     for (int r = 0; r <= k; ++r) {
+        const uint32_t bk = key[0];
         const uint32_t mk = __reduce_max_sync(0xFFFFFFFFu, bk);
-        const uint32_t win = __reduce_min_sync(0xFFFFFFFFu, bk == mk ? bidx : 0xFFFFFFFFu);
-        const float wv = __shfl_sync(0xFFFFFFFFu, bv, (int)(win & 31u));
+        const uint32_t holders = __ballot_sync(0xFFFFFFFFu, bk == mk);
+        // one lane holds the maximum key: its head wins; several (equal
+        // values in different lanes): the lowest index among them wins
+        const uint32_t win = (holders & (holders - 1u)) == 0u
+                                 ? (uint32_t)__shfl_sync(0xFFFFFFFFu, idx[0], __ffs(holders) - 1)
+                                 : __reduce_min_sync(0xFFFFFFFFu, bk == mk ? (uint32_t)idx[0] : 0xFFFFFFFFu);
+        const int wl = (int)(win & 31u);
+        const float wv = __shfl_sync(0xFFFFFFFFu, v[0], wl);
+        if (lane == wl) {                       // pop the head
+#pragma unroll
+            for (int i = 0; i + 1 < EPLM; ++i) {
+                key[i] = key[i + 1];
+                idx[i] = idx[i + 1];
+                v[i] = v[i + 1];
+            }
+            key[EPLM - 1] = 0u;
+        }
         if (r == k) {
             v_rej_max = wv;
             break;
@@ -409,12 +439,6 @@ router_select_kernel(const float *__restrict__ part, int C, void *logits, int lo
             my_id = (int)win;
         }
         v_sel_min = wv;
-        if ((int)(win & 31u) == lane) {
-#pragma unroll
-            for (int i = 0; i < EPLM; ++i)
-                if ((uint32_t)(lane + 32 * i) == win) key[i] = 0u;
-            rescan();
-        }
     }
     if (lane < k) {
         ids[(size_t)m * k + lane] = my_id;
@@ -435,8 +459,8 @@ router_select_kernel(const float *__restrict__ part, int C, void *logits, int lo
 // Small-batch twin: the same reduction contract shaped like a matrix-vector
 // product, for batches too small to fill 32-token tiles.  One warp owns two
 // experts; lane 16*x + q runs partition q's chain for expert x over up to 8
-// tokens (8 accumulators), reading whole 128-wide slabs of X ([8 rows x 128])
-// and of the two gate rows ([2 rows x 128]) that TMA stages in a ring.  The
+// tokens (8 accumulators), reading whole slabs of X and of the gate rows that
+// TMA stages in a ring, two 128-wide slabs per stage.  The
 // 16 partials of a (token, expert) sit in 16 lanes of one half-warp and are
 // added by butterfly shuffles with offsets 1, 2, 4, 8: lanes q and q^d hold
 // the same sum after each level (fp addition is commutative), and the
@@ -447,11 +471,15 @@ router_select_kernel(const float *__restrict__ part, int C, void *logits, int lo
 constexpr int kGemvT = 8;       // tokens per block
 
 // WPB warps per block share one staged X tile; each warp owns 2 experts.
+// One stage holds two slabs (256 h): boxes [8 rows x 256] of X and
+// [2*WPB rows x 256] of W_gate.
+constexpr int kGemvSpan = 2 * kSlab;
+
 template <typename InT, int WPB>
 struct GemvCfg {
-    static constexpr int NST = WPB == 1 ? 16 : 8;                    // ring depth (slabs)
-    static constexpr int XBOX = kGemvT * kSlab * (int)sizeof(InT);   // [8 rows x 128]
-    static constexpr int WBOX = 2 * WPB * kSlab * (int)sizeof(InT);  // [2*WPB rows x 128]
+    static constexpr int NST = WPB == 1 ? 8 : 4;                         // ring depth (stages)
+    static constexpr int XBOX = kGemvT * kGemvSpan * (int)sizeof(InT);
+    static constexpr int WBOX = 2 * WPB * kGemvSpan * (int)sizeof(InT);
     static constexpr int STAGE_BYTES = XBOX + WBOX;
     static constexpr int SMEM = NST * STAGE_BYTES + 1024;
 };
@@ -461,19 +489,21 @@ __global__ void __launch_bounds__(32 * WPB)
 router_gemv_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
                    int M, int E, int H, int logit_bf16, void *__restrict__ out, unsigned int *err)
 {
+    pdl_trigger();   // dependents may launch now; each waits before reading our outputs
     using Cfg = GemvCfg<InT, WPB>;
     constexpr int NST = Cfg::NST;
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[NST];
     __shared__ int released[NST];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                ~uintptr_t(1023));
+    uint8_t *smem = smem_align1024(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, q = lane & 15;
     const int x = 2 * warp + (lane >> 4);               // expert within the block
     const int e0 = blockIdx.x * 2 * WPB, m0 = blockIdx.y * kGemvT;
     const int ns = (H + kSlab - 1) / kSlab;
+    const int nstage = (H + kGemvSpan - 1) / kGemvSpan;
     const int nt = min(kGemvT, M - m0);
-    const int nst = ns < NST ? ns : NST;
+    const int nst = nstage < NST ? nstage : NST;
+    const bool oneshot = nstage <= NST;
 
     if (tid == 0) {
         prefetch_tmap(&tmx);
@@ -484,25 +514,29 @@ router_gemv_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
         }
         mbar_init_fence();
         // the gate rows are weights, not produced by the preceding kernel:
-        // start streaming them before waiting for it
+        // start streaming them before waiting for it.  When the whole of H
+        // fits the ring, one barrier covers every box and the loop below
+        // never waits again.
+        if (oneshot) mbar_arrive_expect_tx(&full_bar[0], (uint32_t)(nstage * Cfg::STAGE_BYTES));
         for (int s = 0; s < nst; ++s) {
             uint8_t *st = smem + s * Cfg::STAGE_BYTES;
-            mbar_arrive_expect_tx(&full_bar[s], (uint32_t)Cfg::STAGE_BYTES);
-            tma_load_2d(st + Cfg::XBOX, &tmw, &full_bar[s], kSlab * s, e0);
+            uint64_t *bar = oneshot ? &full_bar[0] : &full_bar[s];
+            if (!oneshot) mbar_arrive_expect_tx(bar, (uint32_t)Cfg::STAGE_BYTES);
+            tma_load_2d(st + Cfg::XBOX, &tmw, bar, kGemvSpan * s, e0);
         }
     }
     pdl_wait();                  // X may be the preceding kernel's output
-    pdl_trigger();
     if (tid == 0)
         for (int s = 0; s < nst; ++s)
-            tma_load_2d(smem + s * Cfg::STAGE_BYTES, &tmx, &full_bar[s], kSlab * s, m0);
+            tma_load_2d(smem + s * Cfg::STAGE_BYTES, &tmx, oneshot ? &full_bar[0] : &full_bar[s],
+                        kGemvSpan * s, m0);
     __syncthreads();
 
     auto refill = [&](int s, int slot) {
         uint8_t *st = smem + slot * Cfg::STAGE_BYTES;
         mbar_arrive_expect_tx(&full_bar[slot], (uint32_t)Cfg::STAGE_BYTES);
-        tma_load_2d(st + Cfg::XBOX, &tmw, &full_bar[slot], kSlab * s, e0);
-        tma_load_2d(st, &tmx, &full_bar[slot], kSlab * s, m0);
+        tma_load_2d(st + Cfg::XBOX, &tmw, &full_bar[slot], kGemvSpan * s, e0);
+        tma_load_2d(st, &tmx, &full_bar[slot], kGemvSpan * s, m0);
     };
 
     float acc[kGemvT];
@@ -510,59 +544,70 @@ router_gemv_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
     for (int t = 0; t < kGemvT; ++t) acc[t] = 0.0f;
     int slot = 0;
     uint32_t phase = 0;
-    for (int s = 0; s < ns; ++s) {
-        mbar_wait(&full_bar[slot], phase, err, 0x18);
+    for (int s = 0; s < nstage; ++s) {
+        if (!oneshot || s == 0) mbar_wait(&full_bar[slot], phase, err, 0x18);
         const uint8_t *st = smem + slot * Cfg::STAGE_BYTES;
-        if (kSlab * s + kBlk * q < H) {
-            if constexpr (sizeof(InT) == 4) {
-                const float *ws = reinterpret_cast<const float *>(st + Cfg::XBOX) + x * kSlab + kBlk * q;
-                const float4 w0 = *reinterpret_cast<const float4 *>(ws);
-                const float4 w1 = *reinterpret_cast<const float4 *>(ws + 4);
 #pragma unroll
-                for (int t = 0; t < kGemvT; ++t) {
-                    if (t < nt) {
-                        const float *xs = reinterpret_cast<const float *>(st) + t * kSlab + kBlk * q;
-                        const float4 a0 = *reinterpret_cast<const float4 *>(xs);
-                        const float4 a1 = *reinterpret_cast<const float4 *>(xs + 4);
-                        float a = acc[t];
-                        a = __fmaf_rn(a0.x, w0.x, a);
-                        a = __fmaf_rn(a0.y, w0.y, a);
-                        a = __fmaf_rn(a0.z, w0.z, a);
-                        a = __fmaf_rn(a0.w, w0.w, a);
-                        a = __fmaf_rn(a1.x, w1.x, a);
-                        a = __fmaf_rn(a1.y, w1.y, a);
-                        a = __fmaf_rn(a1.z, w1.z, a);
-                        a = __fmaf_rn(a1.w, w1.w, a);
-                        acc[t] = a;
+        for (int sub = 0; sub < 2; ++sub) {          // the stage's two slabs, in order
+            const int slab = 2 * s + sub;
+            if (slab < ns && kSlab * slab + kBlk * q < H) {
+                const int col = sub * kSlab + kBlk * q;   // column of this block in the stage
+                if constexpr (sizeof(InT) == 4) {
+                    const float *ws = reinterpret_cast<const float *>(st + Cfg::XBOX) + x * kGemvSpan + col;
+                    const float4 w0 = *reinterpret_cast<const float4 *>(ws);
+                    const float4 w1 = *reinterpret_cast<const float4 *>(ws + 4);
+#pragma unroll
+                    for (int t = 0; t < kGemvT; ++t) {
+                        if (t < nt) {
+                            const float *xs = reinterpret_cast<const float *>(st) + t * kGemvSpan + col;
+                            const float4 a0 = *reinterpret_cast<const float4 *>(xs);
+                            const float4 a1 = *reinterpret_cast<const float4 *>(xs + 4);
+                            float a = acc[t];
+                            a = __fmaf_rn(a0.x, w0.x, a);
+                            a = __fmaf_rn(a0.y, w0.y, a);
+                            a = __fmaf_rn(a0.z, w0.z, a);
+                            a = __fmaf_rn(a0.w, w0.w, a);
+                            a = __fmaf_rn(a1.x, w1.x, a);
+                            a = __fmaf_rn(a1.y, w1.y, a);
+                            a = __fmaf_rn(a1.z, w1.z, a);
+                            a = __fmaf_rn(a1.w, w1.w, a);
+                            acc[t] = a;
+                        }
                     }
-                }
-            } else {
-                const uint4 wr = *reinterpret_cast<const uint4 *>(st + Cfg::XBOX + 2 * (x * kSlab + kBlk * q));
+                } else {
+                    const uint4 wr =
+                        *reinterpret_cast<const uint4 *>(st + Cfg::XBOX + 2 * (x * kGemvSpan + col));
 #pragma unroll
-                for (int t = 0; t < kGemvT; ++t) {
-                    if (t < nt) {
-                        const uint4 xr = *reinterpret_cast<const uint4 *>(st + 2 * (t * kSlab + kBlk * q));
-                        float a = acc[t];
-                        a = __fmaf_rn(bf16lo(xr.x), bf16lo(wr.x), a);
-                        a = __fmaf_rn(bf16hi(xr.x), bf16hi(wr.x), a);
-                        a = __fmaf_rn(bf16lo(xr.y), bf16lo(wr.y), a);
-                        a = __fmaf_rn(bf16hi(xr.y), bf16hi(wr.y), a);
-                        a = __fmaf_rn(bf16lo(xr.z), bf16lo(wr.z), a);
-                        a = __fmaf_rn(bf16hi(xr.z), bf16hi(wr.z), a);
-                        a = __fmaf_rn(bf16lo(xr.w), bf16lo(wr.w), a);
-                        a = __fmaf_rn(bf16hi(xr.w), bf16hi(wr.w), a);
-                        acc[t] = a;
+                    for (int t = 0; t < kGemvT; ++t) {
+                        if (t < nt) {
+                            const uint4 xr = *reinterpret_cast<const uint4 *>(st + 2 * (t * kGemvSpan + col));
+                            float a = acc[t];
+                            a = __fmaf_rn(bf16lo(xr.x), bf16lo(wr.x), a);
+                            a = __fmaf_rn(bf16hi(xr.x), bf16hi(wr.x), a);
+                            a = __fmaf_rn(bf16lo(xr.y), bf16lo(wr.y), a);
+                            a = __fmaf_rn(bf16hi(xr.y), bf16hi(wr.y), a);
+                            a = __fmaf_rn(bf16lo(xr.z), bf16lo(wr.z), a);
+                            a = __fmaf_rn(bf16hi(xr.z), bf16hi(wr.z), a);
+                            a = __fmaf_rn(bf16lo(xr.w), bf16lo(wr.w), a);
+                            a = __fmaf_rn(bf16hi(xr.w), bf16hi(wr.w), a);
+                            acc[t] = a;
+                        }
                     }
                 }
             }
         }
-        // the last warp done with the slot refills it with slab s + NST
-        __syncwarp();
-        if (lane == 0) {
-            __threadfence_block();
-            if (atomicAdd(&released[slot], 1) == WPB - 1) {
-                released[slot] = 0;
-                if (s + NST < ns) {
+        // release: with one warp the warp itself refills; otherwise the last
+        // warp done with the slot does
+        if (s + NST < nstage) {
+            __syncwarp();
+            if (lane == 0) {
+                bool last = true;
+                if constexpr (WPB > 1) {
+                    __threadfence_block();
+                    last = atomicAdd(&released[slot], 1) == WPB - 1;
+                    if (last) released[slot] = 0;
+                }
+                if (last) {
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     refill(s + NST, slot);
                 }
@@ -607,12 +652,12 @@ bi_status launch_gemv(Device *d, const void *x, const void *w, int M, int E, int
     alignas(64) CUtensorMap tmx, tmw;
     {
         const uint64_t dims[2] = {(uint64_t)H, (uint64_t)M};
-        const uint32_t box[2] = {(uint32_t)kSlab, (uint32_t)kGemvT};
+        const uint32_t box[2] = {(uint32_t)kGemvSpan, (uint32_t)kGemvT};
         if ((st = encode_tiled(&tmx, dt, 2, x, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE)) != BI_OK) return st;
     }
     {
         const uint64_t dims[2] = {(uint64_t)H, (uint64_t)E};
-        const uint32_t box[2] = {(uint32_t)kSlab, (uint32_t)(2 * WPB)};
+        const uint32_t box[2] = {(uint32_t)kGemvSpan, (uint32_t)(2 * WPB)};
         if ((st = encode_tiled(&tmw, dt, 2, w, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE)) != BI_OK) return st;
     }
     dim3 grid((E + 2 * WPB - 1) / (2 * WPB), (M + kGemvT - 1) / kGemvT);
