@@ -56,11 +56,9 @@ struct ProjCfg {
     static constexpr int STAGE_BYTES = XOP + WOP;
     static constexpr int NST_RAW = (192 * 1024) / STAGE_BYTES;
     static constexpr int NST = NST_RAW > 16 ? 16 : (NST_RAW < 2 ? 2 : NST_RAW);
-    static constexpr int TREE_BYTES = (NPL / 2) * 64 * 32 * 4;    // 64 values x 32 lanes per slot
-    static constexpr int OUT_BYTES = kTileM * (kTileE + 1) * 4;
+    static constexpr int TREE_BYTES = NPL * 64 * 33 * 4;           // every warp's 64 partials
     static constexpr int BODY0 = NST * STAGE_BYTES;
-    static constexpr int BODY1 = TREE_BYTES > OUT_BYTES ? TREE_BYTES : OUT_BYTES;
-    static constexpr int BODY = BODY0 > BODY1 ? BODY0 : BODY1;
+    static constexpr int BODY = BODY0 > TREE_BYTES ? BODY0 : TREE_BYTES;
     static constexpr int SMEM = BODY + 1024;                      // + alignment slack
     static_assert(P == 16 || P == 32 || P == 64 || P == 128, "TMA swizzle span");
 };
@@ -256,45 +254,33 @@ router_proj_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
     }
     __syncthreads();                                       // every warp is done with the ring
 
-    // lower levels of the pairwise tree, over this block's NPL partitions
-    float *tree = reinterpret_cast<float *>(smem);
+    // partition tree: every warp parks its 64 partial sums (value v of lane L
+    // at part[(warp * 64 + v) * 33 + L], padded rows); after one barrier each
+    // thread adds the NPL partials of its outputs with the lower levels of the
+    // pairwise tree, in registers, and stores them row-coalesced
+    float *part = reinterpret_cast<float *>(smem);
 #pragma unroll
-    for (int d = 1; d < NPL; d *= 2) {
-        const int p = warp / (2 * d);
-        if ((warp % (2 * d)) == d) {
-            float *dst = tree + p * 2048;
-#pragma unroll
-            for (int v = 0; v < 64; ++v) dst[v * 32 + lane] = acc[v >> 3][v & 7];
-        }
-        __syncthreads();
-        if ((warp % (2 * d)) == 0) {
-            const float *src = tree + p * 2048;
-#pragma unroll
-            for (int v = 0; v < 64; ++v) acc[v >> 3][v & 7] = acc[v >> 3][v & 7] + src[v * 32 + lane];
-        }
-        __syncthreads();
-    }
-
-    // stage the 32x64 result and write it row-coalesced
-    float *tile = reinterpret_cast<float *>(smem);
-    if (warp == 0) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-#pragma unroll
-            for (int i = 0; i < 8; ++i) tile[(tg + 4 * j) * (kTileE + 1) + eg + 8 * i] = acc[j][i];
-    }
+    for (int v = 0; v < 64; ++v) part[(warp * 64 + v) * 33 + lane] = acc[v >> 3][v & 7];
     __syncthreads();
     for (int idx = tid; idx < kTileM * kTileE; idx += Cfg::THREADS) {
         const int t = idx >> 6, e = idx & 63, m = m0 + t;
+        // output (t, e) is value 8*(t/4) + e/8 of lane (t%4) + 4*(e%8)
+        const int v = 8 * (t >> 2) + (e >> 3), L = (t & 3) + 4 * (e & 7);
+        float p[NPL];
+#pragma unroll
+        for (int w = 0; w < NPL; ++w) p[w] = part[(w * 64 + v) * 33 + L];
+#pragma unroll
+        for (int d = 1; d < NPL; d *= 2)
+#pragma unroll
+            for (int w = 0; w + d < NPL; w += 2 * d) p[w] = p[w] + p[w + d];
         if (m < M && e0 + e < E) {
-            const float v = tile[t * (kTileE + 1) + e];
             const size_t o = (size_t)m * E + e0 + e;
             if (out_mode == OUT_F32)
-                static_cast<float *>(out)[o] = v;
+                static_cast<float *>(out)[o] = p[0];
             else if (out_mode == OUT_BF16)
-                static_cast<__nv_bfloat16 *>(out)[o] = __float2bfloat16_rn(v);
+                static_cast<__nv_bfloat16 *>(out)[o] = __float2bfloat16_rn(p[0]);
             else
-                static_cast<float *>(out)[(size_t)g * M * E + o] = v;
+                static_cast<float *>(out)[(size_t)g * M * E + o] = p[0];
         }
     }
 }
