@@ -96,6 +96,23 @@ def dist_setup():
     return ws, rank, local
 
 
+def reduce_max(x: float, device="cpu") -> float:
+    """The maximum of x over all ranks (x itself when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank_per_step: int, world_size: int, steps: int, max_seconds: float) -> float:
+    """Units processed by all ranks divided by the slowest rank's time: every
+    rank runs its own replica of the step (tokens shard with no collective)."""
+    return units_per_rank_per_step * world_size * steps / max_seconds
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -180,11 +197,7 @@ def run_ours(args):
     if ws > 1:
         dist.barrier()
     ck = clocks.stop()
-    ms = t0.elapsed_time(t1)
-    if ws > 1:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = reduce_max(t0.elapsed_time(t1), dev)
     router_ms = [evs[s][l][0].elapsed_time(evs[s][l][1]) for s in range(args.steps) for l in range(LAYERS)]
     gemm_ms = [evs[s][l][2].elapsed_time(evs[s][l][3]) for s in range(args.steps) for l in range(LAYERS)]
     assert bi.bi_get_last_device_error() == 0
@@ -213,17 +226,12 @@ def run_ours(args):
         stream.wait_stream(side)
         res_h.copy_(hashes, non_blocking=True)
         torch.cuda.synchronize()
-    e2e_s = time.perf_counter() - w0
-    if ws > 1:
-        tt = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_s = float(tt.item())
+    e2e_s = reduce_max(time.perf_counter() - w0, dev)
     h2d = LAYERS * (M * H * 4 + M * G_K * 2)
     d2h = M * K_TOP * 8 + N_REQ * 8
 
     hbm, bf16_burst, bf16_sus, src = peaks()
-    tokens = M * ws * args.steps
-    value = tokens / (ms / 1e3)
+    value = whole_job_rate(M, ws, args.steps, ms / 1e3)
     g_avg = statistics.mean(gemm_ms) / 1e3
     r_avg = statistics.mean(router_ms) / 1e3
     g_flop = 2.0 * M * G_N * G_K
@@ -254,7 +262,7 @@ def run_ours(args):
                             "traffic": None, "algorithmic_bytes": r_bytes,
                             "hbm_time_frac": (r_bytes / (hbm * 1e9)) / r_avg,
                             "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 x 2070 MHz"},
-        "e2e": {"value": M * ws * e2e_steps / e2e_s, "unit": "tokens/s",
+        "e2e": {"value": whole_job_rate(M, ws, e2e_steps, e2e_s), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_layer * LAYERS * args.steps,
         "clocks": ck,
@@ -350,13 +358,16 @@ def cpu_baseline(budget_s: float = 15.0):
 
 
 def run_reference(args):
+    """The reference arm: the CPU oracle, as it stands, on this host; rank 0
+    alone under torchrun (the other ranks exit without work).  Each step is
+    a bounded sample of --cpu-seconds of oracle time."""
     ws, rank, _ = dist_setup()
     if rank != 0:
         return
-    budget = max(5.0, min(30.0, 60.0 / max(1, args.steps)))
+    budget = args.cpu_seconds
     vals = []
     for _ in range(args.warmup):
-        cpu_baseline(budget_s=1.0)
+        cpu_baseline(budget_s=min(1.0, budget))
     t = time.perf_counter()
     for _ in range(args.steps):
         vals.append(cpu_baseline(budget_s=budget))

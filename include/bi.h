@@ -234,6 +234,17 @@ BI_API const char *bi_status_string(bi_status st);
  */
 BI_API bi_status bi_get_last_device_error(void);
 
+/*
+ * Self-test of the device-side failure path (no counterpart on the source
+ * pages): launches one thread that waits on a barrier nothing ever completes,
+ * with a wait bound of limit_us microseconds (1 .. 2,000,000).  The wait gives
+ * up, records BI_ERR_TIMEOUT in the sticky device error word and the kernel
+ * returns normally: bi_get_last_device_error() then reports BI_ERR_TIMEOUT and
+ * the context stays usable.  No kernel of this library traps or spins
+ * without a bound; this is how that property is checked on a GPU.
+ */
+BI_API bi_status bi_selftest_wait_timeout(uint32_t limit_us, bi_stream s);
+
 /* ABI version of this header: bumps on any incompatible change. */
 #define BI_ABI_VERSION 1
 BI_API int32_t bi_abi_version(void);

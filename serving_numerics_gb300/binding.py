@@ -30,6 +30,7 @@ SIGNATURES = {
     "bi_status_string": (C.c_char_p, [C.c_int]),
     "bi_get_last_device_error": (C.c_int, []),
     "bi_abi_version": (C.c_int32, []),
+    "bi_selftest_wait_timeout": (C.c_int, [C.c_uint32, _P]),
 }
 
 _lib = None
@@ -136,6 +137,10 @@ def bi_get_last_device_error() -> int:
 
 def bi_abi_version() -> int:
     return load().bi_abi_version()
+
+
+def bi_selftest_wait_timeout(limit_us: int, stream=None) -> int:
+    return load().bi_selftest_wait_timeout(limit_us, _stream(stream))
 
 
 # ------------------------------------------------------------- tensor helpers

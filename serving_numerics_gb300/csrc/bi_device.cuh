@@ -87,8 +87,8 @@ __device__ __forceinline__ unsigned int load_volatile(const unsigned int *p)
 // drains in milliseconds instead of two seconds per wait.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned int *err,
-                                          unsigned int where)
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t *bar, uint32_t parity, unsigned int *err,
+                                                unsigned int where, uint64_t limit_ns)
 {
     const uint32_t addr = smem_u32(bar);
     if (mbar_try_wait(addr, parity)) return true;
@@ -97,12 +97,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsign
         if (mbar_try_wait(addr, parity)) return true;
         if ((i & 255u) == 0) {
             if (load_volatile(err) != 0u) return false;
-            if (global_ns() - t0 > kWaitLimitNs) {
+            if (global_ns() - t0 > limit_ns) {
                 report_error(err, 5u, where);
                 return false;
             }
         }
     }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned int *err,
+                                          unsigned int where)
+{
+    return mbar_wait_limit(bar, parity, err, where, kWaitLimitNs);
 }
 
 // 3-D tiled TMA load into shared memory, completing on `bar`.

@@ -2,6 +2,7 @@
 // encoding and the small ABI utilities (status strings, version).
 #include <mutex>
 
+#include "bi_device.cuh"
 #include "bi_internal.h"
 
 namespace bi {
@@ -79,9 +80,35 @@ bi_status encode_tiled(CUtensorMap *map, CUtensorMapDataType dt, uint32_t rank,
     return r == CUDA_SUCCESS ? BI_OK : BI_ERR_CUDA;
 }
 
+namespace {
+// One thread waits on an mbarrier that nothing ever arrives at; the bounded
+// wait gives up after limit_ns and records BI_ERR_TIMEOUT (where = 0xFE).
+__global__ void selftest_wait_kernel(unsigned int *err, unsigned long long limit_ns)
+{
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        mbar_init_fence();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) mbar_wait_limit(&bar, 0, err, 0xFEu, limit_ns);
+}
+}  // namespace
+
 }  // namespace bi
 
 extern "C" {
+
+bi_status bi_selftest_wait_timeout(uint32_t limit_us, bi_stream s)
+{
+    if (limit_us == 0 || limit_us > 2000000u) return BI_ERR_INVALID_ARG;
+    bi::Device *d = nullptr;
+    bi_status st = bi::current_device(&d);
+    if (st != BI_OK) return st;
+    bi::selftest_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(s)>>>(d->err,
+                                                                          1000ull * limit_us);
+    return bi::from_cuda(cudaGetLastError());
+}
 
 const char *bi_status_string(bi_status st)
 {

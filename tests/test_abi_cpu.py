@@ -25,7 +25,7 @@ def declared_symbols():
 
 def test_header_declares_the_abi():
     names = declared_symbols()
-    for want in ("bi_router_topk", "bi_shared_gate", "bi_gemm_bf16", "bi_route_trace_hash",
+    for want in ("bi_router_topk", "bi_shared_gate", "bi_gemm_bf16", "bi_route_trace_hash", "bi_selftest_wait_timeout",
                  "bi_status_string", "bi_get_last_device_error", "bi_abi_version"):
         assert want in names
 
@@ -115,3 +115,8 @@ def test_hash_validation(lib, offs, M, k, n, want):
 def test_hash_too_many_ranges(lib):
     p, keep = _offs([0] * 300)
     assert lib.bi_route_trace_hash(FAKE, 5, 4, p, 299, None, FAKE, None) == 2
+
+
+def test_selftest_validation(lib):
+    assert lib.bi_selftest_wait_timeout(0, None) == 1
+    assert lib.bi_selftest_wait_timeout(2000001, None) == 1
