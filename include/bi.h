@@ -11,8 +11,8 @@
  *       (a router GEMV whose library picks its reduction order by M moves a
  *       request's logits when co-arrivals change M), "16% of routing
  *       decisions" (top-k turns that drift into different expert sets),
- *       "The fix: m-invariant twins" (one fixed per-row reduction order,
- *       independent of how many rows share the launch).
+ *       "The fix: m-invariant twins" (one fixed reduction order per row,
+ *       whatever the number of rows in the launch).
  *  [P3] "The Illusion of Determinism in Disaggregated Inference": "The
  *       engineering cost of determinism" (cache hit vs miss runs the GEMM at
  *       another M), "The low-level math of tile shapes" (tile shape chosen by
@@ -83,7 +83,7 @@ typedef struct CUstream_st *bi_stream;
  * its ranking), [P4] intro and "Why it is not a defect" (bf16-logit gate,
  * lowest-index tie-break), [P4] "Why a value tap could never have said
  * this" (margin = smallest selected minus largest rejected logit, also in
- * ULPs of the logit dtype under the sign-magnitude total order).
+ * ULPs of the logit dtype ordered by sign and then magnitude).
  *
  *   x           [M, H]  in_dtype   token hidden states
  *   w_gate      [E, H]  in_dtype   router weight (one row per expert)
@@ -134,9 +134,9 @@ BI_API bi_status bi_router_topk(const void *x, const void *w_gate, bi_dtype in_d
  * bi_shared_gate -- the one-output shared-expert gate: dot = X[m,:] . w_sg,
  * gate = 1 / (1 + exp(-dot)).
  *
- * Defined by [P1] "m-scan: the staircase" (the shared-expert gate dot, one
- * output per token) and [P1] "The fix: m-invariant twins" (sigmoid_dot_rows
- * with a fixed per-row order).  Same reduction order as bi_router_topk.
+ * Defined by [P1] "m-scan: the staircase" (a single-output dot product per
+ * token that gates the shared expert) and [P1] "The fix: m-invariant twins"
+ * (sigmoid_dot_rows, reducing each row in one fixed order).  Same reduction order as bi_router_topk.
  *
  *   x            [M, H] f32;  w_sg [H] f32
  *   dot_out      [M] f32 required;  sigmoid_out [M] f32 optional (NULL)
@@ -169,10 +169,10 @@ BI_API bi_status bi_gemm_bf16(const void *A, const void *B, void *C, int32_t M, 
  * bi_route_trace_hash -- per-request route hash: 64-bit FNV-1a over the
  * selected expert SETS of a range of token rows.
  *
- * Defined by [P4] "Why a value tap could never have said this": per call, an
- * FNV-1a hash of every token's sorted id list, so that comparing two arms is
- * one comparison (the combine over the k slots is order-invariant, so the
- * set, not the ranking, is what is compared).
+ * Defined by [P4] "Why a value tap could never have said this": one FNV-1a
+ * value per call over the tokens' sorted id lists, so that two runs compare
+ * with a single equality test (the combine over the k slots ignores their
+ * order, so the set, not the ranking, is what is compared).
  *
  *   ids          [M, k] int32 (device), as written by bi_router_topk
  *   row_offsets  HOST array [n_ranges + 1], non-decreasing, 0 <= . <= M:

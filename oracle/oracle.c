@@ -94,8 +94,8 @@ float orc_double_to_f32(double v) { return (float)v; }
 
 /*
  * Sign-magnitude total order on raw bit patterns ([P4] "Why a value tap
- * could never have said this": the margin is counted in ULPs under the
- * sign-magnitude total order).  Positive patterns map to themselves,
+ * could never have said this": the margin is also reported as a count of
+ * representable steps, ordering patterns by sign and magnitude).  Positive patterns map to themselves,
  * negative ones to minus their magnitude, so +0 and -0 both map to 0 and
  * adjacent representable values differ by exactly 1.
  */
@@ -157,7 +157,7 @@ void orc_router_absdot_f32in(const float *X, int64_t ldx, const float *W, int64_
 /* ------------------------------------------------------------------ */
 /* Top-k selection with the lowest-index tie-break                     */
 /* ([P1] "m-scan": top_k(8 of 256); [P4] intro: at an exact tie the    */
-/* lowest-index tie-break decides the selection)                       */
+/* the selection at an exact tie falls to the lower index)                       */
 /* ------------------------------------------------------------------ */
 
 /* a ranks strictly above b?  NaN ranks above every number (and NaNs
@@ -233,7 +233,7 @@ void orc_softmax_selected(const double *logits, int64_t M, int32_t E, int32_t k,
 /* Routing margin ([P1] "16% of routing decisions": routing margins;   */
 /* [P4] "Why a value tap ...": smallest selected minus largest         */
 /* rejected logit, and the same gap counted in ULPs of the logit dtype */
-/* under the sign-magnitude total order)                               */
+/* ordered by sign and then magnitude)                               */
 /* ------------------------------------------------------------------ */
 
 static void margin_endpoints(const double *row, int32_t E, const int32_t *ids, int32_t k,
@@ -349,8 +349,8 @@ void orc_gemm_bf16(const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ld
 }
 
 /* ------------------------------------------------------------------ */
-/* Route-trace hash ([P4] "Why a value tap ...": per call, an FNV-1a   */
-/* hash of every token's sorted expert list)                           */
+/* Route-trace hash ([P4] "Why a value tap ...": one FNV-1a value per  */
+/* call over the tokens' expert lists, each sorted first)              */
 /* ------------------------------------------------------------------ */
 
 /* 64-bit FNV-1a (Fowler/Noll/Vo): for each byte, xor it into the hash,

@@ -1,7 +1,7 @@
 // bi_hash.cu -- bi_route_trace_hash: 64-bit FNV-1a over the selected expert
 // sets of ranges of token rows ("diag(MODEL-MM-QWEN4-EXP): the MoE expert
 // selections DIFFER ...", section "Why a value tap could never have said
-// this": per call, an FNV-1a hash of every token's sorted id list).
+// this": one FNV-1a value per call over the tokens' sorted id lists).
 //
 // FNV-1a is one sequential chain over bytes, so a range is walked by one
 // warp: the 32 lanes each load and sort one row (an odd-even transposition
