@@ -113,10 +113,14 @@ typedef struct CUstream_st *bi_stream;
  * Logits must be finite for the weights and margins to be meaningful (a
  * NaN ranks above every number and ties other NaNs by index).
  *
- * Scratch: for mid-size batches the partitions of a tile are spread over
- * several thread blocks whose partial sums meet in a library-owned device
- * buffer (allocated once per device on the first call that needs it, never
- * freed before exit).  Make a first call before capturing a CUDA graph.
+ * Scratch: for batches of more than 64 rows that do not fill whole waves
+ * of tiles, the partitions of some tiles (all of them below one wave; the
+ * last rows' beyond it) are spread over several thread blocks whose partial
+ * sums meet in a library-owned device buffer (grown on the first call that
+ * needs more, one buffer per device, never freed before exit).  Make a first
+ * call at the largest M before capturing a CUDA graph.  Two calls that could
+ * run at the same time on one device (different streams with no event
+ * ordering them) must not both need the buffer.
  *
  * Ordering: the kernels start streaming w_gate before they wait for the
  * preceding kernel in the stream (programmatic dependent launch); x is read

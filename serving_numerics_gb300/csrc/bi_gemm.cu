@@ -22,8 +22,13 @@
 //   warps 2..5  epilogue: tcgen05.ld of their 32-lane quarter, bf16 pack,
 //               16-byte global stores; releases the accumulator buffer
 // Double-buffered accumulators let the epilogue of tile t overlap the MMAs
-// of tile t+1.  Every wait on an mbarrier is bounded (about 2 s); on expiry
-// the kernel records BI_ERR_TIMEOUT in the device error word and carries on.
+// of tile t+1.  When the tiles are more than one wave but do not fill the
+// last one, the tiles of that last partial wave are done as two 128 x 128
+// halves each (N = 128 tensor-core steps), so it takes about half the time
+// of a full wave; each output element still gets the same 16-deep steps in
+// the same K order.  Every wait on an mbarrier is bounded (about 2 s); on
+// expiry the kernel records BI_ERR_TIMEOUT in the device error word and
+// carries on.
 #include <cuda_bf16.h>
 
 #include "bi_device.cuh"
@@ -44,8 +49,24 @@ constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;     // 512: the whole tensor memory
 // Instruction descriptor, kind::f16: D f32 (bits 4-5 = 1), A bf16 (bits 7-9
 // = 1), B bf16 (bits 10-12 = 1), A and B K-major (bits 15, 16 = 0),
 // N >> 3 in bits 17-22, M >> 4 in bits 24-28.
-constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
-                           ((uint32_t)(BM >> 4) << 24);
+constexpr uint32_t idesc_n(int n)
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
+constexpr uint32_t IDESC = idesc_n(BN), IDESC_HALF = idesc_n(BN / 2);
+
+// Work item i of a launch: items below n_full are whole tiles (tile = i);
+// the rest are halves of the tiles from n_full on.  Returns the tile and
+// sets `half` to -1 for a whole tile, else 0 or 1 (which 128 columns).
+__device__ __forceinline__ int item_tile(int i, int n_full, int &half)
+{
+    if (i < n_full) {
+        half = -1;
+        return i;
+    }
+    half = (i - n_full) & 1;
+    return n_full + ((i - n_full) >> 1);
+}
 
 // Shared-memory matrix descriptor for a K-major operand laid out by TMA with
 // the 128-byte swizzle: rows of 64 bf16 (128 B), 8-row atoms 1024 B apart
@@ -79,13 +100,14 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t accumulate)
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate)
 {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(IDESC), "r"(accumulate)
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
@@ -121,7 +143,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo, uint32_t hi)
 
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
 gemm_bf16_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__ CUtensorMap tmb,
-                 __nv_bfloat16 *__restrict__ C, int M, int N, int K, long long ldc, unsigned int *err)
+                 const __grid_constant__ CUtensorMap tmb_half, __nv_bfloat16 *__restrict__ C, int M, int N,
+                 int K, long long ldc, int n_full, unsigned int *err)
 {
     pdl_trigger();   // dependents may launch now; each waits before reading our outputs
     extern __shared__ uint8_t smem_raw[];
@@ -132,10 +155,12 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant_
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m_tiles = (M + BM - 1) / BM, n_tiles = (N + BN - 1) / BN;
     const int num_tiles = m_tiles * n_tiles, kblocks = K / BK;
+    const int num_items = n_full + 2 * (num_tiles - n_full);
 
     if (threadIdx.x == 0) {
         prefetch_tmap(&tma);
         prefetch_tmap(&tmb);
+        prefetch_tmap(&tmb_half);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full_bar[s], 1);
             mbar_init(&empty_bar[s], 1);
@@ -157,22 +182,26 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant_
     if (warp == 0) {
         if (lane == 0) {   // TMA producer
             uint32_t it = 0;
-            for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+            for (int item = blockIdx.x; item < num_items; item += gridDim.x) {
+                int half;
+                const int tile = item_tile(item, n_full, half);
                 const int mt = tile % m_tiles, nt = tile / m_tiles;
+                const int n0 = nt * BN + (half > 0 ? BN / 2 : 0);
                 for (int kb = 0; kb < kblocks; ++kb, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
                     mbar_wait(&empty_bar[s], ph ^ 1u, err, 0x21);
                     uint8_t *st = smem + s * STAGE_BYTES;
-                    mbar_arrive_expect_tx(&full_bar[s], STAGE_BYTES);
+                    mbar_arrive_expect_tx(&full_bar[s], half < 0 ? STAGE_BYTES : A_BYTES + B_BYTES / 2);
                     tma_load_2d(st, &tma, &full_bar[s], kb * BK, mt * BM);
-                    tma_load_2d(st + A_BYTES, &tmb, &full_bar[s], kb * BK, nt * BN);
+                    tma_load_2d(st + A_BYTES, half < 0 ? &tmb : &tmb_half, &full_bar[s], kb * BK, n0);
                 }
             }
         }
     } else if (warp == 1) {
         if (lane == 0) {   // MMA issuer
             uint32_t it = 0, tc = 0;
-            for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++tc) {
+            for (int item = blockIdx.x; item < num_items; item += gridDim.x, ++tc) {
+                const uint32_t idesc = item < n_full ? IDESC : IDESC_HALF;
                 const uint32_t b = tc & 1u, tph = (tc >> 1) & 1u;
                 mbar_wait(&tempty_bar[b], tph ^ 1u, err, 0x22);
                 tc_fence_after();
@@ -186,7 +215,7 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant_
 #pragma unroll
                     for (int k = 0; k < BK / UMMA_K; ++k)
                         umma_bf16(d_tmem, sw128_desc(a_addr + k * UMMA_K * 2),
-                                  sw128_desc(b_addr + k * UMMA_K * 2), (kb | k) != 0 ? 1u : 0u);
+                                  sw128_desc(b_addr + k * UMMA_K * 2), idesc, (kb | k) != 0 ? 1u : 0u);
                     umma_commit(&empty_bar[s]);       // stage reusable once these MMAs finish
                 }
                 umma_commit(&tfull_bar[b]);           // accumulator ready for the epilogue
@@ -197,18 +226,21 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant_
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
         uint32_t tc = 0;
-        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++tc) {
+        for (int item = blockIdx.x; item < num_items; item += gridDim.x, ++tc) {
+            int half;
+            const int tile = item_tile(item, n_full, half);
             const int mt = tile % m_tiles, nt = tile / m_tiles;
+            const int nbase = nt * BN + (half > 0 ? BN / 2 : 0), nchunks = half < 0 ? BN / 32 : BN / 64;
             const uint32_t b = tc & 1u, tph = (tc >> 1) & 1u;
             mbar_wait(&tfull_bar[b], tph, err, 0x24);
             tc_fence_after();
             const int m = mt * BM + row;
             __nv_bfloat16 *crow = C + (size_t)(m < M ? m : 0) * (size_t)ldc;
 #pragma unroll 1
-            for (int chunk = 0; chunk < BN / 32; ++chunk) {
+            for (int chunk = 0; chunk < nchunks; ++chunk) {
                 uint32_t r[32];
                 tmem_ld32(tmem_base + ((uint32_t)(quad * 32) << 16) + b * ACC_COLS + chunk * 32, r);
-                const int n0 = nt * BN + chunk * 32;
+                const int n0 = nbase + chunk * 32;
                 if (m < M) {
 #pragma unroll
                     for (int g = 0; g < 4; ++g) {
@@ -264,19 +296,25 @@ extern "C" bi_status bi_gemm_bf16(const void *A, const void *B, void *C, int32_t
                                CU_TENSOR_MAP_SWIZZLE_128B)) != BI_OK)
             return st;
     }
-    {
+    alignas(64) CUtensorMap tmb_half;
+    for (int h = 0; h < 2; ++h) {
         const uint64_t dims[2] = {(uint64_t)K, (uint64_t)N};
         const uint64_t strides[1] = {(uint64_t)ldb * 2};
-        const uint32_t box[2] = {(uint32_t)BK, (uint32_t)BN};
-        if ((st = encode_tiled(&tmb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, dims, strides, box,
+        const uint32_t box[2] = {(uint32_t)BK, (uint32_t)(h ? BN / 2 : BN)};
+        if ((st = encode_tiled(h ? &tmb_half : &tmb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, dims, strides, box,
                                CU_TENSOR_MAP_SWIZZLE_128B)) != BI_OK)
             return st;
     }
     if ((st = set_smem_once(d, KID_GEMM, gemm_bf16_kernel, GEMM_SMEM)) != BI_OK) return st;
 
+    // whole tiles for every full wave; the tiles of a last partial wave go
+    // as halves when that keeps them to one round (2 * rest <= blocks)
     const long long tiles = (long long)((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+    if (tiles > (1ll << 30)) return BI_ERR_UNSUPPORTED_SHAPE;
     const int grid = (int)(tiles < d->sm_count ? tiles : d->sm_count);
+    const long long rest = tiles % grid;
+    const long long n_full = (tiles > grid && rest != 0 && 2 * rest <= grid) ? tiles - rest : tiles;
     return launch_pdl(gemm_bf16_kernel, dim3(grid), dim3(GEMM_THREADS), (size_t)GEMM_SMEM,
-                      reinterpret_cast<cudaStream_t>(s), tma, tmb, static_cast<__nv_bfloat16 *>(C),
-                      (int)M, (int)N, (int)K, (long long)ldc, d->err);
+                      reinterpret_cast<cudaStream_t>(s), tma, tmb, tmb_half, static_cast<__nv_bfloat16 *>(C),
+                      (int)M, (int)N, (int)K, (long long)ldc, (int)n_full, d->err);
 }

@@ -5,14 +5,19 @@
 //
 // FNV-1a is one sequential chain over bytes, so a range is walked by one
 // warp: the 32 lanes each load and sort one row (an odd-even transposition
-// network on registers, ids beyond k padded with INT_MAX), then every lane
-// folds the 32 sorted rows into the same chain, receiving each id by
-// shuffle, and lane 0 stores the result.  The chain's critical path is one
-// xor and one wide multiply per byte.  Ranges (requests) are hashed in
-// parallel, one warp each.
+// network on registers, ids beyond k padded with INT_MAX); then every lane
+// folds the rows into the same chain, receiving each row's ids by shuffle
+// one row ahead of the fold, and lane 0 stores the result.  Ranges
+// (requests) are hashed in parallel, one warp each; with one warp per
+// scheduler the fold's dependent chain is the kernel's whole cost.
 //
 // Per byte: h ^= byte; h *= 0x100000001b3 (mod 2^64).  Per row: the k ids
-// in ascending order, each as 4 little-endian bytes.
+// in ascending order, each as 4 little-endian bytes.  A zero byte leaves
+// h ^ byte = h, so the three steps of an id's zero high bytes are plain
+// multiplications by the prime and fold into the step of its low byte: an
+// id in [0, 256) is one step, h = (h ^ id) * prime^4 (mod 2^64, the same
+// value).  A row whose ids all lie in [0, 256) takes that path; any other
+// row takes the four byte steps per id.
 #include <limits.h>
 
 #include "bi_device.cuh"
@@ -26,17 +31,45 @@ struct HashRanges {
 };
 
 constexpr int kHashWarps = 4;
+constexpr uint64_t kFnvPrime = 0x100000001B3ull;
 
-// One FNV-1a byte step on the hash held as two 32-bit halves:
-// h = (h ^ byte) * (2^40 + 0x1b3) mod 2^64.  With l = lo ^ byte, the product
-// is l*0x1b3 (64-bit) + (hi*0x1b3 + (l << 8)) * 2^32, keeping the dependent
-// chain at one xor and one wide multiply per byte.
-__device__ __forceinline__ void fnv_step(uint32_t &lo, uint32_t &hi, uint32_t byte)
+constexpr uint64_t prime_pow(int n) { return n == 0 ? 1ull : kFnvPrime * prime_pow(n - 1); }
+
+// h = (h with its low half replaced by l) * c mod 2^64, on 32-bit halves;
+// the chain through lo is one multiply per step
+__device__ __forceinline__ void fnv_mul(uint32_t &lo, uint32_t &hi, uint32_t l, uint64_t c)
 {
-    const uint32_t l = lo ^ byte;
-    const uint64_t p = (uint64_t)l * 0x1B3u;
-    lo = (uint32_t)p;
-    hi = hi * 0x1B3u + (uint32_t)(p >> 32) + (l << 8);
+    const uint32_t clo = (uint32_t)c, chi = (uint32_t)(c >> 32);
+    hi = hi * clo + __umulhi(l, clo) + l * chi;
+    lo = l * clo;
+}
+
+// (lo, hi) <- (lo ^ x) * c when `on`, else unchanged; no branch, so the
+// chain never waits on branch resolution
+__device__ __forceinline__ void fnv_step_sel(uint32_t &lo, uint32_t &hi, uint32_t x, uint64_t c, bool on)
+{
+    uint32_t nlo = lo, nhi = hi;
+    fnv_mul(nlo, nhi, lo ^ x, c);
+    lo = on ? nlo : lo;
+    hi = on ? nhi : hi;
+}
+
+template <int KMAX>
+__device__ __forceinline__ void fold_row(uint32_t &lo, uint32_t &hi, const uint32_t (&u)[KMAX], int k,
+                                         bool one_byte)
+{
+    if (one_byte) {
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) fnv_step_sel(lo, hi, u[j], prime_pow(4), j < k);
+    } else {
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) {
+            fnv_step_sel(lo, hi, u[j] & 0xFFu, kFnvPrime, j < k);
+            fnv_step_sel(lo, hi, (u[j] >> 8) & 0xFFu, kFnvPrime, j < k);
+            fnv_step_sel(lo, hi, (u[j] >> 16) & 0xFFu, kFnvPrime, j < k);
+            fnv_step_sel(lo, hi, u[j] >> 24, kFnvPrime, j < k);
+        }
+    }
 }
 
 template <int KMAX>
@@ -52,11 +85,17 @@ route_hash_kernel(const int32_t *__restrict__ ids, int k, HashRanges rr, int n_r
     const uint64_t h0 = basis ? basis[r] : 0xCBF29CE484222325ull;
     uint32_t hlo = (uint32_t)h0, hhi = (uint32_t)(h0 >> 32);
     const int b = rr.off[r], e = rr.off[r + 1];
-    for (int row0 = b; row0 < e; row0 += 32) {
-        const int row = row0 + lane;
-        int32_t v[KMAX];
+    // each lane's row of the next 32 is loaded while the current 32 fold
+    int32_t v[KMAX], vn[KMAX];
 #pragma unroll
-        for (int j = 0; j < KMAX; ++j) v[j] = (row < e && j < k) ? ids[(size_t)row * k + j] : INT_MAX;
+    for (int j = 0; j < KMAX; ++j) vn[j] = (b + lane < e && j < k) ? ids[(size_t)(b + lane) * k + j] : INT_MAX;
+    for (int row0 = b; row0 < e; row0 += 32) {
+        const int nrow = row0 + 32 + lane;
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) {
+            v[j] = vn[j];
+            vn[j] = (nrow < e && j < k) ? ids[(size_t)nrow * k + j] : INT_MAX;
+        }
         // odd-even transposition sort: KMAX rounds make any KMAX values ascending
 #pragma unroll
         for (int round = 0; round < KMAX; ++round) {
@@ -67,18 +106,23 @@ route_hash_kernel(const int32_t *__restrict__ ids, int k, HashRanges rr, int n_r
                 v[j + 1] = hi;
             }
         }
-        const int nrows = min(32, e - row0);
-        for (int t = 0; t < nrows; ++t) {
+        // rows whose ids all lie in [0, 256): sorted, so the ends decide
+        int32_t last = v[0];
 #pragma unroll
-            for (int j = 0; j < KMAX; ++j) {
-                const uint32_t u = (uint32_t)__shfl_sync(0xFFFFFFFFu, v[j], t);
-                if (j < k) {
-                    fnv_step(hlo, hhi, u & 0xFFu);
-                    fnv_step(hlo, hhi, (u >> 8) & 0xFFu);
-                    fnv_step(hlo, hhi, (u >> 16) & 0xFFu);
-                    fnv_step(hlo, hhi, u >> 24);
-                }
-            }
+        for (int j = 1; j < KMAX; ++j)
+            if (j < k) last = v[j];
+        const uint32_t one_byte = __ballot_sync(0xFFFFFFFFu, v[0] >= 0 && last < 256);
+        const int nrows = min(32, e - row0);
+        uint32_t cur[KMAX], nxt[KMAX];
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) cur[j] = (uint32_t)__shfl_sync(0xFFFFFFFFu, v[j], 0);
+        for (int t = 0; t < nrows; ++t) {
+            const int tn = t + 1 < nrows ? t + 1 : t;         // the next row's ids travel meanwhile
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j) nxt[j] = (uint32_t)__shfl_sync(0xFFFFFFFFu, v[j], tn);
+            fold_row<KMAX>(hlo, hhi, cur, k, (one_byte >> t) & 1u);
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j) cur[j] = nxt[j];
         }
     }
     if (lane == 0) out[r] = ((uint64_t)hhi << 32) | hlo;

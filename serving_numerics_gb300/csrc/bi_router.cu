@@ -135,9 +135,10 @@ __device__ __forceinline__ void block_bf16(float (&acc)[8][8], const uint8_t *xs
 enum OutMode : int { OUT_F32 = 0, OUT_BF16 = 1, OUT_PARTIAL = 2 };
 
 template <typename InT, int C>
-__global__ void __launch_bounds__(ProjCfg<InT, C>::THREADS, 1)
+__global__ void __launch_bounds__(ProjCfg<InT, C>::THREADS, C)     // 16 warps per SM in every split
 router_proj_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
-                   int M, int E, int H, int out_mode, void *__restrict__ out, unsigned int *err)
+                   int M, int m_base, int E, int H, int out_mode, void *__restrict__ out,
+                   unsigned int *err)
 {
     pdl_trigger();   // dependents may launch now; each waits before reading our outputs
     using Cfg = ProjCfg<InT, C>;
@@ -149,7 +150,7 @@ router_proj_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int e_tile = blockIdx.x / C, g = blockIdx.x % C;
-    const int m0 = blockIdx.y * kTileM, e0 = e_tile * kTileE, q0 = g * NPL;
+    const int m0 = m_base + blockIdx.y * kTileM, e0 = e_tile * kTileE, q0 = g * NPL;
     const int ns = (H + kSlab - 1) / kSlab;
     const int tg = lane & 3, eg = lane >> 2;
 
@@ -279,8 +280,8 @@ router_proj_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
                 static_cast<float *>(out)[o] = p[0];
             else if (out_mode == OUT_BF16)
                 static_cast<__nv_bfloat16 *>(out)[o] = __float2bfloat16_rn(p[0]);
-            else
-                static_cast<float *>(out)[(size_t)g * M * E + o] = p[0];
+            else        // group sums of rows [m_base, M), group-major
+                static_cast<float *>(out)[((size_t)g * (M - m_base) + (m - m_base)) * E + e0 + e] = p[0];
         }
     }
 }
@@ -312,11 +313,13 @@ constexpr int kSelWarps = 8;
 
 // One warp per token: finish the tree (C > 1), round to the logit dtype,
 // then k+1 rounds of warp arg-max (value desc, index asc).  Round k yields
-// the largest rejected logit for the margin.
+// the largest rejected logit for the margin.  Rows below m_split already
+// have their logits (the projection ran whole for them); rows from m_split
+// on have C group sums in `part`, laid out group-major over those rows.
 template <int EPLM>
 __global__ void __launch_bounds__(32 * kSelWarps)
-router_select_kernel(const float *__restrict__ part, int C, void *logits, int logit_bf16, int M,
-                     int E, int k, int32_t *__restrict__ ids, float *__restrict__ weights,
+router_select_kernel(const float *__restrict__ part, int C, int m_split, void *logits, int logit_bf16,
+                     int M, int E, int k, int32_t *__restrict__ ids, float *__restrict__ weights,
                      float *__restrict__ margin, int32_t *__restrict__ ulps)
 {
     pdl_trigger();   // dependents may launch now; each waits before reading our outputs
@@ -329,7 +332,7 @@ router_select_kernel(const float *__restrict__ part, int C, void *logits, int lo
     // gather this lane's logits (experts lane + 32 i), all loads issued first
     float v[EPLM];
     const size_t row = (size_t)m * E + lane;
-    if (C == 1) {
+    if (m < m_split) {
         if (logit_bf16) {
             const __nv_bfloat16 *lp = static_cast<const __nv_bfloat16 *>(logits) + row;
 #pragma unroll
@@ -342,12 +345,13 @@ router_select_kernel(const float *__restrict__ part, int C, void *logits, int lo
     } else {
         // finish the pairwise tree over the C group sums, then round to the
         // logit dtype and store the logits
-        const size_t gs = (size_t)M * E;
+        const size_t gs = (size_t)(M - m_split) * E;
+        const size_t prow = (size_t)(m - m_split) * E + lane;
 #pragma unroll
         for (int i = 0; i < EPLM; ++i) {
             float p[16];
 #pragma unroll
-            for (int q = 0; q < 16; ++q) p[q] = (i < epl && q < C) ? part[(size_t)q * gs + row + 32 * i] : 0.0f;
+            for (int q = 0; q < 16; ++q) p[q] = (i < epl && q < C) ? part[(size_t)q * gs + prow + 32 * i] : 0.0f;
 #pragma unroll
             for (int d = 1; d < 16; d *= 2)
                 if (d < C) {
@@ -651,8 +655,8 @@ bi_status launch_gemv(Device *d, const void *x, const void *w, int M, int E, int
 }
 
 template <typename InT, int C>
-bi_status launch_proj(Device *d, const void *x, const void *w, int M, int E, int H, int out_mode, void *out,
-                      cudaStream_t s, int kid)
+bi_status launch_proj(Device *d, const void *x, const void *w, int M, int m_base, int m_end, int E, int H,
+                      int out_mode, void *out, cudaStream_t s, int kid)
 {
     using Cfg = ProjCfg<InT, C>;
     auto kern = router_proj_kernel<InT, C>;
@@ -674,60 +678,79 @@ bi_status launch_proj(Device *d, const void *x, const void *w, int M, int E, int
         const uint32_t box[2] = {(uint32_t)(Cfg::PB * kBlk), (uint32_t)kTileE};
         if ((st = encode_tiled(&tmw, dt, 2, w, dims, strides, box, sw)) != BI_OK) return st;
     }
-    dim3 grid(((E + kTileE - 1) / kTileE) * C, (M + kTileM - 1) / kTileM);
-    return launch_pdl(kern, grid, dim3(Cfg::THREADS), (size_t)Cfg::SMEM, s, tmx, tmw, M, E, H,
+    // rows [m_base, m_end); the tensor maps span all M rows, and a tile
+    // never crosses m_end because m_end is M or a multiple of the tile
+    dim3 grid(((E + kTileE - 1) / kTileE) * C, (m_end - m_base + kTileM - 1) / kTileM);
+    return launch_pdl(kern, grid, dim3(Cfg::THREADS), (size_t)Cfg::SMEM, s, tmx, tmw, M, m_base, E, H,
                       out_mode, out, d->err);
 }
 
 template <typename InT>
-bi_status launch_proj_c(Device *d, int C, const void *x, const void *w, int M, int E, int H, int out_mode,
-                        void *out, cudaStream_t s)
+bi_status launch_proj_c(Device *d, int C, const void *x, const void *w, int M, int m_base, int m_end, int E,
+                        int H, int out_mode, void *out, cudaStream_t s)
 {
     const int base = KID_ROUTER_PROJ + (sizeof(InT) == 4 ? 0 : 5);
     switch (C) {
-    case 1: return launch_proj<InT, 1>(d, x, w, M, E, H, out_mode, out, s, base + 0);
-    case 2: return launch_proj<InT, 2>(d, x, w, M, E, H, out_mode, out, s, base + 1);
-    case 4: return launch_proj<InT, 4>(d, x, w, M, E, H, out_mode, out, s, base + 2);
-    case 8: return launch_proj<InT, 8>(d, x, w, M, E, H, out_mode, out, s, base + 3);
-    default: return launch_proj<InT, 16>(d, x, w, M, E, H, out_mode, out, s, base + 4);
+    case 1: return launch_proj<InT, 1>(d, x, w, M, m_base, m_end, E, H, out_mode, out, s, base + 0);
+    case 2: return launch_proj<InT, 2>(d, x, w, M, m_base, m_end, E, H, out_mode, out, s, base + 1);
+    case 4: return launch_proj<InT, 4>(d, x, w, M, m_base, m_end, E, H, out_mode, out, s, base + 2);
+    case 8: return launch_proj<InT, 8>(d, x, w, M, m_base, m_end, E, H, out_mode, out, s, base + 3);
+    default: return launch_proj<InT, 16>(d, x, w, M, m_base, m_end, E, H, out_mode, out, s, base + 4);
     }
 }
 
 template <int EPLM>
 bi_status launch_select1(Device *d, dim3 grid, dim3 block, cudaStream_t cs, const float *pp, int C,
-                         void *logits, int lbf, int M, int E, int k, int32_t *ids, float *w, float *mg,
+                         int m_split, void *logits, int lbf, int M, int E, int k, int32_t *ids, float *w, float *mg,
                          int32_t *mu)
 {
     const int kid = KID_SELECT + (EPLM == 4 ? 0 : EPLM == 8 ? 1 : EPLM == 16 ? 2 : 3);
     bi_status st = set_smem_once(d, kid, router_select_kernel<EPLM>, 0);
     if (st != BI_OK) return st;
-    return launch_pdl(router_select_kernel<EPLM>, grid, block, 0, cs, pp, C, logits, lbf, M, E, k, ids, w, mg, mu);
+    return launch_pdl(router_select_kernel<EPLM>, grid, block, 0, cs, pp, C, m_split, logits, lbf, M, E, k, ids,
+                      w, mg, mu);
 }
 
 bi_status launch_select(Device *d, int epl, dim3 grid, dim3 block, cudaStream_t cs, const float *pp, int C,
-                        void *logits, int lbf, int M, int E, int k, int32_t *ids, float *w, float *mg,
-                        int32_t *mu)
+                        int m_split, void *logits, int lbf, int M, int E, int k, int32_t *ids, float *w,
+                        float *mg, int32_t *mu)
 {
-    if (epl <= 4) return launch_select1<4>(d, grid, block, cs, pp, C, logits, lbf, M, E, k, ids, w, mg, mu);
-    if (epl <= 8) return launch_select1<8>(d, grid, block, cs, pp, C, logits, lbf, M, E, k, ids, w, mg, mu);
-    if (epl <= 16) return launch_select1<16>(d, grid, block, cs, pp, C, logits, lbf, M, E, k, ids, w, mg, mu);
-    return launch_select1<32>(d, grid, block, cs, pp, C, logits, lbf, M, E, k, ids, w, mg, mu);
+    if (epl <= 4) return launch_select1<4>(d, grid, block, cs, pp, C, m_split, logits, lbf, M, E, k, ids, w, mg, mu);
+    if (epl <= 8) return launch_select1<8>(d, grid, block, cs, pp, C, m_split, logits, lbf, M, E, k, ids, w, mg, mu);
+    if (epl <= 16)
+        return launch_select1<16>(d, grid, block, cs, pp, C, m_split, logits, lbf, M, E, k, ids, w, mg, mu);
+    return launch_select1<32>(d, grid, block, cs, pp, C, m_split, logits, lbf, M, E, k, ids, w, mg, mu);
 }
 
 // Batches up to this many tokens take the matrix-vector twin.
 constexpr int kGemvMaxM = 64;
 
-// How many blocks share one tile's 16 partitions: the smallest power of two
-// that gives at least one block per SM, capped at 16 and by the scratch
-// bound.  Any choice gives the same bits; this only trades parallelism for
-// scratch traffic.
-int choose_split(int M, int E, int sms)
+// How the projection's work is cut for a batch of M > kGemvMaxM rows.
+// Rows [0, m_split) run whole: one block holds all 16 partitions of a tile
+// and writes the logits.  Rows [m_split, M) (the tail) are cut into C
+// partition groups per tile, whose sums the selection adds.  Any plan gives
+// the same bits; plans differ only in how well the work fills the SMs.
+// The whole tiles take as many full waves (one tile per SM) as the batch
+// fills, rounded down to whole rows of tiles; the rest is the tail, and C
+// is the largest power of two (at most 16) that still gives every block an
+// SM of its own (tail tiles * C <= SMs) within 16 MiB of group sums.  Split
+// blocks have fewer warps and run best one to an SM: smaller groups that
+// stack several blocks on an SM measured slower.
+struct SplitPlan {
+    int m_split, C;
+};
+
+SplitPlan plan_split(int M, int E, int sms)
 {
-    const long long tiles = (long long)((M + kTileM - 1) / kTileM) * ((E + kTileE - 1) / kTileE);
-    int C = 1;
-    while (C < 16 && tiles * C < sms) C *= 2;
-    while (C > 1 && (long long)C * M * E * 4 > (16ll << 20)) C /= 2;
-    return C;
+    const long long n_et = (E + kTileE - 1) / kTileE, tiles_m = (M + kTileM - 1) / kTileM;
+    const long long waves = tiles_m * n_et / sms;
+    const long long head_tm = waves * sms / n_et;
+    if (head_tm >= tiles_m) return {M, 1};
+    const long long tail = (tiles_m - head_tm) * n_et, tail_rows = M - head_tm * kTileM;
+    int c = 1;
+    while (c < 16 && tail * 2 * c <= sms && 2ll * c * tail_rows * E * 4 <= (16ll << 20)) c *= 2;
+    if (c == 1) return {M, 1};
+    return {(int)(head_tm * kTileM), c};
 }
 
 }  // namespace
@@ -761,34 +784,43 @@ extern "C" bi_status bi_router_topk(const void *x, const void *w_gate, bi_dtype 
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(s);
 
     const bool small = M <= kGemvMaxM;
-    const int C = small ? 1 : choose_split(M, E, d->sm_count);
+    const SplitPlan plan = small ? SplitPlan{M, 1} : plan_split(M, E, d->sm_count);
     void *part = nullptr;
-    if (C > 1) {
-        st = device_scratch(d, (size_t)C * M * E * sizeof(float), &part);
+    if (plan.m_split < M) {
+        st = device_scratch(d, (size_t)plan.C * (M - plan.m_split) * E * sizeof(float), &part);
         if (st != BI_OK) return st;
     }
 
     const bool f32in = in_dtype == BI_F32;
-
     const int lbf = logit_dtype == BI_BF16 ? 1 : 0;
-    const int out_mode = C > 1 ? OUT_PARTIAL : (lbf ? OUT_BF16 : OUT_F32);
-    void *out = C > 1 ? part : logits_out;
-    if (small && M <= kGemvT)
+    if (small && M <= kGemvT) {
         st = f32in ? launch_gemv<float, 1>(d, x, w_gate, M, E, H, lbf, logits_out, cs)
                    : launch_gemv<__nv_bfloat16, 1>(d, x, w_gate, M, E, H, lbf, logits_out, cs);
-    else if (small)
+    } else if (small) {
         st = f32in ? launch_gemv<float, 4>(d, x, w_gate, M, E, H, lbf, logits_out, cs)
                    : launch_gemv<__nv_bfloat16, 4>(d, x, w_gate, M, E, H, lbf, logits_out, cs);
-    else
-        st = f32in ? launch_proj_c<float>(d, C, x, w_gate, M, E, H, out_mode, out, cs)
-                   : launch_proj_c<__nv_bfloat16>(d, C, x, w_gate, M, E, H, out_mode, out, cs);
+    } else {
+        // the tail goes first: it is the shorter launch, and the whole tiles
+        // queue behind it on the SMs it leaves free
+        if (plan.m_split < M) {
+            st = f32in ? launch_proj_c<float>(d, plan.C, x, w_gate, M, plan.m_split, M, E, H, OUT_PARTIAL, part, cs)
+                       : launch_proj_c<__nv_bfloat16>(d, plan.C, x, w_gate, M, plan.m_split, M, E, H, OUT_PARTIAL,
+                                                      part, cs);
+            if (st != BI_OK) return st;
+        }
+        if (plan.m_split > 0) {
+            const int om = lbf ? OUT_BF16 : OUT_F32;
+            st = f32in ? launch_proj_c<float>(d, 1, x, w_gate, M, 0, plan.m_split, E, H, om, logits_out, cs)
+                       : launch_proj_c<__nv_bfloat16>(d, 1, x, w_gate, M, 0, plan.m_split, E, H, om, logits_out, cs);
+        }
+    }
     if (st != BI_OK) return st;
 
     const int epl = E / 32;
     dim3 grid((M + kSelWarps - 1) / kSelWarps), block(32 * kSelWarps);
     const float *pp = static_cast<const float *>(part);
-    return launch_select(d, epl, grid, block, cs, pp, C, logits_out, lbf, M, E, k, ids_out, weights_out,
-                         margin_out, margin_ulps_out);
+    return launch_select(d, epl, grid, block, cs, pp, plan.C, plan.m_split, logits_out, lbf, M, E, k, ids_out,
+                         weights_out, margin_out, margin_ulps_out);
 }
 
 // ---------------------------------------------------------------------------
@@ -858,12 +890,12 @@ extern "C" bi_status bi_router_topk_noalloc(const void *x, const void *w_gate, b
 
     const bool f32in = in_dtype == BI_F32;
     const int lbf = logit_dtype == BI_BF16 ? 1 : 0;
-    st = f32in ? launch_proj_c<float>(d, C, x, w_gate, M, E, H, OUT_PARTIAL, part, cs)
-               : launch_proj_c<__nv_bfloat16>(d, C, x, w_gate, M, E, H, OUT_PARTIAL, part, cs);
+    st = f32in ? launch_proj_c<float>(d, C, x, w_gate, M, 0, M, E, H, OUT_PARTIAL, part, cs)
+               : launch_proj_c<__nv_bfloat16>(d, C, x, w_gate, M, 0, M, E, H, OUT_PARTIAL, part, cs);
     if (st != BI_OK) return st;
     const int epl = E / 32;
     dim3 grid((M + kSelWarps - 1) / kSelWarps), block(32 * kSelWarps);
     const float *pp = static_cast<const float *>(part);
-    return launch_select(d, epl, grid, block, cs, pp, C, logits_out, lbf, M, E, k, ids_out, weights_out,
+    return launch_select(d, epl, grid, block, cs, pp, C, 0, logits_out, lbf, M, E, k, ids_out, weights_out,
                          margin_out, margin_ulps_out);
 }

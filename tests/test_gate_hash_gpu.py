@@ -60,3 +60,26 @@ def test_route_hash_parity(bi, orc):
     h3 = bi.route_hash(torch.from_numpy(perm).cuda(), offs)
     torch.cuda.synchronize()
     assert np.array_equal(h3.cpu().numpy(), h.cpu().numpy())
+
+
+@pytest.mark.parametrize("k", [3, 8, 12, 32])
+def test_route_hash_any_id_values(bi, orc, k):
+    """Ids of every byte length (0, one byte, two, three, four, negative)
+    and every sort width: the kernel folds the high zero bytes of an id into
+    one step, so each length takes its own path; all must equal the oracle's
+    byte-by-byte FNV-1a.  Ranges longer than 32 rows cross the warp's row
+    batches."""
+    import torch
+    g = np.random.default_rng(23 + k)
+    M = 170
+    classes = [np.zeros(1, np.int64), np.arange(1, 256), np.arange(256, 65536, 97),
+               np.arange(65536, 1 << 24, 40009), np.arange(1 << 24, (1 << 31) - 1, 9_000_011),
+               -np.arange(1, 1 << 31, 7_000_003)]
+    pool = np.concatenate(classes)
+    ids = g.choice(pool, size=(M, k)).astype(np.int32)
+    offs = [0, 1, 40, 100, 100, 170]
+    h = bi.route_hash(torch.from_numpy(ids).cuda(), offs)
+    torch.cuda.synchronize()
+    got = h.cpu().numpy().view(np.uint64)
+    for r in range(len(offs) - 1):
+        assert int(got[r]) == orc.route_hash(ids, offs[r], offs[r + 1]), f"range {r}, k={k}"

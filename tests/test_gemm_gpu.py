@@ -83,26 +83,29 @@ def test_gemm_full_size_sampled(bi, orc):
 
 
 def test_gemm_m_invariance_sweep(bi, orc):
-    """Every row at M in {1,19,64,65,75,128,1024,4096,8192} is byte-identical
-    to the same row of the M=8192 product; sampled rows also equal their
-    M=1 solo products.  Self-counting: the number of compared rows is the
-    sum of the M values plus the solo samples."""
+    """Every row at M in {1,19,64,65,75,128,1024,2560,4096,8192} is
+    byte-identical to the same row of the M=8192 product; sampled rows also
+    equal their M=1 solo products.  At M = 2560 and 4096 the tiles of the
+    last partial wave run as 128-column halves (N = 128 tensor-core steps),
+    so those rows also check that the instruction width does not change the
+    bits.  Self-counting: the number of compared rows is the sum of the M
+    values plus the solo samples."""
     N, K = 4096, 4096
     Mmax = 8192
     A = synth.gemm_a(13, Mmax, K)
     B = synth.gemm_b(13, N, K)
     full = gemm(bi, A, B)
     compared = 0
-    for M in (1, 19, 64, 65, 75, 128, 1024, 4096, 8192):
+    for M in (1, 19, 64, 65, 75, 128, 1024, 2560, 4096, 8192):
         C = gemm(bi, A[:M], B)
         assert C.tobytes() == full[:M].tobytes(), f"rows differ at M={M}"
         compared += M
-    solo_rows = [0, 1, 63, 64, 127, 128, 129, 1000, 4095, 8191]
+    solo_rows = [0, 1, 63, 64, 127, 128, 129, 1000, 2559, 4095, 8191]
     for r in solo_rows:
         C = gemm(bi, A[r:r + 1], B)
         assert C.tobytes() == full[r:r + 1].tobytes(), f"row {r} solo differs"
         compared += 1
-    assert compared == 1 + 19 + 64 + 65 + 75 + 128 + 1024 + 4096 + 8192 + len(solo_rows)
+    assert compared == 1 + 19 + 64 + 65 + 75 + 128 + 1024 + 2560 + 4096 + 8192 + len(solo_rows)
     check_close(orc, full, A, B, rows=[0, 8191])
 
 

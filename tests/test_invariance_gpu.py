@@ -48,6 +48,8 @@ def test_tiny_mscan(bi):
 
 
 M_SWEEP = [1, 2, 4, 8, 16, 19, 32] + list(range(35, 65)) + [65, 75, 96, 128, 256, 512, 1024, 2048, 4096]
+# batches past one full wave of tiles, with the request in the split tail
+TAIL_SWEEP = [1235, 1300, 1400, 2500, 3000, 4096]
 
 
 def test_router256_m_sweep(bi):
@@ -85,7 +87,16 @@ def test_router256_m_sweep(bi):
         assert d[off:off + cnt].cpu().numpy().tobytes() == solo_gate[0][:4 * cnt], f"gate dot M={M}"
         assert s[off:off + cnt].cpu().numpy().tobytes() == solo_gate[1][:4 * cnt], f"gate sigmoid M={M}"
         n += 1
-    assert n == len(M_SWEEP) == 46
+    for M in TAIL_SWEEP:
+        off = M - 19                      # the request is the batch's last rows
+        X = np.concatenate([pool[:off], req])
+        out = route(bi, gu.dev_f32(X), W, k)
+        torch.cuda.synchronize()
+        got = rows_bytes(out, off, M)
+        for f in FIELDS:
+            assert got[f] == solo[f], f"{f} differs at M={M} (tail rows)"
+        n += 1
+    assert n == len(M_SWEEP) + len(TAIL_SWEEP) == 52
 
 
 def test_route_trace_760_decisions(bi):

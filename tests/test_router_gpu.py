@@ -1,9 +1,9 @@
 """Router parity: bi_router_topk on the GPU against the CPU oracle.
 
 The library splits each 32x64 tile's 16 partitions over 1, 2, 4, 8 or 16
-thread blocks depending on M; the cases below cover every split in every
-input/logit dtype, including E that is not a multiple of the 64-expert
-tile.
+thread blocks depending on M (beyond one full wave of tiles, only the tail
+rows are split); the cases below cover every split in every input/logit
+dtype, including E that is not a multiple of the 64-expert tile.
 
 Logits within the stated tolerance of the exact dot; ids bit-exact wherever
 the oracle's margin exceeds twice that tolerance; the oracle's top-k applied
@@ -55,6 +55,9 @@ CASES_F32 = [
     (1, 2048, 256, 8), (7, 2048, 256, 8), (75, 2048, 256, 8), (300, 2048, 256, 8),
     (1100, 2048, 256, 8), (520, 200, 128, 6), (3000, 136, 1024, 32),
     (33, 264, 96, 5), (5, 8, 32, 1), (70, 136, 1024, 32), (600, 264, 96, 5),
+    # more tiles than one wave: whole tiles for the head rows, a partition
+    # split for the tail rows (E = 256: 8 groups; E = 64 and 1024: 16)
+    (1300, 2048, 256, 8), (4904, 128, 64, 4), (400, 136, 1024, 32),
 ]
 
 
@@ -110,7 +113,7 @@ def test_tie_heavy_workload_counts(bi, orc):
     assert gpu_ties == orc_ties == 78
 
 
-@pytest.mark.parametrize("M", [40, 900])
+@pytest.mark.parametrize("M", [40, 900, 1400])
 def test_router_bf16_in_f32_logits(bi, orc, M):
     X = synth.to_bf16_bits(synth.tokens(2, 0, 0, M, 512))
     W = synth.to_bf16_bits(synth.router_weights(2, 0, 128, 512))
@@ -121,7 +124,7 @@ def test_router_bf16_in_f32_logits(bi, orc, M):
     check_selection_on_own_logits(orc, g, 6)
 
 
-@pytest.mark.parametrize("M", [50, 1000])
+@pytest.mark.parametrize("M", [50, 1000, 1300])
 def test_router_f32_in_bf16_logits(bi, orc, M):
     """General f32 inputs, bf16 logits.  The GPU rounds its f32 sum (itself
     within the f32 tolerance of the exact dot) to bf16, so it lies within
@@ -148,7 +151,7 @@ def test_router_full_size_sampled(bi, orc):
     X = synth.tokens(4, 0, 0, M, H)
     W = synth.router_weights(4, 0, E, H)
     g = run_router(bi, X, W, k, "f32")
-    rows = np.array([0, 1, 31, 32, 33, 1000, 2047, 2048, 4064, 4095])
+    rows = np.array([0, 1, 31, 32, 33, 1000, 2047, 2048, 3647, 3648, 3700, 4064, 4095])
     exact = orc.router_logits(X[rows], W)
     absdot = orc.router_absdot(X[rows], W)
     assert np.all(np.abs(g["logits"][rows] - exact) <= gu.router_logit_tol(absdot))
@@ -170,17 +173,20 @@ def test_router_nan_and_zero_rules(bi, orc):
     assert np.array_equal(g["ids"], sel["ids"])
 
 
-@pytest.mark.parametrize("E", [64, 256, 1024])
-def test_router_splits_bit_identical(bi, E):
-    """The same tokens under different partition splits: rows 0..299
-    computed in a 300-token batch and inside a 2000-token batch (fewer
-    blocks per tile) give identical bytes in every output."""
+@pytest.mark.parametrize("E,M", [(64, 5000), (256, 1300), (1024, 400)])
+def test_router_splits_bit_identical(bi, E, M):
+    """The same tokens under different work splits: the first and the last
+    300 rows of an M-token batch, each also computed as a 300-token batch,
+    give identical bytes in every output.  In the M-token batch the first
+    rows run as whole tiles and the last rows in the partition-split tail;
+    as 300-token batches they are split differently again."""
     import torch
     H, k = 2048, 8
-    X = synth.tokens(6, 0, 0, 2000, H)
+    X = synth.tokens(6, 0, 0, M, H)
     w = gu.dev_f32(synth.router_weights(6, 0, E, H))
-    small = bi.router_topk(gu.dev_f32(X[:300]), w, k, "f32")
     big = bi.router_topk(gu.dev_f32(X), w, k, "f32")
-    torch.cuda.synchronize()
-    for f in ("logits", "ids", "weights", "margin", "margin_ulps"):
-        assert small[f].cpu().numpy().tobytes() == big[f][:300].cpu().numpy().tobytes(), f
+    for a in (0, M - 300):
+        small = bi.router_topk(gu.dev_f32(X[a:a + 300]), w, k, "f32")
+        torch.cuda.synchronize()
+        for f in ("logits", "ids", "weights", "margin", "margin_ulps"):
+            assert small[f].cpu().numpy().tobytes() == big[f][a:a + 300].cpu().numpy().tobytes(), (a, f)
