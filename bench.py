@@ -48,6 +48,11 @@ def peaks():
     return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+# DRAM bytes (read + write) per launch from one ncu capture of the kernel as it stands
+# (profiles/gemm_bf16_M4096_N4096_K4096.md); None where no capture of the current code
+# exists.  Must be reset to None whenever the kernel changes.
+NCU_TRAFFIC = {"gemm_bf16_kernel": 67_437_056 + 12_296_448, "router_call": None}
+
 # FP32 FMA peak from unit counts and clock: 152 SMs x 128 FP32 lanes x 2 flop x 2070 MHz
 FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
 
@@ -252,12 +257,14 @@ def run_ours(args):
     r_bytes = 4 * E * H + 4 * M * H + 4 * M * E + 8 * M * K_TOP + 8 * M
     g_bytes = 2 * (M * G_K + G_N * G_K + M * G_N)
     roof_gemm = {"bound": "tensor", "achieved": g_flop / g_avg / 1e12, "peak": bf16_sus,
-                 "unit": "TFLOP/s", "frac": g_flop / g_avg / 1e12 / bf16_sus, "traffic": None,
+                 "unit": "TFLOP/s", "frac": g_flop / g_avg / 1e12 / bf16_sus,
+                 "traffic": NCU_TRAFFIC["gemm_bf16_kernel"],
                  "kernel": "gemm_bf16_kernel (one launch per call)",
                  "peak_source": f"{src} bf16 sustained (kernel timed inside a long step), of {src}",
                  "algorithmic_bytes": g_bytes}
     roof_router = {"bound": "alu", "achieved": r_flop / r_avg / 1e12, "peak": FP32_PEAK_TFLOPS,
-                   "unit": "TFLOP/s", "frac": r_flop / r_avg / 1e12 / FP32_PEAK_TFLOPS, "traffic": None,
+                   "unit": "TFLOP/s", "frac": r_flop / r_avg / 1e12 / FP32_PEAK_TFLOPS,
+                   "traffic": NCU_TRAFFIC["router_call"],
                    "kernel": "bi_router_topk call: router_proj_kernel launches + router_select_kernel "
                              "(timed as one call, so the selection counts against the projection)",
                    "algorithmic_bytes": r_bytes, "hbm_time_frac": (r_bytes / (hbm * 1e9)) / r_avg,

@@ -63,14 +63,18 @@ struct ProjCfg {
     static_assert(P == 16 || P == 32 || P == 64 || P == 128, "TMA swizzle span");
 };
 
-// Byte offset of 16-byte chunk `ch` of row r in a box with P-byte rows and
-// the P-byte TMA swizzle: address bits [4, 4+log2(P/16)) are xor-ed with
-// bits [7, 7+log2(P/16)) (every box starts 1024-byte aligned); P = 16 is
-// the unswizzled case.
+// Layout of a staged box: P-byte rows with the P-byte TMA swizzle, so
+// 16-byte chunk `ch` of row r sits at r * P + 16 * (ch ^ sx(r)), where
+// sx(r) is bits [7, 7+log2(P/16)) of r * P (every box starts 1024-byte
+// aligned; P = 16 is unswizzled).  For the rows a thread reads it depends on
+// little: x rows tg + 4j (tg < 4)
+// give sx(tg + 4 (j & 1)), and gate rows eg + 8i (eg < 8) give sx(eg) for
+// every i.  So each half-block needs three base addresses, and the row
+// steps 4P (x) and 8P (w) become immediate offsets of the loads.
 template <int P>
-__device__ __forceinline__ int swz(int r, int ch)
+__device__ __forceinline__ int sx(int r)
 {
-    return r * P + 16 * (ch ^ ((r * P >> 7) & (P / 16 - 1)));
+    return P == 16 ? 0 : ((r * P) >> 7) & (P / 16 - 1);
 }
 
 // One 8-wide block of the chain for the 8x8 thread tile, f32 inputs.  The
@@ -81,15 +85,19 @@ __device__ __forceinline__ void block_f32(float (&acc)[8][8], const uint8_t *xs,
 {
 #pragma unroll 1
     for (int c = 0; c < 2; ++c) {
+        const int ch = 2 * pc + c;
+        const uint8_t *xe = xs + tg * P + 16 * (ch ^ sx<P>(tg));       // rows tg + 4j, j even
+        const uint8_t *xo = xs + tg * P + 16 * (ch ^ sx<P>(tg + 4));   // j odd
+        const uint8_t *wb = ws + eg * P + 16 * (ch ^ sx<P>(eg));        // rows eg + 8i
         float4 xv[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-            xv[j] = *reinterpret_cast<const float4 *>(xs + swz<P>(tg + 4 * j, 2 * pc + c));
-        float4 wn = *reinterpret_cast<const float4 *>(ws + swz<P>(eg, 2 * pc + c));
+            xv[j] = *reinterpret_cast<const float4 *>((j & 1 ? xo : xe) + 4 * j * P);
+        float4 wn = *reinterpret_cast<const float4 *>(wb);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const float4 wv = wn;       // this expert's four values; the next one loads meanwhile
-            if (i + 1 < 8) wn = *reinterpret_cast<const float4 *>(ws + swz<P>(eg + 8 * (i + 1), 2 * pc + c));
+            if (i + 1 < 8) wn = *reinterpret_cast<const float4 *>(wb + 8 * (i + 1) * P);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 float a = acc[j][i];
@@ -110,15 +118,18 @@ template <int P>
 __device__ __forceinline__ void block_bf16(float (&acc)[8][8], const uint8_t *xs, const uint8_t *ws,
                                            int pc, int tg, int eg)
 {
+    const uint8_t *xe = xs + tg * P + 16 * (pc ^ sx<P>(tg));
+    const uint8_t *xo = xs + tg * P + 16 * (pc ^ sx<P>(tg + 4));
+    const uint8_t *wb = ws + eg * P + 16 * (pc ^ sx<P>(eg));
 #pragma unroll 1
     for (int c = 0; c < 2; ++c) {
         uint2 xr[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-            xr[j] = *reinterpret_cast<const uint2 *>(xs + swz<P>(tg + 4 * j, pc) + 8 * c);
+            xr[j] = *reinterpret_cast<const uint2 *>((j & 1 ? xo : xe) + 4 * j * P + 8 * c);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const uint2 wr = *reinterpret_cast<const uint2 *>(ws + swz<P>(eg + 8 * i, pc) + 8 * c);
+            const uint2 wr = *reinterpret_cast<const uint2 *>(wb + 8 * i * P + 8 * c);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 float a = acc[j][i];
