@@ -48,9 +48,9 @@ def peaks():
     return 6800.0, 1900.0, 1700.0, "fallback"
 
 
-# DRAM bytes (read + write) per launch from one ncu capture of the kernel as it stands
-# (profiles/gemm_bf16_M4096_N4096_K4096.md); None where no capture of the current code
-# exists.  Must be reset to None whenever the kernel changes.
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
+# capture of the kernel as it stands, at this launch shape; None where no capture of the
+# current code exists.  Reset to None whenever the kernel changes.
 NCU_TRAFFIC = {"gemm_bf16_kernel": 67_437_056 + 12_296_448, "router_call": None}
 
 # FP32 FMA peak from unit counts and clock: 152 SMs x 128 FP32 lanes x 2 flop x 2070 MHz
