@@ -250,6 +250,70 @@ BI_API bi_status bi_get_last_device_error(void);
 BI_API bi_status bi_selftest_wait_timeout(uint32_t limit_us, bi_stream s);
 
 /* ABI version of this header: bumps on any incompatible change. */
+/*
+ * bi_get_config -- the numeric contract as data, so that a caller (or a
+ * checker comparing two deployments) can verify that two libraries reduce
+ * in the same order before trusting byte equality across them.  [P3] "The
+ * arithmetic cost of batch-invariant kernels" asks for exactly this: one
+ * static reduction tree, fixed accumulator precision and block size, named
+ * rather than chosen by a heuristic.  Host-only: touches no GPU.
+ *
+ *   out       host pointer to a bi_config the caller owns
+ *   out_size  sizeof(bi_config) as the caller compiled it; the library fills
+ *             min(out_size, its own size) bytes (fields are only appended in
+ *             later versions), and struct_size reports its own size
+ * Returns BI_ERR_INVALID_ARG for a NULL `out` or an out_size smaller than
+ * the first two fields.
+ */
+typedef enum { BI_TREE_PAIRWISE = 1 } bi_tree;
+
+typedef struct {
+    int32_t struct_size;            /* sizeof(bi_config) in this library */
+    int32_t abi_version;            /* BI_ABI_VERSION */
+    /* router projection and shared gate (bi_router_topk, bi_shared_gate) */
+    int32_t router_slab;            /* 128: h is cut into slabs of this many */
+    int32_t router_block;           /* 8: each slab into blocks of this many */
+    int32_t router_partitions;      /* 16: partition q owns block q of every slab */
+    int32_t router_partition_order; /* 1: one fused multiply-add chain from +0, h increasing */
+    int32_t router_tree;            /* BI_TREE_PAIRWISE over the 16 partials, 4 levels */
+    int32_t router_accum;           /* BI_F32 */
+    /* bf16 projection (bi_gemm_bf16) */
+    int32_t gemm_tile_m, gemm_tile_n; /* 128 x 256 output tile (the last partial wave as 128 x 128) */
+    int32_t gemm_block_k;           /* 64: K consumed in blocks of this many, increasing */
+    int32_t gemm_mma_k;             /* 16: each block as four tensor-core steps of this depth */
+    int32_t gemm_accum;             /* BI_F32, rounded to bf16 (nearest even) once */
+    int32_t gemm_split_k;           /* 0: K is never split across thread blocks */
+    /* selection */
+    int32_t topk_tie_rule;          /* 1: equal values rank by ascending expert index */
+    int32_t softmax_sum_order;      /* 1: denominators summed in rank order */
+} bi_config;
+
+BI_API bi_status bi_get_config(bi_config *out, size_t out_size);
+
+/*
+ * bi_prefix_split -- which rows a prefix-cache hit recomputes.  [P3] "The
+ * engineering cost of determinism": a request of N tokens runs at M = N on
+ * a cache miss, but on a hit the engine keeps the block-aligned prefix and
+ * runs only the suffix, M = N mod block_size.  When N is a multiple of the
+ * block size that suffix is empty; the plainest reading kept here is that
+ * the last full block is recomputed (so every request yields rows to
+ * compare), and a request shorter than one block is recomputed whole.
+ * Host-only: touches no GPU.
+ *
+ *   lengths            host [n_requests] int32, each >= 0
+ *   block              KV block size in tokens, >= 1
+ *   cached_out         host [n_requests]: tokens kept from the cache (a
+ *                      multiple of block); request r recomputes its rows
+ *                      [cached_out[r], lengths[r])
+ *   suffix_offsets_out host [n_requests + 1]: the recomputed rows packed
+ *                      request after request (offset 0, then running sums),
+ *                      ready to pass as row offsets to bi_route_trace_hash
+ * Returns BI_ERR_INVALID_ARG for NULL pointers, n_requests < 0, block < 1,
+ * a negative length, or a total above INT32_MAX (outputs untouched).
+ */
+BI_API bi_status bi_prefix_split(const int32_t *lengths, int32_t n_requests, int32_t block,
+                                 int32_t *cached_out, int32_t *suffix_offsets_out);
+
 #define BI_ABI_VERSION 1
 BI_API int32_t bi_abi_version(void);
 

@@ -31,7 +31,19 @@ SIGNATURES = {
     "bi_get_last_device_error": (C.c_int, []),
     "bi_abi_version": (C.c_int32, []),
     "bi_selftest_wait_timeout": (C.c_int, [C.c_uint32, _P]),
+    "bi_get_config": (C.c_int, [_P, C.c_size_t]),
+    "bi_prefix_split": (C.c_int, [_P, _I32, _I32, _P, _P]),
 }
+
+BI_TREE_PAIRWISE = 1
+
+
+class BiConfig(C.Structure):
+    """Mirror of bi_config (include/bi.h), field for field."""
+    _fields_ = [(n, C.c_int32) for n in (
+        "struct_size", "abi_version", "router_slab", "router_block", "router_partitions",
+        "router_partition_order", "router_tree", "router_accum", "gemm_tile_m", "gemm_tile_n",
+        "gemm_block_k", "gemm_mma_k", "gemm_accum", "gemm_split_k", "topk_tie_rule", "softmax_sum_order")]
 
 _lib = None
 
@@ -137,6 +149,23 @@ def bi_get_last_device_error() -> int:
 
 def bi_abi_version() -> int:
     return load().bi_abi_version()
+
+
+def get_config() -> dict:
+    """bi_get_config as a dict of the contract's fields."""
+    c = BiConfig()
+    _check(load().bi_get_config(C.byref(c), C.sizeof(c)), "bi_get_config")
+    return {name: getattr(c, name) for name, _ in BiConfig._fields_}
+
+
+def prefix_split(lengths, block: int):
+    """bi_prefix_split: (cached[n], suffix_offsets[n + 1]) as int lists."""
+    n = len(lengths)
+    arr = (C.c_int32 * max(n, 1))(*[int(v) for v in lengths])
+    cached = (C.c_int32 * max(n, 1))()
+    offs = (C.c_int32 * (n + 1))()
+    _check(load().bi_prefix_split(arr, n, int(block), cached, offs), "bi_prefix_split")
+    return list(cached)[:n], list(offs)
 
 
 def bi_selftest_wait_timeout(limit_us: int, stream=None) -> int:

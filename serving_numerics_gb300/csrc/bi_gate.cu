@@ -16,6 +16,9 @@ namespace bi {
 namespace {
 
 constexpr int kGateWarps = 8;
+// the lane layout below is the contract's: 16 lanes = 16 partitions, 8-wide
+// blocks, 128-wide slabs
+static_assert(kRouterParts == 16 && kRouterBlock == 8 && kRouterSlab == 128, "gate lane layout");
 
 __global__ void __launch_bounds__(32 * kGateWarps)
 shared_gate_kernel(const float *__restrict__ x, const float *__restrict__ w, int M, int H,

@@ -37,7 +37,7 @@
 namespace bi {
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, UMMA_K = 16, STAGES = 4;
+constexpr int BM = kGemmTileM, BN = kGemmTileN, BK = kGemmBlockK, UMMA_K = kGemmMmaK, STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;             // 16 KB
 constexpr int B_BYTES = BN * BK * 2;             // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // 48 KB

@@ -10,6 +10,16 @@
 
 namespace bi {
 
+// The numeric contract: the kernels are built from these constants, and
+// bi_get_config reports them.  Changing one changes the bits of the results.
+constexpr int kRouterSlab = 128;      // h is cut into slabs of 128
+constexpr int kRouterBlock = 8;       // each slab into 16 blocks of 8
+constexpr int kRouterParts = 16;      // partition q owns block q of every slab
+constexpr int kGemmTileM = 128, kGemmTileN = 256;
+constexpr int kGemmBlockK = 64;       // K in blocks of 64, increasing
+constexpr int kGemmMmaK = 16;         // each block as four 16-deep tensor-core steps
+static_assert(kRouterSlab == kRouterBlock * kRouterParts, "a slab is one block per partition");
+
 // Per-device state, created on the first call made with that device current.
 struct Device {
     int ordinal = -1;

@@ -38,7 +38,7 @@
 namespace bi {
 namespace {
 
-constexpr int kTileM = 32, kTileE = 64, kSlab = 128, kBlk = 8, kParts = 16;
+constexpr int kTileM = 32, kTileE = 64, kSlab = kRouterSlab, kBlk = kRouterBlock, kParts = kRouterParts;
 
 template <typename InT, int C>
 struct ProjCfg {

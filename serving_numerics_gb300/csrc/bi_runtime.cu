@@ -1,5 +1,8 @@
 // bi_runtime.cu -- per-device state, the sticky device error word, tensor-map
 // encoding and the small ABI utilities (status strings, version).
+#include <limits.h>
+#include <string.h>
+
 #include <mutex>
 
 #include "bi_device.cuh"
@@ -134,5 +137,53 @@ bi_status bi_get_last_device_error(void)
 }
 
 int32_t bi_abi_version(void) { return BI_ABI_VERSION; }
+
+bi_status bi_get_config(bi_config *out, size_t out_size)
+{
+    if (!out || out_size < 2 * sizeof(int32_t)) return BI_ERR_INVALID_ARG;
+    bi_config c;
+    memset(&c, 0, sizeof c);
+    c.struct_size = (int32_t)sizeof(bi_config);
+    c.abi_version = BI_ABI_VERSION;
+    c.router_slab = bi::kRouterSlab;
+    c.router_block = bi::kRouterBlock;
+    c.router_partitions = bi::kRouterParts;
+    c.router_partition_order = 1;
+    c.router_tree = BI_TREE_PAIRWISE;
+    c.router_accum = BI_F32;
+    c.gemm_tile_m = bi::kGemmTileM;
+    c.gemm_tile_n = bi::kGemmTileN;
+    c.gemm_block_k = bi::kGemmBlockK;
+    c.gemm_mma_k = bi::kGemmMmaK;
+    c.gemm_accum = BI_F32;
+    c.gemm_split_k = 0;
+    c.topk_tie_rule = 1;
+    c.softmax_sum_order = 1;
+    memcpy(out, &c, out_size < sizeof c ? out_size : sizeof c);
+    return BI_OK;
+}
+
+bi_status bi_prefix_split(const int32_t *lengths, int32_t n_requests, int32_t block, int32_t *cached_out,
+                          int32_t *suffix_offsets_out)
+{
+    if (!lengths || !cached_out || !suffix_offsets_out || n_requests < 0 || block < 1) return BI_ERR_INVALID_ARG;
+    int64_t total = 0;
+    for (int32_t r = 0; r < n_requests; ++r) {
+        if (lengths[r] < 0) return BI_ERR_INVALID_ARG;
+        total += lengths[r];
+    }
+    if (total > INT32_MAX) return BI_ERR_INVALID_ARG;
+    int32_t off = 0;
+    suffix_offsets_out[0] = 0;
+    for (int32_t r = 0; r < n_requests; ++r) {
+        const int32_t n = lengths[r];
+        int32_t suffix = n % block;            // rows past the last full block
+        if (suffix == 0) suffix = n < block ? n : block;   // none: recompute the last full block
+        cached_out[r] = n - suffix;
+        off += suffix;
+        suffix_offsets_out[r + 1] = off;
+    }
+    return BI_OK;
+}
 
 }  // extern "C"

@@ -1,0 +1,101 @@
+"""The router projection and the shared gate hold the documented reduction
+order bit for bit: every logit and gate dot equals the CPU restatement of
+the contract (oracle/contract.c: 16 partitions owning the 8-wide blocks of
+every 128-wide slab, one f32 fused multiply-add chain each, a pairwise tree
+of the partials), for every work split the library picks (the matrix-vector
+twin, whole tiles, partition-split tiles, whole tiles plus a split tail, the
+no-allocation entry), for f32 and bf16 inputs, and for bf16 logits (the
+same f32 value rounded to nearest even once).
+
+This is stronger than the tolerance parity of test_router_gpu.py: it pins
+the order itself, which is what makes the results independent of M ("batch
+changed the model's mind", section "The fix: m-invariant twins")."""
+import numpy as np
+import pytest
+
+from serving_numerics_gb300 import synth
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+
+def gpu_logits(bi, X, W, k, logit_dtype, noalloc=False):
+    import torch
+    x = gu.dev_f32(X) if X.dtype == np.float32 else gu.dev_bf16(X)
+    w = gu.dev_f32(W) if W.dtype == np.float32 else gu.dev_bf16(W)
+    M, E = X.shape[0], W.shape[0]
+    lg = torch.empty((M, E), dtype=torch.float32 if logit_dtype == "f32" else torch.bfloat16, device="cuda")
+    ids = torch.empty((M, k), dtype=torch.int32, device="cuda")
+    ind = bi.BI_F32 if X.dtype == np.float32 else bi.BI_BF16
+    lod = bi.BI_F32 if logit_dtype == "f32" else bi.BI_BF16
+    call = bi.bi_router_topk_noalloc if noalloc else bi.bi_router_topk
+    call(x, w, ind, lod, M, X.shape[1], E, k, lg, ids)
+    torch.cuda.synchronize()
+    assert bi.bi_get_last_device_error() == 0
+    return gu.host(lg) if logit_dtype == "f32" else gu.host_bf16_bits(lg)
+
+
+# (M, H, E, k): matrix-vector twin (M <= 8, M <= 64), partition-split tiles,
+# whole tiles, whole tiles + split tail; ragged H and E
+SHAPES = [(1, 2048, 256, 8), (7, 264, 96, 5), (20, 2048, 256, 8), (64, 136, 1024, 32), (100, 2048, 256, 8),
+          (300, 136, 64, 4), (700, 264, 256, 8), (1300, 2048, 256, 8), (1235, 128, 256, 8)]
+
+
+@pytest.mark.parametrize("M,H,E,k", SHAPES)
+def test_router_f32_logits_are_the_contract(bi, M, H, E, k):
+    from oracle import contract
+    X = synth.tokens(50, 0, M, M, H)
+    W = synth.router_weights(50, M, E, H)
+    got = gpu_logits(bi, X, W, k, "f32")
+    want = contract.router_logits(X, W)
+    assert got.view(np.uint32).tobytes() == want.view(np.uint32).tobytes(), \
+        f"{np.sum(got.view(np.uint32) != want.view(np.uint32))} logits differ"
+
+
+@pytest.mark.parametrize("M,H,E,k", [(5, 2048, 512, 10), (50, 2048, 512, 10), (700, 2048, 256, 8),
+                                     (1400, 2048, 256, 8)])
+def test_router_bf16_inputs_and_logits_are_the_contract(bi, orc, M, H, E, k):
+    from oracle import contract
+    X = synth.to_bf16_bits(synth.tokens(51, 0, M, M, H))
+    W = synth.to_bf16_bits(synth.router_weights(51, M, E, H))
+    want = contract.router_logits(X, W)
+    got = gpu_logits(bi, X, W, k, "f32")
+    assert got.view(np.uint32).tobytes() == want.view(np.uint32).tobytes()
+    got_b = gpu_logits(bi, X, W, k, "bf16")
+    want_b = orc.round_bf16(want.astype(np.float64))
+    assert np.array_equal(got_b, want_b)
+
+
+def test_router_noalloc_is_the_contract(bi):
+    from oracle import contract
+    M, H, E, k = 40, 2048, 256, 8
+    X = synth.tokens(52, 0, 0, M, H)
+    W = synth.router_weights(52, 0, E, H)
+    got = gpu_logits(bi, X, W, k, "f32", noalloc=True)
+    assert got.view(np.uint32).tobytes() == contract.router_logits(X, W).view(np.uint32).tobytes()
+
+
+def test_router_full_size_sampled_rows_are_the_contract(bi):
+    """M = 4096 (the benchmark's launch: whole tiles for rows 0..3647, a
+    split tail after): sampled rows of both parts."""
+    from oracle import contract
+    M, H, E, k = 4096, 2048, 256, 8
+    X = synth.tokens(53, 0, 0, M, H)
+    W = synth.router_weights(53, 0, E, H)
+    got = gpu_logits(bi, X, W, k, "f32")
+    rows = np.array([0, 31, 32, 1999, 3647, 3648, 3700, 4095])
+    want = contract.router_logits(X[rows], W)
+    assert got[rows].view(np.uint32).tobytes() == want.view(np.uint32).tobytes()
+
+
+@pytest.mark.parametrize("M,H", [(1, 2048), (33, 264), (4096, 2048)])
+def test_shared_gate_dot_is_the_contract(bi, M, H):
+    import torch
+    from oracle import contract
+    X = synth.tokens(54, 0, 0, M, H)
+    w = synth.shared_gate_weights(54, 0, H)
+    dot, _ = bi.shared_gate(gu.dev_f32(X), gu.dev_f32(w))
+    torch.cuda.synchronize()
+    rows = np.arange(M) if M <= 64 else np.array([0, 1, 2047, 4095])
+    want = contract.router_logits(X[rows], w[None, :])[:, 0]
+    assert gu.host(dot)[rows].view(np.uint32).tobytes() == want.view(np.uint32).tobytes()

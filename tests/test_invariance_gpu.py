@@ -167,12 +167,14 @@ def test_mixed_prefill_prefix_split(bi):
         return h.cpu().numpy().view(np.uint64).copy(), outs
 
     batched_h, batched = run([(r, 0, int(lens[r])) for r in range(16)])
+    cached, _ = bi.prefix_split([int(v) for v in lens], blk)     # the library's cache-hit rule
     compared = 0
     for r in range(16):
         n = int(lens[r])
         solo_h, solo = run([(r, 0, n)])
         assert solo_h[0] == batched_h[r], f"request {r}: hash differs solo vs batched"
-        hit = n % blk or blk                        # suffix rows on a cache hit
+        hit = n - cached[r]                         # suffix rows on a cache hit
+        assert hit == (n % blk or blk)
         hit_h, hit_o = run([(r, n - hit, n)])
         hb = None
         for l in range(L):                         # the same suffix rows hashed from the batch
