@@ -135,6 +135,30 @@ BI_API bi_status bi_router_topk(const void *x, const void *w_gate, bi_dtype in_d
                          float *margin_out, int32_t *margin_ulps_out, bi_stream s);
 
 /*
+ * bi_router_gate_topk -- bi_router_topk and bi_shared_gate in one call: the
+ * same router outputs, plus the shared-expert gate of every row computed in
+ * the selection kernel from the rows of X the projection just read (one
+ * launch and one pass over X from device memory fewer than the two calls).
+ * The gate follows the router's reduction contract (above) with w_sg as one
+ * more gate row that never enters the top-k; its dot and sigmoid are
+ * byte-identical to bi_shared_gate's for f32 inputs, and for bf16 inputs it
+ * is the same contract on the widened values (exact products, one rounding
+ * per step).
+ *
+ *   x, w_gate, ...   as bi_router_topk
+ *   w_sg             [H] in in_dtype, 16-byte aligned
+ *   gate_dot_out     [M] f32: the dot of each row with w_sg
+ *   gate_sigmoid_out [M] f32, optional (NULL): 1 / (1 + exp(-dot))
+ * Errors: as bi_router_topk; BI_ERR_INVALID_ARG for a NULL w_sg or
+ * gate_dot_out when M > 0.
+ */
+BI_API bi_status bi_router_gate_topk(const void *x, const void *w_gate, const void *w_sg, bi_dtype in_dtype,
+                              bi_dtype logit_dtype, int32_t M, int32_t H, int32_t E, int32_t k,
+                              void *logits_out, int32_t *ids_out, float *weights_out,
+                              float *margin_out, int32_t *margin_ulps_out, float *gate_dot_out,
+                              float *gate_sigmoid_out, bi_stream s);
+
+/*
  * bi_shared_gate -- the one-output shared-expert gate: dot = X[m,:] . w_sg,
  * gate = 1 / (1 + exp(-dot)).
  *

@@ -25,6 +25,8 @@ SIGNATURES = {
     "bi_router_topk": (C.c_int, [_P, _P, C.c_int, C.c_int, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P]),
     "bi_router_topk_noalloc": (C.c_int, [_P, _P, C.c_int, C.c_int, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P]),
     "bi_shared_gate": (C.c_int, [_P, _P, _I32, _I32, _P, _P, _P]),
+    "bi_router_gate_topk": (C.c_int, [_P, _P, _P, C.c_int, C.c_int, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P,
+                                      _P, _P, _P]),
     "bi_gemm_bf16": (C.c_int, [_P, _P, _P, _I32, _I32, _I32, _I64, _I64, _I64, _P]),
     "bi_route_trace_hash": (C.c_int, [_P, _I32, _I32, _P, _I32, _P, _P, _P]),
     "bi_status_string": (C.c_char_p, [C.c_int]),
@@ -118,6 +120,18 @@ def bi_router_topk_noalloc(x, w_gate, in_dtype, logit_dtype, M, H, E, k, logits_
     return st
 
 
+def bi_router_gate_topk(x, w_gate, w_sg, in_dtype, logit_dtype, M, H, E, k, logits_out, ids_out,
+                        weights_out=None, margin_out=None, margin_ulps_out=None, gate_dot_out=None,
+                        gate_sigmoid_out=None, stream=None, check=True):
+    st = load().bi_router_gate_topk(_ptr(x), _ptr(w_gate), _ptr(w_sg), in_dtype, logit_dtype, M, H, E, k,
+                                    _ptr(logits_out), _ptr(ids_out), _ptr(weights_out), _ptr(margin_out),
+                                    _ptr(margin_ulps_out), _ptr(gate_dot_out), _ptr(gate_sigmoid_out),
+                                    _stream(stream))
+    if check:
+        _check(st, "bi_router_gate_topk")
+    return st
+
+
 def bi_shared_gate(x, w_sg, M, H, dot_out, sigmoid_out=None, stream=None, check=True):
     st = load().bi_shared_gate(_ptr(x), _ptr(w_sg), M, H, _ptr(dot_out), _ptr(sigmoid_out), _stream(stream))
     if check:
@@ -194,6 +208,29 @@ def router_topk(x, w_gate, k: int, logit_dtype: str = "f32", stream=None, out=No
         }
     bi_router_topk(x, w_gate, ind, ld, M, H, E, k, out["logits"], out["ids"], out.get("weights"),
                    out.get("margin"), out.get("margin_ulps"), stream=stream)
+    return out
+
+
+def router_gate_topk(x, w_gate, w_sg, k: int, logit_dtype: str = "f32", stream=None):
+    """Allocate the outputs with torch and run bi_router_gate_topk.
+    Returns the router_topk dict plus gate_dot and gate_sigmoid."""
+    import torch
+    M, H = x.shape
+    E = w_gate.shape[0]
+    ind = BI_F32 if x.dtype == torch.float32 else BI_BF16
+    ld = BI_F32 if logit_dtype == "f32" else BI_BF16
+    dev = x.device
+    out = {
+        "logits": torch.empty((M, E), dtype=torch.float32 if ld == BI_F32 else torch.bfloat16, device=dev),
+        "ids": torch.empty((M, k), dtype=torch.int32, device=dev),
+        "weights": torch.empty((M, k), dtype=torch.float32, device=dev),
+        "margin": torch.empty((M,), dtype=torch.float32, device=dev),
+        "margin_ulps": torch.empty((M,), dtype=torch.int32, device=dev),
+        "gate_dot": torch.empty((M,), dtype=torch.float32, device=dev),
+        "gate_sigmoid": torch.empty((M,), dtype=torch.float32, device=dev),
+    }
+    bi_router_gate_topk(x, w_gate, w_sg, ind, ld, M, H, E, k, out["logits"], out["ids"], out["weights"],
+                        out["margin"], out["margin_ulps"], out["gate_dot"], out["gate_sigmoid"], stream=stream)
     return out
 
 

@@ -321,23 +321,98 @@ __device__ __forceinline__ long long sm_ord(float x, int bf16)
 }
 
 constexpr int kSelWarps = 8;
+constexpr size_t kGateStageMax = 96 * 1024;   // shared memory for the staged gate rows (2 blocks per SM)
+
+// The shared-expert gate fused into the selection: the optional inputs of
+// bi_router_gate_topk (NULL gx = no gate).
+struct GateArgs {
+    const void *gx = nullptr;   // X again ([M, H], the input dtype)
+    const void *gw = nullptr;   // w_sg [H]
+    int bf16 = 0;
+    int staged = 0;             // the block's X rows and w_sg are copied to shared memory first
+    float *dot = nullptr, *sig = nullptr;
+    unsigned int *err = nullptr;   // the library's device error word (bounded wait on the copies)
+};
+
+__device__ __forceinline__ void load8(const float *p, float (&v)[8])
+{
+    const float4 a = *reinterpret_cast<const float4 *>(p), b = *reinterpret_cast<const float4 *>(p + 4);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+__device__ __forceinline__ void load8(const __nv_bfloat16 *p, float (&v)[8])
+{
+    const uint4 r = *reinterpret_cast<const uint4 *>(p);
+    v[0] = bf16lo(r.x); v[1] = bf16hi(r.x); v[2] = bf16lo(r.y); v[3] = bf16hi(r.y);
+    v[4] = bf16lo(r.z); v[5] = bf16hi(r.z); v[6] = bf16lo(r.w); v[7] = bf16hi(r.w);
+}
+
+// Partition q's chain of the gate dot for one row (the router's contract:
+// block q of every slab, one FMA chain from +0, h increasing), with the
+// loads of two slabs in flight at a time.
+template <typename InT>
+__device__ __forceinline__ float gate_partition(const InT *xr, const InT *w, int H, int q)
+{
+    float acc = 0.0f;
+    const int ns = (H + kSlab - 1) / kSlab;
+    for (int s0 = 0; s0 < ns; s0 += 2) {
+        float xv[2][8], wv[2][8];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int h0 = kSlab * (s0 + u) + kBlk * q;
+            if (h0 < H) {
+                load8(xr + h0, xv[u]);
+                load8(w + h0, wv[u]);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int h0 = kSlab * (s0 + u) + kBlk * q;
+            if (h0 < H) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc = __fmaf_rn(xv[u][i], wv[u][i], acc);
+            }
+        }
+    }
+    return acc;
+}
 
 // One warp per token: finish the tree (C > 1), round to the logit dtype,
 // then k+1 rounds of warp arg-max (value desc, index asc).  Round k yields
 // the largest rejected logit for the margin.  Rows below m_split already
 // have their logits (the projection ran whole for them); rows from m_split
 // on have C group sums in `part`, laid out group-major over those rows.
-template <int EPLM>
+template <int EPLM, bool GATE>
 __global__ void __launch_bounds__(32 * kSelWarps)
 router_select_kernel(const float *__restrict__ part, int C, int m_split, void *logits, int logit_bf16,
                      int M, int E, int k, int32_t *__restrict__ ids, float *__restrict__ weights,
-                     float *__restrict__ margin, int32_t *__restrict__ ulps)
+                     float *__restrict__ margin, int32_t *__restrict__ ulps, GateArgs gate, int H)
 {
     pdl_trigger();   // dependents may launch now; each waits before reading our outputs
+    extern __shared__ __align__(16) uint8_t gate_rows[];   // staged gate: kSelWarps rows of X, then w_sg
+    __shared__ __align__(8) uint64_t gate_bar;
+    const bool staged = GATE && gate.staged;
+    const uint32_t row_bytes = (uint32_t)H * (gate.bf16 ? 2u : 4u);
+    if (staged) {
+        if (threadIdx.x == 0) {
+            mbar_init(&gate_bar, 1);
+            mbar_init_fence();
+        }
+        __syncthreads();
+    }
     pdl_wait();
+    if (staged && threadIdx.x == 0) {
+        // the rows land while the selection below runs
+        const int m0 = blockIdx.x * kSelWarps, rows = M - m0 < kSelWarps ? M - m0 : kSelWarps;
+        mbar_arrive_expect_tx(&gate_bar, (uint32_t)(rows + 1) * row_bytes);
+        bulk_load(gate_rows + kSelWarps * row_bytes, gate.gw, row_bytes, &gate_bar);
+        for (int r = 0; r < rows; ++r)
+            bulk_load(gate_rows + r * row_bytes, static_cast<const uint8_t *>(gate.gx) + (size_t)(m0 + r) * row_bytes,
+                      row_bytes, &gate_bar);
+    }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m = blockIdx.x * kSelWarps + warp;
-    if (m >= M) return;
+    if (m >= M) return;     // warp 0's row always exists, so the block outlives its copies
     const int epl = E >> 5;
 
     // gather this lane's logits (experts lane + 32 i), all loads issued first
@@ -452,6 +527,35 @@ router_select_kernel(const float *__restrict__ part, int C, int m_split, void *l
             if (d > INT_MAX) d = INT_MAX;
             if (d < INT_MIN) d = INT_MIN;
             ulps[m] = (int32_t)d;
+        }
+    }
+
+    // the shared gate (bi_router_gate_topk): lanes 0..15 are the 16
+    // partitions; the butterfly with offsets 1, 2, 4, 8 is the pairwise tree
+    // (each pair's lanes hold the same sum: fp addition commutes), as in
+    // bi_shared_gate, so the two give the same bytes
+    if (GATE) {
+        float g = 0.0f;
+        if (staged) {
+            mbar_wait(&gate_bar, 0, gate.err, 0x40);
+            if (lane < 16) {
+                const uint8_t *xr = gate_rows + warp * row_bytes, *wr = gate_rows + kSelWarps * row_bytes;
+                g = gate.bf16 ? gate_partition(reinterpret_cast<const __nv_bfloat16 *>(xr),
+                                               reinterpret_cast<const __nv_bfloat16 *>(wr), H, lane)
+                              : gate_partition(reinterpret_cast<const float *>(xr),
+                                               reinterpret_cast<const float *>(wr), H, lane);
+            }
+        } else if (lane < 16) {
+            g = gate.bf16 ? gate_partition(static_cast<const __nv_bfloat16 *>(gate.gx) + (size_t)m * H,
+                                           static_cast<const __nv_bfloat16 *>(gate.gw), H, lane)
+                          : gate_partition(static_cast<const float *>(gate.gx) + (size_t)m * H,
+                                           static_cast<const float *>(gate.gw), H, lane);
+        }
+#pragma unroll
+        for (int d = 1; d < 16; d *= 2) g = g + __shfl_xor_sync(0xFFFFFFFFu, g, d);
+        if (lane == 0) {
+            gate.dot[m] = g;
+            if (gate.sig) gate.sig[m] = 1.0f / (1.0f + expf(-g));
         }
     }
 }
@@ -713,24 +817,34 @@ bi_status launch_proj_c(Device *d, int C, const void *x, const void *w, int M, i
 template <int EPLM>
 bi_status launch_select1(Device *d, dim3 grid, dim3 block, cudaStream_t cs, const float *pp, int C,
                          int m_split, void *logits, int lbf, int M, int E, int k, int32_t *ids, float *w, float *mg,
-                         int32_t *mu)
+                         int32_t *mu, const GateArgs &gate, int H)
 {
-    const int kid = KID_SELECT + (EPLM == 4 ? 0 : EPLM == 8 ? 1 : EPLM == 16 ? 2 : 3);
-    bi_status st = set_smem_once(d, kid, router_select_kernel<EPLM>, 0);
+    const int kid = (gate.gx ? KID_SELECT_GATE : KID_SELECT) + (EPLM == 4 ? 0 : EPLM == 8 ? 1 : EPLM == 16 ? 2 : 3);
+    auto kern = gate.gx ? router_select_kernel<EPLM, true> : router_select_kernel<EPLM, false>;
+    bi_status st = set_smem_once(d, kid, kern, gate.gx ? kGateStageMax : 0);
     if (st != BI_OK) return st;
-    return launch_pdl(router_select_kernel<EPLM>, grid, block, 0, cs, pp, C, m_split, logits, lbf, M, E, k, ids,
-                      w, mg, mu);
+    GateArgs g = gate;
+    size_t smem = 0;
+    if (g.gx) {
+        g.err = d->err;
+        smem = (size_t)(kSelWarps + 1) * H * (g.bf16 ? 2 : 4);
+        g.staged = smem <= kGateStageMax ? 1 : 0;     // larger rows are read from device memory directly
+        if (!g.staged) smem = 0;
+    }
+    return launch_pdl(kern, grid, block, smem, cs, pp, C, m_split, logits, lbf, M, E, k, ids, w, mg, mu, g, H);
 }
 
 bi_status launch_select(Device *d, int epl, dim3 grid, dim3 block, cudaStream_t cs, const float *pp, int C,
                         int m_split, void *logits, int lbf, int M, int E, int k, int32_t *ids, float *w,
-                        float *mg, int32_t *mu)
+                        float *mg, int32_t *mu, const GateArgs &g = GateArgs(), int H = 0)
 {
-    if (epl <= 4) return launch_select1<4>(d, grid, block, cs, pp, C, m_split, logits, lbf, M, E, k, ids, w, mg, mu);
-    if (epl <= 8) return launch_select1<8>(d, grid, block, cs, pp, C, m_split, logits, lbf, M, E, k, ids, w, mg, mu);
+    if (epl <= 4)
+        return launch_select1<4>(d, grid, block, cs, pp, C, m_split, logits, lbf, M, E, k, ids, w, mg, mu, g, H);
+    if (epl <= 8)
+        return launch_select1<8>(d, grid, block, cs, pp, C, m_split, logits, lbf, M, E, k, ids, w, mg, mu, g, H);
     if (epl <= 16)
-        return launch_select1<16>(d, grid, block, cs, pp, C, m_split, logits, lbf, M, E, k, ids, w, mg, mu);
-    return launch_select1<32>(d, grid, block, cs, pp, C, m_split, logits, lbf, M, E, k, ids, w, mg, mu);
+        return launch_select1<16>(d, grid, block, cs, pp, C, m_split, logits, lbf, M, E, k, ids, w, mg, mu, g, H);
+    return launch_select1<32>(d, grid, block, cs, pp, C, m_split, logits, lbf, M, E, k, ids, w, mg, mu, g, H);
 }
 
 // Batches up to this many tokens take the matrix-vector twin.
@@ -769,10 +883,13 @@ SplitPlan plan_split(int M, int E, int sms)
 
 using namespace bi;
 
-extern "C" bi_status bi_router_topk(const void *x, const void *w_gate, bi_dtype in_dtype,
-                                    bi_dtype logit_dtype, int32_t M, int32_t H, int32_t E, int32_t k,
-                                    void *logits_out, int32_t *ids_out, float *weights_out,
-                                    float *margin_out, int32_t *margin_ulps_out, bi_stream s)
+namespace bi {
+namespace {
+
+// bi_router_topk and bi_router_gate_topk: validation, work plan, launches.
+bi_status router_call(const void *x, const void *w_gate, bi_dtype in_dtype, bi_dtype logit_dtype, int32_t M,
+                      int32_t H, int32_t E, int32_t k, void *logits_out, int32_t *ids_out, float *weights_out,
+                      float *margin_out, int32_t *margin_ulps_out, const GateArgs &gate, bi_stream s)
 {
     if ((in_dtype != BI_F32 && in_dtype != BI_BF16) || (logit_dtype != BI_F32 && logit_dtype != BI_BF16))
         return BI_ERR_INVALID_ARG;
@@ -787,6 +904,9 @@ extern "C" bi_status bi_router_topk(const void *x, const void *w_gate, bi_dtype 
     if ((reinterpret_cast<uintptr_t>(logits_out) & lal) || (reinterpret_cast<uintptr_t>(ids_out) & 3u) ||
         (reinterpret_cast<uintptr_t>(weights_out) & 3u) || (reinterpret_cast<uintptr_t>(margin_out) & 3u) ||
         (reinterpret_cast<uintptr_t>(margin_ulps_out) & 3u))
+        return BI_ERR_MISALIGNED;
+    if (gate.gx && (!aligned16(gate.gw) || (reinterpret_cast<uintptr_t>(gate.dot) & 3u) ||
+                    (reinterpret_cast<uintptr_t>(gate.sig) & 3u)))
         return BI_ERR_MISALIGNED;
 
     Device *d = nullptr;
@@ -830,8 +950,38 @@ extern "C" bi_status bi_router_topk(const void *x, const void *w_gate, bi_dtype 
     const int epl = E / 32;
     dim3 grid((M + kSelWarps - 1) / kSelWarps), block(32 * kSelWarps);
     const float *pp = static_cast<const float *>(part);
+    GateArgs g = gate;
+    g.bf16 = f32in ? 0 : 1;
     return launch_select(d, epl, grid, block, cs, pp, plan.C, plan.m_split, logits_out, lbf, M, E, k, ids_out,
-                         weights_out, margin_out, margin_ulps_out);
+                         weights_out, margin_out, margin_ulps_out, g, H);
+}
+
+}  // namespace
+}  // namespace bi
+
+extern "C" bi_status bi_router_topk(const void *x, const void *w_gate, bi_dtype in_dtype,
+                                    bi_dtype logit_dtype, int32_t M, int32_t H, int32_t E, int32_t k,
+                                    void *logits_out, int32_t *ids_out, float *weights_out,
+                                    float *margin_out, int32_t *margin_ulps_out, bi_stream s)
+{
+    return router_call(x, w_gate, in_dtype, logit_dtype, M, H, E, k, logits_out, ids_out, weights_out, margin_out,
+                       margin_ulps_out, GateArgs(), s);
+}
+
+extern "C" bi_status bi_router_gate_topk(const void *x, const void *w_gate, const void *w_sg, bi_dtype in_dtype,
+                                         bi_dtype logit_dtype, int32_t M, int32_t H, int32_t E, int32_t k,
+                                         void *logits_out, int32_t *ids_out, float *weights_out,
+                                         float *margin_out, int32_t *margin_ulps_out, float *gate_dot_out,
+                                         float *gate_sigmoid_out, bi_stream s)
+{
+    if (M > 0 && (!w_sg || !gate_dot_out)) return BI_ERR_INVALID_ARG;
+    GateArgs g;
+    g.gx = M > 0 ? x : nullptr;
+    g.gw = w_sg;
+    g.dot = gate_dot_out;
+    g.sig = gate_sigmoid_out;
+    return router_call(x, w_gate, in_dtype, logit_dtype, M, H, E, k, logits_out, ids_out, weights_out, margin_out,
+                       margin_ulps_out, g, s);
 }
 
 // ---------------------------------------------------------------------------

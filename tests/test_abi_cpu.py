@@ -71,6 +71,25 @@ def test_router_m0_is_noop(lib):
     assert _router(lib, M=0, x=None, w=None, logits=None, ids=None) == 0
 
 
+def _router_gate(lib, wsg=FAKE, dot=FAKE, sig=None, **kw):
+    a = dict(x=FAKE, w=FAKE, ind=0, ld=0, M=4, H=256, E=64, k=4, logits=FAKE, ids=FAKE)
+    a.update(kw)
+    return lib.bi_router_gate_topk(a["x"], a["w"], wsg, a["ind"], a["ld"], a["M"], a["H"], a["E"], a["k"],
+                                   a["logits"], a["ids"], None, None, None, dot, sig, None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(wsg=None), 1), (dict(dot=None), 1), (dict(M=-1), 1), (dict(k=64), 1), (dict(H=260), 2),
+    (dict(wsg=MIS), 3), (dict(dot=FAKE + 2), 3), (dict(sig=FAKE + 1), 3), (dict(x=MIS), 3),
+])
+def test_router_gate_validation(lib, kw, want):
+    assert _router_gate(lib, **kw) == want
+
+
+def test_router_gate_m0_is_noop(lib):
+    assert _router_gate(lib, M=0, x=None, w=None, logits=None, ids=None, wsg=None, dot=None) == 0
+
+
 @pytest.mark.parametrize("args,want", [
     ((FAKE, FAKE, -1, 256, FAKE, None), 1), ((FAKE, FAKE, 4, 0, FAKE, None), 1),
     ((FAKE, FAKE, 4, 12, FAKE, None), 2), ((None, FAKE, 4, 256, FAKE, None), 1),

@@ -99,3 +99,42 @@ def test_shared_gate_dot_is_the_contract(bi, M, H):
     rows = np.arange(M) if M <= 64 else np.array([0, 1, 2047, 4095])
     want = contract.router_logits(X[rows], w[None, :])[:, 0]
     assert gu.host(dot)[rows].view(np.uint32).tobytes() == want.view(np.uint32).tobytes()
+
+
+# (M, H, E, k, dtype): every work split, f32 and bf16 inputs; rows up to 96 KB
+# per block are staged in shared memory, the last two are too long for that
+# and read the gate rows from device memory directly
+FUSED = [(1, 2048, 256, 8, "f32"), (20, 264, 96, 5, "f32"), (100, 2048, 256, 8, "f32"), (1300, 2048, 256, 8, "f32"),
+         (5, 2048, 512, 10, "bf16"), (700, 2048, 256, 8, "bf16"), (4096, 2048, 256, 8, "f32"),
+         (70, 4096, 64, 4, "f32"), (203, 6000, 64, 4, "bf16")]
+
+
+@pytest.mark.parametrize("M,H,E,k,dt", FUSED)
+def test_router_gate_fused_is_the_two_calls(bi, M, H, E, k, dt):
+    """bi_router_gate_topk gives the router outputs of bi_router_topk byte
+    for byte, and a gate dot that is the contract's (and, for f32 inputs,
+    bi_shared_gate's bytes, dot and sigmoid)."""
+    import torch
+    from oracle import contract
+    X = synth.tokens(55, 0, M, M, H)
+    W = synth.router_weights(55, M, E, H)
+    w = synth.shared_gate_weights(55, M, H)
+    if dt == "bf16":
+        X, W, w = synth.to_bf16_bits(X), synth.to_bf16_bits(W), synth.to_bf16_bits(w)
+        x, Wd, wd = gu.dev_bf16(X), gu.dev_bf16(W), gu.dev_bf16(w)
+    else:
+        x, Wd, wd = gu.dev_f32(X), gu.dev_f32(W), gu.dev_f32(w)
+    fused = bi.router_gate_topk(x, Wd, wd, k)
+    plain = bi.router_topk(x, Wd, k)
+    torch.cuda.synchronize()
+    assert bi.bi_get_last_device_error() == 0
+    for f in ("logits", "ids", "weights", "margin", "margin_ulps"):
+        assert fused[f].cpu().numpy().tobytes() == plain[f].cpu().numpy().tobytes(), f
+    rows = np.arange(M) if M <= 1300 else np.array([0, 5, 3647, 3648, 4095])
+    want = contract.router_logits(X[rows], w[None, :])[:, 0]
+    assert gu.host(fused["gate_dot"])[rows].view(np.uint32).tobytes() == want.view(np.uint32).tobytes()
+    if dt == "f32":
+        d, sg = bi.shared_gate(x, wd)
+        torch.cuda.synchronize()
+        assert gu.host(fused["gate_dot"]).tobytes() == gu.host(d).tobytes()
+        assert gu.host(fused["gate_sigmoid"]).tobytes() == gu.host(sg).tobytes()
