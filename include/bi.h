@@ -275,6 +275,46 @@ BI_API bi_status bi_selftest_wait_timeout(uint32_t limit_us, bi_stream s);
 
 /* ABI version of this header: bumps on any incompatible change. */
 /*
+ * bi_moe_expert_gemm -- the grouped expert projection that consumes the
+ * router's choice: every token-slot (m, j) is one row through its expert,
+ *
+ *   Y[m, j, n] = bf16_rne( sum_k X[m, k] * W[ids[m, j], n, k] )
+ *   out[m, n]  = bf16_rne( sum_{j<k} weights[m, j] * Y[m, j, n] )
+ *
+ * [P4] "Why a value tap could never have said this": the assembled per-slot
+ * expert outputs, and the grouped expert GEMM -- whose per-expert row counts
+ * change with the batch -- as the amplifier of run-to-run differences.  The
+ * pages' experts are quantised; here they are bf16.
+ *
+ * Invariance contract: each Y row is accumulated in f32 over K in blocks of
+ * 64, in increasing order, each block as four 16-deep tensor-core steps,
+ * and rounded to bf16 once -- the schedule of bi_gemm_bf16, whatever the
+ * number of rows its expert receives and wherever the row lands in its
+ * expert's group.  out is one f32 fused multiply-add chain over j = 0..k-1
+ * (rank order, the order ids come in), rounded once.
+ *
+ *   X        [M, K] bf16 (16-byte aligned)
+ *   ids      [M, k] int32 expert of each slot, in [0, E); an id outside
+ *            that range sets BI_ERR_INVALID_ARG in the device error word and
+ *            its slot's outputs are left unwritten
+ *   weights  [M, k] f32, needed when out is requested, else may be NULL
+ *   W        [E, N, K] bf16: expert e's [N, K] projection (16-byte aligned)
+ *   Y_out    [M, k, N] bf16 per-slot outputs, or NULL (then they live in
+ *            the workspace)
+ *   out      [M, N] bf16 combined rows, or NULL; at least one of Y_out, out
+ *   workspace, workspace_bytes  caller-owned device buffer, 256-byte
+ *            aligned, at least bi_moe_workspace_bytes(M, k, E, N, K) bytes;
+ *            nothing is allocated by the call.  Two calls that could overlap
+ *            on the GPU must not share a workspace.
+ * Limits: 1 <= k <= BI_MAX_K, 1 <= E <= BI_MAX_E, K % 64 == 0, N % 16 == 0,
+ * K, N <= 65536, M * k <= 2^24.  M == 0 returns BI_OK.
+ */
+BI_API size_t bi_moe_workspace_bytes(int32_t M, int32_t k, int32_t E, int32_t N, int32_t K);
+BI_API bi_status bi_moe_expert_gemm(const void *X, const int32_t *ids, const float *weights, const void *W,
+                             int32_t M, int32_t k, int32_t E, int32_t N, int32_t K, void *Y_out,
+                             void *out, void *workspace, size_t workspace_bytes, bi_stream s);
+
+/*
  * bi_get_config -- the numeric contract as data, so that a caller (or a
  * checker comparing two deployments) can verify that two libraries reduce
  * in the same order before trusting byte equality across them.  [P3] "The

@@ -34,6 +34,8 @@ SIGNATURES = {
     "bi_abi_version": (C.c_int32, []),
     "bi_selftest_wait_timeout": (C.c_int, [C.c_uint32, _P]),
     "bi_get_config": (C.c_int, [_P, C.c_size_t]),
+    "bi_moe_workspace_bytes": (C.c_size_t, [_I32, _I32, _I32, _I32, _I32]),
+    "bi_moe_expert_gemm": (C.c_int, [_P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, C.c_size_t, _P]),
     "bi_prefix_split": (C.c_int, [_P, _I32, _I32, _P, _P]),
 }
 
@@ -163,6 +165,40 @@ def bi_get_last_device_error() -> int:
 
 def bi_abi_version() -> int:
     return load().bi_abi_version()
+
+
+def bi_moe_expert_gemm(X, ids, weights, W, M, k, E, N, K, Y_out, out, workspace, workspace_bytes, stream=None,
+                       check=True):
+    st = load().bi_moe_expert_gemm(_ptr(X), _ptr(ids), _ptr(weights), _ptr(W), M, k, E, N, K, _ptr(Y_out),
+                                   _ptr(out), _ptr(workspace), workspace_bytes, _stream(stream))
+    if check:
+        _check(st, "bi_moe_expert_gemm")
+    return st
+
+
+def moe_workspace(M, k, E, N, K, device="cuda"):
+    """A caller-owned workspace for bi_moe_expert_gemm (torch uint8 tensor)."""
+    import torch
+    n = int(load().bi_moe_workspace_bytes(M, k, E, N, K))
+    return torch.empty(n + 256, dtype=torch.uint8, device=device), n
+
+
+def moe_expert_gemm(X, ids, weights, W, stream=None, want_y=True, want_out=True, workspace=None):
+    """Allocate outputs with torch and run bi_moe_expert_gemm.  X [M, K] and
+    W [E, N, K] bf16, ids [M, k] int32, weights [M, k] f32 (or None when
+    want_out is False).  Returns dict(Y, out)."""
+    import torch
+    M, K = X.shape
+    E, N, _ = W.shape
+    k = ids.shape[1]
+    if workspace is None:
+        workspace = moe_workspace(M, k, E, N, K, X.device)
+    buf, n = workspace
+    base = (buf.data_ptr() + 255) // 256 * 256           # 256-byte aligned start
+    Y = torch.empty((M, k, N), dtype=torch.bfloat16, device=X.device) if want_y else None
+    out = torch.empty((M, N), dtype=torch.bfloat16, device=X.device) if want_out else None
+    bi_moe_expert_gemm(X, ids, weights if want_out else None, W, M, k, E, N, K, Y, out, base, n, stream=stream)
+    return {"Y": Y, "out": out}
 
 
 def get_config() -> dict:

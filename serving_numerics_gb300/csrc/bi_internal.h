@@ -97,6 +97,7 @@ enum : int {
     KID_HASH = 25,         // 4 instantiations: 25..28
     KID_ROUTER_GEMV = 30,  // 4 instantiations: 30..33
     KID_SELECT_GATE = 34,  // 4 instantiations: 34..37
+    KID_MOE = 40,          // 5 kernels: 40..44
 };
 
 }  // namespace bi

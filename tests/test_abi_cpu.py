@@ -139,3 +139,30 @@ def test_hash_too_many_ranges(lib):
 def test_selftest_validation(lib):
     assert lib.bi_selftest_wait_timeout(0, None) == 1
     assert lib.bi_selftest_wait_timeout(2000001, None) == 1
+
+
+def _moe(lib, **kw):
+    a = dict(X=FAKE, ids=FAKE, w=FAKE, W=FAKE, M=16, k=2, E=8, N=256, K=128, Y=FAKE, out=FAKE,
+             ws=0x100000, wsb=1 << 40)
+    a.update(kw)
+    return lib.bi_moe_expert_gemm(a["X"], a["ids"], a["w"], a["W"], a["M"], a["k"], a["E"], a["N"], a["K"],
+                                  a["Y"], a["out"], a["ws"], a["wsb"], None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(M=-1), 1), (dict(k=0), 1), (dict(E=0), 1), (dict(N=0), 1), (dict(K=0), 1),
+    (dict(K=100), 2), (dict(N=250), 2), (dict(E=2048), 2), (dict(k=33), 2),
+    (dict(X=None), 1), (dict(ids=None), 1), (dict(W=None), 1), (dict(ws=None), 1),
+    (dict(Y=None, out=None), 1), (dict(w=None), 1), (dict(wsb=1024), 1),
+    (dict(X=MIS), 3), (dict(W=MIS), 3), (dict(ws=0x100010), 3), (dict(Y=FAKE + 2), 3),
+])
+def test_moe_validation(lib, kw, want):
+    assert _moe(lib, **kw) == want
+
+
+def test_moe_m0_is_noop_and_workspace_size(lib):
+    assert _moe(lib, M=0, X=None, ids=None, W=None, ws=None) == 0
+    n = lib.bi_moe_workspace_bytes(4096, 8, 256, 1024, 2048)
+    cap = ((4096 * 8 + 256 * 127) + 127) // 128 * 128
+    assert n >= cap * 2048 * 2 + 4096 * 8 * 1024 * 2          # gathered rows + per-slot outputs
+    assert lib.bi_moe_workspace_bytes(-1, 8, 256, 1024, 2048) == 0
