@@ -297,6 +297,7 @@ def run_ours(args):
     if not args.no_sweep:
         out["router_sweep"] = router_sweep(bi, synth, torch, dev, hbm)
         out["context_m_variant"] = m_variant_context(bi, synth, torch, dev)
+        out["moe_expert_gemm"] = moe_measure(bi, synth, torch, dev, hbm, X[0], ids[0], wts[0])
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_seconds)
     if rank == 0:
@@ -353,6 +354,45 @@ def router_sweep(bi, synth, torch, dev, hbm_gbs):
                     "frac_of_hbm": (byt / t / 1e9) / hbm_gbs})
     del Ws
     return res
+
+
+def moe_measure(bi, synth, torch, dev, hbm_gbs, X, ids, wts):
+    """bi_moe_expert_gemm alone, on the router's own choice: the first
+    layer's hidden states (rounded to bf16) through the experts it picked,
+    top-8 of 256 experts of [N=1024, K=2048] bf16 (1 GiB of weights, two
+    expert sets alternated so nothing stays in L2), per-slot outputs and
+    the weighted combine.  Bound by HBM: every expert's weights are read."""
+    En, Nn, Kn = E, 1024, H
+    Ws = [synth.device_normal((En, Nn, Kn), 80000 + i, 1.0 / 64, torch.bfloat16, dev) for i in range(2)]
+    xb = X.to(torch.bfloat16)
+    Y = torch.empty((M, K_TOP, Nn), dtype=torch.bfloat16, device=dev)
+    out = torch.empty((M, Nn), dtype=torch.bfloat16, device=dev)
+    buf, n = bi.moe_workspace(M, K_TOP, En, Nn, Kn, dev)
+    base = (buf.data_ptr() + 255) // 256 * 256
+
+    def call(i):
+        bi.bi_moe_expert_gemm(xb, ids, wts, Ws[i % 2], M, K_TOP, En, Nn, Kn, Y, out, base, n, stream=None)
+    for i in range(4):
+        call(i)
+    reps = 10
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record()
+    for i in range(reps):
+        call(i)
+    b.record()
+    torch.cuda.synchronize()
+    assert bi.bi_get_last_device_error() == 0
+    t = a.elapsed_time(b) / 1e3 / reps
+    flop = 2.0 * M * K_TOP * Nn * Kn
+    byt = 2 * En * Nn * Kn + 2 * M * Kn + 8 * M * K_TOP + 2 * M * K_TOP * Nn + 2 * M * Nn
+    del Ws
+    return {"config": f"M={M} tokens, top-{K_TOP} of {En} experts, expert [N={Nn}, K={Kn}] bf16, "
+                      "ids and weights from the step's router",
+            "us_per_call": t * 1e6, "tflops": flop / t / 1e12,
+            "launches_per_call": 4,
+            "roofline": {"bound": "hbm", "achieved": byt / t / 1e9, "peak": hbm_gbs, "unit": "GB/s",
+                         "frac": byt / t / 1e9 / hbm_gbs, "algorithmic_bytes": byt, "traffic": None}}
 
 
 def m_variant_context(bi, synth, torch, dev):

@@ -21,9 +21,8 @@
 // counters and may differ run to run; nothing numeric depends on it.
 //
 // Launch sequence (all on the caller's stream, no host synchronisation):
-//   memset      counters and the row map
-//   count       rows per expert (atomics)
-//   plan        one block: padded exclusive scan over experts -> tile table
+//   plan        one block: rows per expert, padded exclusive scan over the
+//               experts -> tile table; resets the cursors and the row map
 //   place       one warp per token-slot: claim a row of its expert's group,
 //               record it in the row map, copy X[m] there
 //   gemm        persistent tcgen05 kernel over the tile table (count of
@@ -60,7 +59,7 @@ size_t moe_layout(int64_t M, int64_t k, int64_t E, int64_t N, int64_t K, uint8_t
         off += (bytes + 255) & ~(size_t)255;
         return p;
     };
-    uint8_t *counts = take(sizeof(int32_t) * 2 * E);      // counts then cursor, one memset
+    uint8_t *counts = take(sizeof(int32_t) * 2 * E);      // (spare) then the placement cursors
     uint8_t *offsets = take(sizeof(int32_t) * (E + 1));
     uint8_t *ntiles = take(sizeof(int32_t));
     uint8_t *tr0 = take(sizeof(int32_t) * max_tiles);
@@ -84,35 +83,62 @@ size_t moe_layout(int64_t M, int64_t k, int64_t E, int64_t N, int64_t K, uint8_t
     return off;
 }
 
-// Rows per expert.  An id outside [0, E) is recorded in the device error
-// word (BI_ERR_INVALID_ARG) and its slot is left out everywhere.
-__global__ void __launch_bounds__(256)
-moe_count_kernel(const int32_t *__restrict__ ids, int Mk, int E, int32_t *__restrict__ counts, unsigned int *err)
-{
-    pdl_trigger();
-    pdl_wait();
-    const int i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= Mk) return;
-    const int e = ids[i];
-    if (e < 0 || e >= E) {
-        report_error(err, (unsigned int)BI_ERR_INVALID_ARG, 0x50u);
-        return;
-    }
-    atomicAdd(&counts[e], 1);
-}
-
-// One block: each expert's rows padded up to whole tiles, exclusive scans of
-// rows and tiles over the experts, and the tile table (first gathered row
-// and expert of every tile).
+// One block does the whole plan: rows per expert (a histogram in shared
+// memory), each expert's rows padded up to whole tiles, the exclusive scan
+// over experts, the tile table (first gathered row and expert of every
+// tile), the placement cursors reset to 0 and the row map reset to -1.  An
+// id outside [0, E) is recorded in the device error word
+// (BI_ERR_INVALID_ARG) and its slot is left out everywhere.
 __global__ void __launch_bounds__(kPlanThreads)
-moe_plan_kernel(const int32_t *__restrict__ counts, int E, int32_t *__restrict__ offsets,
-                int32_t *__restrict__ ntiles, int32_t *__restrict__ tile_row0, int32_t *__restrict__ tile_expert)
+moe_plan_kernel(const int32_t *__restrict__ ids, int Mk, int E, int64_t cap, int32_t *__restrict__ cursor,
+                int32_t *__restrict__ offsets, int32_t *__restrict__ ntiles, int32_t *__restrict__ tile_row0,
+                int32_t *__restrict__ tile_expert, int32_t *__restrict__ row_src, unsigned int *err)
 {
     pdl_trigger();
-    pdl_wait();
-    __shared__ int32_t scan_t[kPlanThreads];
+    __shared__ int32_t hist[kPlanThreads], scan_t[kPlanThreads];
     const int e = threadIdx.x;
-    const int c = e < E ? counts[e] : 0;
+    hist[e] = 0;
+    pdl_wait();
+    __syncthreads();
+    auto count = [&](int x) {
+        if (x < 0 || x >= E)
+            report_error(err, (unsigned int)BI_ERR_INVALID_ARG, 0x50u);
+        else
+            atomicAdd(&hist[x], 1);
+    };
+    // one block is latency-bound on the id loads: 16-byte loads, eight in
+    // flight per thread (ids 16-byte aligned; otherwise one id at a time)
+    int done = 0;
+    if ((reinterpret_cast<uintptr_t>(ids) & 15u) == 0) {
+        const int4 *ids4 = reinterpret_cast<const int4 *>(ids);
+        const int n4 = Mk / 4;
+        for (int base = 0; base < n4; base += 8 * kPlanThreads) {
+            int4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int q = base + u * kPlanThreads + e;
+                if (q < n4) v[u] = ids4[q];
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                if (base + u * kPlanThreads + e < n4) {
+                    count(v[u].x);
+                    count(v[u].y);
+                    count(v[u].z);
+                    count(v[u].w);
+                }
+            }
+        }
+        done = n4 * 4;
+    }
+    for (int i = done + e; i < Mk; i += kPlanThreads) count(ids[i]);
+    {   // row map reset (cap is a multiple of 128, the array 256-byte aligned)
+        int4 *rs4 = reinterpret_cast<int4 *>(row_src);
+        const int4 neg = make_int4(-1, -1, -1, -1);
+        for (int64_t r = e; r < cap / 4; r += kPlanThreads) rs4[r] = neg;
+    }
+    __syncthreads();
+    const int c = e < E ? hist[e] : 0;
     const int t = (c + BM - 1) / BM;                  // this expert's tiles
     scan_t[e] = t;
     __syncthreads();
@@ -125,6 +151,7 @@ moe_plan_kernel(const int32_t *__restrict__ counts, int E, int32_t *__restrict__
     const int t0 = scan_t[e] - t;                     // exclusive
     if (e < E) {
         offsets[e] = t0 * BM;
+        cursor[e] = 0;
         for (int i = 0; i < t; ++i) {
             tile_row0[t0 + i] = (t0 + i) * BM;
             tile_expert[t0 + i] = e;
@@ -371,15 +398,9 @@ extern "C" bi_status bi_moe_expert_gemm(const void *X, const int32_t *ids, const
     }
 
     const int Mk = M * k;
-    if (cudaMemsetAsync(ws.counts, 0, sizeof(int32_t) * 2 * E, cs) != cudaSuccess) return BI_ERR_CUDA;
-    if (cudaMemsetAsync(ws.row_src, 0xFF, sizeof(int32_t) * ws.cap, cs) != cudaSuccess) return BI_ERR_CUDA;
-    if ((st = set_smem_once(d, KID_MOE + 0, moe_count_kernel, 0)) != BI_OK) return st;
-    if ((st = launch_pdl(moe_count_kernel, dim3((Mk + 255) / 256), dim3(256), 0, cs, ids, Mk, (int)E, ws.counts,
-                         d->err)) != BI_OK)
-        return st;
     if ((st = set_smem_once(d, KID_MOE + 1, moe_plan_kernel, 0)) != BI_OK) return st;
-    if ((st = launch_pdl(moe_plan_kernel, dim3(1), dim3(kPlanThreads), 0, cs, (const int32_t *)ws.counts, (int)E,
-                         ws.offsets, ws.ntiles, ws.tile_row0, ws.tile_expert)) != BI_OK)
+    if ((st = launch_pdl(moe_plan_kernel, dim3(1), dim3(kPlanThreads), 0, cs, ids, Mk, (int)E, (int64_t)ws.cap,
+                         ws.cursor, ws.offsets, ws.ntiles, ws.tile_row0, ws.tile_expert, ws.row_src, d->err)) != BI_OK)
         return st;
     if ((st = set_smem_once(d, KID_MOE + 2, moe_place_kernel, 0)) != BI_OK) return st;
     if ((st = launch_pdl(moe_place_kernel, dim3((Mk + 7) / 8), dim3(256), 0, cs,
