@@ -134,6 +134,18 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     seed = 1000 + rank
 
+    if args.moe_only:
+        # the grouped expert GEMM alone (a small case for profiling): one
+        # router call supplies the ids and weights
+        x0 = synth.device_normal((M, H), seed * 100 + 200, 1.0, torch.float32, dev)
+        w0 = synth.device_normal((E, H), seed * 100, 0.02, torch.float32, dev)
+        r = bi.router_topk(x0, w0, K_TOP)
+        hbm = peaks()[0]
+        if rank == 0:
+            print(json.dumps({"moe_expert_gemm": moe_measure(bi, synth, torch, dev, hbm, x0, r["ids"],
+                                                             r["weights"], reps=args.moe_reps)}), flush=True)
+        return
+
     # resident weights and inputs (seeded, drawn on the device)
     Wg = [synth.device_normal((E, H), seed * 100 + l, 0.02, torch.float32, dev) for l in range(LAYERS)]
     Wsg = [synth.device_normal((H,), seed * 100 + 50 + l, 0.02, torch.float32, dev) for l in range(LAYERS)]
@@ -356,7 +368,7 @@ def router_sweep(bi, synth, torch, dev, hbm_gbs):
     return res
 
 
-def moe_measure(bi, synth, torch, dev, hbm_gbs, X, ids, wts):
+def moe_measure(bi, synth, torch, dev, hbm_gbs, X, ids, wts, reps=10):
     """bi_moe_expert_gemm alone, on the router's own choice: the first
     layer's hidden states (rounded to bf16) through the experts it picked,
     top-8 of 256 experts of [N=1024, K=2048] bf16 (1 GiB of weights, two
@@ -374,7 +386,6 @@ def moe_measure(bi, synth, torch, dev, hbm_gbs, X, ids, wts):
         bi.bi_moe_expert_gemm(xb, ids, wts, Ws[i % 2], M, K_TOP, En, Nn, Kn, Y, out, base, n, stream=None)
     for i in range(4):
         call(i)
-    reps = 10
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     a.record()
@@ -523,6 +534,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sweep", action="store_true", help="skip the router-only M sweep")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--moe-only", action="store_true",
+                    help="measure only the grouped expert GEMM (a small case for profiling)")
+    ap.add_argument("--moe-reps", type=int, default=10)
     ap.add_argument("--layers", type=int, default=LAYERS,
                     help="fewer layers for a small profiling case (the benchmark uses 40)")
     args = ap.parse_args()
