@@ -310,6 +310,7 @@ def run_ours(args):
         out["router_sweep"] = router_sweep(bi, synth, torch, dev, hbm)
         out["context_m_variant"] = m_variant_context(bi, synth, torch, dev)
         out["moe_expert_gemm"] = moe_measure(bi, synth, torch, dev, hbm, X[0], ids[0], wts[0])
+        out["rmsnorm"] = rmsnorm_measure(bi, synth, torch, dev, hbm, X)
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_seconds)
     if rank == 0:
@@ -402,6 +403,30 @@ def moe_measure(bi, synth, torch, dev, hbm_gbs, X, ids, wts, reps=10):
                       "ids and weights from the step's router",
             "us_per_call": t * 1e6, "tflops": flop / t / 1e12,
             "launches_per_call": 4,
+            "roofline": {"bound": "hbm", "achieved": byt / t / 1e9, "peak": hbm_gbs, "unit": "GB/s",
+                         "frac": byt / t / 1e9 / hbm_gbs, "algorithmic_bytes": byt, "traffic": None}}
+
+
+def rmsnorm_measure(bi, synth, torch, dev, hbm_gbs, Xs):
+    """bi_rmsnorm alone: f32 rows of H=2048 -> bf16, M=4096, one call per
+    layer's hidden states (40 different 32 MiB inputs, so each call reads
+    from HBM), timed back to back.  Bound by HBM."""
+    w = (1.0 + 0.1 * synth.device_normal((H,), 81000, 1.0, torch.float32, dev)).contiguous()
+    y = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+    r = torch.empty((M,), dtype=torch.float32, device=dev)
+    for x in Xs[:4]:
+        bi.bi_rmsnorm(x, w, bi.BI_F32, M, H, 1e-6, y, r)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record()
+    for x in Xs:
+        bi.bi_rmsnorm(x, w, bi.BI_F32, M, H, 1e-6, y, r)
+    b.record()
+    torch.cuda.synchronize()
+    assert bi.bi_get_last_device_error() == 0
+    t = a.elapsed_time(b) / 1e3 / len(Xs)
+    byt = 4 * M * H + 2 * M * H + 4 * H + 4 * M
+    return {"config": f"M={M}, H={H}, f32 in, bf16 out", "us_per_call": t * 1e6, "launches_per_call": 1,
             "roofline": {"bound": "hbm", "achieved": byt / t / 1e9, "peak": hbm_gbs, "unit": "GB/s",
                          "frac": byt / t / 1e9 / hbm_gbs, "algorithmic_bytes": byt, "traffic": None}}
 

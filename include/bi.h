@@ -275,6 +275,29 @@ BI_API bi_status bi_selftest_wait_timeout(uint32_t limit_us, bi_stream s);
 
 /* ABI version of this header: bumps on any incompatible change. */
 /*
+ * bi_rmsnorm -- batch-invariant RMSNorm of every row:
+ *
+ *   r[m]    = 1 / sqrt( (sum_h x[m,h]^2) / H + eps )
+ *   y[m, h] = bf16_rne( (x[m, h] * r[m]) * w[h] )
+ *
+ * [P3] "The physics of the cascade": one root-mean-square over the whole
+ * hidden state divides every element of the row, so the order of that one
+ * reduction decides all of the row's outputs.  The sum of squares follows
+ * the router's reduction contract (above: 16 partitions, one f32 fused
+ * multiply-add chain each, pairwise tree); the division, the square root
+ * and the two products are each rounded once (nearest even), in that order.
+ *
+ *   x        [M, H] in dtype (BI_F32 or BI_BF16), 16-byte aligned
+ *   w        [H] in dtype, 16-byte aligned
+ *   eps      >= 0, finite
+ *   y_out    [M, H] bf16, 16-byte aligned
+ *   rstd_out [M] f32: r[m], optional (NULL)
+ * Limits: 1 <= H <= BI_MAX_H, H % 8 == 0.  M == 0 returns BI_OK.
+ */
+BI_API bi_status bi_rmsnorm(const void *x, const void *w, bi_dtype dtype, int32_t M, int32_t H, float eps,
+                     void *y_out, float *rstd_out, bi_stream s);
+
+/*
  * bi_moe_expert_gemm -- the grouped expert projection that consumes the
  * router's choice: every token-slot (m, j) is one row through its expert,
  *

@@ -34,6 +34,7 @@ SIGNATURES = {
     "bi_abi_version": (C.c_int32, []),
     "bi_selftest_wait_timeout": (C.c_int, [C.c_uint32, _P]),
     "bi_get_config": (C.c_int, [_P, C.c_size_t]),
+    "bi_rmsnorm": (C.c_int, [_P, _P, C.c_int, _I32, _I32, C.c_float, _P, _P, _P]),
     "bi_moe_workspace_bytes": (C.c_size_t, [_I32, _I32, _I32, _I32, _I32]),
     "bi_moe_expert_gemm": (C.c_int, [_P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, C.c_size_t, _P]),
     "bi_prefix_split": (C.c_int, [_P, _I32, _I32, _P, _P]),
@@ -165,6 +166,25 @@ def bi_get_last_device_error() -> int:
 
 def bi_abi_version() -> int:
     return load().bi_abi_version()
+
+
+def bi_rmsnorm(x, w, dtype, M, H, eps, y_out, rstd_out=None, stream=None, check=True):
+    st = load().bi_rmsnorm(_ptr(x), _ptr(w), dtype, M, H, C.c_float(eps), _ptr(y_out), _ptr(rstd_out),
+                           _stream(stream))
+    if check:
+        _check(st, "bi_rmsnorm")
+    return st
+
+
+def rmsnorm(x, w, eps: float, stream=None):
+    """Allocate outputs with torch and run bi_rmsnorm; x [M, H] and w [H]
+    both float32 or both bfloat16.  Returns (y bf16 [M, H], rstd f32 [M])."""
+    import torch
+    M, H = x.shape
+    y = torch.empty((M, H), dtype=torch.bfloat16, device=x.device)
+    r = torch.empty((M,), dtype=torch.float32, device=x.device)
+    bi_rmsnorm(x, w, BI_F32 if x.dtype == torch.float32 else BI_BF16, M, H, eps, y, r, stream=stream)
+    return y, r
 
 
 def bi_moe_expert_gemm(X, ids, weights, W, M, k, E, N, K, Y_out, out, workspace, workspace_bytes, stream=None,

@@ -166,3 +166,16 @@ def test_moe_m0_is_noop_and_workspace_size(lib):
     cap = ((4096 * 8 + 256 * 127) + 127) // 128 * 128
     assert n >= cap * 2048 * 2 + 4096 * 8 * 1024 * 2          # gathered rows + per-slot outputs
     assert lib.bi_moe_workspace_bytes(-1, 8, 256, 1024, 2048) == 0
+
+
+@pytest.mark.parametrize("args,want", [
+    ((FAKE, FAKE, 0, -1, 256, 1e-6, FAKE, None), 1), ((FAKE, FAKE, 0, 4, 0, 1e-6, FAKE, None), 1),
+    ((FAKE, FAKE, 3, 4, 256, 1e-6, FAKE, None), 1), ((FAKE, FAKE, 0, 4, 256, -1.0, FAKE, None), 1),
+    ((FAKE, FAKE, 0, 4, 256, float("nan"), FAKE, None), 1), ((FAKE, FAKE, 0, 4, 12, 1e-6, FAKE, None), 2),
+    ((None, FAKE, 0, 4, 256, 1e-6, FAKE, None), 1), ((FAKE, FAKE, 0, 4, 256, 1e-6, None, None), 1),
+    ((MIS, FAKE, 0, 4, 256, 1e-6, FAKE, None), 3), ((FAKE, FAKE, 0, 4, 256, 1e-6, FAKE, FAKE + 2), 3),
+    ((None, None, 0, 0, 256, 1e-6, None, None), 0),
+])
+def test_rmsnorm_validation(lib, args, want):
+    x, w, dt, M, H, eps, y, r = args
+    assert lib.bi_rmsnorm(x, w, dt, M, H, C.c_float(eps), y, r, None) == want
