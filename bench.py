@@ -168,10 +168,10 @@ def run_ours(args):
     # ordered after that layer's router by an event, chained layer to layer
     side = torch.cuda.Stream(dev)
     ids_ready = [torch.cuda.Event() for _ in range(LAYERS)]
-    # kernels per layer at M = 4096: the router is three launches (the split
-    # tail rows, the whole-tile rows, the selection with the shared gate
+    # kernels per layer: the router call's (as the library plans it for this
+    # M: its projection launches and the selection with the shared gate
     # fused in), then the route hash and the GEMM
-    launches_per_layer = 5
+    launches_per_layer = bi.router_plan(M, E)[2] + 2
 
     def layer(l, ev=None):
         if ev is not None:

@@ -113,11 +113,12 @@ typedef struct CUstream_st *bi_stream;
  * Logits must be finite for the weights and margins to be meaningful (a
  * NaN ranks above every number and ties other NaNs by index).
  *
- * Scratch: for batches of more than 64 rows that do not fill whole waves
- * of tiles, the partitions of some tiles (all of them below one wave; the
- * last rows' beyond it) are spread over several thread blocks whose partial
- * sums meet in a library-owned device buffer (grown on the first call that
- * needs more, one buffer per device, never freed before exit).  Make a first
+ * Scratch: for batches of more than 64 rows the partitions of a tile are
+ * spread over several thread blocks (two once the tiles fill the SMs, 2*M*E*4
+ * bytes of group sums; more below that; for batches whose group sums would
+ * pass 64 MiB only the last rows') whose partial sums meet in a
+ * library-owned device buffer (grown on the first call that needs more, one
+ * buffer per device, never freed before exit).  Make a first
  * call at the largest M before capturing a CUDA graph.  Two calls that could
  * run at the same time on one device (different streams with no event
  * ordering them) must not both need the buffer.
@@ -133,6 +134,17 @@ BI_API bi_status bi_router_topk(const void *x, const void *w_gate, bi_dtype in_d
                          bi_dtype logit_dtype, int32_t M, int32_t H, int32_t E, int32_t k,
                          void *logits_out, int32_t *ids_out, float *weights_out,
                          float *margin_out, int32_t *margin_ulps_out, bi_stream s);
+
+/*
+ * bi_router_plan -- how bi_router_topk (and bi_router_gate_topk) would cut
+ * the work for M rows and E experts on the current device: the rows below
+ * *m_split run as whole tiles, the rest with each tile's partitions split
+ * over *C blocks; *launches is the number of kernels one call launches.
+ * Introspection only (any plan gives the same bits); it launches nothing.
+ * Returns BI_ERR_INVALID_ARG for NULL outputs or bad sizes, BI_ERR_CUDA when
+ * no device is current.
+ */
+BI_API bi_status bi_router_plan(int32_t M, int32_t E, int32_t *m_split, int32_t *C, int32_t *launches);
 
 /*
  * bi_router_gate_topk -- bi_router_topk and bi_shared_gate in one call: the

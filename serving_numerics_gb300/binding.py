@@ -34,6 +34,7 @@ SIGNATURES = {
     "bi_abi_version": (C.c_int32, []),
     "bi_selftest_wait_timeout": (C.c_int, [C.c_uint32, _P]),
     "bi_get_config": (C.c_int, [_P, C.c_size_t]),
+    "bi_router_plan": (C.c_int, [_I32, _I32, _P, _P, _P]),
     "bi_rmsnorm": (C.c_int, [_P, _P, C.c_int, _I32, _I32, C.c_float, _P, _P, _P]),
     "bi_moe_workspace_bytes": (C.c_size_t, [_I32, _I32, _I32, _I32, _I32]),
     "bi_moe_expert_gemm": (C.c_int, [_P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, C.c_size_t, _P]),
@@ -219,6 +220,13 @@ def moe_expert_gemm(X, ids, weights, W, stream=None, want_y=True, want_out=True,
     out = torch.empty((M, N), dtype=torch.bfloat16, device=X.device) if want_out else None
     bi_moe_expert_gemm(X, ids, weights if want_out else None, W, M, k, E, N, K, Y, out, base, n, stream=stream)
     return {"Y": Y, "out": out}
+
+
+def router_plan(M: int, E: int):
+    """bi_router_plan: (m_split, C, launches) for M rows and E experts."""
+    ms, c, n = C.c_int32(), C.c_int32(), C.c_int32()
+    _check(load().bi_router_plan(M, E, C.byref(ms), C.byref(c), C.byref(n)), "bi_router_plan")
+    return ms.value, c.value, n.value
 
 
 def get_config() -> dict:

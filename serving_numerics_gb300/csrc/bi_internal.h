@@ -99,6 +99,7 @@ enum : int {
     KID_SELECT_GATE = 34,  // 4 instantiations: 34..37
     KID_MOE = 40,          // 5 kernels: 40..44
     KID_NORM = 45,         // 4 instantiations: 45..48
+    KID_ROUTER_PROJ_SHALLOW = 49,   // 2 instantiations: 49..50
 };
 
 }  // namespace bi

@@ -40,7 +40,10 @@ namespace {
 
 constexpr int kTileM = 32, kTileE = 64, kSlab = kRouterSlab, kBlk = kRouterBlock, kParts = kRouterParts;
 
-template <typename InT, int C>
+// SHALLOW: a 96 KB ring instead of 192 KB, so that two blocks share an SM
+// (used with C = 2 when the tiles fill the SMs: one block computes while the
+// other starts up or adds its partition tree).
+template <typename InT, int C, bool SHALLOW = false>
 struct ProjCfg {
     static constexpr int ES = (int)sizeof(InT);
     static constexpr int NPL = kParts / C;                       // partitions (= warps) per block
@@ -54,7 +57,7 @@ struct ProjCfg {
     static constexpr int XBOX = kTileM * P, WBOX = kTileE * P;
     static constexpr int XOP = XBOX * NB, WOP = WBOX * NB;       // per stage
     static constexpr int STAGE_BYTES = XOP + WOP;
-    static constexpr int NST_RAW = (192 * 1024) / STAGE_BYTES;
+    static constexpr int NST_RAW = ((SHALLOW ? 96 : 192) * 1024) / STAGE_BYTES;
     static constexpr int NST = NST_RAW > 16 ? 16 : (NST_RAW < 2 ? 2 : NST_RAW);
     static constexpr int TREE_BYTES = NPL * 64 * 33 * 4;           // every warp's 64 partials
     static constexpr int BODY0 = NST * STAGE_BYTES;
@@ -145,14 +148,14 @@ __device__ __forceinline__ void block_bf16(float (&acc)[8][8], const uint8_t *xs
 
 enum OutMode : int { OUT_F32 = 0, OUT_BF16 = 1, OUT_PARTIAL = 2 };
 
-template <typename InT, int C>
-__global__ void __launch_bounds__(ProjCfg<InT, C>::THREADS, C)     // 16 warps per SM in every split
+template <typename InT, int C, bool SHALLOW>
+__global__ void __launch_bounds__(ProjCfg<InT, C, SHALLOW>::THREADS, C)     // 16 warps per SM in every split
 router_proj_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
                    int M, int m_base, int E, int H, int out_mode, void *__restrict__ out,
                    unsigned int *err)
 {
     pdl_trigger();   // dependents may launch now; each waits before reading our outputs
-    using Cfg = ProjCfg<InT, C>;
+    using Cfg = ProjCfg<InT, C, SHALLOW>;
     constexpr int NPL = Cfg::NPL, NST = Cfg::NST;
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[NST];
@@ -769,12 +772,12 @@ bi_status launch_gemv(Device *d, const void *x, const void *w, int M, int E, int
     return launch_pdl(kern, grid, dim3(32 * WPB), (size_t)Cfg::SMEM, s, tmx, tmw, M, E, H, logit_bf16, out, d->err);
 }
 
-template <typename InT, int C>
+template <typename InT, int C, bool SHALLOW = false>
 bi_status launch_proj(Device *d, const void *x, const void *w, int M, int m_base, int m_end, int E, int H,
                       int out_mode, void *out, cudaStream_t s, int kid)
 {
-    using Cfg = ProjCfg<InT, C>;
-    auto kern = router_proj_kernel<InT, C>;
+    using Cfg = ProjCfg<InT, C, SHALLOW>;
+    auto kern = router_proj_kernel<InT, C, SHALLOW>;
     bi_status st = set_smem_once(d, kid, kern, Cfg::SMEM);
     if (st != BI_OK) return st;
     const CUtensorMapDataType dt = sizeof(InT) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -802,9 +805,12 @@ bi_status launch_proj(Device *d, const void *x, const void *w, int M, int m_base
 
 template <typename InT>
 bi_status launch_proj_c(Device *d, int C, const void *x, const void *w, int M, int m_base, int m_end, int E,
-                        int H, int out_mode, void *out, cudaStream_t s)
+                        int H, int out_mode, void *out, cudaStream_t s, bool shallow = false)
 {
     const int base = KID_ROUTER_PROJ + (sizeof(InT) == 4 ? 0 : 5);
+    if (shallow)   // only C = 2 has the shallow ring
+        return launch_proj<InT, 2, true>(d, x, w, M, m_base, m_end, E, H, out_mode, out, s,
+                                         KID_ROUTER_PROJ_SHALLOW + (sizeof(InT) == 4 ? 0 : 1));
     switch (C) {
     case 1: return launch_proj<InT, 1>(d, x, w, M, m_base, m_end, E, H, out_mode, out, s, base + 0);
     case 2: return launch_proj<InT, 2>(d, x, w, M, m_base, m_end, E, H, out_mode, out, s, base + 1);
@@ -850,32 +856,39 @@ bi_status launch_select(Device *d, int epl, dim3 grid, dim3 block, cudaStream_t 
 // Batches up to this many tokens take the matrix-vector twin.
 constexpr int kGemvMaxM = 64;
 
-// How the projection's work is cut for a batch of M > kGemvMaxM rows.
-// Rows [0, m_split) run whole: one block holds all 16 partitions of a tile
-// and writes the logits.  Rows [m_split, M) (the tail) are cut into C
-// partition groups per tile, whose sums the selection adds.  Any plan gives
-// the same bits; plans differ only in how well the work fills the SMs.
-// The whole tiles take as many full waves (one tile per SM) as the batch
-// fills, rounded down to whole rows of tiles; the rest is the tail, and C
-// is the largest power of two (at most 16) that still gives every block an
-// SM of its own (tail tiles * C <= SMs) within 16 MiB of group sums.  Split
-// blocks have fewer warps and run best one to an SM: smaller groups that
-// stack several blocks on an SM measured slower.
+// How the projection's work is cut for a batch of M > kGemvMaxM rows (any
+// plan gives the same bits; plans differ only in how well the work fills
+// the SMs, and each rule below was the fastest measured in its range):
+//  - at least one 32 x 64 tile per SM: every tile's 16 partitions as two
+//    blocks of 8 (C = 2) with the shallow 96 KB ring, two blocks to an SM, so
+//    one block's start-up and partition tree overlap the other's arithmetic;
+//    the selection adds the two group sums (2*M*E*4 bytes of them);
+//  - fewer tiles than SMs: C = the largest power of two (at most 16) that
+//    still gives every block an SM of its own (tiles * C <= SMs), deep rings;
+//  - batches whose group sums would pass 64 MiB: rows [0, m_split) in whole
+//    tiles (all 16 partitions in one block, logits written directly) for as
+//    many full waves as they fill, and the tail rows split as in the
+//    previous rule, within 16 MiB of group sums.
 struct SplitPlan {
     int m_split, C;
+    bool shallow;
 };
 
 SplitPlan plan_split(int M, int E, int sms)
 {
     const long long n_et = (E + kTileE - 1) / kTileE, tiles_m = (M + kTileM - 1) / kTileM;
+    // at least a tile per SM: every tile as two 8-partition blocks with the
+    // shallow ring, two blocks to an SM (their start-up and tree phases then
+    // overlap the other's arithmetic); measured fastest from M = 2048 up
+    if (tiles_m * n_et >= sms && 2ll * M * E * 4 <= (64ll << 20)) return {0, 2, true};
     const long long waves = tiles_m * n_et / sms;
     const long long head_tm = waves * sms / n_et;
-    if (head_tm >= tiles_m) return {M, 1};
+    if (head_tm >= tiles_m) return {M, 1, false};
     const long long tail = (tiles_m - head_tm) * n_et, tail_rows = M - head_tm * kTileM;
     int c = 1;
     while (c < 16 && tail * 2 * c <= sms && 2ll * c * tail_rows * E * 4 <= (16ll << 20)) c *= 2;
-    if (c == 1) return {M, 1};
-    return {(int)(head_tm * kTileM), c};
+    if (c == 1) return {M, 1, false};
+    return {(int)(head_tm * kTileM), c, false};
 }
 
 }  // namespace
@@ -915,7 +928,7 @@ bi_status router_call(const void *x, const void *w_gate, bi_dtype in_dtype, bi_d
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(s);
 
     const bool small = M <= kGemvMaxM;
-    const SplitPlan plan = small ? SplitPlan{M, 1} : plan_split(M, E, d->sm_count);
+    const SplitPlan plan = small ? SplitPlan{M, 1, false} : plan_split(M, E, d->sm_count);
     void *part = nullptr;
     if (plan.m_split < M) {
         st = device_scratch(d, (size_t)plan.C * (M - plan.m_split) * E * sizeof(float), &part);
@@ -934,9 +947,10 @@ bi_status router_call(const void *x, const void *w_gate, bi_dtype in_dtype, bi_d
         // the tail goes first: it is the shorter launch, and the whole tiles
         // queue behind it on the SMs it leaves free
         if (plan.m_split < M) {
-            st = f32in ? launch_proj_c<float>(d, plan.C, x, w_gate, M, plan.m_split, M, E, H, OUT_PARTIAL, part, cs)
+            st = f32in ? launch_proj_c<float>(d, plan.C, x, w_gate, M, plan.m_split, M, E, H, OUT_PARTIAL, part, cs,
+                                              plan.shallow)
                        : launch_proj_c<__nv_bfloat16>(d, plan.C, x, w_gate, M, plan.m_split, M, E, H, OUT_PARTIAL,
-                                                      part, cs);
+                                                      part, cs, plan.shallow);
             if (st != BI_OK) return st;
         }
         if (plan.m_split > 0) {
@@ -958,6 +972,31 @@ bi_status router_call(const void *x, const void *w_gate, bi_dtype in_dtype, bi_d
 
 }  // namespace
 }  // namespace bi
+
+extern "C" bi_status bi_router_plan(int32_t M, int32_t E, int32_t *m_split, int32_t *C, int32_t *launches)
+{
+    if (M < 0 || E <= 0 || !m_split || !C || !launches) return BI_ERR_INVALID_ARG;
+    Device *d = nullptr;
+    int sms = 0;
+    if (current_device(&d) == BI_OK) {
+        sms = d->sm_count;
+    } else {
+        return BI_ERR_CUDA;
+    }
+    if (M == 0) {
+        *m_split = 0;
+        *C = 1;
+        *launches = 0;
+        return BI_OK;
+    }
+    const SplitPlan p = M <= kGemvMaxM ? SplitPlan{M, 1, false} : plan_split(M, E, sms);
+    *m_split = p.m_split;
+    *C = p.C;
+    // projection launches (matrix-vector twin or tiles: a split part and/or a
+    // whole-tile part) plus the selection
+    *launches = M <= kGemvMaxM ? 2 : (p.m_split < M ? 1 : 0) + (p.m_split > 0 ? 1 : 0) + 1;
+    return BI_OK;
+}
 
 extern "C" bi_status bi_router_topk(const void *x, const void *w_gate, bi_dtype in_dtype,
                                     bi_dtype logit_dtype, int32_t M, int32_t H, int32_t E, int32_t k,

@@ -179,3 +179,10 @@ def test_moe_m0_is_noop_and_workspace_size(lib):
 def test_rmsnorm_validation(lib, args, want):
     x, w, dt, M, H, eps, y, r = args
     assert lib.bi_rmsnorm(x, w, dt, M, H, C.c_float(eps), y, r, None) == want
+
+
+def test_router_plan_validation(lib):
+    x = C.c_int32()
+    assert lib.bi_router_plan(-1, 256, C.byref(x), C.byref(x), C.byref(x)) == 1
+    assert lib.bi_router_plan(16, 0, C.byref(x), C.byref(x), C.byref(x)) == 1
+    assert lib.bi_router_plan(16, 256, None, C.byref(x), C.byref(x)) == 1

@@ -35,10 +35,12 @@ def gpu_logits(bi, X, W, k, logit_dtype, noalloc=False):
     return gu.host(lg) if logit_dtype == "f32" else gu.host_bf16_bits(lg)
 
 
-# (M, H, E, k): matrix-vector twin (M <= 8, M <= 64), partition-split tiles,
-# whole tiles, whole tiles + split tail; ragged H and E
+# (M, H, E, k): matrix-vector twin (M <= 8, M <= 64), partition-split tiles
+# one block to an SM, two-block tiles two to an SM, whole tiles + split tail
+# (E = 1024, M = 8300: group sums past 64 MiB); ragged H and E
 SHAPES = [(1, 2048, 256, 8), (7, 264, 96, 5), (20, 2048, 256, 8), (64, 136, 1024, 32), (100, 2048, 256, 8),
-          (300, 136, 64, 4), (700, 264, 256, 8), (1300, 2048, 256, 8), (1235, 128, 256, 8)]
+          (300, 136, 64, 4), (700, 264, 256, 8), (1300, 2048, 256, 8), (1235, 128, 256, 8),
+          (8300, 136, 1024, 16)]
 
 
 @pytest.mark.parametrize("M,H,E,k", SHAPES)
@@ -76,8 +78,8 @@ def test_router_noalloc_is_the_contract(bi):
 
 
 def test_router_full_size_sampled_rows_are_the_contract(bi):
-    """M = 4096 (the benchmark's launch: whole tiles for rows 0..3647, a
-    split tail after): sampled rows of both parts."""
+    """M = 4096 (the benchmark's launch: two-block tiles, two to an SM):
+    sampled rows across the batch."""
     from oracle import contract
     M, H, E, k = 4096, 2048, 256, 8
     X = synth.tokens(53, 0, 0, M, H)

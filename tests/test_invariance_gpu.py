@@ -48,7 +48,7 @@ def test_tiny_mscan(bi):
 
 
 M_SWEEP = [1, 2, 4, 8, 16, 19, 32] + list(range(35, 65)) + [65, 75, 96, 128, 256, 512, 1024, 2048, 4096]
-# batches past one full wave of tiles, with the request in the split tail
+# batches of at least a tile per SM (two-block tiles), with the request last
 TAIL_SWEEP = [1235, 1300, 1400, 2500, 3000, 4096]
 
 
@@ -94,7 +94,7 @@ def test_router256_m_sweep(bi):
         torch.cuda.synchronize()
         got = rows_bytes(out, off, M)
         for f in FIELDS:
-            assert got[f] == solo[f], f"{f} differs at M={M} (tail rows)"
+            assert got[f] == solo[f], f"{f} differs at M={M} (last rows)"
         n += 1
     assert n == len(M_SWEEP) + len(TAIL_SWEEP) == 52
 

@@ -1,9 +1,10 @@
 """Router parity: bi_router_topk on the GPU against the CPU oracle.
 
 The library splits each 32x64 tile's 16 partitions over 1, 2, 4, 8 or 16
-thread blocks depending on M (beyond one full wave of tiles, only the tail
-rows are split); the cases below cover every split in every input/logit
-dtype, including E that is not a multiple of the 64-expert tile.
+thread blocks depending on M (from one tile per SM on, two blocks of 8; for
+batches whose group sums would pass 64 MiB, whole tiles plus a split tail);
+the cases below cover every split in every input/logit dtype, including E
+that is not a multiple of the 64-expert tile.
 
 Logits within the stated tolerance of the exact dot; ids bit-exact wherever
 the oracle's margin exceeds twice that tolerance; the oracle's top-k applied
@@ -55,8 +56,8 @@ CASES_F32 = [
     (1, 2048, 256, 8), (7, 2048, 256, 8), (75, 2048, 256, 8), (300, 2048, 256, 8),
     (1100, 2048, 256, 8), (520, 200, 128, 6), (3000, 136, 1024, 32),
     (33, 264, 96, 5), (5, 8, 32, 1), (70, 136, 1024, 32), (600, 264, 96, 5),
-    # more tiles than one wave: whole tiles for the head rows, a partition
-    # split for the tail rows (E = 256: 8 groups; E = 64 and 1024: 16)
+    # at least a tile per SM: every tile as two 8-partition blocks, two blocks
+    # to an SM (the shallow ring)
     (1300, 2048, 256, 8), (4904, 128, 64, 4), (400, 136, 1024, 32),
 ]
 
@@ -173,15 +174,16 @@ def test_router_nan_and_zero_rules(bi, orc):
     assert np.array_equal(g["ids"], sel["ids"])
 
 
-@pytest.mark.parametrize("E,M", [(64, 5000), (256, 1300), (1024, 400)])
-def test_router_splits_bit_identical(bi, E, M):
+@pytest.mark.parametrize("E,M,H", [(64, 5000, 2048), (256, 1300, 2048), (1024, 400, 2048), (1024, 8300, 136)])
+def test_router_splits_bit_identical(bi, E, M, H):
     """The same tokens under different work splits: the first and the last
     300 rows of an M-token batch, each also computed as a 300-token batch,
-    give identical bytes in every output.  In the M-token batch the first
-    rows run as whole tiles and the last rows in the partition-split tail;
-    as 300-token batches they are split differently again."""
+    give identical bytes in every output.  The M-token batches run as
+    two-block tiles; at E = 1024, M = 8300 the group sums would pass 64 MiB,
+    so rows 0..8191 run as whole tiles and the last rows as a split tail.
+    As 300-token batches the rows are split differently again."""
     import torch
-    H, k = 2048, 8
+    k = 8
     X = synth.tokens(6, 0, 0, M, H)
     w = gu.dev_f32(synth.router_weights(6, 0, E, H))
     big = bi.router_topk(gu.dev_f32(X), w, k, "f32")
@@ -190,3 +192,17 @@ def test_router_splits_bit_identical(bi, E, M):
         torch.cuda.synchronize()
         for f in ("logits", "ids", "weights", "margin", "margin_ulps"):
             assert small[f].cpu().numpy().tobytes() == big[f][a:a + 300].cpu().numpy().tobytes(), (a, f)
+
+
+def test_router_plan_reports_the_cut(bi):
+    """bi_router_plan on a 152-SM GB300: the matrix-vector twin below 65
+    rows, two-block tiles once the tiles fill the SMs, whole tiles plus a
+    split tail where the group sums would pass 64 MiB."""
+    import torch
+    if torch.cuda.get_device_properties(0).multi_processor_count != 152:
+        pytest.skip("plan thresholds are stated for 152 SMs")
+    assert bi.router_plan(1, 256) == (1, 1, 2)
+    assert bi.router_plan(64, 256) == (64, 1, 2)
+    assert bi.router_plan(4096, 256) == (0, 2, 2)
+    assert bi.router_plan(256, 256) == (0, 4, 2)
+    assert bi.router_plan(8300, 1024) == (8192, 2, 3)
