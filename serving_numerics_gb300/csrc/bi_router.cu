@@ -19,11 +19,12 @@
 // warps each, one warp per partition).  A block adds its partitions with the
 // lower levels of the tree; with C > 1 the C group sums meet in library
 // scratch and the selection kernel adds them with the remaining upper
-// levels.  C grows only when there are too few tiles to fill the GPU.
+// levels.  The plan (plan_split below) picks C from M; batches of at most 64
+// rows take the matrix-vector twin instead.
 //
-// Data path: each partition's [32 rows x 8] block of X and [64 rows x 8]
-// block of W_gate are staged by TMA into shared memory (f32: 32-byte
-// swizzle), a ring of stages deep.  Lane (tg, eg) of a warp owns tokens
+// Data path: the X and W_gate blocks of a slab are staged by TMA into
+// shared memory in boxes of 4 (f32) or 8 (bf16) partition blocks, 128-byte
+// rows with the 128-byte swizzle, a ring of stages deep.  Lane (tg, eg) of a warp owns tokens
 // tg + 4j and experts eg + 8i (j, i < 8): 64 accumulators.  A 128-bit
 // shared load moves 512 bytes whatever the lanes share, so the shared-memory
 // path delivers 32 lane-floats per clock against 128 FMAs per clock; an
