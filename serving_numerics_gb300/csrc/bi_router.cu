@@ -386,8 +386,13 @@ __device__ __forceinline__ float gate_partition(const InT *xr, const InT *w, int
 // the largest rejected logit for the margin.  Rows below m_split already
 // have their logits (the projection ran whole for them); rows from m_split
 // on have C group sums in `part`, laid out group-major over those rows.
+// Blocks per SM the register budget is set for: E <= 256 keeps four blocks
+// (three with the gate's 72 KB of staged rows each); larger E is left free.
 template <int EPLM, bool GATE>
-__global__ void __launch_bounds__(32 * kSelWarps)
+constexpr int sel_min_blocks() { return EPLM <= 8 ? (GATE ? 3 : 4) : 1; }
+
+template <int EPLM, bool GATE>
+__global__ void __launch_bounds__(32 * kSelWarps, sel_min_blocks<EPLM, GATE>())
 router_select_kernel(const float *__restrict__ part, int C, int m_split, void *logits, int logit_bf16,
                      int M, int E, int k, int32_t *__restrict__ ids, float *__restrict__ weights,
                      float *__restrict__ margin, int32_t *__restrict__ ulps, GateArgs gate, int H)
