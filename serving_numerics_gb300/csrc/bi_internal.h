@@ -98,7 +98,7 @@ enum : int {
     KID_ROUTER_GEMV = 30,  // 4 instantiations: 30..33
     KID_SELECT_GATE = 34,  // 4 instantiations: 34..37
     KID_MOE = 40,          // 5 kernels: 40..44
-    KID_NORM = 45,         // 4 instantiations: 45..48
+    KID_NORM = 45,         // 2 instantiations: 45..46
     KID_ROUTER_PROJ_SHALLOW = 49,   // 2 instantiations: 49..50
 };
 

@@ -12,10 +12,11 @@
 //
 // Half a warp per row, lane q = partition q (the shared gate's layout): the
 // butterfly shuffles with offsets 1, 2, 4, 8 add the partials in the
-// pairwise tree.  Rows up to H = 2048 stay in registers between the sum and
-// the scaling (one read of the row, all of a lane's loads in flight at
-// once); longer rows are read twice.  y is written in 16-byte stores.
-// Nothing depends on M or on the other rows.
+// pairwise tree.  The row is read twice, eight slabs of loads in flight per
+// pass (the second pass finds it in L2; holding whole rows in registers
+// instead needs 169 registers per thread and measured slower, two waves of
+// rows instead of one).  y is written in 16-byte stores.  Nothing depends
+// on M or on the other rows.
 #include <cuda_bf16.h>
 
 #include "bi_device.cuh"
@@ -46,61 +47,10 @@ __device__ __forceinline__ uint32_t pack2(float a, float b)
     return *reinterpret_cast<const uint32_t *>(&v);
 }
 
-// Rows of at most kRegSlabs slabs (H <= 2048) are held in registers: all of
-// a lane's loads are in flight at once and the row is read once.
-constexpr int kRegSlabs = 16;
+constexpr int kStreamSlabs = 8;
 
-template <typename InT>
-__global__ void __launch_bounds__(32 * kNormWarps)
-rmsnorm_reg_kernel(const InT *__restrict__ x, const InT *__restrict__ w, int M, int H, float eps,
-                   __nv_bfloat16 *__restrict__ y, float *__restrict__ rstd)
-{
-    pdl_trigger();   // dependents may launch now; each waits before reading our outputs
-    pdl_wait();
-    const int lane = threadIdx.x & 31, q = lane & 15;
-    const int m = (blockIdx.x * kNormWarps + (threadIdx.x >> 5)) * 2 + (lane >> 4);
-    const bool active = m < M;
-    const InT *xr = x + (size_t)(active ? m : 0) * H;
-    float v[kRegSlabs][8];
-#pragma unroll
-    for (int s = 0; s < kRegSlabs; ++s) {
-        const int h0 = kRouterSlab * s + kRouterBlock * q;
-        if (h0 < H) ld8(xr + h0, v[s]);
-    }
-    float acc = 0.0f;
-#pragma unroll
-    for (int s = 0; s < kRegSlabs; ++s) {
-        const int h0 = kRouterSlab * s + kRouterBlock * q;
-        if (h0 < H) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) acc = __fmaf_rn(v[s][i], v[s][i], acc);
-        }
-    }
-#pragma unroll
-    for (int d = 1; d < 16; d *= 2) acc = acc + __shfl_xor_sync(0xFFFFFFFFu, acc, d);
-    const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(acc, (float)H), eps)));
-    if (!active) return;
-    if (q == 0 && rstd) rstd[m] = r;
-    __nv_bfloat16 *yr = y + (size_t)m * H;
-#pragma unroll
-    for (int s = 0; s < kRegSlabs; ++s) {
-        const int h0 = kRouterSlab * s + kRouterBlock * q;
-        if (h0 < H) {
-            float wv[8], o[8];
-            ld8(w + h0, wv);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) o[i] = __fmul_rn(__fmul_rn(v[s][i], r), wv[i]);
-            uint4 p;
-            p.x = pack2(o[0], o[1]);
-            p.y = pack2(o[2], o[3]);
-            p.z = pack2(o[4], o[5]);
-            p.w = pack2(o[6], o[7]);
-            *reinterpret_cast<uint4 *>(yr + h0) = p;
-        }
-    }
-}
-
-// Longer rows: two passes over the row, four slabs of loads in flight.
+// Two passes over the row (the second re-reads it from L2), kStreamSlabs
+// slabs of loads in flight per pass.
 template <typename InT>
 __global__ void __launch_bounds__(32 * kNormWarps)
 rmsnorm_kernel(const InT *__restrict__ x, const InT *__restrict__ w, int M, int H, float eps,
@@ -115,15 +65,15 @@ rmsnorm_kernel(const InT *__restrict__ x, const InT *__restrict__ w, int M, int 
     const int ns = (H + kRouterSlab - 1) / kRouterSlab;
 
     float acc = 0.0f;
-    for (int s0 = 0; s0 < ns; s0 += 4) {         // four slabs of loads in flight
-        float v[4][8];
+    for (int s0 = 0; s0 < ns; s0 += kStreamSlabs) {
+        float v[kStreamSlabs][8];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < kStreamSlabs; ++u) {
             const int h0 = kRouterSlab * (s0 + u) + kRouterBlock * q;
             if (h0 < H) ld8(xr + h0, v[u]);
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < kStreamSlabs; ++u) {
             const int h0 = kRouterSlab * (s0 + u) + kRouterBlock * q;
             if (h0 < H) {
 #pragma unroll
@@ -138,10 +88,10 @@ rmsnorm_kernel(const InT *__restrict__ x, const InT *__restrict__ w, int M, int 
     if (q == 0 && rstd) rstd[m] = r;
 
     __nv_bfloat16 *yr = y + (size_t)m * H;
-    for (int s0 = 0; s0 < ns; s0 += 4) {
-        float xv[4][8], wv[4][8];
+    for (int s0 = 0; s0 < ns; s0 += kStreamSlabs / 2) {
+        float xv[kStreamSlabs / 2][8], wv[kStreamSlabs / 2][8];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < kStreamSlabs / 2; ++u) {
             const int h0 = kRouterSlab * (s0 + u) + kRouterBlock * q;
             if (h0 < H) {
                 ld8(xr + h0, xv[u]);
@@ -149,7 +99,7 @@ rmsnorm_kernel(const InT *__restrict__ x, const InT *__restrict__ w, int M, int 
             }
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < kStreamSlabs / 2; ++u) {
             const int h0 = kRouterSlab * (s0 + u) + kRouterBlock * q;
             if (h0 < H) {
                 float o[8];
@@ -188,15 +138,13 @@ extern "C" bi_status bi_rmsnorm(const void *x, const void *w, bi_dtype dtype, in
     dim3 grid((M + rows_per_block - 1) / rows_per_block), block(32 * kNormWarps);
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(s);
     __nv_bfloat16 *y = static_cast<__nv_bfloat16 *>(y_out);
-    const bool in_regs = H <= kRouterSlab * kRegSlabs;
     if (dtype == BI_F32) {
-        auto kern = in_regs ? rmsnorm_reg_kernel<float> : rmsnorm_kernel<float>;
-        if ((st = set_smem_once(d, KID_NORM + (in_regs ? 2 : 0), kern, 0)) != BI_OK) return st;
-        return launch_pdl(kern, grid, block, 0, cs, static_cast<const float *>(x), static_cast<const float *>(w),
-                          (int)M, (int)H, eps, y, rstd_out);
+        if ((st = set_smem_once(d, KID_NORM + 0, rmsnorm_kernel<float>, 0)) != BI_OK) return st;
+        return launch_pdl(rmsnorm_kernel<float>, grid, block, 0, cs, static_cast<const float *>(x),
+                          static_cast<const float *>(w), (int)M, (int)H, eps, y, rstd_out);
     }
-    auto kern = in_regs ? rmsnorm_reg_kernel<__nv_bfloat16> : rmsnorm_kernel<__nv_bfloat16>;
-    if ((st = set_smem_once(d, KID_NORM + (in_regs ? 3 : 1), kern, 0)) != BI_OK) return st;
+    auto kern = rmsnorm_kernel<__nv_bfloat16>;
+    if ((st = set_smem_once(d, KID_NORM + 1, kern, 0)) != BI_OK) return st;
     return launch_pdl(kern, grid, block, 0, cs, static_cast<const __nv_bfloat16 *>(x),
                       static_cast<const __nv_bfloat16 *>(w), (int)M, (int)H, eps, y, rstd_out);
 }
