@@ -413,6 +413,18 @@ BI_API bi_status bi_get_config(bi_config *out, size_t out_size);
 BI_API bi_status bi_prefix_split(const int32_t *lengths, int32_t n_requests, int32_t block,
                                  int32_t *cached_out, int32_t *suffix_offsets_out);
 
+/*
+ * bi_selftest_fma_rate -- measurement aid: launches a kernel of 8 blocks of
+ * 256 threads per SM, each thread running 8 independent f32 fused
+ * multiply-add chains for iters x 16 steps, and reports the floating-point
+ * operations it performs in *flops_launched (2 per FMA).  Timing it with
+ * events on `s` gives the FP32 FMA rate this GPU sustains, the ceiling the
+ * router projection (pure FMA chains) is measured against.
+ *   iters  1 .. 2^20;  sink  device memory for at least 8 * SMs floats
+ *   (written only in a case that does not occur, to keep the work live).
+ */
+BI_API bi_status bi_selftest_fma_rate(int32_t iters, float *sink, bi_stream s, double *flops_launched);
+
 #define BI_ABI_VERSION 1
 BI_API int32_t bi_abi_version(void);
 

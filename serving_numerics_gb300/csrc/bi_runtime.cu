@@ -96,11 +96,46 @@ __global__ void selftest_wait_kernel(unsigned int *err, unsigned long long limit
     __syncthreads();
     if (threadIdx.x == 0) mbar_wait_limit(&bar, 0, err, 0xFEu, limit_ns);
 }
+// FP32 FMA rate probe: every thread runs 8 independent fused multiply-add
+// chains in registers (enough independent work to fill the FMA pipe), and
+// one thread per block writes a value that depends on all of them so that
+// nothing is optimised away.
+constexpr int kFmaChains = 8;
+
+__global__ void __launch_bounds__(256) fma_rate_kernel(int iters, float a, float b, float *sink)
+{
+    float x[kFmaChains];
+#pragma unroll
+    for (int c = 0; c < kFmaChains; ++c) x[c] = (float)(threadIdx.x + c);
+    for (int i = 0; i < iters; ++i) {
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+#pragma unroll
+            for (int c = 0; c < kFmaChains; ++c) x[c] = __fmaf_rn(x[c], a, b);
+        }
+    }
+    float t = 0.0f;
+#pragma unroll
+    for (int c = 0; c < kFmaChains; ++c) t += x[c];
+    if (t == 12345.678f) sink[blockIdx.x] = t;     // practically never true; keeps the chains live
+}
 }  // namespace
 
 }  // namespace bi
 
 extern "C" {
+
+bi_status bi_selftest_fma_rate(int32_t iters, float *sink, bi_stream s, double *flops_launched)
+{
+    if (iters < 1 || iters > (1 << 20) || !sink || !flops_launched) return BI_ERR_INVALID_ARG;
+    bi::Device *d = nullptr;
+    bi_status st = bi::current_device(&d);
+    if (st != BI_OK) return st;
+    const int blocks = 8 * d->sm_count;      // 8 blocks of 256 threads per SM: 64 warps
+    *flops_launched = 2.0 * blocks * 256.0 * (double)iters * 16.0 * bi::kFmaChains;
+    bi::fma_rate_kernel<<<blocks, 256, 0, reinterpret_cast<cudaStream_t>(s)>>>(iters, 0.999f, 0.001f, sink);
+    return bi::from_cuda(cudaGetLastError());
+}
 
 bi_status bi_selftest_wait_timeout(uint32_t limit_us, bi_stream s)
 {

@@ -70,5 +70,7 @@ def test_reference_arm_line(orc):
     assert r.returncode == 0, r.stderr
     line = json.loads(r.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["value"] > 0
-    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] == len(os.sched_getaffinity(0))
+    assert cb["single_thread_value"] > 0 and cb["nproc"] == os.cpu_count()
     assert line["e2e"]["h2d_bytes_per_step"] == 0
