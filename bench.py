@@ -58,40 +58,63 @@ FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
 
 
 class Clocks:
-    """nvidia-smi sampled every 200 ms during the timed region."""
+    """nvidia-smi sampled every 25 ms, each sample stamped by nvidia-smi
+    itself; only the samples whose stamps fall inside the timed region count
+    (mark() opens it, stop() closes it).  The region of a default run is
+    about 0.1 s, so it holds a few samples."""
 
     def __init__(self, gpu_index: int):
-        q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+        q = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        self.t_begin = None
         try:
             self.p = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={q}",
-                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                       "--format=csv,noheader,nounits", "-lms", "25"],
                                       stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.5)          # let nvidia-smi start sampling before the region opens
         except OSError:
             self.p = None
 
+    def mark(self):
+        import datetime
+        self.t_begin = datetime.datetime.now()
+
     def stop(self):
+        import datetime
+        t_end = datetime.datetime.now()
         if self.p is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)              # the sample that straddles the end
         self.p.terminate()
         out, _ = self.p.communicate(timeout=10)
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []
         for line in out.strip().splitlines():
             f = [x.strip() for x in line.split(",")]
-            if len(f) < 8:
+            if len(f) < 9:
                 continue
             try:
-                sm.append(float(f[0]))
-                mx.append(float(f[1]))
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f")
+                rows.append((ts, float(f[1]), float(f[2]), f[5:9]))
             except ValueError:
                 continue
-            for n, v in zip(names, f[4:8]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons), "samples": len(sm)}
+        t0 = self.t_begin or t_end
+        inside = [r for r in rows if t0 <= r[0] <= t_end]
+        widened = False
+        if not inside:               # region shorter than the sampling interval
+            pad = datetime.timedelta(milliseconds=100)
+            inside = [r for r in rows if t0 - pad <= r[0] <= t_end + pad]
+            widened = True
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = {n for r in inside for n, v in zip(names, r[3]) if v.lower() == "active"}
+        sm = [r[1] for r in inside]
+        out = {"sm_mhz": statistics.median(sm) if sm else None,
+               "sm_max_mhz": max(r[2] for r in inside) if inside else None,
+               "reasons": sorted(reasons), "samples": len(sm),
+               "region_s": (t_end - t0).total_seconds()}
+        if widened:
+            out["window"] = "widened by 100 ms on each side (no sample inside the region)"
+        return out
 
 
 def dist_setup():
@@ -208,6 +231,7 @@ def run_ours(args):
     if ws > 1:
         dist.barrier()
     torch.cuda.synchronize()
+    clocks.mark()
     t0.record(stream)
     for s in range(args.steps):
         step(evs[s])
@@ -263,6 +287,7 @@ def run_ours(args):
     d2h = M * K_TOP * 8 + N_REQ * 8
 
     fma_tflops = fma_probe(bi, torch, dev)
+    fma2_tflops = fma_probe(bi, torch, dev, packed=True)
     hbm, bf16_burst, bf16_sus, src = peaks()
     value = whole_job_rate(M, ws, args.steps, ms / 1e3)
     g_avg = statistics.mean(gemm_ms) / 1e3
@@ -284,7 +309,7 @@ def run_ours(args):
                              "(timed as one call, so the selection counts against the projection)",
                    "algorithmic_bytes": r_bytes, "hbm_time_frac": (r_bytes / (hbm * 1e9)) / r_avg,
                    "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 flop x 2070 MHz",
-                   "fma_probe_tflops": fma_tflops,
+                   "fma_probe_tflops": fma_tflops, "fma_probe_packed_tflops": fma2_tflops,
                    "frac_of_fma_probe": r_flop / r_avg / 1e12 / fma_tflops}
     out = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
@@ -410,20 +435,21 @@ def moe_measure(bi, synth, torch, dev, hbm_gbs, X, ids, wts, reps=10):
                          "frac": byt / t / 1e9 / hbm_gbs, "algorithmic_bytes": byt, "traffic": None}}
 
 
-def fma_probe(bi, torch, dev) -> float:
+def fma_probe(bi, torch, dev, packed: bool = False) -> float:
     """The FP32 FMA rate this GPU sustains, in TFLOP/s: the library's probe
     kernel (8 blocks of 256 threads per SM, 8 independent register-resident
-    fused multiply-add chains per thread), timed with CUDA events on the
-    launching stream; the best of five launches of about 20 ms each."""
+    fused multiply-add chains per thread; packed: each chain two lanes of the
+    two-wide f32 FMA instruction), timed with CUDA events on the launching
+    stream; the best of five launches of about 20 ms each."""
     sink = torch.empty((8 * 1024,), dtype=torch.float32, device=dev)
     iters = 20000
-    bi.selftest_fma_rate(iters, sink)
+    bi.selftest_fma_rate(iters, sink, packed=packed)
     best = 0.0
     for _ in range(5):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
         a.record()
-        flop = bi.selftest_fma_rate(iters, sink)
+        flop = bi.selftest_fma_rate(iters, sink, packed=packed)
         b.record()
         torch.cuda.synchronize()
         best = max(best, flop / (a.elapsed_time(b) / 1e3) / 1e12)

@@ -420,10 +420,14 @@ BI_API bi_status bi_prefix_split(const int32_t *lengths, int32_t n_requests, int
  * operations it performs in *flops_launched (2 per FMA).  Timing it with
  * events on `s` gives the FP32 FMA rate this GPU sustains, the ceiling the
  * router projection (pure FMA chains) is measured against.
- *   iters  1 .. 2^20;  sink  device memory for at least 8 * SMs floats
- *   (written only in a case that does not occur, to keep the work live).
+ *   iters   1 .. 2^20
+ *   packed  0: scalar f32 FMAs; 1: each chain a pair of lanes of the two-wide
+ *           f32 FMA instruction (two independent FMAs, each rounded once)
+ *   sink    device memory for at least 8 * SMs floats (written only in a
+ *           case that does not occur, to keep the work live)
  */
-BI_API bi_status bi_selftest_fma_rate(int32_t iters, float *sink, bi_stream s, double *flops_launched);
+BI_API bi_status bi_selftest_fma_rate(int32_t iters, int32_t packed, float *sink, bi_stream s,
+                                      double *flops_launched);
 
 #define BI_ABI_VERSION 1
 BI_API int32_t bi_abi_version(void);

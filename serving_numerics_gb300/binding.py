@@ -33,7 +33,7 @@ SIGNATURES = {
     "bi_get_last_device_error": (C.c_int, []),
     "bi_abi_version": (C.c_int32, []),
     "bi_selftest_wait_timeout": (C.c_int, [C.c_uint32, _P]),
-    "bi_selftest_fma_rate": (C.c_int, [_I32, _P, _P, _P]),
+    "bi_selftest_fma_rate": (C.c_int, [_I32, _I32, _P, _P, _P]),
     "bi_get_config": (C.c_int, [_P, C.c_size_t]),
     "bi_router_plan": (C.c_int, [_I32, _I32, _P, _P, _P]),
     "bi_rmsnorm": (C.c_int, [_P, _P, C.c_int, _I32, _I32, C.c_float, _P, _P, _P]),
@@ -223,10 +223,11 @@ def moe_expert_gemm(X, ids, weights, W, stream=None, want_y=True, want_out=True,
     return {"Y": Y, "out": out}
 
 
-def selftest_fma_rate(iters: int, sink, stream=None) -> float:
+def selftest_fma_rate(iters: int, sink, packed: bool = False, stream=None) -> float:
     """Launch the FP32 FMA rate probe; returns the FLOPs it performs."""
     f = C.c_double()
-    _check(load().bi_selftest_fma_rate(iters, _ptr(sink), _stream(stream), C.byref(f)), "bi_selftest_fma_rate")
+    _check(load().bi_selftest_fma_rate(iters, int(packed), _ptr(sink), _stream(stream), C.byref(f)),
+           "bi_selftest_fma_rate")
     return f.value
 
 

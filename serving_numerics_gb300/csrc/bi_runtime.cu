@@ -99,24 +99,48 @@ __global__ void selftest_wait_kernel(unsigned int *err, unsigned long long limit
 // FP32 FMA rate probe: every thread runs 8 independent fused multiply-add
 // chains in registers (enough independent work to fill the FMA pipe), and
 // one thread per block writes a value that depends on all of them so that
-// nothing is optimised away.
+// nothing is optimised away.  PACKED runs each chain as a pair of lanes of
+// the two-wide f32 FMA (fma.rn.f32x2: two independent f32 fused
+// multiply-adds, each rounded once, in one instruction).
 constexpr int kFmaChains = 8;
 
+template <bool PACKED>
 __global__ void __launch_bounds__(256) fma_rate_kernel(int iters, float a, float b, float *sink)
 {
-    float x[kFmaChains];
-#pragma unroll
-    for (int c = 0; c < kFmaChains; ++c) x[c] = (float)(threadIdx.x + c);
-    for (int i = 0; i < iters; ++i) {
-#pragma unroll
-        for (int u = 0; u < 16; ++u) {
-#pragma unroll
-            for (int c = 0; c < kFmaChains; ++c) x[c] = __fmaf_rn(x[c], a, b);
-        }
-    }
     float t = 0.0f;
+    if constexpr (!PACKED) {
+        float x[kFmaChains];
 #pragma unroll
-    for (int c = 0; c < kFmaChains; ++c) t += x[c];
+        for (int c = 0; c < kFmaChains; ++c) x[c] = (float)(threadIdx.x + c);
+        for (int i = 0; i < iters; ++i) {
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+#pragma unroll
+                for (int c = 0; c < kFmaChains; ++c) x[c] = __fmaf_rn(x[c], a, b);
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < kFmaChains; ++c) t += x[c];
+    } else {
+        uint64_t x[kFmaChains];
+        const uint64_t a2 = (uint64_t)__float_as_uint(a) | ((uint64_t)__float_as_uint(a) << 32);
+        const uint64_t b2 = (uint64_t)__float_as_uint(b) | ((uint64_t)__float_as_uint(b) << 32);
+#pragma unroll
+        for (int c = 0; c < kFmaChains; ++c)
+            x[c] = (uint64_t)__float_as_uint((float)(threadIdx.x + c)) |
+                   ((uint64_t)__float_as_uint((float)(threadIdx.x + 2 * c)) << 32);
+        for (int i = 0; i < iters; ++i) {
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+#pragma unroll
+                for (int c = 0; c < kFmaChains; ++c)
+                    asm("fma.rn.f32x2 %0, %0, %1, %2;" : "+l"(x[c]) : "l"(a2), "l"(b2));
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < kFmaChains; ++c)
+            t += __uint_as_float((uint32_t)x[c]) + __uint_as_float((uint32_t)(x[c] >> 32));
+    }
     if (t == 12345.678f) sink[blockIdx.x] = t;     // practically never true; keeps the chains live
 }
 }  // namespace
@@ -125,15 +149,19 @@ __global__ void __launch_bounds__(256) fma_rate_kernel(int iters, float a, float
 
 extern "C" {
 
-bi_status bi_selftest_fma_rate(int32_t iters, float *sink, bi_stream s, double *flops_launched)
+bi_status bi_selftest_fma_rate(int32_t iters, int32_t packed, float *sink, bi_stream s, double *flops_launched)
 {
-    if (iters < 1 || iters > (1 << 20) || !sink || !flops_launched) return BI_ERR_INVALID_ARG;
+    if (iters < 1 || iters > (1 << 20) || (packed != 0 && packed != 1) || !sink || !flops_launched)
+        return BI_ERR_INVALID_ARG;
     bi::Device *d = nullptr;
     bi_status st = bi::current_device(&d);
     if (st != BI_OK) return st;
     const int blocks = 8 * d->sm_count;      // 8 blocks of 256 threads per SM: 64 warps
-    *flops_launched = 2.0 * blocks * 256.0 * (double)iters * 16.0 * bi::kFmaChains;
-    bi::fma_rate_kernel<<<blocks, 256, 0, reinterpret_cast<cudaStream_t>(s)>>>(iters, 0.999f, 0.001f, sink);
+    *flops_launched = 2.0 * blocks * 256.0 * (double)iters * 16.0 * bi::kFmaChains * (packed ? 2 : 1);
+    if (packed)
+        bi::fma_rate_kernel<true><<<blocks, 256, 0, reinterpret_cast<cudaStream_t>(s)>>>(iters, 0.999f, 0.001f, sink);
+    else
+        bi::fma_rate_kernel<false><<<blocks, 256, 0, reinterpret_cast<cudaStream_t>(s)>>>(iters, 0.999f, 0.001f, sink);
     return bi::from_cuda(cudaGetLastError());
 }
 

@@ -141,10 +141,11 @@ def test_selftest_validation(lib):
     assert lib.bi_selftest_wait_timeout(2000001, None) == 1
     import ctypes as C
     f = C.c_double()
-    assert lib.bi_selftest_fma_rate(0, FAKE, None, C.byref(f)) == 1
-    assert lib.bi_selftest_fma_rate((1 << 20) + 1, FAKE, None, C.byref(f)) == 1
-    assert lib.bi_selftest_fma_rate(10, None, None, C.byref(f)) == 1
-    assert lib.bi_selftest_fma_rate(10, FAKE, None, None) == 1
+    assert lib.bi_selftest_fma_rate(0, 0, FAKE, None, C.byref(f)) == 1
+    assert lib.bi_selftest_fma_rate((1 << 20) + 1, 0, FAKE, None, C.byref(f)) == 1
+    assert lib.bi_selftest_fma_rate(10, 2, FAKE, None, C.byref(f)) == 1
+    assert lib.bi_selftest_fma_rate(10, 0, None, None, C.byref(f)) == 1
+    assert lib.bi_selftest_fma_rate(10, 1, FAKE, None, None) == 1
 
 
 def _moe(lib, **kw):
