@@ -285,6 +285,16 @@ def run_ours(args):
     e2e_s = reduce_max(time.perf_counter() - w0, dev)
     h2d = LAYERS * (M * H * 4 + M * G_K * 2)
     d2h = M * K_TOP * 8 + N_REQ * 8
+    # the host link's own rate: one layer's inputs copied alone, as above
+    torch.cuda.synchronize()
+    c0 = time.perf_counter()
+    for l in range(8):
+        with torch.cuda.stream(copy):
+            X[l].copy_(pin_X[l], non_blocking=True)
+            A[l].copy_(pin_A[l], non_blocking=True)
+    copy.synchronize()
+    h2d_gbs = 8 * (M * H * 4 + M * G_K * 2) / (time.perf_counter() - c0) / 1e9
+    copy_bound = M * ws / (h2d / (h2d_gbs * 1e9))
 
     fma_tflops = fma_probe(bi, torch, dev)
     fma2_tflops = fma_probe(bi, torch, dev, packed=True)
@@ -330,7 +340,9 @@ def run_ours(args):
         # the kernel with the larger share of the step's device time
         "roofline": roof_router if r_avg >= g_avg else roof_gemm,
         "e2e": {"value": whole_job_rate(M, ws, e2e_steps, e2e_s), "unit": "tokens/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "h2d_gbs_measured": h2d_gbs, "copy_bound_tokens_per_s": copy_bound,
+                "frac_of_copy_bound": whole_job_rate(M, ws, e2e_steps, e2e_s) / copy_bound},
         "gpu_launches": launches_per_layer * LAYERS * args.steps,
         "clocks": ck,
     }
