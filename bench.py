@@ -50,8 +50,13 @@ def peaks():
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
 # capture of the kernel as it stands, at this launch shape; None where no capture of the
-# current code exists.  Reset to None whenever the kernel changes.
-NCU_TRAFFIC = {"gemm_bf16_kernel": 67_437_056 + 12_296_448, "router_call": None}
+# current code exists.  Reset to None whenever the kernel changes.  The router call is
+# its two launches (projection + selection) captured inside the layer sequence with the
+# caches as the preceding kernels left them; its writes include L2 evictions of the
+# preceding kernels' dirty lines.
+NCU_TRAFFIC = {"gemm_bf16_kernel": 67_437_056 + 12_296_448,
+               "router_call": (35_696_384 + 16_336_128 + 72_448 + 1_716_224
+                               + 35_652_608 + 17_161_216 + 17_664 + 1_986_816) // 2}
 
 # FP32 FMA peak from unit counts and clock: 152 SMs x 128 FP32 lanes x 2 flop x 2070 MHz
 FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
@@ -288,12 +293,13 @@ def run_ours(args):
     # the host link's own rate: one layer's inputs copied alone, as above
     torch.cuda.synchronize()
     c0 = time.perf_counter()
-    for l in range(8):
+    n_probe = min(8, len(X))
+    for l in range(n_probe):
         with torch.cuda.stream(copy):
             X[l].copy_(pin_X[l], non_blocking=True)
             A[l].copy_(pin_A[l], non_blocking=True)
     copy.synchronize()
-    h2d_gbs = 8 * (M * H * 4 + M * G_K * 2) / (time.perf_counter() - c0) / 1e9
+    h2d_gbs = n_probe * (M * H * 4 + M * G_K * 2) / (time.perf_counter() - c0) / 1e9
     copy_bound = M * ws / (h2d / (h2d_gbs * 1e9))
 
     fma_tflops = fma_probe(bi, torch, dev)
