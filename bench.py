@@ -54,9 +54,7 @@ def peaks():
 # its two launches (projection + selection) captured inside the layer sequence with the
 # caches as the preceding kernels left them; its writes include L2 evictions of the
 # preceding kernels' dirty lines.
-NCU_TRAFFIC = {"gemm_bf16_kernel": 67_437_056 + 12_296_448,
-               "router_call": (35_696_384 + 16_336_128 + 72_448 + 1_716_224
-                               + 35_652_608 + 17_161_216 + 17_664 + 1_986_816) // 2}
+NCU_TRAFFIC = {"gemm_bf16_kernel": 67_437_056 + 12_296_448, "router_call": None}
 
 # FP32 FMA peak from unit counts and clock: 152 SMs x 128 FP32 lanes x 2 flop x 2070 MHz
 FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12

@@ -92,14 +92,16 @@ bi_status set_smem_once(Device *d, int kernel_id, K kernel, size_t bytes)
 enum : int {
     KID_ROUTER_PROJ = 0,   // 10 instantiations: 0..9
     KID_GEMM = 16,
-    KID_SELECT = 20,       // 4 instantiations: 20..23
+    KID_SELECT = 20,       // 4 instantiations: 20..23 (two group sums or none)
     KID_GATE = 24,
     KID_HASH = 25,         // 4 instantiations: 25..28
     KID_ROUTER_GEMV = 30,  // 4 instantiations: 30..33
-    KID_SELECT_GATE = 34,  // 4 instantiations: 34..37
+    KID_SELECT_GATE = 34,  // 4 instantiations: 34..37 (two group sums or none)
     KID_MOE = 40,          // 5 kernels: 40..44
     KID_NORM = 45,         // 2 instantiations: 45..46
     KID_ROUTER_PROJ_SHALLOW = 49,   // 2 instantiations: 49..50
+    KID_SELECT_GENERAL = 51,        // 4 instantiations: 51..54
+    KID_SELECT_GATE_GENERAL = 55,   // 4 instantiations: 55..58
 };
 
 }  // namespace bi

@@ -381,6 +381,34 @@ __device__ __forceinline__ float gate_partition(const InT *xr, const InT *w, int
     return acc;
 }
 
+// The top log2(CC) levels of the pairwise tree for a split row: lane's
+// logits i (experts lane + 32 i) from the CC group sums (group-major planes
+// gs floats apart), loaded about 32 at a time before their adds.
+template <int EPLM, int CC>
+__device__ __forceinline__ void group_tree(const float *__restrict__ part, size_t gs, size_t prow, int epl,
+                                           float (&v)[EPLM])
+{
+    constexpr int IB0 = 32 / CC > 0 ? 32 / CC : 1;
+    constexpr int IB = IB0 < EPLM ? IB0 : EPLM;      // logits per batch of loads
+#pragma unroll
+    for (int i0 = 0; i0 < EPLM; i0 += IB) {
+        float p[IB][CC];
+#pragma unroll
+        for (int u = 0; u < IB; ++u)
+#pragma unroll
+            for (int q = 0; q < CC; ++q)
+                p[u][q] = i0 + u < epl ? part[(size_t)q * gs + prow + 32 * (i0 + u)] : 0.0f;
+#pragma unroll
+        for (int u = 0; u < IB; ++u) {
+#pragma unroll
+            for (int d = 1; d < CC; d *= 2)
+#pragma unroll
+                for (int q = 0; q + d < CC; q += 2 * d) p[u][q] = p[u][q] + p[u][q + d];
+            v[i0 + u] = p[u][0];
+        }
+    }
+}
+
 // One warp per token: finish the tree (C > 1), round to the logit dtype,
 // then k+1 rounds of warp arg-max (value desc, index asc).  Round k yields
 // the largest rejected logit for the margin.  Rows below m_split already
@@ -391,7 +419,12 @@ __device__ __forceinline__ float gate_partition(const InT *xr, const InT *w, int
 template <int EPLM, bool GATE>
 constexpr int sel_min_blocks() { return EPLM <= 8 ? (GATE ? 3 : 4) : 1; }
 
-template <int EPLM, bool GATE>
+// TWO: the instantiation for split rows with two group sums (or none), with
+// a run-time-C loop as its general case; the other instantiation adds 4, 8
+// or 16 sums with trees unrolled at compile time.  (Same-box timings: the
+// compile-time trees in the two-sum kernel cost it 1.5 us per call at
+// M = 4096; in their own kernel they take 2 us off the calls at M = 128-256.)
+template <int EPLM, bool GATE, bool TWO>
 __global__ void __launch_bounds__(32 * kSelWarps, sel_min_blocks<EPLM, GATE>())
 router_select_kernel(const float *__restrict__ part, int C, int m_split, void *logits, int logit_bf16,
                      int M, int E, int k, int32_t *__restrict__ ids, float *__restrict__ weights,
@@ -442,18 +475,39 @@ router_select_kernel(const float *__restrict__ part, int C, int m_split, void *l
         // logit dtype and store the logits
         const size_t gs = (size_t)(M - m_split) * E;
         const size_t prow = (size_t)(m - m_split) * E + lane;
+        if constexpr (TWO) {
+            if (C == 2) {      // the common split (two-block tiles): the tree's top level only
+                const float *p0 = part + prow, *p1 = part + gs + prow;
+                float a[EPLM], b[EPLM];
 #pragma unroll
-        for (int i = 0; i < EPLM; ++i) {
-            float p[16];
-#pragma unroll
-            for (int q = 0; q < 16; ++q) p[q] = (i < epl && q < C) ? part[(size_t)q * gs + prow + 32 * i] : 0.0f;
-#pragma unroll
-            for (int d = 1; d < 16; d *= 2)
-                if (d < C) {
-#pragma unroll
-                    for (int q = 0; q + d < 16; q += 2 * d) p[q] = p[q] + p[q + d];
+                for (int i = 0; i < EPLM; ++i) {
+                    a[i] = i < epl ? p0[32 * i] : 0.0f;
+                    b[i] = i < epl ? p1[32 * i] : 0.0f;
                 }
-            v[i] = p[0];
+#pragma unroll
+                for (int i = 0; i < EPLM; ++i) v[i] = a[i] + b[i];
+            } else {           // any C, with C taken at run time
+#pragma unroll
+                for (int i = 0; i < EPLM; ++i) {
+                    float p[16];
+#pragma unroll
+                    for (int q = 0; q < 16; ++q)
+                        p[q] = (i < epl && q < C) ? part[(size_t)q * gs + prow + 32 * i] : 0.0f;
+#pragma unroll
+                    for (int d = 1; d < 16; d *= 2)
+                        if (d < C) {
+#pragma unroll
+                            for (int q = 0; q + d < 16; q += 2 * d) p[q] = p[q] + p[q + d];
+                        }
+                    v[i] = p[0];
+                }
+            }
+        } else if (C == 4) {   // a split row of the general instantiation has 4, 8 or 16 group sums
+            group_tree<EPLM, 4>(part, gs, prow, epl, v);
+        } else if (C == 8) {
+            group_tree<EPLM, 8>(part, gs, prow, epl, v);
+        } else {
+            group_tree<EPLM, 16>(part, gs, prow, epl, v);
         }
 #pragma unroll
         for (int i = 0; i < EPLM; ++i) {
@@ -831,8 +885,12 @@ bi_status launch_select1(Device *d, dim3 grid, dim3 block, cudaStream_t cs, cons
                          int m_split, void *logits, int lbf, int M, int E, int k, int32_t *ids, float *w, float *mg,
                          int32_t *mu, const GateArgs &gate, int H)
 {
-    const int kid = (gate.gx ? KID_SELECT_GATE : KID_SELECT) + (EPLM == 4 ? 0 : EPLM == 8 ? 1 : EPLM == 16 ? 2 : 3);
-    auto kern = gate.gx ? router_select_kernel<EPLM, true> : router_select_kernel<EPLM, false>;
+    const bool two = C <= 2;
+    const int kid = (gate.gx ? (two ? KID_SELECT_GATE : KID_SELECT_GATE_GENERAL)
+                             : (two ? KID_SELECT : KID_SELECT_GENERAL)) +
+                    (EPLM == 4 ? 0 : EPLM == 8 ? 1 : EPLM == 16 ? 2 : 3);
+    auto kern = gate.gx ? (two ? router_select_kernel<EPLM, true, true> : router_select_kernel<EPLM, true, false>)
+                        : (two ? router_select_kernel<EPLM, false, true> : router_select_kernel<EPLM, false, false>);
     bi_status st = set_smem_once(d, kid, kern, gate.gx ? kGateStageMax : 0);
     if (st != BI_OK) return st;
     GateArgs g = gate;
