@@ -54,7 +54,9 @@ def peaks():
 # its two launches (projection + selection) captured inside the layer sequence with the
 # caches as the preceding kernels left them; its writes include L2 evictions of the
 # preceding kernels' dirty lines.
-NCU_TRAFFIC = {"gemm_bf16_kernel": 67_437_056 + 12_296_448, "router_call": None}
+NCU_TRAFFIC = {"gemm_bf16_kernel": 67_437_056 + 12_296_448,
+               "router_call": (35_668_224 + 16_139_520 + 67_328 + 1_476_864
+                               + 35_651_584 + 17_229_824 + 11_008 + 1_525_248) // 2}
 
 # FP32 FMA peak from unit counts and clock: 152 SMs x 128 FP32 lanes x 2 flop x 2070 MHz
 FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12

@@ -95,13 +95,14 @@ enum : int {
     KID_SELECT = 20,       // 4 instantiations: 20..23 (two group sums or none)
     KID_GATE = 24,
     KID_HASH = 25,         // 4 instantiations: 25..28
-    KID_ROUTER_GEMV = 30,  // 4 instantiations: 30..33
+    KID_ROUTER_GEMV = 30,  // 2 instantiations (8 tokens per block): 30..31
     KID_SELECT_GATE = 34,  // 4 instantiations: 34..37 (two group sums or none)
     KID_MOE = 40,          // 5 kernels: 40..44
     KID_NORM = 45,         // 2 instantiations: 45..46
     KID_ROUTER_PROJ_SHALLOW = 49,   // 2 instantiations: 49..50
     KID_SELECT_GENERAL = 51,        // 4 instantiations: 51..54
     KID_SELECT_GATE_GENERAL = 55,   // 4 instantiations: 55..58
+    KID_ROUTER_GEMV1 = 59,          // 2 instantiations (one token per block): 59..60
 };
 
 }  // namespace bi

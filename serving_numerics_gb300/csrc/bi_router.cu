@@ -626,9 +626,9 @@ router_select_kernel(const float *__restrict__ part, int C, int m_split, void *l
 // ---------------------------------------------------------------------------
 // Small-batch twin: the same reduction contract shaped like a matrix-vector
 // product, for batches too small to fill 32-token tiles.  One warp owns two
-// experts; lane 16*x + q runs partition q's chain for expert x over up to 8
-// tokens (8 accumulators), reading whole slabs of X and of the gate rows that
-// TMA stages in a ring, two 128-wide slabs per stage.  The
+// experts; lane 16*x + q runs partition q's chain for expert x over the
+// block's T tokens (T accumulators), reading whole slabs of X and of the gate
+// rows that TMA stages in a ring, two 128-wide slabs per stage.  The
 // 16 partials of a (token, expert) sit in 16 lanes of one half-warp and are
 // added by butterfly shuffles with offsets 1, 2, 4, 8: lanes q and q^d hold
 // the same sum after each level (fp addition is commutative), and the
@@ -636,29 +636,35 @@ router_select_kernel(const float *__restrict__ part, int C, int m_split, void *l
 // and every gate row is read by one warp of its own, so even M = 1 spreads
 // W_gate over E/2 thread blocks.
 // ---------------------------------------------------------------------------
-constexpr int kGemvT = 8;       // tokens per block
+// Tokens per block: 8 for 32 < M <= 64 (four warps share the staged rows);
+// up to M = 32, one token and one warp per block: E/2 * M warps spread over
+// the SMs beat fewer warps that each carry several tokens' chains (same-box
+// timings of the router call: 7.7 against 9.8 us at M = 1, 9.6 against
+// 13.7 at M = 8, 20.0 against 21.3 at M = 32; 26 against 22 at M = 48).
+constexpr int kGemvT = 8;
+constexpr int kGemvOneTokenMaxM = 32;
 
-// WPB warps per block share one staged X tile; each warp owns 2 experts.
-// One stage holds two slabs (256 h): boxes [8 rows x 256] of X and
+// WPB warps per block share one staged X tile of T rows; each warp owns 2
+// experts.  One stage holds two slabs (256 h): boxes [T rows x 256] of X and
 // [2*WPB rows x 256] of W_gate.
 constexpr int kGemvSpan = 2 * kSlab;
 
-template <typename InT, int WPB>
+template <typename InT, int WPB, int T>
 struct GemvCfg {
     static constexpr int NST = WPB == 1 ? 8 : 4;                         // ring depth (stages)
-    static constexpr int XBOX = kGemvT * kGemvSpan * (int)sizeof(InT);
+    static constexpr int XBOX = T * kGemvSpan * (int)sizeof(InT);
     static constexpr int WBOX = 2 * WPB * kGemvSpan * (int)sizeof(InT);
     static constexpr int STAGE_BYTES = XBOX + WBOX;
     static constexpr int SMEM = NST * STAGE_BYTES + 1024;
 };
 
-template <typename InT, int WPB>
+template <typename InT, int WPB, int T>
 __global__ void __launch_bounds__(32 * WPB)
 router_gemv_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
                    int M, int E, int H, int logit_bf16, void *__restrict__ out, unsigned int *err)
 {
     pdl_trigger();   // dependents may launch now; each waits before reading our outputs
-    using Cfg = GemvCfg<InT, WPB>;
+    using Cfg = GemvCfg<InT, WPB, T>;
     constexpr int NST = Cfg::NST;
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[NST];
@@ -666,10 +672,10 @@ router_gemv_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
     uint8_t *smem = smem_align1024(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, q = lane & 15;
     const int x = 2 * warp + (lane >> 4);               // expert within the block
-    const int e0 = blockIdx.x * 2 * WPB, m0 = blockIdx.y * kGemvT;
+    const int e0 = blockIdx.x * 2 * WPB, m0 = blockIdx.y * T;
     const int ns = (H + kSlab - 1) / kSlab;
     const int nstage = (H + kGemvSpan - 1) / kGemvSpan;
-    const int nt = min(kGemvT, M - m0);
+    const int nt = min(T, M - m0);
     const int nst = nstage < NST ? nstage : NST;
     const bool oneshot = nstage <= NST;
 
@@ -707,9 +713,9 @@ router_gemv_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
         tma_load_2d(st, &tmx, &full_bar[slot], kGemvSpan * s, m0);
     };
 
-    float acc[kGemvT];
+    float acc[T];
 #pragma unroll
-    for (int t = 0; t < kGemvT; ++t) acc[t] = 0.0f;
+    for (int t = 0; t < T; ++t) acc[t] = 0.0f;
     int slot = 0;
     uint32_t phase = 0;
     for (int s = 0; s < nstage; ++s) {
@@ -725,7 +731,7 @@ router_gemv_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
                     const float4 w0 = *reinterpret_cast<const float4 *>(ws);
                     const float4 w1 = *reinterpret_cast<const float4 *>(ws + 4);
 #pragma unroll
-                    for (int t = 0; t < kGemvT; ++t) {
+                    for (int t = 0; t < T; ++t) {
                         if (t < nt) {
                             const float *xs = reinterpret_cast<const float *>(st) + t * kGemvSpan + col;
                             const float4 a0 = *reinterpret_cast<const float4 *>(xs);
@@ -746,7 +752,7 @@ router_gemv_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
                     const uint4 wr =
                         *reinterpret_cast<const uint4 *>(st + Cfg::XBOX + 2 * (x * kGemvSpan + col));
 #pragma unroll
-                    for (int t = 0; t < kGemvT; ++t) {
+                    for (int t = 0; t < T; ++t) {
                         if (t < nt) {
                             const uint4 xr = *reinterpret_cast<const uint4 *>(st + 2 * (t * kGemvSpan + col));
                             float a = acc[t];
@@ -787,14 +793,14 @@ router_gemv_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
         }
     }
 #pragma unroll
-    for (int t = 0; t < kGemvT; ++t) {
+    for (int t = 0; t < T; ++t) {
 #pragma unroll
         for (int d = 1; d < 16; d *= 2) acc[t] = acc[t] + __shfl_xor_sync(0xFFFFFFFFu, acc[t], d);
     }
     const int e = e0 + x;
     if (q == 0 && e < E) {
 #pragma unroll
-        for (int t = 0; t < kGemvT; ++t) {
+        for (int t = 0; t < T; ++t) {
             if (t < nt) {
                 const size_t o = (size_t)(m0 + t) * E + e;
                 if (logit_bf16)
@@ -806,21 +812,22 @@ router_gemv_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
     }
 }
 
-template <typename InT, int WPB>
+template <typename InT, int WPB, int T = kGemvT>
 bi_status launch_gemv(Device *d, const void *x, const void *w, int M, int E, int H, int logit_bf16, void *out,
                       cudaStream_t s)
 {
-    using Cfg = GemvCfg<InT, WPB>;
-    auto kern = router_gemv_kernel<InT, WPB>;
-    bi_status st = set_smem_once(d, KID_ROUTER_GEMV + (sizeof(InT) == 4 ? 0 : 2) + (WPB == 1 ? 0 : 1), kern,
-                                 Cfg::SMEM);
+    using Cfg = GemvCfg<InT, WPB, T>;
+    auto kern = router_gemv_kernel<InT, WPB, T>;
+    static_assert((T == 1 && WPB == 1) || (T == kGemvT && WPB == 4), "instantiations with a kernel id");
+    const int kid = (T == 1 ? KID_ROUTER_GEMV1 : KID_ROUTER_GEMV) + (sizeof(InT) == 4 ? 0 : 1);
+    bi_status st = set_smem_once(d, kid, kern, Cfg::SMEM);
     if (st != BI_OK) return st;
     const CUtensorMapDataType dt = sizeof(InT) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const uint64_t strides[1] = {(uint64_t)H * sizeof(InT)};
     alignas(64) CUtensorMap tmx, tmw;
     {
         const uint64_t dims[2] = {(uint64_t)H, (uint64_t)M};
-        const uint32_t box[2] = {(uint32_t)kGemvSpan, (uint32_t)kGemvT};
+        const uint32_t box[2] = {(uint32_t)kGemvSpan, (uint32_t)T};
         if ((st = encode_tiled(&tmx, dt, 2, x, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE)) != BI_OK) return st;
     }
     {
@@ -828,7 +835,7 @@ bi_status launch_gemv(Device *d, const void *x, const void *w, int M, int E, int
         const uint32_t box[2] = {(uint32_t)kGemvSpan, (uint32_t)(2 * WPB)};
         if ((st = encode_tiled(&tmw, dt, 2, w, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE)) != BI_OK) return st;
     }
-    dim3 grid((E + 2 * WPB - 1) / (2 * WPB), (M + kGemvT - 1) / kGemvT);
+    dim3 grid((E + 2 * WPB - 1) / (2 * WPB), (M + T - 1) / T);
     return launch_pdl(kern, grid, dim3(32 * WPB), (size_t)Cfg::SMEM, s, tmx, tmw, M, E, H, logit_bf16, out, d->err);
 }
 
@@ -1001,9 +1008,9 @@ bi_status router_call(const void *x, const void *w_gate, bi_dtype in_dtype, bi_d
 
     const bool f32in = in_dtype == BI_F32;
     const int lbf = logit_dtype == BI_BF16 ? 1 : 0;
-    if (small && M <= kGemvT) {
-        st = f32in ? launch_gemv<float, 1>(d, x, w_gate, M, E, H, lbf, logits_out, cs)
-                   : launch_gemv<__nv_bfloat16, 1>(d, x, w_gate, M, E, H, lbf, logits_out, cs);
+    if (small && M <= kGemvOneTokenMaxM) {      // one warp per (token, expert pair)
+        st = f32in ? launch_gemv<float, 1, 1>(d, x, w_gate, M, E, H, lbf, logits_out, cs)
+                   : launch_gemv<__nv_bfloat16, 1, 1>(d, x, w_gate, M, E, H, lbf, logits_out, cs);
     } else if (small) {
         st = f32in ? launch_gemv<float, 4>(d, x, w_gate, M, E, H, lbf, logits_out, cs)
                    : launch_gemv<__nv_bfloat16, 4>(d, x, w_gate, M, E, H, lbf, logits_out, cs);
