@@ -86,11 +86,13 @@ size_t moe_layout(int64_t M, int64_t k, int64_t E, int64_t N, int64_t K, uint8_t
 // One block does the whole plan: rows per expert (a histogram in shared
 // memory), each expert's rows padded up to whole tiles, the exclusive scan
 // over experts, the tile table (first gathered row and expert of every
-// tile), the placement cursors reset to 0 and the row map reset to -1.  An
+// tile), the placement cursors reset to 0 and the padding rows of every
+// expert's last tile marked -1 in the row map (the placement writes every
+// other row the tiles cover).  An
 // id outside [0, E) is recorded in the device error word
 // (BI_ERR_INVALID_ARG) and its slot is left out everywhere.
 __global__ void __launch_bounds__(kPlanThreads)
-moe_plan_kernel(const int32_t *__restrict__ ids, int Mk, int E, int64_t cap, int32_t *__restrict__ cursor,
+moe_plan_kernel(const int32_t *__restrict__ ids, int Mk, int E, int32_t *__restrict__ cursor,
                 int32_t *__restrict__ offsets, int32_t *__restrict__ ntiles, int32_t *__restrict__ tile_row0,
                 int32_t *__restrict__ tile_expert, int32_t *__restrict__ row_src, unsigned int *err)
 {
@@ -132,11 +134,6 @@ moe_plan_kernel(const int32_t *__restrict__ ids, int Mk, int E, int64_t cap, int
         done = n4 * 4;
     }
     for (int i = done + e; i < Mk; i += kPlanThreads) count(ids[i]);
-    {   // row map reset (cap is a multiple of 128, the array 256-byte aligned)
-        int4 *rs4 = reinterpret_cast<int4 *>(row_src);
-        const int4 neg = make_int4(-1, -1, -1, -1);
-        for (int64_t r = e; r < cap / 4; r += kPlanThreads) rs4[r] = neg;
-    }
     __syncthreads();
     const int c = e < E ? hist[e] : 0;
     const int t = (c + BM - 1) / BM;                  // this expert's tiles
@@ -156,6 +153,12 @@ moe_plan_kernel(const int32_t *__restrict__ ids, int Mk, int E, int64_t cap, int
             tile_row0[t0 + i] = (t0 + i) * BM;
             tile_expert[t0 + i] = e;
         }
+    }
+    // padding rows of every expert's last tile, one warp per expert
+    for (int x = e >> 5; x < E; x += kPlanThreads / 32) {
+        const int cx = hist[x], end = scan_t[x] * BM;                 // expert x's rows end here
+        const int first = end - (cx + BM - 1) / BM * BM + cx;         // its first unclaimed row
+        for (int r = first + (e & 31); r < end; r += 32) row_src[r] = -1;
     }
     if (e == kPlanThreads - 1) {
         *ntiles = scan_t[e];
@@ -184,7 +187,20 @@ moe_place_kernel(const __nv_bfloat16 *__restrict__ X, const int32_t *__restrict_
     if (lane == 0) row_src[pos] = i;
     const uint4 *src = reinterpret_cast<const uint4 *>(X + (int64_t)(i / k) * K);
     uint4 *dst = reinterpret_cast<uint4 *>(Ag + pos * K);
-    for (int c = lane; c < K / 8; c += 32) dst[c] = src[c];
+    const int n16 = K / 8;                            // 16-byte pieces of the row
+    for (int c0 = 0; c0 < n16; c0 += 8 * 32) {         // eight loads in flight per lane
+        uint4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int c = c0 + u * 32 + lane;
+            if (c < n16) v[u] = src[c];
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int c = c0 + u * 32 + lane;
+            if (c < n16) dst[c] = v[u];
+        }
+    }
 }
 
 // The grouped projection: persistent, one block per SM, the dense kernel's
@@ -399,8 +415,8 @@ extern "C" bi_status bi_moe_expert_gemm(const void *X, const int32_t *ids, const
 
     const int Mk = M * k;
     if ((st = set_smem_once(d, KID_MOE + 1, moe_plan_kernel, 0)) != BI_OK) return st;
-    if ((st = launch_pdl(moe_plan_kernel, dim3(1), dim3(kPlanThreads), 0, cs, ids, Mk, (int)E, (int64_t)ws.cap,
-                         ws.cursor, ws.offsets, ws.ntiles, ws.tile_row0, ws.tile_expert, ws.row_src, d->err)) != BI_OK)
+    if ((st = launch_pdl(moe_plan_kernel, dim3(1), dim3(kPlanThreads), 0, cs, ids, Mk, (int)E, ws.cursor,
+                         ws.offsets, ws.ntiles, ws.tile_row0, ws.tile_expert, ws.row_src, d->err)) != BI_OK)
         return st;
     if ((st = set_smem_once(d, KID_MOE + 2, moe_place_kernel, 0)) != BI_OK) return st;
     if ((st = launch_pdl(moe_place_kernel, dim3((Mk + 7) / 8), dim3(256), 0, cs,
