@@ -930,10 +930,12 @@ constexpr int kGemvMaxM = 64;
 // How the projection's work is cut for a batch of M > kGemvMaxM rows (any
 // plan gives the same bits; plans differ only in how well the work fills
 // the SMs, and each rule below was the fastest measured in its range):
-//  - at least one 32 x 64 tile per SM: every tile's 16 partitions as two
-//    blocks of 8 (C = 2) with the shallow 96 KB ring, two blocks to an SM, so
-//    one block's start-up and partition tree overlap the other's arithmetic;
-//    the selection adds the two group sums (2*M*E*4 bytes of them);
+//  - at least one two-block tile half per SM: every tile's 16 partitions as
+//    two blocks of 8 (C = 2) with the shallow 96 KB ring, up to two blocks to
+//    an SM, so one block's start-up and partition tree overlap the other's
+//    arithmetic; the selection adds the two group sums (2*M*E*4 bytes of
+//    them).  (Same-box timings at M = 768 and 1024, where whole tiles had
+//    been used: 38.4 and 42.6 us against 43.8 and 44.2.)
 //  - fewer tiles than SMs: C = the largest power of two (at most 16) that
 //    still gives every block an SM of its own (tiles * C <= SMs), deep rings;
 //  - batches whose group sums would pass 64 MiB: rows [0, m_split) in whole
@@ -948,10 +950,10 @@ struct SplitPlan {
 SplitPlan plan_split(int M, int E, int sms)
 {
     const long long n_et = (E + kTileE - 1) / kTileE, tiles_m = (M + kTileM - 1) / kTileM;
-    // at least a tile per SM: every tile as two 8-partition blocks with the
-    // shallow ring, two blocks to an SM (their start-up and tree phases then
-    // overlap the other's arithmetic); measured fastest from M = 2048 up
-    if (tiles_m * n_et >= sms && 2ll * M * E * 4 <= (64ll << 20)) return {0, 2, true};
+    // at least a tile half per SM: every tile as two 8-partition blocks with
+    // the shallow ring, up to two blocks to an SM (their start-up and tree
+    // phases then overlap the other's arithmetic)
+    if (tiles_m * n_et * 2 >= sms && 2ll * M * E * 4 <= (64ll << 20)) return {0, 2, true};
     const long long waves = tiles_m * n_et / sms;
     const long long head_tm = waves * sms / n_et;
     if (head_tm >= tiles_m) return {M, 1, false};

@@ -196,8 +196,9 @@ def test_router_splits_bit_identical(bi, E, M, H):
 
 def test_router_plan_reports_the_cut(bi):
     """bi_router_plan on a 152-SM GB300: the matrix-vector twin below 65
-    rows, two-block tiles once the tiles fill the SMs, whole tiles plus a
-    split tail where the group sums would pass 64 MiB."""
+    rows, partition-split tiles below that, two-block tiles once their
+    blocks fill the SMs, whole tiles plus a split tail where the group sums
+    would pass 64 MiB."""
     import torch
     if torch.cuda.get_device_properties(0).multi_processor_count != 152:
         pytest.skip("plan thresholds are stated for 152 SMs")
@@ -205,4 +206,6 @@ def test_router_plan_reports_the_cut(bi):
     assert bi.router_plan(64, 256) == (64, 1, 2)
     assert bi.router_plan(4096, 256) == (0, 2, 2)
     assert bi.router_plan(256, 256) == (0, 4, 2)
+    assert bi.router_plan(640, 256) == (0, 2, 2)       # 80 tiles: 160 two-block halves
+    assert bi.router_plan(1024, 256) == (0, 2, 2)
     assert bi.router_plan(8300, 1024) == (8192, 2, 3)
