@@ -114,8 +114,8 @@ typedef struct CUstream_st *bi_stream;
  * NaN ranks above every number and ties other NaNs by index).
  *
  * Scratch: for batches of more than 64 rows the partitions of a tile are
- * spread over several thread blocks (two once the tiles fill the SMs, 2*M*E*4
- * bytes of group sums; more below that; for batches whose group sums would
+ * spread over several thread blocks (two once those halves fill the SMs,
+ * 2*M*E*4 bytes of group sums; more below that; for batches whose group sums would
  * pass 64 MiB only the last rows') whose partial sums meet in a
  * library-owned device buffer (grown on the first call that needs more, one
  * buffer per device, never freed before exit).  Make a first
