@@ -55,6 +55,9 @@ def peaks():
 # caches as the preceding kernels left them; its writes include L2 evictions of the
 # preceding kernels' dirty lines.
 NCU_TRAFFIC = {"gemm_bf16_kernel": 67_437_056 + 12_296_448,
+               # the grouped expert projection's four launches (plan, place, gemm, combine),
+               # each captured with the caches flushed
+               "moe_call": 153_088 + 16_920_576 + 69_718_528 + 1_283_893_504 + 58_558_976 + 67_250_176 + 5_120,
                "router_call": (35_668_224 + 16_139_520 + 67_328 + 1_476_864
                                + 35_651_584 + 17_229_824 + 11_008 + 1_525_248) // 2}
 
@@ -450,7 +453,8 @@ def moe_measure(bi, synth, torch, dev, hbm_gbs, X, ids, wts, reps=10):
             "us_per_call": t * 1e6, "tflops": flop / t / 1e12,
             "launches_per_call": 4,
             "roofline": {"bound": "hbm", "achieved": byt / t / 1e9, "peak": hbm_gbs, "unit": "GB/s",
-                         "frac": byt / t / 1e9 / hbm_gbs, "algorithmic_bytes": byt, "traffic": None}}
+                         "frac": byt / t / 1e9 / hbm_gbs, "algorithmic_bytes": byt,
+                         "traffic": NCU_TRAFFIC["moe_call"]}}
 
 
 def fma_probe(bi, torch, dev, packed: bool = False) -> float:
