@@ -88,9 +88,11 @@ class Clocks:
         import datetime
         self.t_begin = datetime.datetime.now()
 
-    def stop(self):
+    def stop(self, t_end=None):
+        """Close the region (now, unless t_end is given) and summarise the
+        samples stamped inside it."""
         import datetime
-        t_end = datetime.datetime.now()
+        t_end = t_end or datetime.datetime.now()
         if self.p is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         time.sleep(0.1)              # the sample that straddles the end

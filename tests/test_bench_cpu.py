@@ -7,7 +7,6 @@ import datetime
 import os
 import subprocess
 import sys
-import time
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 sys.path.insert(0, ROOT)
@@ -38,8 +37,7 @@ def test_only_samples_inside_the_region_count():
              sample(t0 + datetime.timedelta(seconds=30), 900,
                     ("Active", "Not Active", "Not Active", "Not Active"))]     # after: ignored
     c = fake_clocks(lines, t0)
-    time.sleep(0.15)                # the region closes after the three samples inside it
-    r = c.stop()
+    r = c.stop(t_end=t0 + datetime.timedelta(milliseconds=100))   # after the three samples inside
     assert r["samples"] == 3
     assert r["sm_mhz"] == 2070.0 and r["sm_max_mhz"] == 2070.0
     assert r["reasons"] == ["sw_power_cap"]
@@ -51,7 +49,7 @@ def test_short_region_widens_the_window():
     lines = [sample(t0 - datetime.timedelta(milliseconds=40), 2070),
              sample(t0 - datetime.timedelta(seconds=5), 800)]
     c = fake_clocks(lines, t0)
-    r = c.stop()
+    r = c.stop(t_end=t0 + datetime.timedelta(milliseconds=20))
     assert r["samples"] == 1 and r["sm_mhz"] == 2070.0
     assert "widened" in r["window"]
 
@@ -59,7 +57,7 @@ def test_short_region_widens_the_window():
 def test_unparseable_lines_are_skipped():
     t0 = datetime.datetime.now()
     lines = ["[N/A], [N/A]", "garbage", sample(t0 + datetime.timedelta(milliseconds=5), 2070)]
-    r = fake_clocks(lines, t0).stop()
+    r = fake_clocks(lines, t0).stop(t_end=t0 + datetime.timedelta(milliseconds=50))
     assert r["samples"] == 1
 
 
