@@ -638,14 +638,41 @@ def _cpu_pool_task(arg):
     return _cpu_layer_sample(2_000 + i, budget)
 
 
+def oracle_sweep() -> dict:
+    """The oracle, single-threaded, per call over M (about 7 s): the router
+    (F32, H=2048, E=256, top-8) at M = 1 ... 4096 in full; the K=N=4096
+    projection in full at M = 1 and 19, and as an 8-row sample standing for
+    any larger M (the oracle's cost is linear in the rows)."""
+    from oracle import oracle as orc
+    from serving_numerics_gb300 import synth
+    orc.build()
+    W = synth.router_weights(7, 0, E, H)
+    router = {}
+    for m in (1, 19, 64, 256, 1024, 4096):
+        X = synth.tokens(7, 0, 5000 + m, m, H)
+        t = time.perf_counter()
+        orc.router_full(X, W, K_TOP, "f32")
+        router[str(m)] = m / (time.perf_counter() - t)
+    B = synth.gemm_b(7, G_N, G_K)
+    gemm = {}
+    for m, label in ((1, "1"), (19, "19"), (8, "per-row rate from an 8-row sample (any larger M)")):
+        A = synth.gemm_a(7, m, G_K, layer=6000 + m)
+        t = time.perf_counter()
+        orc.gemm_bf16(A, B)
+        gemm[label] = 2.0 * m * G_N * G_K / (time.perf_counter() - t) / 1e9
+    return {"router_tokens_per_s_by_M": router, "gemm_gflops_by_M": gemm, "threads": 1}
+
+
 def cpu_baseline(budget_s: float = 15.0):
     """About budget_s of host time: two thirds on one thread, the rest on all
-    cores at once."""
+    cores at once; then the oracle's per-call rates over M."""
     cb = CpuBaseline()
     try:
-        return cb.sample(budget_s * 2 / 3, budget_s / 3)
+        out = cb.sample(budget_s * 2 / 3, budget_s / 3)
     finally:
         cb.close()
+    out["oracle_sweep"] = oracle_sweep()
+    return out
 
 
 def run_reference(args):
