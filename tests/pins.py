@@ -194,6 +194,58 @@ def pin_shared_gate(orc, rng=None):
     assert np.allclose(sn, 1.0 - sig, rtol=0, atol=1e-15)
 
 
+def pin_shared_gate_onehot(orc, rng=None):
+    """A one-hot w_sg picks one input column exactly: dot(X, e_j) = X[:, j],
+    for every column j including the first and the last (a dropped term or a
+    gate row indexed by token instead of by h gives another value)."""
+    rng = rng or np.random.default_rng(21)
+    M, H = 5, 48
+    X = rng.standard_normal((M, H)).astype(np.float32)
+    for j in (0, 1, H // 2, H - 1):
+        w = np.zeros(H, np.float32)
+        w[j] = 1.0
+        dot, _ = orc.shared_gate(X, w)
+        assert np.array_equal(dot, X[:, j].astype(np.float64)), j
+    # a scaled one-hot: a power of two scales exactly
+    w = np.zeros(H, np.float32)
+    w[H - 1] = -0.25
+    dot, _ = orc.shared_gate(X, w)
+    assert np.array_equal(dot, -0.25 * X[:, H - 1].astype(np.float64))
+
+
+def pin_shared_gate_integer_grid(orc, rng=None):
+    """Inputs on an integer grid times 2^-4: every product and partial sum
+    is exact in double, so the dot must equal integer arithmetic exactly,
+    and the sigmoid at an exact dot of 0 is exactly 1/2."""
+    rng = rng or np.random.default_rng(22)
+    M, H = 6, 200
+    xi = rng.integers(-7, 8, (M, H))
+    wi = rng.integers(-7, 8, H)
+    wi[-1] = 5                                   # the last term is never zero
+    xi[:, -1] = np.arange(1, M + 1)
+    X = (xi * 2.0 ** -4).astype(np.float32)
+    w = (wi * 2.0 ** -4).astype(np.float32)
+    dot, sig = orc.shared_gate(X, w)
+    exact = (xi.astype(np.int64) @ wi.astype(np.int64)).astype(np.float64) * 2.0 ** -8
+    assert np.array_equal(dot, exact)
+    # rows built to cancel: dot exactly 0, sigmoid exactly 1/2
+    Xc = np.zeros((2, H), np.float32)
+    Xc[0, 0], Xc[0, 1] = 1.0, 1.0
+    wc = np.zeros(H, np.float32)
+    wc[0], wc[1] = 0.5, -0.5
+    Xc[1, H - 2], Xc[1, H - 1] = 3.0, 3.0
+    wc[H - 2], wc[H - 1] = 2.0, -2.0
+    d, s = orc.shared_gate(Xc, wc)
+    assert np.array_equal(d, [0.0, 0.0]) and np.array_equal(s, [0.5, 0.5])
+    # sigmoid(ln 3) = 3/4 and sigmoid(-ln 3) = 1/4 (closed forms), the dot
+    # being exactly representable: X = [ln3 as f32], w = [1]
+    l3 = np.float32(np.log(3.0))
+    d, s = orc.shared_gate(np.array([[l3], [-l3]], np.float32), np.ones(1, np.float32))
+    expect = 1.0 / (1.0 + np.array([1.0 / 3.0, 3.0]) * np.exp(np.log(3.0) - float(l3)) ** np.array([1, -1]))
+    assert np.allclose(s, expect, rtol=4e-16, atol=0)
+    assert abs(s[0] - 0.75) < 1e-7 and abs(s[1] - 0.25) < 1e-7
+
+
 # ------------------------------------------------------------------ top-k
 def pin_topk_bruteforce(orc, rng=None):
     rng = rng or np.random.default_rng(11)
@@ -402,6 +454,7 @@ def pin_route_hash(orc, rng=None):
 ALL_PINS = [
     pin_bf16_rounding, pin_f32_rounding, pin_ulp_order,
     pin_router_integer_grid, pin_router_onehot, pin_router_vs_matmul, pin_shared_gate,
+    pin_shared_gate_onehot, pin_shared_gate_integer_grid,
     pin_topk_bruteforce, pin_topk_special, pin_topk_permutation, pin_planted_ties,
     pin_softmax, pin_margin,
     pin_gemm_identity, pin_gemm_integer_grid, pin_gemm_vs_matmul,

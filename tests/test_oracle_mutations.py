@@ -34,6 +34,11 @@ MUTANTS = {
     "fnv_wrong_prime": ("#define ORC_FNV64_PRIME 0x00000100000001B3ull",
                         "#define ORC_FNV64_PRIME 0x00000100000001B1ull"),
     "gate_sigmoid_sign": ("sig[m] = 1.0 / (1.0 + exp(-s));", "sig[m] = 1.0 / (1.0 + exp(s));"),
+    "gate_drop_last_term": (
+        "for (int64_t h = 0; h < H; ++h)\n            s += (double)X[m * ldx + h] * (double)w[h];",
+        "for (int64_t h = 0; h < H - 1; ++h)\n            s += (double)X[m * ldx + h] * (double)w[h];"),
+    "gate_w_indexed_by_row": ("s += (double)X[m * ldx + h] * (double)w[h];",
+                              "s += (double)X[m * ldx + h] * (double)w[m];"),
 }
 
 
