@@ -61,8 +61,21 @@ NCU_TRAFFIC = {"gemm_bf16_kernel": 67_437_056 + 12_296_448,
                "router_call": (35_668_224 + 16_139_520 + 67_328 + 1_476_864
                                + 35_651_584 + 17_229_824 + 11_008 + 1_525_248) // 2}
 
-# FP32 FMA peak from unit counts and clock: 152 SMs x 128 FP32 lanes x 2 flop x 2070 MHz
-FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
+def fp32_peak(torch, dev) -> dict:
+    """The FP32 FMA peak from this GPU's unit counts and its maximum SM clock:
+    SMs (device properties) x 128 FP32 lanes x 2 flop x the maximum SM clock
+    (nvidia-smi clocks.max.sm).  None where the clock cannot be read."""
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    mhz = None
+    try:
+        out = subprocess.run(["nvidia-smi", "-i", str(dev.index or 0), "--query-gpu=clocks.max.sm",
+                              "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=20)
+        mhz = float(out.stdout.strip().splitlines()[0])
+    except (OSError, ValueError, IndexError, subprocess.SubprocessError):
+        pass
+    tflops = sms * 128 * 2 * mhz * 1e6 / 1e12 if mhz else None
+    return {"tflops": tflops, "sms": sms, "sm_max_mhz": mhz,
+            "source": f"derived: {sms} SMs x 128 FP32 lanes x 2 flop x {mhz} MHz (nvidia-smi clocks.max.sm)"}
 
 
 class Clocks:
@@ -194,6 +207,7 @@ def run_ours(args):
     gsig = torch.empty((LAYERS, M), dtype=torch.float32, device=dev)
     Cout = torch.empty((M, G_N), dtype=torch.bfloat16, device=dev)
     hashes = torch.empty((N_REQ,), dtype=torch.int64, device=dev)
+    ws_router = bi.router_workspace(M, E, dev)      # caller-owned: the library allocates nothing
     offs = [i * (M // N_REQ) for i in range(N_REQ + 1)]
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
@@ -210,7 +224,7 @@ def run_ours(args):
         if ev is not None:
             ev[0].record(stream)
         bi.bi_router_gate_topk(X[l], Wg[l], Wsg[l], bi.BI_F32, bi.BI_F32, M, H, E, K_TOP, logits[l], ids[l],
-                               wts[l], mg[l], mu[l], gdot[l], gsig[l], stream=sh)
+                               wts[l], mg[l], mu[l], gdot[l], gsig[l], workspace=ws_router, stream=sh)
         ids_ready[l].record(stream)
         if ev is not None:
             ev[1].record(stream)
@@ -261,14 +275,20 @@ def run_ours(args):
     for l in range(LAYERS):
         pin_X[l].copy_(X[l])
         pin_A[l].copy_(A[l])
-    res_ids = torch.empty((M, K_TOP), dtype=torch.int32, pin_memory=True)
-    res_w = torch.empty((M, K_TOP), dtype=torch.float32, pin_memory=True)
+    # every layer's routing decision comes back (ids, weights, margins, gate),
+    # plus the per-request route hashes; the logits and the projection output
+    # stay on the device, where the next layer of a model would read them
+    res = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+           for n, t in (("ids", ids), ("weights", wts), ("margin", mg), ("margin_ulps", mu),
+                        ("gate_dot", gdot), ("gate_sigmoid", gsig))}
     res_h = torch.empty((N_REQ,), dtype=torch.int64, pin_memory=True)
     # inputs stream in on a copy stream ahead of the compute that needs them;
     # a layer's buffers are refilled only once the previous step's compute of
-    # that layer is done with them
+    # that layer is done with them; each layer's results go back on a second
+    # copy stream as soon as that layer's router is done
     e2e_steps = max(1, min(args.steps, 5))
     copy = torch.cuda.Stream(dev)
+    back = torch.cuda.Stream(dev)
     arrived = [torch.cuda.Event() for _ in range(LAYERS)]
     consumed = [torch.cuda.Event() for _ in range(LAYERS)]
     if ws > 1:
@@ -287,14 +307,19 @@ def run_ours(args):
             stream.wait_event(arrived[l])
             layer(l)
             consumed[l].record(stream)
-        res_ids.copy_(ids[LAYERS - 1], non_blocking=True)
-        res_w.copy_(wts[LAYERS - 1], non_blocking=True)
-        stream.wait_stream(side)
-        res_h.copy_(hashes, non_blocking=True)
-        stream.synchronize()       # this step's results are on the host
+            back.wait_event(ids_ready[l])
+            with torch.cuda.stream(back):
+                for n, src in (("ids", ids), ("weights", wts), ("margin", mg), ("margin_ulps", mu),
+                               ("gate_dot", gdot), ("gate_sigmoid", gsig)):
+                    res[n][l].copy_(src[l], non_blocking=True)
+        back.wait_stream(side)
+        with torch.cuda.stream(back):
+            res_h.copy_(hashes, non_blocking=True)
+        back.synchronize()         # this step's results are on the host
+        stream.synchronize()
     e2e_s = reduce_max(time.perf_counter() - w0, dev)
     h2d = LAYERS * (M * H * 4 + M * G_K * 2)
-    d2h = M * K_TOP * 8 + N_REQ * 8
+    d2h = sum(t.numel() * t.element_size() for t in res.values()) + N_REQ * 8
     # the host link's own rate: one layer's inputs copied alone, as above
     torch.cuda.synchronize()
     c0 = time.perf_counter()
@@ -309,6 +334,9 @@ def run_ours(args):
 
     fma_tflops = fma_probe(bi, torch, dev)
     fma2_tflops = fma_probe(bi, torch, dev, packed=True)
+    fp32 = fp32_peak(torch, dev)
+    FP32_PEAK_TFLOPS = fp32["tflops"] or fma_tflops
+    margins_bf16 = margin_histogram_bf16(torch, logits, K_TOP)
     hbm, bf16_burst, bf16_sus, src = peaks()
     value = whole_job_rate(M, ws, args.steps, ms / 1e3)
     g_avg = statistics.mean(gemm_ms) / 1e3
@@ -329,7 +357,7 @@ def run_ours(args):
                    "kernel": "bi_router_gate_topk call: router_proj_kernel launches + router_select_kernel "
                              "(timed as one call, so the selection counts against the projection)",
                    "algorithmic_bytes": r_bytes, "hbm_time_frac": (r_bytes / (hbm * 1e9)) / r_avg,
-                   "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 flop x 2070 MHz",
+                   "peak_source": fp32["source"] if fp32["tflops"] else "the FMA probe (clock not readable)",
                    "fma_probe_tflops": fma_tflops, "fma_probe_packed_tflops": fma2_tflops,
                    "frac_of_fma_probe": r_flop / r_avg / 1e12 / fma_tflops}
     out = {
@@ -352,36 +380,79 @@ def run_ours(args):
         "roofline": roof_router if r_avg >= g_avg else roof_gemm,
         "e2e": {"value": whole_job_rate(M, ws, e2e_steps, e2e_s), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "returns": "every layer's ids, weights, margin, margin_ulps, gate dot and sigmoid, and the "
+                           "16 chained route hashes; logits and projection outputs stay on the device",
                 "h2d_gbs_measured": h2d_gbs, "copy_bound_tokens_per_s": copy_bound,
                 "frac_of_copy_bound": whole_job_rate(M, ws, e2e_steps, e2e_s) / copy_bound},
         "gpu_launches": launches_per_layer * LAYERS * args.steps,
         "clocks": ck,
     }
+    out["margins_f32_router_in_bf16_ulps"] = margins_bf16
+    out["fp32_peak"] = {"derived_tflops": fp32["tflops"], "source": fp32["source"],
+                        "fma_probe_tflops": fma_tflops, "fma_probe_packed_tflops": fma2_tflops}
     if not args.no_sweep:
-        out["router_sweep"] = router_sweep(bi, synth, torch, dev, hbm)
+        del X, A, Bw, Wg, Wsg, pin_X, pin_A
+        torch.cuda.empty_cache()
+        out["router_sweep"] = router_sweep(bi, synth, torch, dev, hbm, FP32_PEAK_TFLOPS)
+        out["gemm_sweep"] = gemm_sweep(bi, synth, torch, dev, bf16_burst, bf16_sus)
+        out["tie_heavy_bf16_router"] = tie_heavy_measure(bi, synth, torch, dev)
+        out["mixed_prefill"] = mixed_prefill_measure(bi, synth, torch, dev)
         out["context_m_variant"] = m_variant_context(bi, synth, torch, dev)
-        out["moe_expert_gemm"] = moe_measure(bi, synth, torch, dev, hbm, X[0], ids[0], wts[0])
-        out["rmsnorm"] = rmsnorm_measure(bi, synth, torch, dev, hbm, X)
+        xs0 = synth.device_normal((M, H), seed * 100 + 200, 1.0, torch.float32, dev)
+        out["moe_expert_gemm"] = moe_measure(bi, synth, torch, dev, hbm, xs0, ids[0], wts[0])
+        xs = [synth.device_normal((M, H), seed * 100 + 200 + l, 1.0, torch.float32, dev) for l in range(LAYERS)]
+        out["rmsnorm"] = rmsnorm_measure(bi, synth, torch, dev, hbm, xs)
+        del xs
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_seconds)
+    out["digest"] = digest(out)
     if rank == 0:
         print(json.dumps(out), flush=True)
     if ws > 1:
         dist.destroy_process_group()
 
 
-def router_sweep(bi, synth, torch, dev, hbm_gbs):
-    """bi_router_topk alone (F32, H=2048, E=256, top-8, all outputs) at
-    several M: back-to-back calls cycling through 96 gate matrices (192 MiB,
-    more than L2) so every call reads its weights from HBM, captured in a
-    CUDA graph and replayed (the calls keep their programmatic-dependent
-    launch edges); the per-call time is against the binding roofline
-    max(bytes / HBM, flops / FP32)."""
+ROUTER_SWEEP_M = ([1, 2, 4, 8, 16, 19, 32] + list(range(35, 65)) +
+                  [65, 75, 96, 128, 129, 256, 512, 1024, 2048, 4096])
+
+
+def graph_time(torch, stream, fn, n, reps=3):
+    """Seconds per call of fn(i) for i < n, captured once in a CUDA graph
+    (so host launch cost is not timed; the calls keep their programmatic-
+    dependent-launch edges) and replayed reps times between CUDA events."""
+    fn_range = range(n)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in fn_range:
+            fn(i)
+    g.replay()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(reps):
+        g.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    del g
+    return a.elapsed_time(b) / 1e3 / (reps * n)
+
+
+def router_sweep(bi, synth, torch, dev, hbm_gbs, fp32_tflops):
+    """bi_router_topk alone (F32, H=2048, E=256, top-8, all outputs) at every M
+    of ROUTER_SWEEP_M: back-to-back calls cycling through 96 gate matrices
+    (192 MiB, more than L2) so every call reads its weights from HBM, in a
+    CUDA graph; the per-call time is against the binding roofline
+    max(bytes / HBM, flops / FP32).  floor_us: the same graph of the
+    dependent-launch probe (one cluster launch that waits for its
+    predecessor, reads one word and writes one), the fixed cost under any
+    one-launch call."""
     pool = 96
     Ws = [synth.device_normal((E, H), 77000 + i, 0.02, torch.float32, dev) for i in range(pool)]
     res = []
     stream = torch.cuda.current_stream(dev)
-    for Mi in (1, 4, 16, 64, 128, 256, 1024, 4096):
+    ws = bi.router_workspace(max(ROUTER_SWEEP_M), E, dev)
+    for Mi in ROUTER_SWEEP_M:
         xs = [synth.device_normal((Mi, H), 78000 + i, 1.0, torch.float32, dev) for i in range(8)]
         lg = torch.empty((Mi, E), dtype=torch.float32, device=dev)
         ids = torch.empty((Mi, K_TOP), dtype=torch.int32, device=dev)
@@ -389,35 +460,210 @@ def router_sweep(bi, synth, torch, dev, hbm_gbs):
         mg = torch.empty((Mi,), dtype=torch.float32, device=dev)
         mu = torch.empty((Mi,), dtype=torch.int32, device=dev)
 
-        def calls(n):
-            for i in range(n):
-                bi.bi_router_topk(xs[i % 8], Ws[i % pool], bi.BI_F32, bi.BI_F32, Mi, H, E, K_TOP, lg, ids, w,
-                                  mg, mu, stream=None)
-        calls(pool)                       # warm-up (also sizes the library's scratch)
+        def call(i):
+            bi.bi_router_topk(xs[i % 8], Ws[i % pool], bi.BI_F32, bi.BI_F32, Mi, H, E, K_TOP, lg, ids, w,
+                              mg, mu, workspace=ws, stream=None)
         n = pool if Mi <= 1024 else pool // 2
-        torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()        # replayed, so host launch cost is not timed
-        with torch.cuda.graph(g):
-            calls(n)
-        g.replay()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        a.record(stream)
-        for _ in range(3):
-            g.replay()
-        b.record(stream)
-        torch.cuda.synchronize()
-        t = a.elapsed_time(b) / 1e3 / (3 * n)
-        del g
+        t = graph_time(torch, stream, call, n)
         byt = 4 * E * H + 4 * Mi * H + 4 * Mi * E + 8 * Mi * K_TOP + 8 * Mi
         flop = 2.0 * Mi * E * H
-        t_hbm, t_alu = byt / (hbm_gbs * 1e9), flop / (FP32_PEAK_TFLOPS * 1e12)
-        res.append({"M": Mi, "us_per_call": t * 1e6, "GBps": byt / t / 1e9, "TFLOPs": flop / t / 1e12,
+        t_hbm, t_alu = byt / (hbm_gbs * 1e9), flop / (fp32_tflops * 1e12)
+        res.append({"M": Mi, "us": round(t * 1e6, 2), "launches": bi.router_plan(Mi, E)[2],
                     "bound": "hbm" if t_hbm >= t_alu else "alu",
-                    "frac_of_binding_roofline": max(t_hbm, t_alu) / t,
-                    "frac_of_hbm": (byt / t / 1e9) / hbm_gbs})
+                    "frac_binding": round(max(t_hbm, t_alu) / t, 4),
+                    "frac_hbm": round((byt / t / 1e9) / hbm_gbs, 4)})
     del Ws
-    return res
+    a_ = torch.zeros(64, dtype=torch.float32, device=dev)
+    b_ = torch.zeros(64, dtype=torch.float32, device=dev)
+    floor = graph_time(torch, stream, lambda i: bi.selftest_dependent_floor(a_ if i % 2 == 0 else b_,
+                                                                         b_ if i % 2 == 0 else a_), pool)
+    return {"calls": res, "floor_us": round(floor * 1e6, 3),
+            "note": "F32 H=2048 E=256 top-8, all outputs; 96 gate matrices cycled (192 MiB > L2), CUDA graph; "
+                    "floor_us = one dependent cluster launch doing no arithmetic"}
+
+
+def gemm_sweep(bi, synth, torch, dev, bf16_burst, bf16_sus):
+    """bi_gemm_bf16 at every M of the projection workload (K = N = 4096,
+    A, B ~ N(0,1)/64): back-to-back calls cycling 8 weight matrices and
+    2 input matrices (256 MiB + 128 MiB, far more than L2), timed with
+    CUDA events in a CUDA graph."""
+    Ms = [1, 19, 64, 65, 75, 128, 1024, 2048, 4096, 8192]
+    Bs = [synth.device_normal((G_N, G_K), 82000 + i, 1 / 64, torch.bfloat16, dev) for i in range(8)]
+    As = [synth.device_normal((max(Ms), G_K), 82100 + i, 1 / 64, torch.bfloat16, dev) for i in range(2)]
+    C_ = torch.empty((max(Ms), G_N), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    out = []
+    for Mi in Ms:
+        def call(i):
+            bi.bi_gemm_bf16(As[i % 2], Bs[i % 8], C_, Mi, G_N, G_K, G_K, G_K, G_N, stream=None)
+        n = 64 if Mi <= 1024 else 16
+        t = graph_time(torch, stream, call, n)
+        tf = 2.0 * Mi * G_N * G_K / t / 1e12
+        out.append({"M": Mi, "us": round(t * 1e6, 2), "tflops": round(tf, 1),
+                    "frac_sustained": round(tf / bf16_sus, 4), "frac_burst": round(tf / bf16_burst, 4)})
+    del Bs, As
+    return {"calls": out, "note": "K=N=4096 bf16, f32 accumulate; 8 weight matrices cycled (beyond L2), "
+                                  "CUDA graph; peaks: measured bf16 sustained / burst"}
+
+
+def tie_heavy_measure(bi, synth, torch, dev):
+    """The tie-heavy bf16-logit router: H=2048, E=512, top-10, bf16 inputs on
+    the {-1, +1} * 2^-8 grid, 48 calls of 5 tokens, each call with its own
+    gate matrix (as in the pages' 48 prefill calls).  Reports the time per
+    call in a CUDA graph of the 48 calls, the exact-tie count at the k
+    boundary (margin_ulps == 0) over the 240 token-slots, the histogram of
+    the boundary margins in bf16 ULPs, and the chained route hash of the 48
+    calls' sorted id sets."""
+    import numpy as np
+    n_calls, n_tok, Et, kt = 48, 5, 512, 10
+    xs, ws = [], []
+    for c in range(n_calls):
+        X, W = synth.tie_heavy_call(0, c)
+        xs.append(torch.from_numpy(X.view(np.int16)).to(dev).view(torch.bfloat16))
+        ws.append(torch.from_numpy(W.view(np.int16)).to(dev).view(torch.bfloat16))
+    lg = torch.empty((n_calls, n_tok, Et), dtype=torch.bfloat16, device=dev)
+    ids = torch.empty((n_calls, n_tok, kt), dtype=torch.int32, device=dev)
+    w = torch.empty((n_calls, n_tok, kt), dtype=torch.float32, device=dev)
+    mg = torch.empty((n_calls, n_tok), dtype=torch.float32, device=dev)
+    mu = torch.empty((n_calls, n_tok), dtype=torch.int32, device=dev)
+    h = torch.empty((1,), dtype=torch.int64, device=dev)
+
+    def call(c):
+        bi.bi_router_topk(xs[c], ws[c], bi.BI_BF16, bi.BI_BF16, n_tok, H, Et, kt, lg[c], ids[c], w[c], mg[c],
+                          mu[c], stream=None)
+    stream = torch.cuda.current_stream(dev)
+    t = graph_time(torch, stream, call, n_calls)
+    for c in range(n_calls):
+        call(c)
+        bi.bi_route_trace_hash(ids[c], n_tok, kt, [0, n_tok], None if c == 0 else h, h, stream=None)
+    torch.cuda.synchronize()
+    u = mu.flatten().cpu().numpy()
+    edges = [0, 1, 2, 3, 4, 8, 16, 64, 256, 2 ** 31]
+    hist = {(f"{lo}" if hi == lo + 1 else f"{lo}-{hi - 1}" if hi < 2 ** 31 else f">={lo}"):
+            int(np.sum((u >= lo) & (u < hi))) for lo, hi in zip(edges[:-1], edges[1:])}
+    byt = 2 * Et * H + 2 * n_tok * H + 2 * n_tok * Et + 8 * n_tok * kt + 8 * n_tok
+    return {"config": "bf16 H=2048 E=512 top-10, 48 calls x 5 tokens, X, W in {-1,+1}*2^-8",
+            "us_per_call": round(t * 1e6, 2), "tokens_per_s": n_tok / t,
+            "frac_hbm": None, "GBps": round(byt / t / 1e9, 1),
+            "slots": int(u.size), "exact_ties": int(np.sum(u == 0)), "ulp_histogram": hist,
+            "chained_hash": f"{int(h.cpu().numpy().view(np.uint64)[0]):016x}"}
+
+
+def margin_histogram_bf16(torch, logits, k):
+    """The F32 router's boundary margins of the timed step (all 40 layers,
+    4096 tokens each) with both endpoints -- the smallest selected and the
+    largest rejected logit -- rounded to bf16 (nearest even) and their
+    distance counted in bf16 ULPs under the sign-magnitude order.  Analysis
+    of the step's outputs, outside any timed region."""
+    import numpy as np
+    top = torch.topk(logits.reshape(-1, logits.shape[-1]), k + 1, dim=1).values
+    b = top[:, k - 1:k + 1].to(torch.bfloat16).view(torch.int16).to(torch.int32) & 0xFFFF
+    o = torch.where(b >= 0x8000, -(b & 0x7FFF), b)
+    d = (o[:, 0] - o[:, 1]).cpu().numpy()
+    edges = [0, 1, 2, 3, 4, 8, 16, 64, 256, 2 ** 31]
+    hist = {(f"{lo}" if hi == lo + 1 else f"{lo}-{hi - 1}" if hi < 2 ** 31 else f">={lo}"):
+            int(np.sum((d >= lo) & (d < hi))) for lo, hi in zip(edges[:-1], edges[1:])}
+    return {"tokens": int(d.size), "ulp_histogram": hist, "bf16_ties": int(np.sum(d == 0)),
+            "note": "F32 router, 40 layers x 4096 tokens, both boundary logits rounded to bf16"}
+
+
+def mixed_prefill_measure(bi, synth, torch, dev, reps=3):
+    """The mixed prefill with a prefix cache: 16 requests of lengths U[5, 300]
+    (seed 0), H = 2048, 40 layers, each running the router with the shared
+    gate (E = 256, top-8), a 2048 x 2048 bf16 projection and the per-request
+    route hashes, chained over the layers.  Run as a cache miss (every row,
+    M = sum N) and as a suffix-only cache hit (M = sum of N mod 16, the last
+    full block where that is 0; bi_prefix_split).  Reports the time per
+    layer of each (a CUDA graph of the 40 layers) and whether each request's
+    chained hash over its suffix rows is the same in both runs."""
+    import numpy as np
+    Hm, Em, km, L, blk = 2048, 256, 8, LAYERS, 16
+    lens = [int(v) for v in synth.request_lengths(0)]
+    offs = np.concatenate([[0], np.cumsum(lens)]).astype(int).tolist()
+    Mtot = offs[-1]
+    cached, sub = bi.prefix_split(lens, blk)
+    Mhit = sub[-1]
+    rows_hit = np.concatenate([np.arange(offs[r] + cached[r], offs[r + 1]) for r in range(16)])
+    idx_hit = torch.from_numpy(rows_hit).to(dev)
+    Wg = [synth.device_normal((Em, Hm), 83000 + l, 0.02, torch.float32, dev) for l in range(L)]
+    Wsg = [synth.device_normal((Hm,), 83100 + l, 0.02, torch.float32, dev) for l in range(L)]
+    Bw = [synth.device_normal((Hm, Hm), 83200 + l, 1 / 64, torch.bfloat16, dev) for l in range(L)]
+    Xm = [synth.device_normal((Mtot, Hm), 83300 + l, 1.0, torch.float32, dev) for l in range(L)]
+    Am = [synth.device_normal((Mtot, Hm), 83400 + l, 1 / 64, torch.bfloat16, dev) for l in range(L)]
+    Xh = [x.index_select(0, idx_hit).contiguous() for x in Xm]
+    Ah = [a.index_select(0, idx_hit).contiguous() for a in Am]
+
+    def make(Mr, Xs, As, ranges):
+        o = {"lg": torch.empty((Mr, Em), dtype=torch.float32, device=dev),
+             "ids": torch.empty((Mr, km), dtype=torch.int32, device=dev),
+             "w": torch.empty((Mr, km), dtype=torch.float32, device=dev),
+             "mg": torch.empty((Mr,), dtype=torch.float32, device=dev),
+             "mu": torch.empty((Mr,), dtype=torch.int32, device=dev),
+             "gd": torch.empty((Mr,), dtype=torch.float32, device=dev),
+             "gs": torch.empty((Mr,), dtype=torch.float32, device=dev),
+             "C": torch.empty((Mr, Hm), dtype=torch.bfloat16, device=dev),
+             "h": torch.empty((len(ranges) - 1,), dtype=torch.int64, device=dev),
+             "ws": bi.router_workspace(Mr, Em, dev)}
+
+        def lay(l):
+            bi.bi_router_gate_topk(Xs[l], Wg[l], Wsg[l], bi.BI_F32, bi.BI_F32, Mr, Hm, Em, km, o["lg"], o["ids"],
+                                   o["w"], o["mg"], o["mu"], o["gd"], o["gs"], workspace=o["ws"], stream=None)
+            bi.bi_route_trace_hash(o["ids"], Mr, km, ranges, None if l == 0 else o["h"], o["h"], stream=None)
+            bi.bi_gemm_bf16(As[l], Bw[l], o["C"], Mr, Hm, Hm, Hm, Hm, Hm, stream=None)
+        return o, lay
+
+    miss, lay_miss = make(Mtot, Xm, Am, offs)
+    hit, lay_hit = make(Mhit, Xh, Ah, sub)
+    stream = torch.cuda.current_stream(dev)
+    t_miss = graph_time(torch, stream, lay_miss, L, reps) * L
+    t_hit = graph_time(torch, stream, lay_hit, L, reps) * L
+    # invariance: per-request chained hash of the suffix rows (the rows a hit
+    # recomputes), taken from the miss's ids and from the hit's
+    hsub = torch.empty((16,), dtype=torch.int64, device=dev)
+    for l in range(L):
+        lay_miss(l)
+        ids_suffix = miss["ids"].index_select(0, idx_hit).contiguous()
+        bi.bi_route_trace_hash(ids_suffix, Mhit, km, sub, None if l == 0 else hsub, hsub, stream=None)
+    for l in range(L):
+        lay_hit(l)
+    torch.cuda.synchronize()
+    equal = bool(torch.equal(hsub, hit["h"]))
+    return {"config": f"16 requests U[5,300] seed 0 (total {Mtot} rows; hit recomputes {Mhit}), 40 layers x "
+                      "(router E=256 top-8 + shared gate + route hash + 2048x2048 bf16 projection)",
+            "miss_us_per_layer": round(t_miss / L * 1e6, 2), "hit_us_per_layer": round(t_hit / L * 1e6, 2),
+            "miss_tokens_per_s": Mtot / t_miss, "hit_tokens_per_s": Mhit / t_hit,
+            "suffix_hashes_equal_miss_vs_hit": equal}
+
+
+def digest(out) -> dict:
+    """A compact restatement of the headline figures, printed last in the
+    JSON line (readers that keep only the line's tail still get them)."""
+    d = {"ms_per_step": round(out["ms_per_step"], 3), "tokens_per_s": round(out["value"]),
+         "router_call_us_M4096": round(out["parts"]["router_call_us"], 1),
+         "router_frac_fp32": round(out["roofline_router"]["frac"], 3),
+         "gemm_call_us_M4096": round(out["parts"]["gemm_call_us"], 1),
+         "gemm_frac_sustained": round(out["roofline_gemm"]["frac"], 3),
+         "e2e_tokens_per_s": round(out["e2e"]["value"])}
+    rs = out.get("router_sweep")
+    if rs:
+        d["router_us_by_M"] = {str(r["M"]): r["us"] for r in rs["calls"]
+                               if r["M"] in (1, 4, 16, 19, 32, 48, 64, 65, 75, 128, 129, 256, 1024, 4096)}
+        d["router_frac_hbm_M1_16_64"] = [r["frac_hbm"] for r in rs["calls"] if r["M"] in (1, 16, 64)]
+        d["dependent_launch_floor_us"] = rs["floor_us"]
+    gs = out.get("gemm_sweep")
+    if gs:
+        d["gemm_tflops_by_M"] = {str(r["M"]): r["tflops"] for r in gs["calls"]}
+    th = out.get("tie_heavy_bf16_router")
+    if th:
+        d["tie_heavy"] = {"us_per_call": th["us_per_call"], "exact_ties": th["exact_ties"], "slots": th["slots"]}
+    mp = out.get("mixed_prefill")
+    if mp:
+        d["mixed_prefill_us_per_layer"] = {"miss": mp["miss_us_per_layer"], "hit": mp["hit_us_per_layer"],
+                                           "hashes_equal": mp["suffix_hashes_equal_miss_vs_hit"]}
+    for key in ("moe_expert_gemm", "rmsnorm"):
+        if key in out:
+            d[key] = {"us": round(out[key]["us_per_call"], 1), "frac_hbm": round(out[key]["roofline"]["frac"], 3)}
+    return d
 
 
 def moe_measure(bi, synth, torch, dev, hbm_gbs, X, ids, wts, reps=10):
@@ -552,8 +798,9 @@ def m_variant_context(bi, synth, torch, dev):
     ids = torch.empty((M, K_TOP), dtype=torch.int32, device=dev)
     wt = torch.empty((M, K_TOP), dtype=torch.float32, device=dev)
     Cb = torch.empty((M, G_N), dtype=torch.bfloat16, device=dev)
+    wsp = bi.router_workspace(M, E, dev)
     t_r_bi = timed(lambda: bi.bi_router_topk(X, W, bi.BI_F32, bi.BI_F32, M, H, E, K_TOP, lg, ids, wt, None, None,
-                                             stream=None))
+                                             workspace=wsp, stream=None))
     t_g_bi = timed(lambda: bi.bi_gemm_bf16(A, B, Cb, M, G_N, G_K, G_K, G_K, G_N, stream=None))
     return {"router_f32_matmul_topk": {"first_M_row0_logits_differ": first_l, "first_M_row0_ids_differ": first_i,
                                        "swept_M": r_sweep, "tokens_per_s_at_4096": M / t_r,
@@ -639,23 +886,24 @@ def _cpu_pool_task(arg):
 
 
 def oracle_sweep() -> dict:
-    """The oracle, single-threaded, per call over M (about 7 s): the router
-    (F32, H=2048, E=256, top-8) at M = 1 ... 4096 in full; the K=N=4096
-    projection in full at M = 1 and 19, and as an 8-row sample standing for
-    any larger M (the oracle's cost is linear in the rows)."""
+    """The oracle, single-threaded, per call over M (about 15 s): the router
+    (F32, H=2048, E=256, top-8) in full at every M listed; the K=N=4096
+    projection in full at every M up to 128, and as a fixed 64-row sample
+    standing for any larger M (the oracle's cost is linear in the rows)."""
     from oracle import oracle as orc
     from serving_numerics_gb300 import synth
     orc.build()
     W = synth.router_weights(7, 0, E, H)
     router = {}
-    for m in (1, 19, 64, 256, 1024, 4096):
+    for m in (1, 19, 64, 65, 75, 128, 256, 1024, 4096):
         X = synth.tokens(7, 0, 5000 + m, m, H)
         t = time.perf_counter()
         orc.router_full(X, W, K_TOP, "f32")
         router[str(m)] = m / (time.perf_counter() - t)
     B = synth.gemm_b(7, G_N, G_K)
     gemm = {}
-    for m, label in ((1, "1"), (19, "19"), (8, "per-row rate from an 8-row sample (any larger M)")):
+    for m, label in ((1, "1"), (19, "19"), (64, "64"), (65, "65"), (75, "75"), (128, "128"),
+                     (64, "per-row rate from a 64-row sample (any larger M)")):
         A = synth.gemm_a(7, m, G_K, layer=6000 + m)
         t = time.perf_counter()
         orc.gemm_bf16(A, B)

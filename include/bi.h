@@ -113,15 +113,23 @@ typedef struct CUstream_st *bi_stream;
  * Logits must be finite for the weights and margins to be meaningful (a
  * NaN ranks above every number and ties other NaNs by index).
  *
- * Scratch: for batches of more than 64 rows the partitions of a tile are
- * spread over several thread blocks (two once those halves fill the SMs,
- * 2*M*E*4 bytes of group sums; more below that; for batches whose group sums would
- * pass 64 MiB only the last rows') whose partial sums meet in a
- * library-owned device buffer (grown on the first call that needs more, one
- * buffer per device, never freed before exit).  Make a first
- * call at the largest M before capturing a CUDA graph.  Two calls that could
- * run at the same time on one device (different streams with no event
- * ordering them) must not both need the buffer.
+ * Work and memory.  Batches of at most 128 rows run as ONE launch: thread
+ * block clusters in which each block computes the logits of a slice of the
+ * experts and sends them, through distributed shared memory, to the block
+ * that selects their token.  Larger batches run the projection as 32 x 64
+ * tiles whose 16 partitions may be spread over several thread blocks; their
+ * group sums meet in `workspace` and the selection kernel adds them.  The
+ * library allocates nothing: the caller passes the workspace.
+ *   workspace        device buffer, 16-byte aligned, owned by the caller; may
+ *                    be NULL when workspace_bytes is 0
+ *   workspace_bytes  its size; must be at least bi_router_workspace_bytes(M, E)
+ *                    (0 for M <= 128 and E <= 512), else BI_ERR_INVALID_ARG
+ *                    before anything is launched
+ * Calls that could run at the same time on the GPU (different streams with
+ * no event between them) need workspaces that do not overlap; calls queued
+ * on one stream may share one.  BI_ERR_UNSUPPORTED_SHAPE is returned (before
+ * any launch) only on a GPU that cannot place clusters of 8 blocks, for a
+ * call of at most 128 rows given less workspace than its tiled plan needs.
  *
  * Ordering: the kernels start streaming w_gate before they wait for the
  * preceding kernel in the stream (programmatic dependent launch); x is read
@@ -133,13 +141,26 @@ typedef struct CUstream_st *bi_stream;
 BI_API bi_status bi_router_topk(const void *x, const void *w_gate, bi_dtype in_dtype,
                          bi_dtype logit_dtype, int32_t M, int32_t H, int32_t E, int32_t k,
                          void *logits_out, int32_t *ids_out, float *weights_out,
-                         float *margin_out, int32_t *margin_ulps_out, bi_stream s);
+                         float *margin_out, int32_t *margin_ulps_out, void *workspace,
+                         size_t workspace_bytes, bi_stream s);
+
+/*
+ * bi_router_workspace_bytes -- the workspace bi_router_topk and
+ * bi_router_gate_topk need for M rows and E experts, on any GPU: 0 for
+ * M <= 128 with E <= 512 (the one-launch cluster router); otherwise the
+ * largest group-sum area any of the tiled plans may use, 8*M*E bytes while
+ * that is at most 64 MiB, never less than min(64*M*E, 16 MiB) and never more
+ * than 64 MiB.  Host-only: touches no GPU.  Returns 0 for M <= 0.
+ */
+BI_API size_t bi_router_workspace_bytes(int32_t M, int32_t E);
 
 /*
  * bi_router_plan -- how bi_router_topk (and bi_router_gate_topk) would cut
- * the work for M rows and E experts on the current device: the rows below
- * *m_split run as whole tiles, the rest with each tile's partitions split
- * over *C blocks; *launches is the number of kernels one call launches.
+ * the work for M rows and E experts on the current device.  For the
+ * one-launch cluster router (M <= 128): *m_split = M, *C = minus the number
+ * of blocks per cluster, *launches = 1.  Otherwise the rows below *m_split
+ * run as whole tiles and the rest with each tile's partitions split over *C
+ * blocks, and *launches counts the projection launches plus the selection.
  * Introspection only (any plan gives the same bits); it launches nothing.
  * Returns BI_ERR_INVALID_ARG for NULL outputs or bad sizes, BI_ERR_CUDA when
  * no device is current.
@@ -161,6 +182,7 @@ BI_API bi_status bi_router_plan(int32_t M, int32_t E, int32_t *m_split, int32_t 
  *   w_sg             [H] in in_dtype, 16-byte aligned
  *   gate_dot_out     [M] f32: the dot of each row with w_sg
  *   gate_sigmoid_out [M] f32, optional (NULL): 1 / (1 + exp(-dot))
+ *   workspace, workspace_bytes  as bi_router_topk
  * Errors: as bi_router_topk; BI_ERR_INVALID_ARG for a NULL w_sg or
  * gate_dot_out when M > 0.
  */
@@ -168,7 +190,8 @@ BI_API bi_status bi_router_gate_topk(const void *x, const void *w_gate, const vo
                               bi_dtype logit_dtype, int32_t M, int32_t H, int32_t E, int32_t k,
                               void *logits_out, int32_t *ids_out, float *weights_out,
                               float *margin_out, int32_t *margin_ulps_out, float *gate_dot_out,
-                              float *gate_sigmoid_out, bi_stream s);
+                              float *gate_sigmoid_out, void *workspace, size_t workspace_bytes,
+                              bi_stream s);
 
 /*
  * bi_shared_gate -- the one-output shared-expert gate: dot = X[m,:] . w_sg,
@@ -236,27 +259,30 @@ BI_API bi_status bi_route_trace_hash(const int32_t *ids, int32_t M, int32_t k,
  * allocate device memory, with the same arguments and bit-identical results.
  *
  * No counterpart on the source pages: it exists for the caller, not for the
- * method.  bi_router_topk allocates its partial-sum scratch lazily with
- * cudaMalloc the first time a small batch needs it.  Some callers cannot let
- * a library do that: a serving engine that owns all device memory through
- * its own pool and forbids allocations outside it, or code that records the
- * router into a CUDA graph, where a first-time cudaMalloc inside the capture
- * is not allowed.  This entry point instead uses a fixed device array of
- * BI_NOALLOC_SCRATCH_BYTES compiled into the library (held by every GPU that
- * loads the library until the process exits) and never calls cudaMalloc,
- * cudaFree or any allocating routine.
+ * method.  bi_router_topk needs a device workspace from its caller for
+ * batches of more than 128 rows (and, with E = 1024, wherever 16-block
+ * clusters cannot be placed).  Some callers cannot provide one: a plugin or
+ * an embedded runtime that is handed device pointers for its inputs and
+ * outputs but owns no device memory and has no allocator to call, or code
+ * that must not let device memory be reserved on its behalf at all.  This
+ * entry point instead uses a fixed device array of BI_NOALLOC_SCRATCH_BYTES
+ * compiled into the library (held by every GPU that loads the library until
+ * the process exits) and never calls cudaMalloc, cudaFree or any allocating
+ * routine.
  *
- * It always spreads each 32x32 tile's 16 partitions over 16 thread blocks
- * (the small-batch decomposition), needing 16*M*E*4 bytes of scratch, so it
- * serves M*E <= BI_NOALLOC_SCRATCH_BYTES / 64 (M <= 64 at E = 256, M <= 32
- * at E = 512, M <= 16 at E = 1024); larger problems return
- * BI_ERR_UNSUPPORTED_SHAPE.  The first call on each device looks up the
- * array's device address (cudaGetSymbolAddress, with that device current):
- * make that first call before any stream capture.  Every call shares the one
- * array, whose contents persist between calls; each call overwrites all of
- * the scratch it reads before reading it, so nothing needs clearing.  Calls
- * that overlap on the GPU (on different streams, or from different host
- * threads) race on the array and must be serialised by the caller.
+ * It always spreads each 32x64 tile's 16 partitions over 16 thread blocks,
+ * needing 16*M*E*4 bytes of the array, so it serves M*E <=
+ * BI_NOALLOC_SCRATCH_BYTES / 64 (M <= 64 at E = 256, M <= 32 at E = 512,
+ * M <= 16 at E = 1024); larger problems return BI_ERR_UNSUPPORTED_SHAPE.
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current): make that first call
+ * before any stream capture.  Every call shares the one array, whose
+ * contents persist between calls; each call overwrites all of the scratch
+ * it reads before reading it, so nothing needs clearing.  Calls that overlap
+ * on the GPU (on different streams, or from different host threads) race on
+ * the array and must be serialised by the caller.  The cached address is
+ * only valid for the CUDA context it was looked up in: do not use the
+ * library across a cudaDeviceReset.
  */
 #define BI_NOALLOC_SCRATCH_BYTES (1u << 20)
 BI_API bi_status bi_router_topk_noalloc(const void *x, const void *w_gate, bi_dtype in_dtype,
@@ -285,7 +311,6 @@ BI_API bi_status bi_get_last_device_error(void);
  */
 BI_API bi_status bi_selftest_wait_timeout(uint32_t limit_us, bi_stream s);
 
-/* ABI version of this header: bumps on any incompatible change. */
 /*
  * bi_rmsnorm -- batch-invariant RMSNorm of every row:
  *
@@ -429,7 +454,25 @@ BI_API bi_status bi_prefix_split(const int32_t *lengths, int32_t n_requests, int
 BI_API bi_status bi_selftest_fma_rate(int32_t iters, int32_t packed, float *sink, bi_stream s,
                                       double *flops_launched);
 
-#define BI_ABI_VERSION 1
+/* ABI version of this header: bumps on any incompatible change (2: the
+ * router calls take a caller-owned workspace). */
+/*
+ * bi_selftest_dependent_floor -- measurement aid (no counterpart on the
+ * source pages): launches one thread-block cluster shaped like the
+ * one-launch router's at a single token (16 blocks, or 8 where 16 cannot be
+ * placed) whose blocks wait for the preceding kernel in the stream (the same
+ * programmatic dependent launch as the router), read in[block], pass two
+ * cluster barriers and write out[block] = in[block] + 1.  Timing a chain of
+ * these calls (each reading the previous call's out) gives the fixed cost of
+ * a dependent one-launch call with no arithmetic: the floor under the
+ * router's time at small M.
+ *   in, out  device arrays of at least 16 floats
+ * Returns BI_ERR_INVALID_ARG for NULL pointers, BI_ERR_UNSUPPORTED_SHAPE on
+ * a GPU that cannot place the cluster.
+ */
+BI_API bi_status bi_selftest_dependent_floor(const float *in, float *out, bi_stream s);
+
+#define BI_ABI_VERSION 2
 BI_API int32_t bi_abi_version(void);
 
 #ifdef __cplusplus

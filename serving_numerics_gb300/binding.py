@@ -22,11 +22,13 @@ FNV64_BASIS = 0xCBF29CE484222325
 # name -> (restype, argtypes), mirroring include/bi.h
 _P, _I32, _I64 = C.c_void_p, C.c_int32, C.c_int64
 SIGNATURES = {
-    "bi_router_topk": (C.c_int, [_P, _P, C.c_int, C.c_int, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P]),
+    "bi_router_topk": (C.c_int, [_P, _P, C.c_int, C.c_int, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P,
+                                 C.c_size_t, _P]),
+    "bi_router_workspace_bytes": (C.c_size_t, [_I32, _I32]),
     "bi_router_topk_noalloc": (C.c_int, [_P, _P, C.c_int, C.c_int, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P]),
     "bi_shared_gate": (C.c_int, [_P, _P, _I32, _I32, _P, _P, _P]),
     "bi_router_gate_topk": (C.c_int, [_P, _P, _P, C.c_int, C.c_int, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P,
-                                      _P, _P, _P]),
+                                      _P, _P, _P, C.c_size_t, _P]),
     "bi_gemm_bf16": (C.c_int, [_P, _P, _P, _I32, _I32, _I32, _I64, _I64, _I64, _P]),
     "bi_route_trace_hash": (C.c_int, [_P, _I32, _I32, _P, _I32, _P, _P, _P]),
     "bi_status_string": (C.c_char_p, [C.c_int]),
@@ -34,6 +36,7 @@ SIGNATURES = {
     "bi_abi_version": (C.c_int32, []),
     "bi_selftest_wait_timeout": (C.c_int, [C.c_uint32, _P]),
     "bi_selftest_fma_rate": (C.c_int, [_I32, _I32, _P, _P, _P]),
+    "bi_selftest_dependent_floor": (C.c_int, [_P, _P, _P]),
     "bi_get_config": (C.c_int, [_P, C.c_size_t]),
     "bi_router_plan": (C.c_int, [_I32, _I32, _P, _P, _P]),
     "bi_rmsnorm": (C.c_int, [_P, _P, C.c_int, _I32, _I32, C.c_float, _P, _P, _P]),
@@ -104,14 +107,39 @@ def _check(st: int, where: str):
 
 
 # ------------------------------------------------------------- raw ABI calls
+def _workspace(ws):
+    """(pointer, bytes) of a router workspace given as None, a torch tensor
+    (its whole storage) or a (pointer, bytes) pair."""
+    if ws is None:
+        return None, 0
+    if isinstance(ws, tuple):
+        return ws[0], int(ws[1])
+    return ws.data_ptr(), ws.numel() * ws.element_size()
+
+
 def bi_router_topk(x, w_gate, in_dtype, logit_dtype, M, H, E, k, logits_out, ids_out,
-                   weights_out=None, margin_out=None, margin_ulps_out=None, stream=None, check=True):
+                   weights_out=None, margin_out=None, margin_ulps_out=None, workspace=None, stream=None,
+                   check=True):
+    wp, wn = _workspace(workspace)
     st = load().bi_router_topk(_ptr(x), _ptr(w_gate), in_dtype, logit_dtype, M, H, E, k,
                                _ptr(logits_out), _ptr(ids_out), _ptr(weights_out), _ptr(margin_out),
-                               _ptr(margin_ulps_out), _stream(stream))
+                               _ptr(margin_ulps_out), wp, wn, _stream(stream))
     if check:
         _check(st, "bi_router_topk")
     return st
+
+
+def router_workspace_bytes(M: int, E: int) -> int:
+    return int(load().bi_router_workspace_bytes(M, E))
+
+
+def router_workspace(M: int, E: int, device="cuda"):
+    """A caller-owned workspace for bi_router_topk / bi_router_gate_topk (a
+    torch uint8 tensor of bi_router_workspace_bytes(M, E) bytes; None when
+    none is needed).  torch's allocations are 256-byte aligned."""
+    import torch
+    n = router_workspace_bytes(M, E)
+    return torch.empty(n, dtype=torch.uint8, device=device) if n > 0 else None
 
 
 def bi_router_topk_noalloc(x, w_gate, in_dtype, logit_dtype, M, H, E, k, logits_out, ids_out,
@@ -127,11 +155,12 @@ def bi_router_topk_noalloc(x, w_gate, in_dtype, logit_dtype, M, H, E, k, logits_
 
 def bi_router_gate_topk(x, w_gate, w_sg, in_dtype, logit_dtype, M, H, E, k, logits_out, ids_out,
                         weights_out=None, margin_out=None, margin_ulps_out=None, gate_dot_out=None,
-                        gate_sigmoid_out=None, stream=None, check=True):
+                        gate_sigmoid_out=None, workspace=None, stream=None, check=True):
+    wp, wn = _workspace(workspace)
     st = load().bi_router_gate_topk(_ptr(x), _ptr(w_gate), _ptr(w_sg), in_dtype, logit_dtype, M, H, E, k,
                                     _ptr(logits_out), _ptr(ids_out), _ptr(weights_out), _ptr(margin_out),
                                     _ptr(margin_ulps_out), _ptr(gate_dot_out), _ptr(gate_sigmoid_out),
-                                    _stream(stream))
+                                    wp, wn, _stream(stream))
     if check:
         _check(st, "bi_router_gate_topk")
     return st
@@ -232,7 +261,8 @@ def selftest_fma_rate(iters: int, sink, packed: bool = False, stream=None) -> fl
 
 
 def router_plan(M: int, E: int):
-    """bi_router_plan: (m_split, C, launches) for M rows and E experts."""
+    """bi_router_plan: (m_split, C, launches) for M rows and E experts; C < 0
+    means the one-launch cluster router with -C blocks per cluster."""
     ms, c, n = C.c_int32(), C.c_int32(), C.c_int32()
     _check(load().bi_router_plan(M, E, C.byref(ms), C.byref(c), C.byref(n)), "bi_router_plan")
     return ms.value, c.value, n.value
@@ -255,13 +285,20 @@ def prefix_split(lengths, block: int):
     return list(cached)[:n], list(offs)
 
 
+def selftest_dependent_floor(inp, out, stream=None):
+    """One launch of the dependent-cluster floor probe (in, out: >= 16 floats)."""
+    _check(load().bi_selftest_dependent_floor(_ptr(inp), _ptr(out), _stream(stream)),
+           "bi_selftest_dependent_floor")
+
+
 def bi_selftest_wait_timeout(limit_us: int, stream=None) -> int:
     return load().bi_selftest_wait_timeout(limit_us, _stream(stream))
 
 
 # ------------------------------------------------------------- tensor helpers
-def router_topk(x, w_gate, k: int, logit_dtype: str = "f32", stream=None, out=None):
-    """Allocate the outputs with torch and run bi_router_topk.
+def router_topk(x, w_gate, k: int, logit_dtype: str = "f32", stream=None, out=None, workspace=None):
+    """Allocate the outputs (and, for batches that need one, a workspace)
+    with torch and run bi_router_topk.
 
     x [M,H], w_gate [E,H]: both float32 or both bfloat16 CUDA tensors.
     Returns dict(logits, ids, weights, margin, margin_ulps)."""
@@ -279,14 +316,17 @@ def router_topk(x, w_gate, k: int, logit_dtype: str = "f32", stream=None, out=No
             "margin": torch.empty((M,), dtype=torch.float32, device=dev),
             "margin_ulps": torch.empty((M,), dtype=torch.int32, device=dev),
         }
+    if workspace is None:
+        workspace = router_workspace(M, E, x.device)
     bi_router_topk(x, w_gate, ind, ld, M, H, E, k, out["logits"], out["ids"], out.get("weights"),
-                   out.get("margin"), out.get("margin_ulps"), stream=stream)
+                   out.get("margin"), out.get("margin_ulps"), workspace=workspace, stream=stream)
     return out
 
 
-def router_gate_topk(x, w_gate, w_sg, k: int, logit_dtype: str = "f32", stream=None):
-    """Allocate the outputs with torch and run bi_router_gate_topk.
-    Returns the router_topk dict plus gate_dot and gate_sigmoid."""
+def router_gate_topk(x, w_gate, w_sg, k: int, logit_dtype: str = "f32", stream=None, workspace=None):
+    """Allocate the outputs (and a workspace where needed) with torch and run
+    bi_router_gate_topk.  Returns the router_topk dict plus gate_dot and
+    gate_sigmoid."""
     import torch
     M, H = x.shape
     E = w_gate.shape[0]
@@ -302,8 +342,11 @@ def router_gate_topk(x, w_gate, w_sg, k: int, logit_dtype: str = "f32", stream=N
         "gate_dot": torch.empty((M,), dtype=torch.float32, device=dev),
         "gate_sigmoid": torch.empty((M,), dtype=torch.float32, device=dev),
     }
+    if workspace is None:
+        workspace = router_workspace(M, E, dev)
     bi_router_gate_topk(x, w_gate, w_sg, ind, ld, M, H, E, k, out["logits"], out["ids"], out["weights"],
-                        out["margin"], out["margin_ulps"], out["gate_dot"], out["gate_sigmoid"], stream=stream)
+                        out["margin"], out["margin_ulps"], out["gate_dot"], out["gate_sigmoid"],
+                        workspace=workspace, stream=stream)
     return out
 
 

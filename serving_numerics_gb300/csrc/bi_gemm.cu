@@ -22,11 +22,15 @@
 //   warps 2..5  epilogue: tcgen05.ld of their 32-lane quarter, bf16 pack,
 //               16-byte global stores; releases the accumulator buffer
 // Double-buffered accumulators let the epilogue of tile t overlap the MMAs
-// of tile t+1.  When the tiles are more than one wave but do not fill the
-// last one, the tiles of that last partial wave are done as two 128 x 128
-// halves each (N = 128 tensor-core steps), so it takes about half the time
-// of a full wave; each output element still gets the same 16-deep steps in
-// the same K order.  Every wait on an mbarrier is bounded (about 2 s); on
+// of tile t+1.  Tiles can be cut along N into 2, 4 or 8 pieces (N = 128, 64
+// or 32 tensor-core steps) without changing any element's arithmetic: each
+// output element still gets the same 16-deep steps in the same K order.
+// Pieces serve two cases: when the tiles are more than one wave but do not
+// fill the last one, the tiles of that last partial wave run as halves, so
+// it takes about half the time of a full wave; and when there are fewer
+// tiles than SMs (small M: one 128-row tile holds up to 128 tokens), every
+// tile is cut into the most pieces that still fit one per SM, so that
+// 8 times as many SMs stream the weight matrix.  Every wait on an mbarrier is bounded (about 2 s); on
 // expiry the kernel records BI_ERR_TIMEOUT in the device error word and
 // carries on.
 #include <cuda_bf16.h>
@@ -41,8 +45,8 @@ namespace {
 
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
 gemm_bf16_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__ CUtensorMap tmb,
-                 const __grid_constant__ CUtensorMap tmb_half, __nv_bfloat16 *__restrict__ C, int M, int N,
-                 int K, long long ldc, int n_full, unsigned int *err)
+                 const __grid_constant__ CUtensorMap tmb_piece, __nv_bfloat16 *__restrict__ C, int M, int N,
+                 int K, long long ldc, int n_full, int lg_s, unsigned int *err)
 {
     pdl_trigger();   // dependents may launch now; each waits before reading our outputs
     extern __shared__ uint8_t smem_raw[];
@@ -53,12 +57,13 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant_
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m_tiles = (M + BM - 1) / BM, n_tiles = (N + BN - 1) / BN;
     const int num_tiles = m_tiles * n_tiles, kblocks = K / BK;
-    const int num_items = n_full + 2 * (num_tiles - n_full);
+    const int num_items = n_full + ((num_tiles - n_full) << lg_s);
+    const int pn = BN >> lg_s;                           // columns of a piece
 
     if (threadIdx.x == 0) {
         prefetch_tmap(&tma);
         prefetch_tmap(&tmb);
-        prefetch_tmap(&tmb_half);
+        prefetch_tmap(&tmb_piece);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full_bar[s], 1);
             mbar_init(&empty_bar[s], 1);
@@ -81,17 +86,17 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant_
         if (lane == 0) {   // TMA producer
             uint32_t it = 0;
             for (int item = blockIdx.x; item < num_items; item += gridDim.x) {
-                int half;
-                const int tile = item_tile(item, n_full, half);
+                int piece;
+                const int tile = item_tile(item, n_full, lg_s, piece);
                 const int mt = tile % m_tiles, nt = tile / m_tiles;
-                const int n0 = nt * BN + (half > 0 ? BN / 2 : 0);
+                const int n0 = nt * BN + (piece > 0 ? piece * pn : 0);
                 for (int kb = 0; kb < kblocks; ++kb, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
                     mbar_wait(&empty_bar[s], ph ^ 1u, err, 0x21);
                     uint8_t *st = smem + s * STAGE_BYTES;
-                    mbar_arrive_expect_tx(&full_bar[s], half < 0 ? STAGE_BYTES : A_BYTES + B_BYTES / 2);
+                    mbar_arrive_expect_tx(&full_bar[s], piece < 0 ? STAGE_BYTES : A_BYTES + (B_BYTES >> lg_s));
                     tma_load_2d(st, &tma, &full_bar[s], kb * BK, mt * BM);
-                    tma_load_2d(st + A_BYTES, half < 0 ? &tmb : &tmb_half, &full_bar[s], kb * BK, n0);
+                    tma_load_2d(st + A_BYTES, piece < 0 ? &tmb : &tmb_piece, &full_bar[s], kb * BK, n0);
                 }
             }
         }
@@ -99,7 +104,7 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant_
         if (lane == 0) {   // MMA issuer
             uint32_t it = 0, tc = 0;
             for (int item = blockIdx.x; item < num_items; item += gridDim.x, ++tc) {
-                const uint32_t idesc = item < n_full ? IDESC : IDESC_HALF;
+                const uint32_t idesc = item < n_full ? IDESC : idesc_n(pn);
                 const uint32_t b = tc & 1u, tph = (tc >> 1) & 1u;
                 mbar_wait(&tempty_bar[b], tph ^ 1u, err, 0x22);
                 tc_fence_after();
@@ -125,10 +130,10 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant_
         const int row = quad * 32 + lane;
         uint32_t tc = 0;
         for (int item = blockIdx.x; item < num_items; item += gridDim.x, ++tc) {
-            int half;
-            const int tile = item_tile(item, n_full, half);
+            int piece;
+            const int tile = item_tile(item, n_full, lg_s, piece);
             const int mt = tile % m_tiles, nt = tile / m_tiles;
-            const int nbase = nt * BN + (half > 0 ? BN / 2 : 0), nchunks = half < 0 ? BN / 32 : BN / 64;
+            const int nbase = nt * BN + (piece > 0 ? piece * pn : 0), nchunks = piece < 0 ? BN / 32 : pn / 32;
             const uint32_t b = tc & 1u, tph = (tc >> 1) & 1u;
             mbar_wait(&tfull_bar[b], tph, err, 0x24);
             tc_fence_after();
@@ -194,25 +199,39 @@ extern "C" bi_status bi_gemm_bf16(const void *A, const void *B, void *C, int32_t
                                CU_TENSOR_MAP_SWIZZLE_128B)) != BI_OK)
             return st;
     }
-    alignas(64) CUtensorMap tmb_half;
+    // The work plan (any plan gives the same bits):
+    //  - fewer tiles than SMs: every tile cut into 2^lg_s pieces, the most
+    //    (at most 8) that still give each piece an SM of its own;
+    //  - otherwise whole tiles for every full wave, and the tiles of a last
+    //    partial wave as halves when that keeps them to one round
+    //    (2 * rest <= blocks).
+    const long long tiles = (long long)((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+    if (tiles > (1ll << 30)) return BI_ERR_UNSUPPORTED_SHAPE;
+    long long n_full, items;
+    int lg_s = 1;
+    if (tiles < d->sm_count) {
+        lg_s = 0;
+        while (lg_s < 3 && (tiles << (lg_s + 1)) <= d->sm_count) ++lg_s;
+        n_full = lg_s == 0 ? tiles : 0;
+        items = tiles << lg_s;
+    } else {
+        const long long rest = tiles % d->sm_count;
+        n_full = (rest != 0 && 2 * rest <= d->sm_count) ? tiles - rest : tiles;
+        items = n_full + 2 * (tiles - n_full);
+    }
+    if (lg_s == 0) lg_s = 1;             // no pieces in this launch; the piece map is then unused
+    const int grid = (int)(items < d->sm_count ? items : d->sm_count);
+    alignas(64) CUtensorMap tmb_piece;
     for (int h = 0; h < 2; ++h) {
         const uint64_t dims[2] = {(uint64_t)K, (uint64_t)N};
         const uint64_t strides[1] = {(uint64_t)ldb * 2};
-        const uint32_t box[2] = {(uint32_t)BK, (uint32_t)(h ? BN / 2 : BN)};
-        if ((st = encode_tiled(h ? &tmb_half : &tmb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, dims, strides, box,
+        const uint32_t box[2] = {(uint32_t)BK, (uint32_t)(h ? BN >> lg_s : BN)};
+        if ((st = encode_tiled(h ? &tmb_piece : &tmb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, dims, strides, box,
                                CU_TENSOR_MAP_SWIZZLE_128B)) != BI_OK)
             return st;
     }
     if ((st = set_smem_once(d, KID_GEMM, gemm_bf16_kernel, GEMM_SMEM)) != BI_OK) return st;
-
-    // whole tiles for every full wave; the tiles of a last partial wave go
-    // as halves when that keeps them to one round (2 * rest <= blocks)
-    const long long tiles = (long long)((M + BM - 1) / BM) * ((N + BN - 1) / BN);
-    if (tiles > (1ll << 30)) return BI_ERR_UNSUPPORTED_SHAPE;
-    const int grid = (int)(tiles < d->sm_count ? tiles : d->sm_count);
-    const long long rest = tiles % grid;
-    const long long n_full = (tiles > grid && rest != 0 && 2 * rest <= grid) ? tiles - rest : tiles;
     return launch_pdl(gemm_bf16_kernel, dim3(grid), dim3(GEMM_THREADS), (size_t)GEMM_SMEM,
-                      reinterpret_cast<cudaStream_t>(s), tma, tmb, tmb_half, static_cast<__nv_bfloat16 *>(C),
-                      (int)M, (int)N, (int)K, (long long)ldc, (int)n_full, d->err);
+                      reinterpret_cast<cudaStream_t>(s), tma, tmb, tmb_piece, static_cast<__nv_bfloat16 *>(C),
+                      (int)M, (int)N, (int)K, (long long)ldc, (int)n_full, lg_s, d->err);
 }

@@ -6,6 +6,8 @@
 #include <cudaTypedefs.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "bi.h"
 
 namespace bi {
@@ -21,21 +23,20 @@ constexpr int kGemmMmaK = 16;         // each block as four 16-deep tensor-core 
 static_assert(kRouterSlab == kRouterBlock * kRouterParts, "a slab is one block per partition");
 
 // Per-device state, created on the first call made with that device current.
+// The library keeps no device buffers of its own beyond the sticky error word
+// (and the fixed array of bi_router_topk_noalloc): every call's working
+// memory is the caller's.
 struct Device {
     int ordinal = -1;
     int sm_count = 0;
     unsigned int *err = nullptr;   // device address of the sticky error word
-    void *scratch = nullptr;       // router partial sums (see router.cu)
-    size_t scratch_bytes = 0;
-    uint64_t attr_done = 0;        // kernels whose smem attribute is set (bit per kernel id)
+    // kernels whose attributes are set (bit per kernel id); concurrent first
+    // calls from several host threads may both set them, which is harmless
+    std::atomic<uint64_t> attr_done[2] = {};
 };
 
 // The state of the current device (never NULL on BI_OK).
 bi_status current_device(Device **out);
-
-// Grow-only device scratch owned by the library (allocated at most a few
-// times per device over the process lifetime, never per call).
-bi_status device_scratch(Device *d, size_t bytes, void **out);
 
 // cuTensorMapEncodeTiled, resolved once through the runtime.
 bi_status encode_tiled(CUtensorMap *map, CUtensorMapDataType dt, uint32_t rank,
@@ -67,42 +68,74 @@ bi_status launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
     return from_cuda(e);
 }
 
-// Once per device and kernel: the dynamic shared memory limit, and the
-// largest shared-memory carveout.  Every kernel of the library asks for the
-// same carveout, so a small kernel resident on an SM never leaves it
-// configured for less shared memory than the next large-tile block needs
-// (an SM changes its carveout only when it is empty, so a mismatch would
-// make the large block wait for the small one to finish).
-template <typename K>
-bi_status set_smem_once(Device *d, int kernel_id, K kernel, size_t bytes)
+// Once per device and kernel: run `set` (which sets the kernel's function
+// attributes and returns false on a CUDA error) unless it already succeeded.
+template <typename F>
+bi_status set_attr_once(Device *d, int kernel_id, F &&set)
 {
-    uint64_t bit = 1ull << kernel_id;
-    if (d->attr_done & bit) return BI_OK;
-    if (bytes > 0 &&
-        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess)
-        return BI_ERR_CUDA;
-    if (cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess)
-        return BI_ERR_CUDA;
-    d->attr_done |= bit;
+    const uint64_t bit = 1ull << (kernel_id & 63);
+    std::atomic<uint64_t> &word = d->attr_done[kernel_id >> 6];
+    if (word.load(std::memory_order_acquire) & bit) return BI_OK;
+    if (!set()) return BI_ERR_CUDA;
+    word.fetch_or(bit, std::memory_order_acq_rel);
     return BI_OK;
 }
 
-// kernel ids for set_smem_once (one bit each)
+// The dynamic shared memory limit and the largest shared-memory carveout.
+// Every kernel of the library asks for the same carveout, so a small kernel
+// resident on an SM never leaves it configured for less shared memory than
+// the next large-tile block needs (an SM changes its carveout only when it
+// is empty, so a mismatch would make the large block wait for the small one
+// to finish).
+template <typename K>
+bi_status set_smem_once(Device *d, int kernel_id, K kernel, size_t bytes)
+{
+    return set_attr_once(d, kernel_id, [&]() -> bool {
+        if (bytes > 0 &&
+            cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess)
+            return false;
+        return cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                    (int)cudaSharedmemCarveoutMaxShared) == cudaSuccess;
+    });
+}
+
+// kernel ids for set_attr_once (one bit each, 128 in all)
 enum : int {
     KID_ROUTER_PROJ = 0,   // 10 instantiations: 0..9
     KID_GEMM = 16,
     KID_SELECT = 20,       // 4 instantiations: 20..23 (two group sums or none)
     KID_GATE = 24,
     KID_HASH = 25,         // 4 instantiations: 25..28
-    KID_ROUTER_GEMV = 30,  // 2 instantiations (8 tokens per block): 30..31
     KID_SELECT_GATE = 34,  // 4 instantiations: 34..37 (two group sums or none)
     KID_MOE = 40,          // 5 kernels: 40..44
-    KID_NORM = 45,         // 2 instantiations: 45..46
-    KID_ROUTER_PROJ_SHALLOW = 49,   // 2 instantiations: 49..50
+    KID_NORM = 45,         // 4 instantiations: 45..48
+    KID_ROUTER_PROJ_SHALLOW = 49,   // 2 instantiations: 49..50 (after the norms' 45..48)
     KID_SELECT_GENERAL = 51,        // 4 instantiations: 51..54
     KID_SELECT_GATE_GENERAL = 55,   // 4 instantiations: 55..58
-    KID_ROUTER_GEMV1 = 59,          // 2 instantiations (one token per block): 59..60
+    KID_ROUTER_CLUSTER = 64,        // 10 instantiations: 64..73
+    KID_FLOOR = 74,
 };
+
+// Batches of at most this many rows take the one-launch cluster router
+// (csrc/bi_router_cluster.cu); larger ones the tiled projection + selection.
+constexpr int kClusterMaxM = 128, kClusterMaxE = 512;
+
+// How the cluster router cuts one call (see bi_router_cluster.cu).
+struct ClusterPlan {
+    bool ok;          // false: the cluster router does not apply to this call
+    int CS;           // blocks per cluster (each owns E / CS experts)
+    int TM, NT;       // tokens per cluster; the compiled token tile (>= TM)
+    int NC;           // clusters
+    int warps;        // warps per block
+    int Eb4;          // gate rows per block, rounded up to a multiple of 4
+    int nst, stage_bytes, x_off, g_off, gather_off, smem;   // shared-memory layout
+};
+
+ClusterPlan cluster_plan(Device *d, int M, int E, int H, int es, bool gate);
+
+bi_status router_cluster_call(Device *d, const ClusterPlan &p, const void *x, const void *w_gate, bool f32in,
+                              int logit_bf16, int M, int H, int E, int k, void *logits, int32_t *ids,
+                              float *weights, float *margin, int32_t *ulps, const void *w_sg, float *gdot,
+                              float *gsig, cudaStream_t s);
 
 }  // namespace bi

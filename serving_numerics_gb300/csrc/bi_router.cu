@@ -33,8 +33,11 @@
 #include <cuda_bf16.h>
 #include <limits.h>
 
+#include <algorithm>
+
 #include "bi_device.cuh"
 #include "bi_internal.h"
+#include "bi_select.cuh"
 
 namespace bi {
 namespace {
@@ -301,29 +304,6 @@ router_proj_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
     }
 }
 
-// Order key of an f32 value: larger key = ranks higher.  NaN ranks above
-// everything; -0 is folded onto +0 so the two compare equal.  Key 0 is below
-// every real value (the smallest, -inf, maps to 0x007FFFFF) and marks a
-// taken expert.
-__device__ __forceinline__ uint32_t rank_key(float x)
-{
-    uint32_t u = __float_as_uint(x);
-    if ((u & 0x7FFFFFFFu) > 0x7F800000u) return 0xFFFFFFFFu;
-    if (u == 0x80000000u) u = 0u;
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-// Sign-magnitude ordinal of a logit-dtype pattern (+0 and -0 both 0).
-__device__ __forceinline__ long long sm_ord(float x, int bf16)
-{
-    uint32_t u = __float_as_uint(x);
-    if (bf16) {
-        const uint32_t b = u >> 16;
-        return (b & 0x8000u) ? -(long long)(b & 0x7FFFu) : (long long)b;
-    }
-    return (u & 0x80000000u) ? -(long long)(u & 0x7FFFFFFFu) : (long long)u;
-}
-
 constexpr int kSelWarps = 8;
 constexpr size_t kGateStageMax = 96 * 1024;   // shared memory for the staged gate rows (2 blocks per SM)
 
@@ -523,75 +503,7 @@ router_select_kernel(const float *__restrict__ part, int C, int m_split, void *l
         }
     }
 
-    // each lane sorts its (key, index) pairs once, best first (ascending
-    // index among equal keys); a round then only compares lane heads
-    uint32_t key[EPLM];
-    int idx[EPLM];
-#pragma unroll
-    for (int i = 0; i < EPLM; ++i) {
-        key[i] = i < epl ? rank_key(v[i]) : 0u;
-        idx[i] = lane + 32 * i;
-    }
-#pragma unroll
-    for (int a = 0; a < EPLM; ++a) {            // odd-even transposition network
-#pragma unroll
-        for (int i = a & 1; i + 1 < EPLM; i += 2) {
-            const bool sw = key[i + 1] > key[i];    // equal keys keep the lower index first
-            const uint32_t k0 = sw ? key[i + 1] : key[i], k1 = sw ? key[i] : key[i + 1];
-            const int i0 = sw ? idx[i + 1] : idx[i], i1 = sw ? idx[i] : idx[i + 1];
-            const float v0 = sw ? v[i + 1] : v[i], v1 = sw ? v[i] : v[i + 1];
-            key[i] = k0; key[i + 1] = k1; idx[i] = i0; idx[i + 1] = i1; v[i] = v0; v[i + 1] = v1;
-        }
-    }
-
-    float l0 = 0.0f, den = 0.0f, my_e = 0.0f, v_sel_min = 0.0f, v_rej_max = 0.0f;
-    int my_id = 0;
-    for (int r = 0; r <= k; ++r) {
-        const uint32_t bk = key[0];
-        const uint32_t mk = __reduce_max_sync(0xFFFFFFFFu, bk);
-        const uint32_t holders = __ballot_sync(0xFFFFFFFFu, bk == mk);
-        // one lane holds the maximum key: its head wins; several (equal
-        // values in different lanes): the lowest index among them wins
-        const uint32_t win = (holders & (holders - 1u)) == 0u
-                                 ? (uint32_t)__shfl_sync(0xFFFFFFFFu, idx[0], __ffs(holders) - 1)
-                                 : __reduce_min_sync(0xFFFFFFFFu, bk == mk ? (uint32_t)idx[0] : 0xFFFFFFFFu);
-        const int wl = (int)(win & 31u);
-        const float wv = __shfl_sync(0xFFFFFFFFu, v[0], wl);
-        if (lane == wl) {                       // pop the head
-#pragma unroll
-            for (int i = 0; i + 1 < EPLM; ++i) {
-                key[i] = key[i + 1];
-                idx[i] = idx[i + 1];
-                v[i] = v[i + 1];
-            }
-            key[EPLM - 1] = 0u;
-        }
-        if (r == k) {
-            v_rej_max = wv;
-            break;
-        }
-        if (r == 0) l0 = wv;
-        const float ex = expf(wv - l0);
-        den += ex;                           // rank order
-        if (lane == r) {
-            my_e = ex;
-            my_id = (int)win;
-        }
-        v_sel_min = wv;
-    }
-    if (lane < k) {
-        ids[(size_t)m * k + lane] = my_id;
-        if (weights) weights[(size_t)m * k + lane] = my_e / den;
-    }
-    if (lane == 0) {
-        if (margin) margin[m] = v_sel_min - v_rej_max;
-        if (ulps) {
-            long long d = sm_ord(v_sel_min, logit_bf16) - sm_ord(v_rej_max, logit_bf16);
-            if (d > INT_MAX) d = INT_MAX;
-            if (d < INT_MIN) d = INT_MIN;
-            ulps[m] = (int32_t)d;
-        }
-    }
+    warp_select<EPLM>(v, lane, epl, k, logit_bf16, (size_t)m, ids, weights, margin, ulps);
 
     // the shared gate (bi_router_gate_topk): lanes 0..15 are the 16
     // partitions; the butterfly with offsets 1, 2, 4, 8 is the pairwise tree
@@ -621,222 +533,6 @@ router_select_kernel(const float *__restrict__ part, int C, int m_split, void *l
             if (gate.sig) gate.sig[m] = 1.0f / (1.0f + expf(-g));
         }
     }
-}
-
-// ---------------------------------------------------------------------------
-// Small-batch twin: the same reduction contract shaped like a matrix-vector
-// product, for batches too small to fill 32-token tiles.  One warp owns two
-// experts; lane 16*x + q runs partition q's chain for expert x over the
-// block's T tokens (T accumulators), reading whole slabs of X and of the gate
-// rows that TMA stages in a ring, two 128-wide slabs per stage.  The
-// 16 partials of a (token, expert) sit in 16 lanes of one half-warp and are
-// added by butterfly shuffles with offsets 1, 2, 4, 8: lanes q and q^d hold
-// the same sum after each level (fp addition is commutative), and the
-// levels pair exactly the partitions the pairwise tree pairs.  No scratch,
-// and every gate row is read by one warp of its own, so even M = 1 spreads
-// W_gate over E/2 thread blocks.
-// ---------------------------------------------------------------------------
-// Tokens per block: 8 for 32 < M <= 64 (four warps share the staged rows);
-// up to M = 32, one token and one warp per block: E/2 * M warps spread over
-// the SMs beat fewer warps that each carry several tokens' chains (same-box
-// timings of the router call: 7.7 against 9.8 us at M = 1, 9.6 against
-// 13.7 at M = 8, 20.0 against 21.3 at M = 32; 26 against 22 at M = 48).
-constexpr int kGemvT = 8;
-constexpr int kGemvOneTokenMaxM = 32;
-
-// WPB warps per block share one staged X tile of T rows; each warp owns 2
-// experts.  One stage holds two slabs (256 h): boxes [T rows x 256] of X and
-// [2*WPB rows x 256] of W_gate.
-constexpr int kGemvSpan = 2 * kSlab;
-
-template <typename InT, int WPB, int T>
-struct GemvCfg {
-    static constexpr int NST = WPB == 1 ? 8 : 4;                         // ring depth (stages)
-    static constexpr int XBOX = T * kGemvSpan * (int)sizeof(InT);
-    static constexpr int WBOX = 2 * WPB * kGemvSpan * (int)sizeof(InT);
-    static constexpr int STAGE_BYTES = XBOX + WBOX;
-    static constexpr int SMEM = NST * STAGE_BYTES + 1024;
-};
-
-template <typename InT, int WPB, int T>
-__global__ void __launch_bounds__(32 * WPB)
-router_gemv_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
-                   int M, int E, int H, int logit_bf16, void *__restrict__ out, unsigned int *err)
-{
-    pdl_trigger();   // dependents may launch now; each waits before reading our outputs
-    using Cfg = GemvCfg<InT, WPB, T>;
-    constexpr int NST = Cfg::NST;
-    extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t full_bar[NST];
-    __shared__ int released[NST];
-    uint8_t *smem = smem_align1024(smem_raw);
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, q = lane & 15;
-    const int x = 2 * warp + (lane >> 4);               // expert within the block
-    const int e0 = blockIdx.x * 2 * WPB, m0 = blockIdx.y * T;
-    const int ns = (H + kSlab - 1) / kSlab;
-    const int nstage = (H + kGemvSpan - 1) / kGemvSpan;
-    const int nt = min(T, M - m0);
-    const int nst = nstage < NST ? nstage : NST;
-    const bool oneshot = nstage <= NST;
-
-    if (tid == 0) {
-        prefetch_tmap(&tmx);
-        prefetch_tmap(&tmw);
-        for (int s = 0; s < NST; ++s) {
-            mbar_init(&full_bar[s], 1);
-            released[s] = 0;
-        }
-        mbar_init_fence();
-        // the gate rows are weights, not produced by the preceding kernel:
-        // start streaming them before waiting for it.  When the whole of H
-        // fits the ring, one barrier covers every box and the loop below
-        // never waits again.
-        if (oneshot) mbar_arrive_expect_tx(&full_bar[0], (uint32_t)(nstage * Cfg::STAGE_BYTES));
-        for (int s = 0; s < nst; ++s) {
-            uint8_t *st = smem + s * Cfg::STAGE_BYTES;
-            uint64_t *bar = oneshot ? &full_bar[0] : &full_bar[s];
-            if (!oneshot) mbar_arrive_expect_tx(bar, (uint32_t)Cfg::STAGE_BYTES);
-            tma_load_2d(st + Cfg::XBOX, &tmw, bar, kGemvSpan * s, e0);
-        }
-    }
-    pdl_wait();                  // X may be the preceding kernel's output
-    if (tid == 0)
-        for (int s = 0; s < nst; ++s)
-            tma_load_2d(smem + s * Cfg::STAGE_BYTES, &tmx, oneshot ? &full_bar[0] : &full_bar[s],
-                        kGemvSpan * s, m0);
-    __syncthreads();
-
-    auto refill = [&](int s, int slot) {
-        uint8_t *st = smem + slot * Cfg::STAGE_BYTES;
-        mbar_arrive_expect_tx(&full_bar[slot], (uint32_t)Cfg::STAGE_BYTES);
-        tma_load_2d(st + Cfg::XBOX, &tmw, &full_bar[slot], kGemvSpan * s, e0);
-        tma_load_2d(st, &tmx, &full_bar[slot], kGemvSpan * s, m0);
-    };
-
-    float acc[T];
-#pragma unroll
-    for (int t = 0; t < T; ++t) acc[t] = 0.0f;
-    int slot = 0;
-    uint32_t phase = 0;
-    for (int s = 0; s < nstage; ++s) {
-        if (!oneshot || s == 0) mbar_wait(&full_bar[slot], phase, err, 0x18);
-        const uint8_t *st = smem + slot * Cfg::STAGE_BYTES;
-#pragma unroll
-        for (int sub = 0; sub < 2; ++sub) {          // the stage's two slabs, in order
-            const int slab = 2 * s + sub;
-            if (slab < ns && kSlab * slab + kBlk * q < H) {
-                const int col = sub * kSlab + kBlk * q;   // column of this block in the stage
-                if constexpr (sizeof(InT) == 4) {
-                    const float *ws = reinterpret_cast<const float *>(st + Cfg::XBOX) + x * kGemvSpan + col;
-                    const float4 w0 = *reinterpret_cast<const float4 *>(ws);
-                    const float4 w1 = *reinterpret_cast<const float4 *>(ws + 4);
-#pragma unroll
-                    for (int t = 0; t < T; ++t) {
-                        if (t < nt) {
-                            const float *xs = reinterpret_cast<const float *>(st) + t * kGemvSpan + col;
-                            const float4 a0 = *reinterpret_cast<const float4 *>(xs);
-                            const float4 a1 = *reinterpret_cast<const float4 *>(xs + 4);
-                            float a = acc[t];
-                            a = __fmaf_rn(a0.x, w0.x, a);
-                            a = __fmaf_rn(a0.y, w0.y, a);
-                            a = __fmaf_rn(a0.z, w0.z, a);
-                            a = __fmaf_rn(a0.w, w0.w, a);
-                            a = __fmaf_rn(a1.x, w1.x, a);
-                            a = __fmaf_rn(a1.y, w1.y, a);
-                            a = __fmaf_rn(a1.z, w1.z, a);
-                            a = __fmaf_rn(a1.w, w1.w, a);
-                            acc[t] = a;
-                        }
-                    }
-                } else {
-                    const uint4 wr =
-                        *reinterpret_cast<const uint4 *>(st + Cfg::XBOX + 2 * (x * kGemvSpan + col));
-#pragma unroll
-                    for (int t = 0; t < T; ++t) {
-                        if (t < nt) {
-                            const uint4 xr = *reinterpret_cast<const uint4 *>(st + 2 * (t * kGemvSpan + col));
-                            float a = acc[t];
-                            a = __fmaf_rn(bf16lo(xr.x), bf16lo(wr.x), a);
-                            a = __fmaf_rn(bf16hi(xr.x), bf16hi(wr.x), a);
-                            a = __fmaf_rn(bf16lo(xr.y), bf16lo(wr.y), a);
-                            a = __fmaf_rn(bf16hi(xr.y), bf16hi(wr.y), a);
-                            a = __fmaf_rn(bf16lo(xr.z), bf16lo(wr.z), a);
-                            a = __fmaf_rn(bf16hi(xr.z), bf16hi(wr.z), a);
-                            a = __fmaf_rn(bf16lo(xr.w), bf16lo(wr.w), a);
-                            a = __fmaf_rn(bf16hi(xr.w), bf16hi(wr.w), a);
-                            acc[t] = a;
-                        }
-                    }
-                }
-            }
-        }
-        // release: with one warp the warp itself refills; otherwise the last
-        // warp done with the slot does
-        if (s + NST < nstage) {
-            __syncwarp();
-            if (lane == 0) {
-                bool last = true;
-                if constexpr (WPB > 1) {
-                    __threadfence_block();
-                    last = atomicAdd(&released[slot], 1) == WPB - 1;
-                    if (last) released[slot] = 0;
-                }
-                if (last) {
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    refill(s + NST, slot);
-                }
-            }
-        }
-        if (++slot == NST) {
-            slot = 0;
-            phase ^= 1u;
-        }
-    }
-#pragma unroll
-    for (int t = 0; t < T; ++t) {
-#pragma unroll
-        for (int d = 1; d < 16; d *= 2) acc[t] = acc[t] + __shfl_xor_sync(0xFFFFFFFFu, acc[t], d);
-    }
-    const int e = e0 + x;
-    if (q == 0 && e < E) {
-#pragma unroll
-        for (int t = 0; t < T; ++t) {
-            if (t < nt) {
-                const size_t o = (size_t)(m0 + t) * E + e;
-                if (logit_bf16)
-                    static_cast<__nv_bfloat16 *>(out)[o] = __float2bfloat16_rn(acc[t]);
-                else
-                    static_cast<float *>(out)[o] = acc[t];
-            }
-        }
-    }
-}
-
-template <typename InT, int WPB, int T = kGemvT>
-bi_status launch_gemv(Device *d, const void *x, const void *w, int M, int E, int H, int logit_bf16, void *out,
-                      cudaStream_t s)
-{
-    using Cfg = GemvCfg<InT, WPB, T>;
-    auto kern = router_gemv_kernel<InT, WPB, T>;
-    static_assert((T == 1 && WPB == 1) || (T == kGemvT && WPB == 4), "instantiations with a kernel id");
-    const int kid = (T == 1 ? KID_ROUTER_GEMV1 : KID_ROUTER_GEMV) + (sizeof(InT) == 4 ? 0 : 1);
-    bi_status st = set_smem_once(d, kid, kern, Cfg::SMEM);
-    if (st != BI_OK) return st;
-    const CUtensorMapDataType dt = sizeof(InT) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    const uint64_t strides[1] = {(uint64_t)H * sizeof(InT)};
-    alignas(64) CUtensorMap tmx, tmw;
-    {
-        const uint64_t dims[2] = {(uint64_t)H, (uint64_t)M};
-        const uint32_t box[2] = {(uint32_t)kGemvSpan, (uint32_t)T};
-        if ((st = encode_tiled(&tmx, dt, 2, x, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE)) != BI_OK) return st;
-    }
-    {
-        const uint64_t dims[2] = {(uint64_t)H, (uint64_t)E};
-        const uint32_t box[2] = {(uint32_t)kGemvSpan, (uint32_t)(2 * WPB)};
-        if ((st = encode_tiled(&tmw, dt, 2, w, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE)) != BI_OK) return st;
-    }
-    dim3 grid((E + 2 * WPB - 1) / (2 * WPB), (M + T - 1) / T);
-    return launch_pdl(kern, grid, dim3(32 * WPB), (size_t)Cfg::SMEM, s, tmx, tmw, M, E, H, logit_bf16, out, d->err);
 }
 
 template <typename InT, int C, bool SHALLOW = false>
@@ -924,11 +620,8 @@ bi_status launch_select(Device *d, int epl, dim3 grid, dim3 block, cudaStream_t 
     return launch_select1<32>(d, grid, block, cs, pp, C, m_split, logits, lbf, M, E, k, ids, w, mg, mu, g, H);
 }
 
-// Batches up to this many tokens take the matrix-vector twin.
-constexpr int kGemvMaxM = 64;
-
-// How the projection's work is cut for a batch of M > kGemvMaxM rows (any
-// plan gives the same bits; plans differ only in how well the work fills
+// How the projection's work is cut for a batch of more than kClusterMaxM rows
+// (any plan gives the same bits; plans differ only in how well the work fills
 // the SMs, and each rule below was the fastest measured in its range):
 //  - at least one two-block tile half per SM: every tile's 16 partitions as
 //    two blocks of 8 (C = 2) with the shallow 96 KB ring, up to two blocks to
@@ -942,10 +635,14 @@ constexpr int kGemvMaxM = 64;
 //    tiles (all 16 partitions in one block, logits written directly) for as
 //    many full waves as they fill, and the tail rows split as in the
 //    previous rule, within 16 MiB of group sums.
+// The group sums live in the caller's workspace; router_workspace_bytes
+// bounds what any of these plans needs on any GPU.
 struct SplitPlan {
     int m_split, C;
     bool shallow;
 };
+
+constexpr long long kSplitAllMax = 64ll << 20, kSplitTailMax = 16ll << 20;
 
 SplitPlan plan_split(int M, int E, int sms)
 {
@@ -953,15 +650,34 @@ SplitPlan plan_split(int M, int E, int sms)
     // at least a tile half per SM: every tile as two 8-partition blocks with
     // the shallow ring, up to two blocks to an SM (their start-up and tree
     // phases then overlap the other's arithmetic)
-    if (tiles_m * n_et * 2 >= sms && 2ll * M * E * 4 <= (64ll << 20)) return {0, 2, true};
+    if (tiles_m * n_et * 2 >= sms && 2ll * M * E * 4 <= kSplitAllMax) return {0, 2, true};
     const long long waves = tiles_m * n_et / sms;
     const long long head_tm = waves * sms / n_et;
     if (head_tm >= tiles_m) return {M, 1, false};
     const long long tail = (tiles_m - head_tm) * n_et, tail_rows = M - head_tm * kTileM;
     int c = 1;
-    while (c < 16 && tail * 2 * c <= sms && 2ll * c * tail_rows * E * 4 <= (16ll << 20)) c *= 2;
+    while (c < 16 && tail * 2 * c <= sms && 2ll * c * tail_rows * E * 4 <= kSplitTailMax) c *= 2;
     if (c == 1) return {M, 1, false};
     return {(int)(head_tm * kTileM), c, false};
+}
+
+// Bytes of group sums any tiled plan above may need for M rows and E experts,
+// whatever the GPU's SM count: the two-block plan's 8*M*E when it is within
+// its 64 MiB cap, and the tail plan's at most min(64*M*E, 16 MiB).
+size_t tiled_workspace_bound(long long M, long long E)
+{
+    const long long two = 8 * M * E;
+    const long long tail = std::min(64 * M * E, kSplitTailMax);
+    return (size_t)(two <= kSplitAllMax ? std::max(two, tail) : tail);
+}
+
+// Calls of at most kClusterMaxM rows with E <= kClusterMaxE take the cluster
+// router (clusters of 16 blocks, or of 8 where 16 cannot be placed: at most
+// 64 experts per block either way) and need no workspace.
+size_t router_workspace_bound(long long M, long long E)
+{
+    if (M <= 0 || (M <= kClusterMaxM && E <= kClusterMaxE)) return 0;
+    return tiled_workspace_bound(M, E);
 }
 
 }  // namespace
@@ -975,7 +691,8 @@ namespace {
 // bi_router_topk and bi_router_gate_topk: validation, work plan, launches.
 bi_status router_call(const void *x, const void *w_gate, bi_dtype in_dtype, bi_dtype logit_dtype, int32_t M,
                       int32_t H, int32_t E, int32_t k, void *logits_out, int32_t *ids_out, float *weights_out,
-                      float *margin_out, int32_t *margin_ulps_out, const GateArgs &gate, bi_stream s)
+                      float *margin_out, int32_t *margin_ulps_out, const GateArgs &gate, void *workspace,
+                      size_t workspace_bytes, bi_stream s)
 {
     if ((in_dtype != BI_F32 && in_dtype != BI_BF16) || (logit_dtype != BI_F32 && logit_dtype != BI_BF16))
         return BI_ERR_INVALID_ARG;
@@ -985,7 +702,9 @@ bi_status router_call(const void *x, const void *w_gate, bi_dtype in_dtype, bi_d
     if (M > (1 << 21)) return BI_ERR_UNSUPPORTED_SHAPE;
     if (M == 0) return BI_OK;
     if (!x || !w_gate || !logits_out || !ids_out) return BI_ERR_INVALID_ARG;
-    if (!aligned16(x) || !aligned16(w_gate)) return BI_ERR_MISALIGNED;
+    const size_t need = router_workspace_bound(M, E);
+    if (workspace_bytes < need || (need > 0 && !workspace)) return BI_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w_gate) || (workspace && !aligned16(workspace))) return BI_ERR_MISALIGNED;
     const uintptr_t lal = logit_dtype == BI_F32 ? 3u : 1u;
     if ((reinterpret_cast<uintptr_t>(logits_out) & lal) || (reinterpret_cast<uintptr_t>(ids_out) & 3u) ||
         (reinterpret_cast<uintptr_t>(weights_out) & 3u) || (reinterpret_cast<uintptr_t>(margin_out) & 3u) ||
@@ -999,40 +718,41 @@ bi_status router_call(const void *x, const void *w_gate, bi_dtype in_dtype, bi_d
     bi_status st = current_device(&d);
     if (st != BI_OK) return st;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(s);
-
-    const bool small = M <= kGemvMaxM;
-    const SplitPlan plan = small ? SplitPlan{M, 1, false} : plan_split(M, E, d->sm_count);
-    void *part = nullptr;
-    if (plan.m_split < M) {
-        st = device_scratch(d, (size_t)plan.C * (M - plan.m_split) * E * sizeof(float), &part);
-        if (st != BI_OK) return st;
-    }
-
     const bool f32in = in_dtype == BI_F32;
     const int lbf = logit_dtype == BI_BF16 ? 1 : 0;
-    if (small && M <= kGemvOneTokenMaxM) {      // one warp per (token, expert pair)
-        st = f32in ? launch_gemv<float, 1, 1>(d, x, w_gate, M, E, H, lbf, logits_out, cs)
-                   : launch_gemv<__nv_bfloat16, 1, 1>(d, x, w_gate, M, E, H, lbf, logits_out, cs);
-    } else if (small) {
-        st = f32in ? launch_gemv<float, 4>(d, x, w_gate, M, E, H, lbf, logits_out, cs)
-                   : launch_gemv<__nv_bfloat16, 4>(d, x, w_gate, M, E, H, lbf, logits_out, cs);
-    } else {
-        // the tail goes first: it is the shorter launch, and the whole tiles
-        // queue behind it on the SMs it leaves free
-        if (plan.m_split < M) {
-            st = f32in ? launch_proj_c<float>(d, plan.C, x, w_gate, M, plan.m_split, M, E, H, OUT_PARTIAL, part, cs,
-                                              plan.shallow)
-                       : launch_proj_c<__nv_bfloat16>(d, plan.C, x, w_gate, M, plan.m_split, M, E, H, OUT_PARTIAL,
-                                                      part, cs, plan.shallow);
-            if (st != BI_OK) return st;
-        }
-        if (plan.m_split > 0) {
-            const int om = lbf ? OUT_BF16 : OUT_F32;
-            st = f32in ? launch_proj_c<float>(d, 1, x, w_gate, M, 0, plan.m_split, E, H, om, logits_out, cs)
-                       : launch_proj_c<__nv_bfloat16>(d, 1, x, w_gate, M, 0, plan.m_split, E, H, om, logits_out, cs);
-        }
+
+    // small batches: projection and selection in one cluster launch
+    const ClusterPlan cp = cluster_plan(d, M, E, H, f32in ? 4 : 2, gate.gx != nullptr);
+    if (cp.ok)
+        return router_cluster_call(d, cp, x, w_gate, f32in, lbf, M, H, E, k, logits_out, ids_out, weights_out,
+                                   margin_out, margin_ulps_out, gate.gx ? gate.gw : nullptr, gate.dot, gate.sig,
+                                   cs);
+
+    const SplitPlan plan = plan_split(M, E, d->sm_count);
+    void *part = nullptr;
+    if (plan.m_split < M) {
+        // a workspace within the bound always holds the plan's group sums;
+        // below it only a call that expected the cluster router lands here
+        if ((size_t)plan.C * (size_t)(M - plan.m_split) * (size_t)E * sizeof(float) > workspace_bytes ||
+            !workspace)
+            return BI_ERR_UNSUPPORTED_SHAPE;
+        part = workspace;
     }
-    if (st != BI_OK) return st;
+    // the tail goes first: it is the shorter launch, and the whole tiles
+    // queue behind it on the SMs it leaves free
+    if (plan.m_split < M) {
+        st = f32in ? launch_proj_c<float>(d, plan.C, x, w_gate, M, plan.m_split, M, E, H, OUT_PARTIAL, part, cs,
+                                          plan.shallow)
+                   : launch_proj_c<__nv_bfloat16>(d, plan.C, x, w_gate, M, plan.m_split, M, E, H, OUT_PARTIAL,
+                                                  part, cs, plan.shallow);
+        if (st != BI_OK) return st;
+    }
+    if (plan.m_split > 0) {
+        const int om = lbf ? OUT_BF16 : OUT_F32;
+        st = f32in ? launch_proj_c<float>(d, 1, x, w_gate, M, 0, plan.m_split, E, H, om, logits_out, cs)
+                   : launch_proj_c<__nv_bfloat16>(d, 1, x, w_gate, M, 0, plan.m_split, E, H, om, logits_out, cs);
+        if (st != BI_OK) return st;
+    }
 
     const int epl = E / 32;
     dim3 grid((M + kSelWarps - 1) / kSelWarps), block(32 * kSelWarps);
@@ -1046,45 +766,54 @@ bi_status router_call(const void *x, const void *w_gate, bi_dtype in_dtype, bi_d
 }  // namespace
 }  // namespace bi
 
+extern "C" size_t bi_router_workspace_bytes(int32_t M, int32_t E)
+{
+    return router_workspace_bound(M, E);
+}
+
 extern "C" bi_status bi_router_plan(int32_t M, int32_t E, int32_t *m_split, int32_t *C, int32_t *launches)
 {
     if (M < 0 || E <= 0 || !m_split || !C || !launches) return BI_ERR_INVALID_ARG;
     Device *d = nullptr;
-    int sms = 0;
-    if (current_device(&d) == BI_OK) {
-        sms = d->sm_count;
-    } else {
-        return BI_ERR_CUDA;
-    }
+    if (current_device(&d) != BI_OK) return BI_ERR_CUDA;
     if (M == 0) {
         *m_split = 0;
         *C = 1;
         *launches = 0;
         return BI_OK;
     }
-    const SplitPlan p = M <= kGemvMaxM ? SplitPlan{M, 1, false} : plan_split(M, E, sms);
+    // the f32 shape of the call decides; the bf16 one gives the same cut
+    const ClusterPlan cp = cluster_plan(d, M, E, kRouterSlab, 4, false);
+    if (cp.ok) {
+        *m_split = M;
+        *C = -cp.CS;          // negative: a cluster of this many blocks, one launch
+        *launches = 1;
+        return BI_OK;
+    }
+    const SplitPlan p = plan_split(M, E, d->sm_count);
     *m_split = p.m_split;
     *C = p.C;
-    // projection launches (matrix-vector twin or tiles: a split part and/or a
-    // whole-tile part) plus the selection
-    *launches = M <= kGemvMaxM ? 2 : (p.m_split < M ? 1 : 0) + (p.m_split > 0 ? 1 : 0) + 1;
+    // projection launches (a split part and/or a whole-tile part) plus the selection
+    *launches = (p.m_split < M ? 1 : 0) + (p.m_split > 0 ? 1 : 0) + 1;
     return BI_OK;
 }
 
 extern "C" bi_status bi_router_topk(const void *x, const void *w_gate, bi_dtype in_dtype,
                                     bi_dtype logit_dtype, int32_t M, int32_t H, int32_t E, int32_t k,
                                     void *logits_out, int32_t *ids_out, float *weights_out,
-                                    float *margin_out, int32_t *margin_ulps_out, bi_stream s)
+                                    float *margin_out, int32_t *margin_ulps_out, void *workspace,
+                                    size_t workspace_bytes, bi_stream s)
 {
     return router_call(x, w_gate, in_dtype, logit_dtype, M, H, E, k, logits_out, ids_out, weights_out, margin_out,
-                       margin_ulps_out, GateArgs(), s);
+                       margin_ulps_out, GateArgs(), workspace, workspace_bytes, s);
 }
 
 extern "C" bi_status bi_router_gate_topk(const void *x, const void *w_gate, const void *w_sg, bi_dtype in_dtype,
                                          bi_dtype logit_dtype, int32_t M, int32_t H, int32_t E, int32_t k,
                                          void *logits_out, int32_t *ids_out, float *weights_out,
                                          float *margin_out, int32_t *margin_ulps_out, float *gate_dot_out,
-                                         float *gate_sigmoid_out, bi_stream s)
+                                         float *gate_sigmoid_out, void *workspace, size_t workspace_bytes,
+                                         bi_stream s)
 {
     if (M > 0 && (!w_sg || !gate_dot_out)) return BI_ERR_INVALID_ARG;
     GateArgs g;
@@ -1093,17 +822,16 @@ extern "C" bi_status bi_router_gate_topk(const void *x, const void *w_gate, cons
     g.dot = gate_dot_out;
     g.sig = gate_sigmoid_out;
     return router_call(x, w_gate, in_dtype, logit_dtype, M, H, E, k, logits_out, ids_out, weights_out, margin_out,
-                       margin_ulps_out, g, s);
+                       margin_ulps_out, g, workspace, workspace_bytes, s);
 }
 
 // ---------------------------------------------------------------------------
-// bi_router_topk_noalloc: the same router for callers that cannot allocate
-// device memory (an engine whose memory all comes from its own pool, or code
-// recording the router into a CUDA graph).  The partial sums of the 16
-// partition groups live in a fixed array compiled into the library instead
-// of the lazily allocated scratch of bi_router_topk.  Host code must not pass
-// the array's name to a kernel (that is a host-side stand-in); its device
-// address is looked up once per device with cudaGetSymbolAddress.
+// bi_router_topk_noalloc: the same router for callers that cannot provide
+// any device memory beyond their inputs and outputs.  The partial sums of the
+// 16 partition groups live in a fixed array compiled into the library
+// instead of the caller's workspace of bi_router_topk.  Host code must not
+// pass the array's name to a kernel (that is a host-side stand-in); its
+// device address is looked up once per device with cudaGetSymbolAddress.
 // ---------------------------------------------------------------------------
 #include <mutex>
 

@@ -41,22 +41,6 @@ bi_status current_device(Device **out)
     return BI_OK;
 }
 
-bi_status device_scratch(Device *d, size_t bytes, void **out)
-{
-    std::lock_guard<std::mutex> lk(g_mu);
-    if (d->scratch_bytes < bytes) {
-        // grow-only; the old buffer may still be in use by queued kernels, so
-        // it is kept (leaked) rather than freed under their feet
-        size_t want = bytes < (size_t(2) << 20) ? (size_t(2) << 20) : bytes;
-        void *p = nullptr;
-        if (cudaMalloc(&p, want) != cudaSuccess) return BI_ERR_CUDA;
-        d->scratch = p;
-        d->scratch_bytes = want;
-    }
-    *out = d->scratch;
-    return BI_OK;
-}
-
 bi_status encode_tiled(CUtensorMap *map, CUtensorMapDataType dt, uint32_t rank,
                        const void *gaddr, const uint64_t *dims, const uint64_t *strides_bytes,
                        const uint32_t *box, CUtensorMapSwizzle swizzle)

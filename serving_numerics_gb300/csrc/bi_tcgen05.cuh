@@ -28,19 +28,20 @@ constexpr uint32_t idesc_n(int n)
 {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 }
-constexpr uint32_t IDESC = idesc_n(BN), IDESC_HALF = idesc_n(BN / 2);
+constexpr uint32_t IDESC = idesc_n(BN);
 
 // Work item i of a launch: items below n_full are whole tiles (tile = i);
-// the rest are halves of the tiles from n_full on.  Returns the tile and
-// sets `half` to -1 for a whole tile, else 0 or 1 (which 128 columns).
-__device__ __forceinline__ int item_tile(int i, int n_full, int &half)
+// the rest are pieces of the tiles from n_full on, each tile cut into
+// 2^lg_s pieces of BN >> lg_s columns.  Returns the tile and sets `piece` to
+// -1 for a whole tile, else the piece's index within its tile.
+__device__ __forceinline__ int item_tile(int i, int n_full, int lg_s, int &piece)
 {
     if (i < n_full) {
-        half = -1;
+        piece = -1;
         return i;
     }
-    half = (i - n_full) & 1;
-    return n_full + ((i - n_full) >> 1);
+    piece = (i - n_full) & ((1 << lg_s) - 1);
+    return n_full + ((i - n_full) >> lg_s);
 }
 
 // Shared-memory matrix descriptor for a K-major operand laid out by TMA with

@@ -35,7 +35,7 @@ def test_library_exports_every_declared_symbol(lib):
     for name in declared_symbols():
         assert hasattr(lib, name), f"libbi.so does not export {name}"
         assert name in binding.SIGNATURES, f"binding lacks {name}"
-    assert lib.bi_abi_version() == 1
+    assert lib.bi_abi_version() == 2
 
 
 def test_status_strings(lib):
@@ -50,10 +50,11 @@ MIS = FAKE + 4          # not 16-byte aligned
 
 def _router(lib, **kw):
     a = dict(x=FAKE, w=FAKE, ind=0, ld=0, M=4, H=256, E=64, k=4, logits=FAKE, ids=FAKE,
-             weights=None, margin=None, ulps=None)
+             weights=None, margin=None, ulps=None, ws=None, wsb=0)
     a.update(kw)
     return lib.bi_router_topk(a["x"], a["w"], a["ind"], a["ld"], a["M"], a["H"], a["E"], a["k"],
-                              a["logits"], a["ids"], a["weights"], a["margin"], a["ulps"], None)
+                              a["logits"], a["ids"], a["weights"], a["margin"], a["ulps"], a["ws"], a["wsb"],
+                              None)
 
 
 @pytest.mark.parametrize("kw,want", [
@@ -71,11 +72,39 @@ def test_router_m0_is_noop(lib):
     assert _router(lib, M=0, x=None, w=None, logits=None, ids=None) == 0
 
 
+def test_router_workspace_bytes(lib):
+    """No workspace for the one-launch cluster router (M <= 128, E <= 512);
+    above that the bound of the tiled plans, the same on every GPU."""
+    for M, E in ((1, 256), (64, 256), (128, 256), (128, 512), (5, 512)):
+        assert lib.bi_router_workspace_bytes(M, E) == 0
+    assert lib.bi_router_workspace_bytes(0, 256) == 0
+    assert lib.bi_router_workspace_bytes(-3, 256) == 0
+    # two-block plan: 8*M*E within its 64 MiB cap, never below the tail
+    # plan's min(64*M*E, 16 MiB)
+    assert lib.bi_router_workspace_bytes(4096, 256) == 16 << 20
+    assert lib.bi_router_workspace_bytes(8192, 512) == 32 << 20
+    assert lib.bi_router_workspace_bytes(129, 256) == 129 * 256 * 64
+    assert lib.bi_router_workspace_bytes(64, 1024) == 64 * 1024 * 64
+    assert lib.bi_router_workspace_bytes(1 << 20, 256) == 16 << 20     # past 64 MiB: the tail plan only
+
+
+@pytest.mark.parametrize("M,E", [(129, 256), (4096, 256), (64, 1024)])
+def test_router_rejects_a_small_workspace(lib, M, E):
+    """A workspace below bi_router_workspace_bytes is refused on the host,
+    before any CUDA call (so this runs without a GPU)."""
+    need = lib.bi_router_workspace_bytes(M, E)
+    assert need > 0
+    assert _router(lib, M=M, E=E, k=8, ws=0x100000, wsb=need - 1) == 1
+    assert _router(lib, M=M, E=E, k=8, ws=None, wsb=need) == 1
+    assert _router(lib, M=M, E=E, k=8, ws=0x100008, wsb=need) == 3          # not 16-byte aligned
+    assert _router_gate(lib, M=M, E=E, k=8, ws=0x100000, wsb=need - 1) == 1
+
+
 def _router_gate(lib, wsg=FAKE, dot=FAKE, sig=None, **kw):
-    a = dict(x=FAKE, w=FAKE, ind=0, ld=0, M=4, H=256, E=64, k=4, logits=FAKE, ids=FAKE)
+    a = dict(x=FAKE, w=FAKE, ind=0, ld=0, M=4, H=256, E=64, k=4, logits=FAKE, ids=FAKE, ws=None, wsb=0)
     a.update(kw)
     return lib.bi_router_gate_topk(a["x"], a["w"], wsg, a["ind"], a["ld"], a["M"], a["H"], a["E"], a["k"],
-                                   a["logits"], a["ids"], None, None, None, dot, sig, None)
+                                   a["logits"], a["ids"], None, None, None, dot, sig, a["ws"], a["wsb"], None)
 
 
 @pytest.mark.parametrize("kw,want", [

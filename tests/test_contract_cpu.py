@@ -25,7 +25,7 @@ def lib():
 def test_config_reports_the_contract(lib):
     c = binding.get_config()
     assert c["struct_size"] == C.sizeof(binding.BiConfig)
-    assert c["abi_version"] == lib.bi_abi_version() == 1
+    assert c["abi_version"] == lib.bi_abi_version() == 2
     assert (c["router_slab"], c["router_block"], c["router_partitions"]) == (128, 8, 16)
     assert c["router_slab"] == c["router_block"] * c["router_partitions"]
     assert c["router_partition_order"] == 1 and c["router_tree"] == binding.BI_TREE_PAIRWISE
@@ -38,7 +38,7 @@ def test_config_reports_the_contract(lib):
 def test_config_short_buffer_and_null(lib):
     buf = (C.c_int32 * 4)(-1, -1, -1, -1)
     assert lib.bi_get_config(buf, 8) == binding.BI_OK          # only the first two fields
-    assert list(buf) == [C.sizeof(binding.BiConfig), 1, -1, -1]
+    assert list(buf) == [C.sizeof(binding.BiConfig), 2, -1, -1]
     assert lib.bi_get_config(buf, 7) == binding.BI_ERR_INVALID_ARG
     assert lib.bi_get_config(None, 64) == binding.BI_ERR_INVALID_ARG
 

@@ -2,10 +2,11 @@
 order bit for bit: every logit and gate dot equals the CPU restatement of
 the contract (oracle/contract.c: 16 partitions owning the 8-wide blocks of
 every 128-wide slab, one f32 fused multiply-add chain each, a pairwise tree
-of the partials), for every work split the library picks (the matrix-vector
-twin, whole tiles, partition-split tiles, whole tiles plus a split tail, the
-no-allocation entry), for f32 and bf16 inputs, and for bf16 logits (the
-same f32 value rounded to nearest even once).
+of the partials), for every work split the library picks (the one-launch
+cluster router at every token tile it compiles, whole tiles,
+partition-split tiles, whole tiles plus a split tail, the no-allocation
+entry), for f32 and bf16 inputs, and for bf16 logits (the same f32 value
+rounded to nearest even once).
 
 This is stronger than the tolerance parity of test_router_gpu.py: it pins
 the order itself, which is what makes the results independent of M ("batch
@@ -28,17 +29,22 @@ def gpu_logits(bi, X, W, k, logit_dtype, noalloc=False):
     ids = torch.empty((M, k), dtype=torch.int32, device="cuda")
     ind = bi.BI_F32 if X.dtype == np.float32 else bi.BI_BF16
     lod = bi.BI_F32 if logit_dtype == "f32" else bi.BI_BF16
-    call = bi.bi_router_topk_noalloc if noalloc else bi.bi_router_topk
-    call(x, w, ind, lod, M, X.shape[1], E, k, lg, ids)
+    if noalloc:
+        bi.bi_router_topk_noalloc(x, w, ind, lod, M, X.shape[1], E, k, lg, ids)
+    else:
+        bi.bi_router_topk(x, w, ind, lod, M, X.shape[1], E, k, lg, ids, workspace=bi.router_workspace(M, E))
     torch.cuda.synchronize()
     assert bi.bi_get_last_device_error() == 0
     return gu.host(lg) if logit_dtype == "f32" else gu.host_bf16_bits(lg)
 
 
-# (M, H, E, k): matrix-vector twin (M <= 8, M <= 64), partition-split tiles
-# one block to an SM, two-block tiles two to an SM, whole tiles + split tail
-# (E = 1024, M = 8300: group sums past 64 MiB); ragged H and E
-SHAPES = [(1, 2048, 256, 8), (7, 264, 96, 5), (20, 2048, 256, 8), (64, 136, 1024, 32), (100, 2048, 256, 8),
+# (M, H, E, k): the cluster router (M <= 128, E <= 512) at token tiles of
+# 1, 2, 4, 8 and 16 rows, 2 to 32 experts per block, one-slab and ragged H
+# (H = 8: a single 8-wide block); partition-split tiles one block to an SM
+# (and E = 1024 at small M), two-block tiles two to an SM, whole tiles +
+# split tail (E = 1024, M = 8300: group sums past 64 MiB); ragged H and E
+SHAPES = [(1, 2048, 256, 8), (7, 264, 96, 5), (20, 2048, 256, 8), (33, 2048, 32, 4), (3, 8, 64, 4),
+          (64, 136, 1024, 32), (100, 2048, 256, 8), (128, 2048, 512, 10), (57, 4104, 256, 8),
           (300, 136, 64, 4), (700, 264, 256, 8), (1300, 2048, 256, 8), (1235, 128, 256, 8),
           (8300, 136, 1024, 16)]
 

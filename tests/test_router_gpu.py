@@ -195,17 +195,54 @@ def test_router_splits_bit_identical(bi, E, M, H):
 
 
 def test_router_plan_reports_the_cut(bi):
-    """bi_router_plan on a 152-SM GB300: the matrix-vector twin below 65
-    rows, partition-split tiles below that, two-block tiles once their
-    blocks fill the SMs, whole tiles plus a split tail where the group sums
-    would pass 64 MiB."""
+    """bi_router_plan on a 152-SM GB300: one cluster launch up to 128 rows
+    (E <= 512), partition-split tiles below a tile half per SM, two-block
+    tiles once their blocks fill the SMs, whole tiles plus a split tail
+    where the group sums would pass 64 MiB."""
     import torch
     if torch.cuda.get_device_properties(0).multi_processor_count != 152:
         pytest.skip("plan thresholds are stated for 152 SMs")
-    assert bi.router_plan(1, 256) == (1, 1, 2)
-    assert bi.router_plan(64, 256) == (64, 1, 2)
+    for M in (1, 64, 128):
+        m, c, n = bi.router_plan(M, 256)
+        assert m == M and c in (-16, -8) and n == 1, (M, m, c, n)
+    assert bi.router_plan(129, 256) == (0, 4, 2)       # 20 tiles: 4 blocks each fill 80 SMs
     assert bi.router_plan(4096, 256) == (0, 2, 2)
     assert bi.router_plan(256, 256) == (0, 4, 2)
     assert bi.router_plan(640, 256) == (0, 2, 2)       # 80 tiles: 160 two-block halves
     assert bi.router_plan(1024, 256) == (0, 2, 2)
     assert bi.router_plan(8300, 1024) == (8192, 2, 3)
+    assert bi.router_plan(64, 1024)[2] == 2            # E = 1024: always the tiled kernels
+
+
+def test_router_two_streams_separate_workspaces(bi):
+    """Two tiled calls (M > 128, so their group sums go through the caller's
+    workspace) queued on two streams with no ordering between them, each with
+    its own workspace: every output is byte-identical to the same call run
+    alone.  The library keeps no buffer of its own that the two could share."""
+    import torch
+    M, H, E, k = 3000, 2048, 256, 8
+    Xa = gu.dev_f32(synth.tokens(61, 0, 0, M, H))
+    Xb = gu.dev_f32(synth.tokens(61, 1, 0, M, H))
+    wa = gu.dev_f32(synth.router_weights(61, 0, E, H))
+    wb = gu.dev_f32(synth.router_weights(61, 1, E, H))
+    ref_a = bi.router_topk(Xa, wa, k)
+    torch.cuda.synchronize()
+    ref_b = bi.router_topk(Xb, wb, k)
+    torch.cuda.synchronize()
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    wsa, wsb = bi.router_workspace(M, E), bi.router_workspace(M, E)
+    assert wsa is not None and wsa.numel() == bi.router_workspace_bytes(M, E)
+    torch.cuda.synchronize()
+    outs = []
+    for rep in range(3):
+        with torch.cuda.stream(sa):
+            oa = bi.router_topk(Xa, wa, k, workspace=wsa, stream=sa)
+        with torch.cuda.stream(sb):
+            ob = bi.router_topk(Xb, wb, k, workspace=wsb, stream=sb)
+        outs.append((oa, ob))
+    torch.cuda.synchronize()
+    assert bi.bi_get_last_device_error() == 0
+    for oa, ob in outs:
+        for f in ("logits", "ids", "weights", "margin", "margin_ulps"):
+            assert oa[f].cpu().numpy().tobytes() == ref_a[f].cpu().numpy().tobytes(), f
+            assert ob[f].cpu().numpy().tobytes() == ref_b[f].cpu().numpy().tobytes(), f

@@ -1,13 +1,16 @@
-"""bi_router_topk_noalloc: the router for callers that cannot allocate device
-memory (an engine that owns all device memory through its own pool, or code
-recording the router into a CUDA graph, where a first-time cudaMalloc is not
-allowed).  Its partial sums live in a fixed array compiled into the library.
+"""bi_router_topk_noalloc: the router for callers that cannot provide device
+memory beyond their inputs and outputs (a plugin or embedded runtime handed
+device pointers but no allocator; bi_router_topk needs a caller workspace for
+large batches).  Its partial sums live in a fixed array compiled into the
+library.
 
 Checked through the C ABI against bi_router_topk on the same inputs, on two
 calls in a row (the array keeps the previous call's contents, which must not
-leak into the next), and for the rejection of a problem too large for the
-array.  This file is collected last on purpose; it passes alone in a fresh
-process and after the rest of the suite."""
+leak into the next), on two calls queued back to back on one stream with no
+host synchronisation between them, with the device's free memory unchanged
+across a call, and for the rejection of a problem too large for the array.
+This file is collected last on purpose; it passes alone in a fresh process
+and after the rest of the suite."""
 import numpy as np
 import pytest
 
@@ -37,8 +40,16 @@ def call(bi, fn, x, w, k, logit_dtype):
     o = outputs(torch, M, E, k, logit_dtype)
     ind = bi.BI_F32 if x.dtype == torch.float32 else bi.BI_BF16
     ld = bi.BI_F32 if logit_dtype == "f32" else bi.BI_BF16
-    fn(x, w, ind, ld, M, H, E, k, o["logits"], o["ids"], o["weights"], o["margin"], o["margin_ulps"])
+    args = (x, w, ind, ld, M, H, E, k, o["logits"], o["ids"], o["weights"], o["margin"], o["margin_ulps"])
+    if fn is bi.bi_router_topk:
+        fn(*args, workspace=bi.router_workspace(M, E))
+    else:
+        fn(*args)
     torch.cuda.synchronize()
+    return host(torch, o)
+
+
+def host(torch, o):
     return {f: o[f].contiguous().view(torch.uint8).cpu().numpy().tobytes() if o[f].dtype == torch.bfloat16
             else o[f].cpu().numpy() for f in FIELDS}
 
@@ -84,3 +95,47 @@ def test_noalloc_rejects_problems_beyond_its_array(bi):
                                        None, None, None, check=False)
         assert st == want, (M, st)
     torch.cuda.synchronize()
+
+
+def test_noalloc_back_to_back_on_one_stream(bi):
+    """Two calls with different inputs and outputs queued on one stream with
+    no synchronisation between them (the second call's kernels may start
+    while the first call's selection still reads the shared array; the
+    array is written only after each kernel's wait on its predecessor): each
+    output equals its own bi_router_topk result."""
+    import torch
+    M, H, E, k = 48, 2048, 256, 8
+    xs = [gu.dev_f32(synth.tokens(70 + i, 0, 0, M, H)) for i in range(2)]
+    ws = [gu.dev_f32(synth.router_weights(70 + i, 0, E, H)) for i in range(2)]
+    refs = [call(bi, bi.bi_router_topk, xs[i], ws[i], k, "f32") for i in range(2)]
+    outs = [outputs(torch, M, E, k, "f32") for _ in range(2)]
+    torch.cuda.synchronize()
+    for i in range(2):
+        o = outs[i]
+        bi.bi_router_topk_noalloc(xs[i], ws[i], bi.BI_F32, bi.BI_F32, M, H, E, k, o["logits"], o["ids"],
+                                  o["weights"], o["margin"], o["margin_ulps"])
+    torch.cuda.synchronize()
+    assert bi.bi_get_last_device_error() == 0
+    for i in range(2):
+        got = host(torch, outs[i])
+        for f in FIELDS:
+            assert np.asarray(got[f]).tobytes() == np.asarray(refs[i][f]).tobytes(), (i, f)
+
+
+def test_noalloc_call_leaves_free_memory_unchanged(bi):
+    """After a first call on the device, a call allocates nothing: the
+    device's free memory is the same before and after it."""
+    import torch
+    M, H, E, k = 64, 2048, 256, 8
+    x = gu.dev_f32(synth.tokens(72, 0, 0, M, H))
+    w = gu.dev_f32(synth.router_weights(72, 0, E, H))
+    o = outputs(torch, M, E, k, "f32")
+    args = (x, w, bi.BI_F32, bi.BI_F32, M, H, E, k, o["logits"], o["ids"], o["weights"], o["margin"],
+            o["margin_ulps"])
+    bi.bi_router_topk_noalloc(*args)
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    for _ in range(3):
+        bi.bi_router_topk_noalloc(*args)
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
