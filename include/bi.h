@@ -113,7 +113,7 @@ typedef struct CUstream_st *bi_stream;
  * Logits must be finite for the weights and margins to be meaningful (a
  * NaN ranks above every number and ties other NaNs by index).
  *
- * Work and memory.  Batches of at most 128 rows run as ONE launch: thread
+ * Work and memory.  Batches of at most 112 rows run as ONE launch: thread
  * block clusters in which each block computes the logits of a slice of the
  * experts and sends them, through distributed shared memory, to the block
  * that selects their token.  Larger batches run the projection as 32 x 64
@@ -123,13 +123,13 @@ typedef struct CUstream_st *bi_stream;
  *   workspace        device buffer, 16-byte aligned, owned by the caller; may
  *                    be NULL when workspace_bytes is 0
  *   workspace_bytes  its size; must be at least bi_router_workspace_bytes(M, E)
- *                    (0 for M <= 128 and E <= 512), else BI_ERR_INVALID_ARG
+ *                    (0 for M <= 112 and E <= 512), else BI_ERR_INVALID_ARG
  *                    before anything is launched
  * Calls that could run at the same time on the GPU (different streams with
  * no event between them) need workspaces that do not overlap; calls queued
  * on one stream may share one.  BI_ERR_UNSUPPORTED_SHAPE is returned (before
  * any launch) only on a GPU that cannot place clusters of 8 blocks, for a
- * call of at most 128 rows given less workspace than its tiled plan needs.
+ * call of at most 112 rows given less workspace than its tiled plan needs.
  *
  * Ordering: the kernels start streaming w_gate before they wait for the
  * preceding kernel in the stream (programmatic dependent launch); x is read
@@ -147,7 +147,7 @@ BI_API bi_status bi_router_topk(const void *x, const void *w_gate, bi_dtype in_d
 /*
  * bi_router_workspace_bytes -- the workspace bi_router_topk and
  * bi_router_gate_topk need for M rows and E experts, on any GPU: 0 for
- * M <= 128 with E <= 512 (the one-launch cluster router); otherwise the
+ * M <= 112 with E <= 512 (the one-launch cluster router); otherwise the
  * largest group-sum area any of the tiled plans may use, 8*M*E bytes while
  * that is at most 64 MiB, never less than min(64*M*E, 16 MiB) and never more
  * than 64 MiB.  Host-only: touches no GPU.  Returns 0 for M <= 0.
@@ -157,7 +157,7 @@ BI_API size_t bi_router_workspace_bytes(int32_t M, int32_t E);
 /*
  * bi_router_plan -- how bi_router_topk (and bi_router_gate_topk) would cut
  * the work for M rows and E experts on the current device.  For the
- * one-launch cluster router (M <= 128): *m_split = M, *C = minus the number
+ * one-launch cluster router (M <= 112): *m_split = M, *C = minus the number
  * of blocks per cluster, *launches = 1.  Otherwise the rows below *m_split
  * run as whole tiles and the rest with each tile's partitions split over *C
  * blocks, and *launches counts the projection launches plus the selection.
@@ -260,9 +260,8 @@ BI_API bi_status bi_route_trace_hash(const int32_t *ids, int32_t M, int32_t k,
  *
  * No counterpart on the source pages: it exists for the caller, not for the
  * method.  bi_router_topk needs a device workspace from its caller for
- * batches of more than 128 rows (and, with E = 1024, wherever 16-block
- * clusters cannot be placed).  Some callers cannot provide one: a plugin or
- * an embedded runtime that is handed device pointers for its inputs and
+ * batches of more than 112 rows or with E = 1024.  Some callers cannot
+ * provide one: a plugin or an embedded runtime that is handed device pointers for its inputs and
  * outputs but owns no device memory and has no allocator to call, or code
  * that must not let device memory be reserved on its behalf at all.  This
  * entry point instead uses a fixed device array of BI_NOALLOC_SCRATCH_BYTES

@@ -116,9 +116,11 @@ enum : int {
     KID_FLOOR = 74,
 };
 
-// Batches of at most this many rows take the one-launch cluster router
-// (csrc/bi_router_cluster.cu); larger ones the tiled projection + selection.
-constexpr int kClusterMaxM = 128, kClusterMaxE = 512;
+// Batches of at most this many rows (and E <= kClusterMaxE) take the
+// one-launch cluster router (csrc/bi_router_cluster.cu); larger ones the
+// tiled projection + selection.  112 = 7 clusters of 16 tokens, the clusters
+// of 16 blocks a GB300 places at once.
+constexpr int kClusterMaxM = 112, kClusterMaxE = 512;
 
 // How the cluster router cuts one call (see bi_router_cluster.cu).
 struct ClusterPlan {
@@ -128,7 +130,7 @@ struct ClusterPlan {
     int NC;           // clusters
     int warps;        // warps per block
     int Eb4;          // gate rows per block, rounded up to a multiple of 4
-    int nst, stage_bytes, x_off, g_off, gather_off, smem;   // shared-memory layout
+    int nst, stage_bytes, x_off, g_off, gather_off, tile_off, smem;   // shared-memory layout
 };
 
 ClusterPlan cluster_plan(Device *d, int M, int E, int H, int es, bool gate);

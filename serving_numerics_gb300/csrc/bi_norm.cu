@@ -323,7 +323,7 @@ extern "C" bi_status bi_rmsnorm(const void *x, const void *w, bi_dtype dtype, in
                                        CU_TENSOR_MAP_SWIZZLE_32B)) != BI_OK)
                     return st;
                 auto kern = rmsnorm_staged_kernel<float>;
-                if ((st = set_smem_once(d, KID_NORM + 2, kern, smem)) != BI_OK) return st;
+                if ((st = set_smem_once(d, KID_NORM + 2, kern, kStagedSmemMax)) != BI_OK) return st;
                 return launch_pdl(kern, dim3(grid), dim3(32 * kStagedWarps), smem, cs0, tmx,
                                   static_cast<const float *>(w), a);
             }
@@ -334,7 +334,7 @@ extern "C" bi_status bi_rmsnorm(const void *x, const void *w, bi_dtype dtype, in
                                    CU_TENSOR_MAP_SWIZZLE_NONE)) != BI_OK)
                 return st;
             auto kern = rmsnorm_staged_kernel<__nv_bfloat16>;
-            if ((st = set_smem_once(d, KID_NORM + 3, kern, smem)) != BI_OK) return st;
+            if ((st = set_smem_once(d, KID_NORM + 3, kern, kStagedSmemMax)) != BI_OK) return st;
             return launch_pdl(kern, dim3(grid), dim3(32 * kStagedWarps), smem, cs0, tmx,
                               static_cast<const __nv_bfloat16 *>(w), a);
         }

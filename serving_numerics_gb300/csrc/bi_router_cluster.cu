@@ -29,22 +29,27 @@
 // launch; a batch of M tokens runs as ceil(M / TM) clusters with TM chosen
 // so that the clusters fill the GPU.
 //
-// Data path.  Per slab (128 values of h), the block's gate rows (E/CS rows,
-// padded to a multiple of 4), the cluster's X rows (TM rows) and, for the
-// fused shared gate, the slab of w_sg are copied into a ring of shared-
-// memory stages with 16-byte asynchronous copies (cp.async), the weight rows
-// of every stage the ring holds before the dependency wait (weights are
-// never the preceding kernel's output), the X rows after it; each thread's
-// completion arrives on the stage's mbarrier.  Within a staged f32 row the
-// first halves of the 16 partition blocks come first, then the second
-// halves, so lane q reads its 8 values as two 16-byte loads at 16 q and at
-// 256 + 16 q: each quarter-warp's load covers 128 contiguous bytes, every
-// bank once.  (bf16 blocks are 16 bytes: lane q reads 16 q.)
+// Data path.  Per slab (128 values of h), the block's gate rows (E/CS rows),
+// the cluster's X rows and, for the fused shared gate, the slab of w_sg are
+// staged by TMA (one 2-D box per operand and stage, 512-byte rows for f32)
+// into a ring of shared-memory stages; the weight rows of every stage the
+// ring holds stream in before the dependency wait (weights are never the
+// preceding kernel's output), the X rows after it.  Reading partition q's
+// 8 values as two 16-byte loads would put lanes q and q + 4 on the same
+// banks (their blocks are 128 bytes apart), so lanes with bit 2 of q set
+// load their second half first and swap the two in registers: each quarter-
+// warp's load then meets every bank once, and the fused multiply-adds still
+// run in h order.  (bf16 blocks are 16 bytes: lane q reads 16 q.)
 //
-// Work per block: a half-warp owns 4 experts and up to 8 of the cluster's
-// tokens; lane q runs partition q's 32 chains (4 experts x 8 tokens), which
-// reuse each loaded value 4 or 8 times and keep 32 independent fused
-// multiply-add chains in flight per lane.
+// Work per block: a half-warp owns NE experts and TJ of the cluster's tokens
+// (2 x NT for up to 4 tokens per cluster, 4 x 4 at 8, 4 x 8 at 16); lane q
+// runs partition q's NE x TJ chains.  One warp per scheduler is all the
+// parallelism a block has at these sizes, so the shapes trade operand reuse
+// (fewer shared-memory loads per multiply-add) against independent chains
+// and warps; each was the fastest of those measured at its token count.  The block's logits are gathered
+// in its own shared memory first, then pushed to the selecting blocks one
+// contiguous run of E/CS values per token (a remote store whose lanes all
+// go to one block is one transaction).
 #include <cuda_bf16.h>
 
 #include <mutex>
@@ -59,15 +64,19 @@ namespace {
 constexpr int kSlab = kRouterSlab, kBlk = kRouterBlock;
 constexpr int kCluMaxStages = 32;
 constexpr int kCluMaxWarps = 16;
-constexpr int kCluNE = 4;                         // experts per half-warp
-constexpr int kCluTokJob = 8;                     // tokens per half-warp at most
+// The half-warp job for NT tokens per cluster: NE experts x TJ tokens, the
+// fastest shape measured for each NT at 16 experts per block (all give four
+// warps there): 2 x NT up to 4 tokens, 4 x 4 at 8, 4 x 8 at 16.
+constexpr int clu_ne(int NT) { return NT <= 4 ? 2 : 4; }
+constexpr int clu_tj(int NT) { return NT <= 4 ? NT : NT == 8 ? 4 : 8; }
+constexpr int kCluEbAlign = 4;                    // gate rows per block padded to a multiple of this
 constexpr size_t kCluSmemMax = 226 * 1024;        // the per-block opt-in maximum less static shared memory
 
 struct CluArgs {
     const void *x, *w;
     int M, E, H, k, logit_bf16;
-    int Eb4;                 // gate rows per block, rounded up to a multiple of kCluNE
-    int nst, stage_bytes, x_off, g_off, gather_off;
+    int Eb4;                 // gate rows per block, rounded up to a multiple of kCluEbAlign
+    int nst, stage_bytes, x_off, g_off, gather_off, tile_off;
     void *logits;
     int32_t *ids;
     float *weights, *margin;
@@ -89,43 +98,23 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v)
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
-// 16-byte asynchronous copy global -> shared; src_bytes = 0 fills zeros.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes)
+// Partition q's 8 values of a staged row (h increasing).  f32 rows are 512
+// bytes, block q at 32 q; lanes with bit 2 of q set load the block's second
+// half first (see the data path above) and swap.
+// Bitwise select (no branch): m all ones picks b, all zeros picks a.
+__device__ __forceinline__ float pick(float a, float b, uint32_t m)
 {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+    return __uint_as_float((__float_as_uint(a) & ~m) | (__float_as_uint(b) & m));
 }
 
-// The barrier's phase gets one arrival from this thread once every
-// cp.async it issued so far has landed.
-__device__ __forceinline__ void cp_async_arrive(uint64_t *bar)
-{
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-// One slab-row of `src` (row pointer, h0 = start of the slab) into a staged
-// row: f32 as [half][block][4 values], bf16 as [block][8 values].  Copies
-// chunk i of the row's CPR chunks; values past H are zero-filled.
-template <typename InT>
-__device__ __forceinline__ void copy_chunk(uint32_t row_dst, const InT *row_src, int h0, int H, int i, bool valid)
-{
-    if constexpr (sizeof(InT) == 4) {
-        const int q = i >> 1, h = i & 1;                      // global order: block q, half h
-        const int hh = h0 + 8 * q + 4 * h;
-        const bool in = valid && hh < H;
-        cp_async16(row_dst + 16u * (uint32_t)(16 * h + q), in ? row_src + hh : row_src, in ? 16u : 0u);
-    } else {
-        const int hh = h0 + 8 * i;
-        const bool in = valid && hh < H;
-        cp_async16(row_dst + 16u * (uint32_t)i, in ? row_src + hh : row_src, in ? 16u : 0u);
-    }
-}
-
-// Partition q's 8 values of a staged row (h increasing).
 __device__ __forceinline__ void load_block(const uint8_t *row, int q, float (&v)[8], float)
 {
-    const float4 a = *reinterpret_cast<const float4 *>(row + 16 * q);
-    const float4 b = *reinterpret_cast<const float4 *>(row + 256 + 16 * q);
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    const int sw = (q >> 2) & 1;
+    const uint32_t m = 0u - (uint32_t)sw;
+    const float4 a = *reinterpret_cast<const float4 *>(row + 32 * q + 16 * sw);
+    const float4 b = *reinterpret_cast<const float4 *>(row + 32 * q + 16 * (sw ^ 1));
+    v[0] = pick(a.x, b.x, m); v[1] = pick(a.y, b.y, m); v[2] = pick(a.z, b.z, m); v[3] = pick(a.w, b.w, m);
+    v[4] = pick(b.x, a.x, m); v[5] = pick(b.y, a.y, m); v[6] = pick(b.z, a.z, m); v[7] = pick(b.w, a.w, m);
 }
 
 __device__ __forceinline__ void load_block(const uint8_t *row, int q, float (&v)[8], __nv_bfloat16)
@@ -155,13 +144,13 @@ __device__ __forceinline__ void select_gathered(const float *g, int lane, const 
 
 // NT: tokens per cluster (1, 2, 4, 8 or 16); a half-warp takes TJ of them.
 template <typename InT, int NT>
-__global__ void __launch_bounds__(32 * kCluMaxWarps, 1) router_cluster_kernel(CluArgs a)
+__global__ void __launch_bounds__(32 * kCluMaxWarps, 1)
+router_cluster_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw, CluArgs a)
 {
     pdl_trigger();   // dependents may launch now; each waits before reading our outputs
     constexpr int ES = (int)sizeof(InT);
     constexpr int ROW = kSlab * ES;                         // bytes of one staged slab row
-    constexpr int CPR = ROW / 16;                           // 16-byte chunks per row
-    constexpr int TJ = NT < kCluTokJob ? NT : kCluTokJob;   // tokens per half-warp
+    constexpr int NE = clu_ne(NT), TJ = clu_tj(NT);         // a half-warp's experts and tokens
     constexpr int TG = NT / TJ;                             // token groups
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kCluMaxStages];
@@ -169,20 +158,22 @@ __global__ void __launch_bounds__(32 * kCluMaxWarps, 1) router_cluster_kernel(Cl
 
     const int CS = gridDim.x, b = blockIdx.x;               // the cluster spans gridDim.x: rank = blockIdx.x
     const int tid = threadIdx.x, nthreads = blockDim.x, warp = tid >> 5, lane = tid & 31, q = lane & 15;
-    const int Eb = a.E / CS, e0 = b * Eb, EG = a.Eb4 / kCluNE;
+    const int nwarps = nthreads >> 5;
+    const int Eb = a.E / CS, e0 = b * Eb, EG = a.Eb4 / NE;
     const int m0 = blockIdx.y * NT;
     const int nt = min(NT, a.M - m0);                       // >= 1 by the grid
     const int H = a.H, ns = (H + kSlab - 1) / kSlab, NST = a.nst;
     const bool gate_here = a.gw != nullptr && b < nt;       // block b computes the gate of its token b
     const int job = 2 * warp + (lane >> 4);
     const bool active = job < EG * TG;
-    const int eg = job % EG, tg = job / EG;                 // experts 4 eg .. 4 eg + 3, tokens TJ tg ..
-    const InT *X = static_cast<const InT *>(a.x), *W = static_cast<const InT *>(a.w);
+    const int eg = job % EG, tg = job / EG;                 // experts NE eg .., tokens TJ tg ..
     float *gather = reinterpret_cast<float *>(smem + a.gather_off);
-    const uint32_t sbase = smem_u32(smem);
+    float *tile = reinterpret_cast<float *>(smem + a.tile_off);     // this block's logits [NT][Eb4]
 
     if (tid == 0) {
-        for (int s = 0; s < NST; ++s) mbar_init(&full_bar[s], (uint32_t)nthreads);
+        prefetch_tmap(&tmx);
+        prefetch_tmap(&tmw);
+        for (int s = 0; s < NST; ++s) mbar_init(&full_bar[s], 1);
         mbar_init_fence();
     }
     __syncthreads();
@@ -190,124 +181,163 @@ __global__ void __launch_bounds__(32 * kCluMaxWarps, 1) router_cluster_kernel(Cl
     // for just before the first store into another block's shared memory
     asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 
+    auto stage_tx = [&](int s) -> uint32_t {
+        uint32_t tx = (uint32_t)(Eb + NT) * ROW;
+        if (gate_here) tx += (uint32_t)min(kSlab, H - kSlab * s) * ES;
+        return tx;
+    };
     auto issue_w = [&](int s, int slot) {
-        const uint32_t st = sbase + (uint32_t)(slot * a.stage_bytes);
-        for (int i = tid; i < Eb * CPR; i += nthreads) {
-            const int r = i / CPR;
-            copy_chunk<InT>(st + (uint32_t)(r * ROW), W + (size_t)(e0 + r) * H, kSlab * s, H, i % CPR, true);
-        }
+        uint8_t *st = smem + slot * a.stage_bytes;
+        tma_load_2d(st, &tmw, &full_bar[slot], kSlab * s, e0);
         if (gate_here)
-            for (int i = tid; i < CPR; i += nthreads)
-                copy_chunk<InT>(st + (uint32_t)a.g_off, static_cast<const InT *>(a.gw), kSlab * s, H, i, true);
+            bulk_load(st + a.g_off, static_cast<const InT *>(a.gw) + (size_t)kSlab * s,
+                      (uint32_t)min(kSlab, H - kSlab * s) * ES, &full_bar[slot]);
     };
     auto issue_x = [&](int s, int slot) {
-        const uint32_t st = sbase + (uint32_t)(slot * a.stage_bytes + a.x_off);
-        for (int i = tid; i < NT * CPR; i += nthreads) {
-            const int t = i / CPR;
-            const bool in = t < nt;
-            copy_chunk<InT>(st + (uint32_t)(t * ROW), X + (size_t)(in ? m0 + t : 0) * H, kSlab * s, H, i % CPR, in);
-        }
+        tma_load_2d(smem + slot * a.stage_bytes + a.x_off, &tmx, &full_bar[slot], kSlab * s, m0);
     };
 
     const int nst = ns < NST ? ns : NST;
-    for (int s = 0; s < nst; ++s) issue_w(s, s);
+    if (tid == 0)
+        for (int s = 0; s < nst; ++s) {
+            mbar_arrive_expect_tx(&full_bar[s], stage_tx(s));
+            issue_w(s, s);
+        }
     pdl_wait();       // X may be the preceding kernel's output
-    for (int s = 0; s < nst; ++s) {
-        issue_x(s, s);
-        cp_async_arrive(&full_bar[s]);
-    }
+    if (tid == 0)
+        for (int s = 0; s < nst; ++s) issue_x(s, s);
 
-    float acc[kCluNE][TJ];
+    float acc[NE][TJ];
 #pragma unroll
-    for (int j = 0; j < kCluNE; ++j)
+    for (int j = 0; j < NE; ++j)
 #pragma unroll
         for (int t = 0; t < TJ; ++t) acc[j][t] = 0.0f;
     float gacc = 0.0f;
-    int slot = 0;
-    uint32_t phase = 0;
-    for (int s = 0; s < ns; ++s) {
-        mbar_wait(&full_bar[slot], phase, a.err, 0x1C);
-        if (kSlab * s + kBlk * q < H) {
-            const uint8_t *st = smem + slot * a.stage_bytes;
-            const uint8_t *xs = st + a.x_off + (size_t)(tg * TJ) * ROW;
-            if (active) {
-                float w[kCluNE][8];
-#pragma unroll
-                for (int j = 0; j < kCluNE; ++j) load_block(st + (kCluNE * eg + j) * ROW, q, w[j], InT());
-#pragma unroll
-                for (int t = 0; t < TJ; ++t) {
-                    float x[8];
-                    load_block(xs + t * ROW, q, x, InT());
-#pragma unroll
-                    for (int j = 0; j < kCluNE; ++j) acc[j][t] = chain8(x, w[j], acc[j][t]);
-                }
-            }
-            if (gate_here && job == 0) {
-                float gv[8], x[8];
-                load_block(st + a.g_off, q, gv, InT());
-                load_block(st + a.x_off + b * ROW, q, x, InT());
-                gacc = chain8(x, gv, gacc);
-            }
-        }
-        if (s + NST < ns) {              // refill the slot once every warp is done with it
-            __syncthreads();
-            issue_w(s + NST, slot);
-            issue_x(s + NST, slot);
-            cp_async_arrive(&full_bar[slot]);
-        }
-        if (++slot == NST) {
-            slot = 0;
-            phase ^= 1u;
-        }
-    }
 
-    // the pairwise tree over the 16 partitions of every (expert, token)
+    // one slab of the partition chains from ring slot `slot`
+    auto slab = [&](int s, int slot) {
+        if (kSlab * s + kBlk * q >= H) return;
+        const uint8_t *st = smem + slot * a.stage_bytes;
+        const uint8_t *xs = st + a.x_off + (size_t)(tg * TJ) * ROW;
+        if (active) {
+            float w[NE][8];
 #pragma unroll
-    for (int j = 0; j < kCluNE; ++j)
-#pragma unroll
-        for (int t = 0; t < TJ; ++t)
-#pragma unroll
-            for (int d = 1; d < 16; d *= 2) acc[j][t] = acc[j][t] + __shfl_xor_sync(0xFFFFFFFFu, acc[j][t], d);
-#pragma unroll
-    for (int d = 1; d < 16; d *= 2) gacc = gacc + __shfl_xor_sync(0xFFFFFFFFu, gacc, d);
-
-    // every block of the cluster is running: logits go to this call's output
-    // and to the shared memory of the block that selects their token
-    __syncwarp();
-    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
-    if (active) {
-        const uint32_t gbase = smem_u32(gather);
-#pragma unroll
-        for (int j = 0; j < kCluNE; ++j)
+            for (int j = 0; j < NE; ++j) load_block(st + (NE * eg + j) * ROW, q, w[j], InT());
 #pragma unroll
             for (int t = 0; t < TJ; ++t) {
-                const int el = kCluNE * eg + j, tt = tg * TJ + t;
-                if (((j * TJ + t) & 15) == q && el < Eb && tt < nt) {
-                    float v = acc[j][t];
-                    const int e = e0 + el;
-                    const size_t o = (size_t)(m0 + tt) * a.E + e;
-                    if (a.logit_bf16) {
-                        const __nv_bfloat16 r = __float2bfloat16_rn(v);
-                        static_cast<__nv_bfloat16 *>(a.logits)[o] = r;
-                        v = __bfloat162float(r);
-                    } else {
-                        static_cast<float *>(a.logits)[o] = v;
-                    }
-                    const uint32_t dst = gbase + 4u * (uint32_t)((tt / CS) * a.E + e);
-                    st_cluster_f32(mapa_u32(dst, (uint32_t)(tt % CS)), v);
+                float x[8];
+                load_block(xs + t * ROW, q, x, InT());
+                // each chain is h-ordered; the NE chains of a token advance
+                // together (independent multiply-adds)
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+#pragma unroll
+                    for (int j = 0; j < NE; ++j) acc[j][t] = __fmaf_rn(x[i], w[j][i], acc[j][t]);
+            }
+        }
+        if (gate_here && job == 0) {
+            float x[8], gv[8];
+            load_block(st + a.x_off + b * ROW, q, x, InT());
+            if constexpr (ES == 4) {      // the w_sg slab is a plain bulk copy: block q at 32 q
+                const float4 g0 = *reinterpret_cast<const float4 *>(st + a.g_off + 32 * q);
+                const float4 g1 = *reinterpret_cast<const float4 *>(st + a.g_off + 32 * q + 16);
+                gv[0] = g0.x; gv[1] = g0.y; gv[2] = g0.z; gv[3] = g0.w;
+                gv[4] = g1.x; gv[5] = g1.y; gv[6] = g1.z; gv[7] = g1.w;
+            } else {
+                load_block(st + a.g_off, q, gv, InT());
+            }
+            gacc = chain8(x, gv, gacc);
+        }
+    };
+
+    if (ns <= NST) {
+        // the ring holds all of H: every stage is waited for up front, and
+        // the loop has no waits in it, so that the loads of one slab can be
+        // scheduled under the arithmetic of the previous one
+        for (int s = 0; s < ns; ++s) mbar_wait(&full_bar[s], 0, a.err, 0x1C);
+#pragma unroll 2
+        for (int s = 0; s < ns; ++s) slab(s, s);
+    } else {
+        int slot = 0;
+        uint32_t phase = 0;
+        for (int s = 0; s < ns; ++s) {
+            mbar_wait(&full_bar[slot], phase, a.err, 0x1C);
+            slab(s, slot);
+            if (s + NST < ns) {          // refill the slot once every warp is done with it
+                __syncthreads();
+                if (tid == 0) {
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    mbar_arrive_expect_tx(&full_bar[slot], stage_tx(s + NST));
+                    issue_w(s + NST, slot);
+                    issue_x(s + NST, slot);
                 }
             }
+            if (++slot == NST) {
+                slot = 0;
+                phase ^= 1u;
+            }
+        }
     }
-    if (gate_here && tid == 0) {
-        a.gdot[m0 + b] = gacc;
-        if (a.gsig) a.gsig[m0 + b] = 1.0f / (1.0f + expf(-gacc));
+
+    // the pairwise tree over the 16 partitions of every (expert, token), then
+    // the block's logits (in the logit dtype's values) into its own tile
+#pragma unroll
+    for (int d = 1; d < 16; d *= 2) {         // one tree level at a time: its shuffles are independent
+        float o[NE][TJ];
+#pragma unroll
+        for (int j = 0; j < NE; ++j)
+#pragma unroll
+            for (int t = 0; t < TJ; ++t) o[j][t] = __shfl_xor_sync(0xFFFFFFFFu, acc[j][t], d);
+#pragma unroll
+        for (int j = 0; j < NE; ++j)
+#pragma unroll
+            for (int t = 0; t < TJ; ++t) acc[j][t] = acc[j][t] + o[j][t];
+    }
+#pragma unroll
+    for (int d = 1; d < 16; d *= 2) gacc = gacc + __shfl_xor_sync(0xFFFFFFFFu, gacc, d);
+    if (active && q == 0) {              // every lane of the half-warp holds the sums
+#pragma unroll
+        for (int j = 0; j < NE; ++j)
+#pragma unroll
+            for (int t = 0; t < TJ; ++t) {
+                const float v = acc[j][t];
+                tile[(tg * TJ + t) * a.Eb4 + NE * eg + j] =
+                    a.logit_bf16 ? __bfloat162float(__float2bfloat16_rn(v)) : v;
+            }
+    }
+    __syncthreads();
+
+    // every block of the cluster is running: each token's run of Eb logits
+    // goes to the block that selects the token (the barrier's release then
+    // waits for these remote stores only; this call's global outputs are
+    // written after it)
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+    const uint32_t gbase = smem_u32(gather);
+    for (int t = warp; t < nt; t += nwarps) {
+        const uint32_t dst = mapa_u32(gbase + 4u * (uint32_t)((t / CS) * a.E + e0), (uint32_t)(t % CS));
+        for (int e = lane; e < Eb; e += 32) st_cluster_f32(dst + 4u * (uint32_t)e, tile[t * a.Eb4 + e]);
     }
     __syncwarp();
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
     asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 
+    for (int t = warp; t < nt; t += nwarps) {
+        const size_t orow = (size_t)(m0 + t) * a.E + e0;
+        for (int e = lane; e < Eb; e += 32) {
+            const float v = tile[t * a.Eb4 + e];
+            if (a.logit_bf16)
+                static_cast<__nv_bfloat16 *>(a.logits)[orow + e] = __float2bfloat16_rn(v);
+            else
+                static_cast<float *>(a.logits)[orow + e] = v;
+        }
+    }
+    if (gate_here && tid == 0) {
+        a.gdot[m0 + b] = gacc;
+        if (a.gsig) a.gsig[m0 + b] = 1.0f / (1.0f + expf(-gacc));
+    }
+
     // the tokens whose logits this block received: t = r * CS + b
-    const int epl = a.E >> 5, nwarps = nthreads >> 5;
+    const int epl = a.E >> 5;
     for (int r = warp; r * CS + b < nt; r += nwarps) {
         const float *gr = gather + r * a.E;
         const size_t m = (size_t)(m0 + r * CS + b);
@@ -400,9 +430,8 @@ ClusterPlan cluster_plan(Device *d, int M, int E, int H, int es, bool gate)
     if (E > kClusterMaxE || E % CS != 0 || Eb < 2) return p;
     int NT = 1;
     while (NT < 16 && (M + NT - 1) / NT > cd.max_active) NT *= 2;
-    const int Eb4 = (Eb + kCluNE - 1) / kCluNE * kCluNE;
-    const int TJ = NT < kCluTokJob ? NT : kCluTokJob;
-    const int jobs = (Eb4 / kCluNE) * (NT / TJ);
+    const int Eb4 = (Eb + kCluEbAlign - 1) / kCluEbAlign * kCluEbAlign;
+    const int jobs = (Eb4 / clu_ne(NT)) * (NT / clu_tj(NT));
     const int warps = (jobs + 1) / 2;
     if (warps > kCluMaxWarps) return p;
     const int ROW = kSlab * es, ns = (H + kSlab - 1) / kSlab;
@@ -416,14 +445,16 @@ ClusterPlan cluster_plan(Device *d, int M, int E, int H, int es, bool gate)
     p.g_off = p.x_off + NT * ROW;
     p.stage_bytes = p.g_off + (gate ? ROW : 0);
     const int gather = ((NT + CS - 1) / CS) * E * 4;
-    const long budget = (long)kCluSmemMax - 1024 - gather;
+    const int tile = NT * Eb4 * 4;
+    const long budget = (long)kCluSmemMax - 1024 - gather - tile;
     long nst = budget / p.stage_bytes;
     if (nst > kCluMaxStages) nst = kCluMaxStages;
     if (nst > ns) nst = ns;
     if (nst < (ns < 2 ? ns : 2)) return p;
     p.nst = (int)nst;
     p.gather_off = p.nst * p.stage_bytes;
-    p.smem = p.gather_off + gather + 1024;
+    p.tile_off = p.gather_off + gather;
+    p.smem = p.tile_off + tile + 1024;
     p.ok = true;
     return p;
 }
@@ -435,6 +466,21 @@ bi_status launch_cluster(Device *d, const ClusterPlan &p, const CluArgs &args, c
 {
     bi_status st = set_cluster_attrs<InT, NT>(d, kid_cluster((int)sizeof(InT), NT));
     if (st != BI_OK) return st;
+    const CUtensorMapDataType dt = sizeof(InT) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const uint64_t strides[1] = {(uint64_t)args.H * sizeof(InT)};
+    alignas(64) CUtensorMap tmx, tmw;
+    {
+        const uint64_t dims[2] = {(uint64_t)args.H, (uint64_t)args.M};
+        const uint32_t box[2] = {(uint32_t)kSlab, (uint32_t)NT};
+        if ((st = encode_tiled(&tmx, dt, 2, args.x, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE)) != BI_OK)
+            return st;
+    }
+    {
+        const uint64_t dims[2] = {(uint64_t)args.H, (uint64_t)args.E};
+        const uint32_t box[2] = {(uint32_t)kSlab, (uint32_t)(args.E / p.CS)};
+        if ((st = encode_tiled(&tmw, dt, 2, args.w, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE)) != BI_OK)
+            return st;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.CS, p.NC);
     cfg.blockDim = dim3(32 * p.warps);
@@ -449,7 +495,7 @@ bi_status launch_cluster(Device *d, const ClusterPlan &p, const CluArgs &args, c
     at[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
     cfg.numAttrs = 2;
-    return from_cuda(cudaLaunchKernelEx(&cfg, router_cluster_kernel<InT, NT>, args));
+    return from_cuda(cudaLaunchKernelEx(&cfg, router_cluster_kernel<InT, NT>, tmx, tmw, args));
 }
 
 template <typename InT>
@@ -485,6 +531,7 @@ bi_status router_cluster_call(Device *d, const ClusterPlan &p, const void *x, co
     a.x_off = p.x_off;
     a.g_off = p.g_off;
     a.gather_off = p.gather_off;
+    a.tile_off = p.tile_off;
     a.logits = logits;
     a.ids = ids;
     a.weights = weights;

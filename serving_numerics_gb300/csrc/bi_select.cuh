@@ -76,13 +76,17 @@ __device__ __forceinline__ void warp_select(float (&v)[EPLM], int lane, int epl,
         const uint32_t bk = key[0];
         const uint32_t mk = __reduce_max_sync(0xFFFFFFFFu, bk);
         const uint32_t holders = __ballot_sync(0xFFFFFFFFu, bk == mk);
-        // one lane holds the maximum key: its head wins; several (equal
-        // values in different lanes): the lowest index among them wins
-        const uint32_t win = (holders & (holders - 1u)) == 0u
-                                 ? (uint32_t)__shfl_sync(0xFFFFFFFFu, idx[0], __ffs(holders) - 1)
-                                 : __reduce_min_sync(0xFFFFFFFFu, bk == mk ? (uint32_t)idx[0] : 0xFFFFFFFFu);
-        const int wl = (int)(win & 31u);
-        const float wv = __shfl_sync(0xFFFFFFFFu, v[0], wl);
+        // one lane holds the maximum key: its head wins (its index and value
+        // read in parallel); several (equal values in different lanes): the
+        // lowest index among them wins
+        int wl = __ffs(holders) - 1;
+        uint32_t win = (uint32_t)__shfl_sync(0xFFFFFFFFu, idx[0], wl);
+        float wv = __shfl_sync(0xFFFFFFFFu, v[0], wl);
+        if ((holders & (holders - 1u)) != 0u) {
+            win = __reduce_min_sync(0xFFFFFFFFu, bk == mk ? (uint32_t)idx[0] : 0xFFFFFFFFu);
+            wl = (int)(win & 31u);
+            wv = __shfl_sync(0xFFFFFFFFu, v[0], wl);
+        }
         if (lane == wl) {                       // pop the head
 #pragma unroll
             for (int i = 0; i + 1 < EPLM; ++i) {

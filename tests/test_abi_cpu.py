@@ -73,10 +73,11 @@ def test_router_m0_is_noop(lib):
 
 
 def test_router_workspace_bytes(lib):
-    """No workspace for the one-launch cluster router (M <= 128, E <= 512);
+    """No workspace for the one-launch cluster router (M <= 112, E <= 512);
     above that the bound of the tiled plans, the same on every GPU."""
-    for M, E in ((1, 256), (64, 256), (128, 256), (128, 512), (5, 512)):
+    for M, E in ((1, 256), (64, 256), (112, 256), (112, 512), (5, 512)):
         assert lib.bi_router_workspace_bytes(M, E) == 0
+    assert lib.bi_router_workspace_bytes(113, 256) == 113 * 256 * 64
     assert lib.bi_router_workspace_bytes(0, 256) == 0
     assert lib.bi_router_workspace_bytes(-3, 256) == 0
     # two-block plan: 8*M*E within its 64 MiB cap, never below the tail

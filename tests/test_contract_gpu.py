@@ -38,13 +38,13 @@ def gpu_logits(bi, X, W, k, logit_dtype, noalloc=False):
     return gu.host(lg) if logit_dtype == "f32" else gu.host_bf16_bits(lg)
 
 
-# (M, H, E, k): the cluster router (M <= 128, E <= 512) at token tiles of
+# (M, H, E, k): the cluster router (M <= 112, E <= 512) at token tiles of
 # 1, 2, 4, 8 and 16 rows, 2 to 32 experts per block, one-slab and ragged H
 # (H = 8: a single 8-wide block); partition-split tiles one block to an SM
 # (and E = 1024 at small M), two-block tiles two to an SM, whole tiles +
 # split tail (E = 1024, M = 8300: group sums past 64 MiB); ragged H and E
 SHAPES = [(1, 2048, 256, 8), (7, 264, 96, 5), (20, 2048, 256, 8), (33, 2048, 32, 4), (3, 8, 64, 4),
-          (64, 136, 1024, 32), (100, 2048, 256, 8), (128, 2048, 512, 10), (57, 4104, 256, 8),
+          (64, 136, 1024, 32), (100, 2048, 256, 8), (112, 2048, 512, 10), (128, 2048, 512, 10), (57, 4104, 256, 8),
           (300, 136, 64, 4), (700, 264, 256, 8), (1300, 2048, 256, 8), (1235, 128, 256, 8),
           (8300, 136, 1024, 16)]
 

@@ -99,6 +99,45 @@ def test_router256_m_sweep(bi):
     assert n == len(M_SWEEP) + len(TAIL_SWEEP) == 52
 
 
+def test_router_bf16_m_sweep(bi):
+    """The bf16-logit router with bf16 inputs (H=2048, E=512, top-10, the
+    tie-heavy workload's shape) and the fused shared gate: the 19-token
+    request is byte-identical solo and inside batches of every M in the
+    sweep, in logits, ids, weights, margins, gate dot and sigmoid."""
+    import torch
+    H, E, k = 2048, 512, 10
+    W = gu.dev_bf16(synth.to_bf16_bits(synth.router_weights(32, 0, E, H)))
+    wsg = gu.dev_bf16(synth.to_bf16_bits(synth.shared_gate_weights(32, 0, H)))
+    req = synth.to_bf16_bits(synth.tokens(32, 0, 0, 19, H))
+    pool = synth.to_bf16_bits(synth.tokens(32, 0, 1, 4096, H))
+    keys = FIELDS + ("gate_dot", "gate_sigmoid")
+
+    def call(X):
+        o = bi.router_gate_topk(gu.dev_bf16(X), W, wsg, k, "bf16")
+        torch.cuda.synchronize()
+        return o
+
+    def bytes_of(o, a, b):
+        return {f: (o[f][a:b].contiguous().view(torch.int16) if o[f].dtype == torch.bfloat16
+                    else o[f][a:b].contiguous()).cpu().numpy().tobytes() for f in keys}
+
+    solo = bytes_of(call(req), 0, 19)
+    n = 0
+    for M in M_SWEEP + TAIL_SWEEP:
+        if M <= 19:
+            X, off, cnt = req[:M], 0, M
+        else:
+            off = (M - 19) // 2 if M in M_SWEEP else M - 19
+            X = np.concatenate([pool[:off], req, pool[off:M - 19]])
+            cnt = 19
+        got = bytes_of(call(X), off, off + cnt)
+        for f in keys:
+            width = len(solo[f]) // 19
+            assert got[f] == solo[f][:width * cnt], f"{f} differs at M={M}"
+        n += 1
+    assert n == len(M_SWEEP) + len(TAIL_SWEEP) == 52
+
+
 def test_route_trace_760_decisions(bi):
     """The 19-token request through 40 layers (each with its own gate
     weights and hidden states), solo versus at total M = 75: all 760
@@ -133,10 +172,10 @@ def test_mixed_prefill_prefix_split(bi):
     request is run batched (all 16 together), solo, as a cache miss (M = N)
     and as a suffix-only cache hit (M = N mod 16, the last full block when
     that is 0).  Per-request route hashes chained over the layers must be
-    equal across all runs, and the suffix rows must be byte-identical.
-    Eight layers keep the test short; the benchmark runs forty."""
+    equal across all runs, and the suffix rows must be byte-identical, at
+    all forty layers of the workload."""
     import torch
-    H, E, k, L, blk = 2048, 256, 8, 8, 16
+    H, E, k, L, blk = 2048, 256, 8, 40, 16
     lens = synth.request_lengths(0)
     assert len(lens) == 16 and lens.min() >= 5 and lens.max() <= 300
     offs = np.concatenate([[0], np.cumsum(lens)]).tolist()
@@ -144,23 +183,26 @@ def test_mixed_prefill_prefix_split(bi):
     Ws = [gu.dev_f32(synth.router_weights(40, l, E, H)) for l in range(L)]
     wsg = [gu.dev_f32(synth.shared_gate_weights(40, l, H)) for l in range(L)]
     Bs = [gu.dev_bf16(synth.gemm_b(40, H, H, layer=l)) for l in range(L)]
-    Xs = [np.concatenate([synth.tokens(40, l, r, int(lens[r]), H) for r in range(16)]) for l in range(L)]
-    As = [synth.gemm_a(41, Mtot, H, layer=l) for l in range(L)]
+    # every layer's rows live on the device; a run gathers its rows there
+    Xd = [gu.dev_f32(np.concatenate([synth.tokens(40, l, r, int(lens[r]), H) for r in range(16)]))
+          for l in range(L)]
+    Ad = [gu.dev_bf16(synth.gemm_a(41, Mtot, H, layer=l)) for l in range(L)]
 
     def run(rows_by_req):
         """rows_by_req: list of (request, row_begin, row_end) packed into one
         batch; returns per-request chained hashes and per-layer outputs."""
         idx = np.concatenate([np.arange(offs[r] + a, offs[r] + b) for r, a, b in rows_by_req])
+        idx_d = torch.from_numpy(idx).cuda()
         sub = [0]
         for _, a, b in rows_by_req:
             sub.append(sub[-1] + (b - a))
         h = None
         outs = []
         for l in range(L):
-            x = gu.dev_f32(Xs[l][idx])
+            x = Xd[l].index_select(0, idx_d).contiguous()
             o = route(bi, x, Ws[l], k)
             d, s = bi.shared_gate(x, wsg[l])
-            c = bi.gemm_bf16(gu.dev_bf16(As[l][idx]), Bs[l])
+            c = bi.gemm_bf16(Ad[l].index_select(0, idx_d).contiguous(), Bs[l])
             h = bi.route_hash(o["ids"], sub, basis=h)
             outs.append((o, d, c, sub))
         torch.cuda.synchronize()
