@@ -46,7 +46,7 @@ namespace {
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
 gemm_bf16_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__ CUtensorMap tmb,
                  const __grid_constant__ CUtensorMap tmb_piece, __nv_bfloat16 *__restrict__ C, int M, int N,
-                 int K, long long ldc, int n_full, int lg_s, unsigned int *err)
+                 int K, long long ldc, int n_full, int lg_s, int a_rows, unsigned int *err)
 {
     pdl_trigger();   // dependents may launch now; each waits before reading our outputs
     extern __shared__ uint8_t smem_raw[];
@@ -59,6 +59,7 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant_
     const int num_tiles = m_tiles * n_tiles, kblocks = K / BK;
     const int num_items = n_full + ((num_tiles - n_full) << lg_s);
     const int pn = BN >> lg_s;                           // columns of a piece
+    const int a_bytes = a_rows * BK * 2;                 // A rows staged per K block (BM, or fewer for small M)
 
     if (threadIdx.x == 0) {
         prefetch_tmap(&tma);
@@ -94,7 +95,7 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant_
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
                     mbar_wait(&empty_bar[s], ph ^ 1u, err, 0x21);
                     uint8_t *st = smem + s * STAGE_BYTES;
-                    mbar_arrive_expect_tx(&full_bar[s], piece < 0 ? STAGE_BYTES : A_BYTES + (B_BYTES >> lg_s));
+                    mbar_arrive_expect_tx(&full_bar[s], (uint32_t)a_bytes + (piece < 0 ? B_BYTES : (B_BYTES >> lg_s)));
                     tma_load_2d(st, &tma, &full_bar[s], kb * BK, mt * BM);
                     tma_load_2d(st + A_BYTES, piece < 0 ? &tmb : &tmb_piece, &full_bar[s], kb * BK, n0);
                 }
@@ -190,11 +191,17 @@ extern "C" bi_status bi_gemm_bf16(const void *A, const void *B, void *C, int32_t
     bi_status st = current_device(&d);
     if (st != BI_OK) return st;
 
+    // A single M tile of fewer than BM rows stages only its rows rounded up to
+    // a whole 8-row swizzle atom: the tile's other rows of A in shared memory
+    // then hold whatever the stage held before, which only reaches output
+    // rows past M, and those are never stored (an output row's value is a
+    // function of its own A row and B alone).
+    const int a_rows = M < BM ? (M + 7) / 8 * 8 : BM;
     alignas(64) CUtensorMap tma, tmb;
     {
         const uint64_t dims[2] = {(uint64_t)K, (uint64_t)M};
         const uint64_t strides[1] = {(uint64_t)lda * 2};
-        const uint32_t box[2] = {(uint32_t)BK, (uint32_t)BM};
+        const uint32_t box[2] = {(uint32_t)BK, (uint32_t)a_rows};
         if ((st = encode_tiled(&tma, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, dims, strides, box,
                                CU_TENSOR_MAP_SWIZZLE_128B)) != BI_OK)
             return st;
@@ -233,5 +240,5 @@ extern "C" bi_status bi_gemm_bf16(const void *A, const void *B, void *C, int32_t
     if ((st = set_smem_once(d, KID_GEMM, gemm_bf16_kernel, GEMM_SMEM)) != BI_OK) return st;
     return launch_pdl(gemm_bf16_kernel, dim3(grid), dim3(GEMM_THREADS), (size_t)GEMM_SMEM,
                       reinterpret_cast<cudaStream_t>(s), tma, tmb, tmb_piece, static_cast<__nv_bfloat16 *>(C),
-                      (int)M, (int)N, (int)K, (long long)ldc, (int)n_full, lg_s, d->err);
+                      (int)M, (int)N, (int)K, (long long)ldc, (int)n_full, lg_s, a_rows, d->err);
 }

@@ -108,8 +108,8 @@ enum : int {
     KID_HASH = 25,         // 4 instantiations: 25..28
     KID_SELECT_GATE = 34,  // 4 instantiations: 34..37 (two group sums or none)
     KID_MOE = 40,          // 5 kernels: 40..44
-    KID_NORM = 45,         // 4 instantiations: 45..48
-    KID_ROUTER_PROJ_SHALLOW = 49,   // 2 instantiations: 49..50 (after the norms' 45..48)
+    KID_NORM = 45,         // 2 instantiations: 45..46
+    KID_ROUTER_PROJ_SHALLOW = 49,   // 2 instantiations: 49..50
     KID_SELECT_GENERAL = 51,        // 4 instantiations: 51..54
     KID_SELECT_GATE_GENERAL = 55,   // 4 instantiations: 55..58
     KID_ROUTER_CLUSTER = 64,        // 10 instantiations: 64..73
