@@ -85,42 +85,48 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant_
 
     if (warp == 0) {
         if (lane == 0) {   // TMA producer
-            uint32_t it = 0;
+            uint32_t s = 0, ph = 0;          // ring slot and its phase parity, advanced per K block
             for (int item = blockIdx.x; item < num_items; item += gridDim.x) {
                 int piece;
                 const int tile = item_tile(item, n_full, lg_s, piece);
                 const int mt = tile % m_tiles, nt = tile / m_tiles;
                 const int n0 = nt * BN + (piece > 0 ? piece * pn : 0);
-                for (int kb = 0; kb < kblocks; ++kb, ++it) {
-                    const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+                for (int kb = 0; kb < kblocks; ++kb) {
                     mbar_wait(&empty_bar[s], ph ^ 1u, err, 0x21);
                     uint8_t *st = smem + s * STAGE_BYTES;
                     mbar_arrive_expect_tx(&full_bar[s], (uint32_t)a_bytes + (piece < 0 ? B_BYTES : (B_BYTES >> lg_s)));
                     tma_load_2d(st, &tma, &full_bar[s], kb * BK, mt * BM);
-                    tma_load_2d(st + A_BYTES, piece < 0 ? &tmb : &tmb_piece, &full_bar[s], kb * BK, n0);
+                    tma_load_2d(st + a_bytes, piece < 0 ? &tmb : &tmb_piece, &full_bar[s], kb * BK, n0);
+                    if (++s == (uint32_t)STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
                 }
             }
         }
     } else if (warp == 1) {
         if (lane == 0) {   // MMA issuer
-            uint32_t it = 0, tc = 0;
+            uint32_t s = 0, ph = 0, tc = 0;
             for (int item = blockIdx.x; item < num_items; item += gridDim.x, ++tc) {
                 const uint32_t idesc = item < n_full ? IDESC : idesc_n(pn);
                 const uint32_t b = tc & 1u, tph = (tc >> 1) & 1u;
                 mbar_wait(&tempty_bar[b], tph ^ 1u, err, 0x22);
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + b * ACC_COLS;
-                for (int kb = 0; kb < kblocks; ++kb, ++it) {
-                    const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+                for (int kb = 0; kb < kblocks; ++kb) {
                     mbar_wait(&full_bar[s], ph, err, 0x23);
                     tc_fence_after();
                     const uint32_t a_addr = smem_u32(smem + s * STAGE_BYTES);
-                    const uint32_t b_addr = a_addr + A_BYTES;
+                    const uint32_t b_addr = a_addr + a_bytes;
 #pragma unroll
                     for (int k = 0; k < BK / UMMA_K; ++k)
                         umma_bf16(d_tmem, sw128_desc(a_addr + k * UMMA_K * 2),
                                   sw128_desc(b_addr + k * UMMA_K * 2), idesc, (kb | k) != 0 ? 1u : 0u);
                     umma_commit(&empty_bar[s]);       // stage reusable once these MMAs finish
+                    if (++s == (uint32_t)STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
                 }
                 umma_commit(&tfull_bar[b]);           // accumulator ready for the epilogue
             }
