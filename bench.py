@@ -52,14 +52,17 @@ def peaks():
 # capture of the kernel as it stands, at this launch shape; None where no capture of the
 # current code exists.  Reset to None whenever the kernel changes.  The router call is
 # its two launches (projection + selection) captured inside the layer sequence with the
-# caches as the preceding kernels left them; its writes include L2 evictions of the
-# preceding kernels' dirty lines.
-NCU_TRAFFIC = {"gemm_bf16_kernel": 67_437_056 + 12_296_448,
+# caches as the preceding kernels left them (mean of two layers); its writes include L2
+# evictions of the preceding kernels' dirty lines.
+NCU_TRAFFIC = {"gemm_bf16_kernel": None,
                # the grouped expert projection's four launches (plan, place, gemm, combine),
                # each captured with the caches flushed
                "moe_call": 153_088 + 16_920_576 + 69_718_528 + 1_283_893_504 + 58_558_976 + 67_250_176 + 5_120,
-               "router_call": (35_668_224 + 16_139_520 + 67_328 + 1_476_864
-                               + 35_651_584 + 17_229_824 + 11_008 + 1_525_248) // 2}
+               "router_call": (35_667_968 + 15_844_096 + 58_368 + 1_188_352
+                               + 35_674_368 + 16_492_800 + 20_992 + 1_418_752) // 2,
+               # one launch with the caches flushed: the reads; its bf16 output stays in L2
+               "rmsnorm_kernel": 33_574_400 + 0}
+
 
 def fp32_peak(torch, dev) -> dict:
     """The FP32 FMA peak from this GPU's unit counts and its maximum SM clock:
@@ -747,7 +750,8 @@ def rmsnorm_measure(bi, synth, torch, dev, hbm_gbs, Xs):
     byt = 4 * M * H + 2 * M * H + 4 * H + 4 * M
     return {"config": f"M={M}, H={H}, f32 in, bf16 out", "us_per_call": t * 1e6, "launches_per_call": 1,
             "roofline": {"bound": "hbm", "achieved": byt / t / 1e9, "peak": hbm_gbs, "unit": "GB/s",
-                         "frac": byt / t / 1e9 / hbm_gbs, "algorithmic_bytes": byt, "traffic": None}}
+                         "frac": byt / t / 1e9 / hbm_gbs, "algorithmic_bytes": byt,
+                         "traffic": NCU_TRAFFIC["rmsnorm_kernel"]}}
 
 
 def m_variant_context(bi, synth, torch, dev):
