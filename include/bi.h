@@ -158,9 +158,12 @@ BI_API size_t bi_router_workspace_bytes(int32_t M, int32_t E);
  * bi_router_plan -- how bi_router_topk (and bi_router_gate_topk) would cut
  * the work for M rows and E experts on the current device.  For the
  * one-launch cluster router (M <= 112): *m_split = M, *C = minus the number
- * of blocks per cluster, *launches = 1.  Otherwise the rows below *m_split
- * run as whole tiles and the rest with each tile's partitions split over *C
- * blocks, and *launches counts the projection launches plus the selection.
+ * of blocks per cluster, *launches = 1.  For the persistent projection
+ * (large batches, one CTA per SM, each with the same number of steps):
+ * *m_split = minus the number of CTAs, *C = 2 (each tile's partitions as two
+ * halves), *launches = 2.  Otherwise the rows below *m_split run as whole
+ * tiles and the rest with each tile's partitions split over *C blocks, and
+ * *launches counts the projection launches plus the selection.
  * Introspection only (any plan gives the same bits); it launches nothing.
  * Returns BI_ERR_INVALID_ARG for NULL outputs or bad sizes, BI_ERR_CUDA when
  * no device is current.

@@ -262,7 +262,8 @@ def selftest_fma_rate(iters: int, sink, packed: bool = False, stream=None) -> fl
 
 def router_plan(M: int, E: int):
     """bi_router_plan: (m_split, C, launches) for M rows and E experts; C < 0
-    means the one-launch cluster router with -C blocks per cluster."""
+    means the one-launch cluster router with -C blocks per cluster, m_split <
+    0 the persistent projection with -m_split CTAs."""
     ms, c, n = C.c_int32(), C.c_int32(), C.c_int32()
     _check(load().bi_router_plan(M, E, C.byref(ms), C.byref(c), C.byref(n)), "bi_router_plan")
     return ms.value, c.value, n.value

@@ -408,7 +408,8 @@ template <int EPLM, bool GATE, bool TWO>
 __global__ void __launch_bounds__(32 * kSelWarps, sel_min_blocks<EPLM, GATE>())
 router_select_kernel(const float *__restrict__ part, int C, int m_split, void *logits, int logit_bf16,
                      int M, int E, int k, int32_t *__restrict__ ids, float *__restrict__ weights,
-                     float *__restrict__ margin, int32_t *__restrict__ ulps, GateArgs gate, int H)
+                     float *__restrict__ margin, int32_t *__restrict__ ulps, GateArgs gate, int H,
+                     unsigned int *epoch)
 {
     pdl_trigger();   // dependents may launch now; each waits before reading our outputs
     extern __shared__ __align__(16) uint8_t gate_rows[];   // staged gate: kSelWarps rows of X, then w_sg
@@ -423,6 +424,9 @@ router_select_kernel(const float *__restrict__ part, int C, int m_split, void *l
         __syncthreads();
     }
     pdl_wait();
+    // the persistent projection's call epoch: advanced once that projection
+    // is complete (its hand-off flags of this call then never match again)
+    if (epoch && blockIdx.x == 0 && threadIdx.x == 0) atomicAdd(epoch, 1u);
     if (staged && threadIdx.x == 0) {
         // the rows land while the selection below runs
         const int m0 = blockIdx.x * kSelWarps, rows = M - m0 < kSelWarps ? M - m0 : kSelWarps;
@@ -586,7 +590,7 @@ bi_status launch_proj_c(Device *d, int C, const void *x, const void *w, int M, i
 template <int EPLM>
 bi_status launch_select1(Device *d, dim3 grid, dim3 block, cudaStream_t cs, const float *pp, int C,
                          int m_split, void *logits, int lbf, int M, int E, int k, int32_t *ids, float *w, float *mg,
-                         int32_t *mu, const GateArgs &gate, int H)
+                         int32_t *mu, const GateArgs &gate, int H, unsigned int *epoch)
 {
     const bool two = C <= 2;
     const int kid = (gate.gx ? (two ? KID_SELECT_GATE : KID_SELECT_GATE_GENERAL)
@@ -604,20 +608,26 @@ bi_status launch_select1(Device *d, dim3 grid, dim3 block, cudaStream_t cs, cons
         g.staged = smem <= kGateStageMax ? 1 : 0;     // larger rows are read from device memory directly
         if (!g.staged) smem = 0;
     }
-    return launch_pdl(kern, grid, block, smem, cs, pp, C, m_split, logits, lbf, M, E, k, ids, w, mg, mu, g, H);
+    return launch_pdl(kern, grid, block, smem, cs, pp, C, m_split, logits, lbf, M, E, k, ids, w, mg, mu, g, H,
+                      epoch);
 }
 
 bi_status launch_select(Device *d, int epl, dim3 grid, dim3 block, cudaStream_t cs, const float *pp, int C,
                         int m_split, void *logits, int lbf, int M, int E, int k, int32_t *ids, float *w,
-                        float *mg, int32_t *mu, const GateArgs &g = GateArgs(), int H = 0)
+                        float *mg, int32_t *mu, const GateArgs &g = GateArgs(), int H = 0,
+                        unsigned int *epoch = nullptr)
 {
     if (epl <= 4)
-        return launch_select1<4>(d, grid, block, cs, pp, C, m_split, logits, lbf, M, E, k, ids, w, mg, mu, g, H);
+        return launch_select1<4>(d, grid, block, cs, pp, C, m_split, logits, lbf, M, E, k, ids, w, mg, mu, g, H,
+                                 epoch);
     if (epl <= 8)
-        return launch_select1<8>(d, grid, block, cs, pp, C, m_split, logits, lbf, M, E, k, ids, w, mg, mu, g, H);
+        return launch_select1<8>(d, grid, block, cs, pp, C, m_split, logits, lbf, M, E, k, ids, w, mg, mu, g, H,
+                                 epoch);
     if (epl <= 16)
-        return launch_select1<16>(d, grid, block, cs, pp, C, m_split, logits, lbf, M, E, k, ids, w, mg, mu, g, H);
-    return launch_select1<32>(d, grid, block, cs, pp, C, m_split, logits, lbf, M, E, k, ids, w, mg, mu, g, H);
+        return launch_select1<16>(d, grid, block, cs, pp, C, m_split, logits, lbf, M, E, k, ids, w, mg, mu, g, H,
+                                  epoch);
+    return launch_select1<32>(d, grid, block, cs, pp, C, m_split, logits, lbf, M, E, k, ids, w, mg, mu, g, H,
+                              epoch);
 }
 
 // How the projection's work is cut for a batch of more than kClusterMaxM rows
@@ -677,7 +687,13 @@ size_t tiled_workspace_bound(long long M, long long E)
 size_t router_workspace_bound(long long M, long long E)
 {
     if (M <= 0 || (M <= kClusterMaxM && E <= kClusterMaxE)) return 0;
-    return tiled_workspace_bound(M, E);
+    size_t need = tiled_workspace_bound(M, E);
+    // the persistent projection (bi_router_persist.cu) wherever some GPU may
+    // choose it: enough items for its smallest grid, group sums within its cap
+    const long long n_items = ((M + 63) / 64) * ((E + 63) / 64) * 2;
+    if (n_items >= kPersistMinItems && 8 * M * E <= kPersistSumsMax)
+        need = std::max(need, persist_workspace_bytes(M, E));
+    return need;
 }
 
 }  // namespace
@@ -728,6 +744,24 @@ bi_status router_call(const void *x, const void *w_gate, bi_dtype in_dtype, bi_d
                                    margin_out, margin_ulps_out, gate.gx ? gate.gw : nullptr, gate.dot, gate.sig,
                                    cs);
 
+    const int epl = E / 32;
+    dim3 grid((M + kSelWarps - 1) / kSelWarps), block(32 * kSelWarps);
+    GateArgs g = gate;
+    g.bf16 = f32in ? 0 : 1;
+
+    // large batches: the persistent projection, every SM the same share of
+    // the steps, then the selection adds the two halves' group sums
+    const PersistPlan pp = persist_plan(d, M, E, f32in);
+    if (pp.ok) {
+        if (!workspace || workspace_bytes < persist_workspace_bytes(M, E)) return BI_ERR_UNSUPPORTED_SHAPE;
+        st = launch_persist(d, pp, f32in, x, w_gate, M, E, H, workspace, cs);
+        if (st != BI_OK) return st;
+        uint8_t *ws = static_cast<uint8_t *>(workspace);
+        return launch_select(d, epl, grid, block, cs, reinterpret_cast<const float *>(ws + kPersistGroupSumsOffset),
+                             2, 0, logits_out, lbf, M, E, k, ids_out, weights_out, margin_out, margin_ulps_out, g, H,
+                             reinterpret_cast<unsigned int *>(ws));
+    }
+
     const SplitPlan plan = plan_split(M, E, d->sm_count);
     void *part = nullptr;
     if (plan.m_split < M) {
@@ -754,13 +788,8 @@ bi_status router_call(const void *x, const void *w_gate, bi_dtype in_dtype, bi_d
         if (st != BI_OK) return st;
     }
 
-    const int epl = E / 32;
-    dim3 grid((M + kSelWarps - 1) / kSelWarps), block(32 * kSelWarps);
-    const float *pp = static_cast<const float *>(part);
-    GateArgs g = gate;
-    g.bf16 = f32in ? 0 : 1;
-    return launch_select(d, epl, grid, block, cs, pp, plan.C, plan.m_split, logits_out, lbf, M, E, k, ids_out,
-                         weights_out, margin_out, margin_ulps_out, g, H);
+    return launch_select(d, epl, grid, block, cs, static_cast<const float *>(part), plan.C, plan.m_split,
+                         logits_out, lbf, M, E, k, ids_out, weights_out, margin_out, margin_ulps_out, g, H);
 }
 
 }  // namespace
@@ -788,6 +817,13 @@ extern "C" bi_status bi_router_plan(int32_t M, int32_t E, int32_t *m_split, int3
         *m_split = M;
         *C = -cp.CS;          // negative: a cluster of this many blocks, one launch
         *launches = 1;
+        return BI_OK;
+    }
+    const PersistPlan pp = persist_plan(d, M, E, true);
+    if (pp.ok) {      // the persistent projection: minus its CTA count, two halves per tile
+        *m_split = -pp.G;
+        *C = 2;
+        *launches = 2;
         return BI_OK;
     }
     const SplitPlan p = plan_split(M, E, d->sm_count);

@@ -197,8 +197,9 @@ def test_router_splits_bit_identical(bi, E, M, H):
 def test_router_plan_reports_the_cut(bi):
     """bi_router_plan on a 152-SM GB300: one cluster launch up to 112 rows
     (E <= 512), partition-split tiles below a tile half per SM, two-block
-    tiles once their blocks fill the SMs, whole tiles plus a split tail
-    where the group sums would pass 64 MiB."""
+    tiles once their blocks fill the SMs, the persistent projection from one
+    64 x 64 x 8-partition item per SM, whole tiles plus a split tail where
+    the group sums would pass 64 MiB."""
     import torch
     if torch.cuda.get_device_properties(0).multi_processor_count != 152:
         pytest.skip("plan thresholds are stated for 152 SMs")
@@ -207,7 +208,10 @@ def test_router_plan_reports_the_cut(bi):
         assert m == M and c in (-16, -8) and n == 1, (M, m, c, n)
     assert bi.router_plan(128, 256) == (0, 8, 2)       # past the cluster router: 16 tiles, 8 blocks each
     assert bi.router_plan(129, 256) == (0, 4, 2)       # 20 tiles: 4 blocks each fill 80 SMs
-    assert bi.router_plan(4096, 256) == (0, 2, 2)
+    assert bi.router_plan(4096, 256) == (-152, 2, 2)     # the persistent projection: 512 items, 152 CTAs
+    assert bi.router_plan(1217, 256) == (-152, 2, 2)     # 160 items
+    assert bi.router_plan(1216, 256) == (-152, 2, 2)     # 152 items: one a CTA
+    assert bi.router_plan(1152, 256) == (0, 2, 2)        # 144 items: fewer than the SMs, two-block tiles
     assert bi.router_plan(256, 256) == (0, 4, 2)
     assert bi.router_plan(640, 256) == (0, 2, 2)       # 80 tiles: 160 two-block halves
     assert bi.router_plan(1024, 256) == (0, 2, 2)
