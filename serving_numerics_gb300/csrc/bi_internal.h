@@ -34,8 +34,9 @@ struct Device {
     // calls from several host threads may both set them, which is harmless
     std::atomic<uint64_t> attr_done[2] = {};
     // whether one block of the persistent router projection fits an SM
-    // (f32, bf16 inputs): -1 not yet asked, 0 no, 1 yes
-    std::atomic<int> persist_fits[2] = {-1, -1};
+    // (f32, bf16 inputs; without, with the shared gate): -1 not yet asked,
+    // 0 no, 1 yes
+    std::atomic<int> persist_fits[4] = {-1, -1, -1, -1};
 };
 
 // The state of the current device (never NULL on BI_OK).
@@ -117,7 +118,7 @@ enum : int {
     KID_SELECT_GATE_GENERAL = 55,   // 4 instantiations: 55..58
     KID_ROUTER_CLUSTER = 64,        // 10 instantiations: 64..73
     KID_FLOOR = 74,
-    KID_ROUTER_PERSIST = 75,        // 2 instantiations: 75..76
+    KID_ROUTER_PERSIST = 75,        // 4 instantiations: 75..78
 };
 
 // Batches of at most this many rows (and E <= kClusterMaxE) take the
@@ -146,14 +147,16 @@ bi_status router_cluster_call(Device *d, const ClusterPlan &p, const void *x, co
 
 // The persistent projection for large batches (csrc/bi_router_persist.cu).
 // Workspace layout of that plan: the call epoch (one word), the hand-off
-// flags (8 words per CTA), the hand-off accumulators (128 KB per CTA), then
-// the two halves' group sums [2][M][E] read by the selection kernel.
+// flags (8 words per CTA), the hand-off accumulators (128 KB per CTA), the
+// shared gate's hand-off (2 KB per CTA), then the two halves' group sums
+// [2][M][E] and the gate's [2][M], read by the selection kernel.
 constexpr int kPersistMaxCtas = 160;        // CTAs at most (one per SM)
 constexpr int kPersistMinItems = 128;       // below this many items the split plans are used
 constexpr long long kPersistSumsMax = 64ll << 20;
 constexpr size_t kPersistFlagsOffset = 256;
 constexpr size_t kPersistHandoffOffset = 8192;
-constexpr size_t kPersistGroupSumsOffset = kPersistHandoffOffset + (size_t)kPersistMaxCtas * 8 * 128 * 32 * 4;
+constexpr size_t kPersistGateHandoffOffset = kPersistHandoffOffset + (size_t)kPersistMaxCtas * 8 * 128 * 32 * 4;
+constexpr size_t kPersistGroupSumsOffset = kPersistGateHandoffOffset + (size_t)kPersistMaxCtas * 8 * 2 * 32 * 4;
 static_assert(kPersistFlagsOffset + (size_t)kPersistMaxCtas * 8 * 4 <= kPersistHandoffOffset, "flag words");
 
 struct PersistArgs {
@@ -162,6 +165,9 @@ struct PersistArgs {
     unsigned int *epoch;      // advanced by the selection kernel of each call
     unsigned int *flags;      // [G][8]
     float *handoff;           // [G][8][128][32]
+    const void *w_sg;         // the shared gate's row (NULL: no gate)
+    float *gpart;             // the gate's group sums [2][M]
+    float *ghandoff;          // [G][8][2][32]
     unsigned int *err;
 };
 
@@ -170,9 +176,9 @@ struct PersistPlan {
     int G, n_et, n_items;
 };
 
-PersistPlan persist_plan(Device *d, int M, int E, bool f32in);
+PersistPlan persist_plan(Device *d, int M, int E, bool f32in, bool gate);
 size_t persist_workspace_bytes(long long M, long long E);
-bi_status launch_persist(Device *d, const PersistPlan &p, bool f32in, const void *x, const void *w, int M, int E,
-                         int H, void *workspace, cudaStream_t s);
+bi_status launch_persist(Device *d, const PersistPlan &p, bool f32in, const void *x, const void *w,
+                         const void *w_sg, int M, int E, int H, void *workspace, cudaStream_t s);
 
 }  // namespace bi

@@ -312,6 +312,7 @@ constexpr size_t kGateStageMax = 96 * 1024;   // shared memory for the staged ga
 struct GateArgs {
     const void *gx = nullptr;   // X again ([M, H], the input dtype)
     const void *gw = nullptr;   // w_sg [H]
+    const float *gsum = nullptr;   // or the gate's two group sums [2][M], from the persistent projection
     int bf16 = 0;
     int staged = 0;             // the block's X rows and w_sg are copied to shared memory first
     float *dot = nullptr, *sig = nullptr;
@@ -508,6 +509,13 @@ router_select_kernel(const float *__restrict__ part, int C, int m_split, void *l
     }
 
     warp_select<EPLM>(v, lane, epl, k, logit_bf16, (size_t)m, ids, weights, margin, ulps);
+
+    // the gate from the persistent projection: its top tree level
+    if (gate.gsum && lane == 0) {
+        const float g = gate.gsum[m] + gate.gsum[(size_t)M + m];
+        gate.dot[m] = g;
+        if (gate.sig) gate.sig[m] = 1.0f / (1.0f + expf(-g));
+    }
 
     // the shared gate (bi_router_gate_topk): lanes 0..15 are the 16
     // partitions; the butterfly with offsets 1, 2, 4, 8 is the pairwise tree
@@ -751,15 +759,21 @@ bi_status router_call(const void *x, const void *w_gate, bi_dtype in_dtype, bi_d
 
     // large batches: the persistent projection, every SM the same share of
     // the steps, then the selection adds the two halves' group sums
-    const PersistPlan pp = persist_plan(d, M, E, f32in);
+    const PersistPlan pp = persist_plan(d, M, E, f32in, gate.gx != nullptr);
     if (pp.ok) {
         if (!workspace || workspace_bytes < persist_workspace_bytes(M, E)) return BI_ERR_UNSUPPORTED_SHAPE;
-        st = launch_persist(d, pp, f32in, x, w_gate, M, E, H, workspace, cs);
+        st = launch_persist(d, pp, f32in, x, w_gate, gate.gx ? gate.gw : nullptr, M, E, H, workspace, cs);
         if (st != BI_OK) return st;
         uint8_t *ws = static_cast<uint8_t *>(workspace);
-        return launch_select(d, epl, grid, block, cs, reinterpret_cast<const float *>(ws + kPersistGroupSumsOffset),
-                             2, 0, logits_out, lbf, M, E, k, ids_out, weights_out, margin_out, margin_ulps_out, g, H,
-                             reinterpret_cast<unsigned int *>(ws));
+        const float *sums = reinterpret_cast<const float *>(ws + kPersistGroupSumsOffset);
+        GateArgs pg;                         // the gate needs only its two group sums here
+        if (gate.gx) {
+            pg.gsum = sums + (size_t)2 * M * E;
+            pg.dot = gate.dot;
+            pg.sig = gate.sig;
+        }
+        return launch_select(d, epl, grid, block, cs, sums, 2, 0, logits_out, lbf, M, E, k, ids_out, weights_out,
+                             margin_out, margin_ulps_out, pg, H, reinterpret_cast<unsigned int *>(ws));
     }
 
     const SplitPlan plan = plan_split(M, E, d->sm_count);
@@ -819,7 +833,7 @@ extern "C" bi_status bi_router_plan(int32_t M, int32_t E, int32_t *m_split, int3
         *launches = 1;
         return BI_OK;
     }
-    const PersistPlan pp = persist_plan(d, M, E, true);
+    const PersistPlan pp = persist_plan(d, M, E, true, false);
     if (pp.ok) {      // the persistent projection: minus its CTA count, two halves per tile
         *m_split = -pp.G;
         *C = 2;

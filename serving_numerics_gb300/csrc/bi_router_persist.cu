@@ -49,7 +49,7 @@ constexpr int PT_WARPS = 8;                  // partitions per item
 constexpr int PT_VALS = 128;                 // accumulators per thread (16 x 8)
 constexpr int PT_SLOT = PT_VALS * 32;        // floats per warp in the tree / hand-off
 
-template <typename InT>
+template <typename InT, bool GATE>
 struct PersistCfg {
     static constexpr int ES = (int)sizeof(InT);
     static constexpr int PB = 128 / (kBlk * ES);   // partition blocks per 128-byte box row: 4 (f32), 8 (bf16)
@@ -58,9 +58,10 @@ struct PersistCfg {
     static constexpr int XBOX = PT_M * P, WBOX = PT_E * P;
     static constexpr int XOP = XBOX * NB, WOP = WBOX * NB;
     static constexpr int STAGE = XOP + WOP;        // 32 KB (f32), 16 KB (bf16)
-    static constexpr int NST = (160 * 1024) / STAGE;
-    static constexpr int TREE = 4 * PT_SLOT * 4;   // four warps' 128 partials: 64 KB
-    static constexpr int SMEM = NST * STAGE + TREE + 1024;
+    static constexpr int NST = ((GATE ? 128 : 160) * 1024) / STAGE;
+    static constexpr int TREE = 4 * PT_SLOT * 4;   // 8 warps x 64 partials: 64 KB
+    static constexpr int GTREE = GATE ? 2 * PT_WARPS * PT_M * 4 : 0;   // gate partials, two buffers: 4 KB
+    static constexpr int SMEM = NST * STAGE + TREE + GTREE + 1024;
 };
 
 // 16-byte chunk `ch` of row r of a 128-byte-swizzled box sits at
@@ -131,6 +132,50 @@ __device__ __forceinline__ void pblock_bf16(float (&acc)[16][8], const uint8_t *
                 acc[j][i] = a;
             }
         }
+    }
+}
+
+// The shared gate's chains for this step: lane (tg, eg) owns tokens
+// t0 = tg + 8 eg and t0 + 4 of the tile, the warp's partition block of the
+// slab (the same staged X rows the logits use) against w_sg's 8 values
+// there, one FMA each in increasing h (the router's contract, w_sg being one
+// more gate row).
+__device__ __forceinline__ void gate_f32(float &g0, float &g1, const uint8_t *xs, int pc, int t0,
+                                         const float *wsg)
+{
+    const float4 w0 = __ldg(reinterpret_cast<const float4 *>(wsg));
+    const float4 w1 = __ldg(reinterpret_cast<const float4 *>(wsg + 4));
+    const int t1 = t0 + 4;
+    const float4 a0 = *reinterpret_cast<const float4 *>(xs + t0 * 128 + 16 * ((2 * pc) ^ sw8(t0)));
+    const float4 a1 = *reinterpret_cast<const float4 *>(xs + t0 * 128 + 16 * ((2 * pc + 1) ^ sw8(t0)));
+    const float4 b0 = *reinterpret_cast<const float4 *>(xs + t1 * 128 + 16 * ((2 * pc) ^ sw8(t1)));
+    const float4 b1 = *reinterpret_cast<const float4 *>(xs + t1 * 128 + 16 * ((2 * pc + 1) ^ sw8(t1)));
+    g0 = __fmaf_rn(a0.x, w0.x, g0); g0 = __fmaf_rn(a0.y, w0.y, g0);
+    g0 = __fmaf_rn(a0.z, w0.z, g0); g0 = __fmaf_rn(a0.w, w0.w, g0);
+    g0 = __fmaf_rn(a1.x, w1.x, g0); g0 = __fmaf_rn(a1.y, w1.y, g0);
+    g0 = __fmaf_rn(a1.z, w1.z, g0); g0 = __fmaf_rn(a1.w, w1.w, g0);
+    g1 = __fmaf_rn(b0.x, w0.x, g1); g1 = __fmaf_rn(b0.y, w0.y, g1);
+    g1 = __fmaf_rn(b0.z, w0.z, g1); g1 = __fmaf_rn(b0.w, w0.w, g1);
+    g1 = __fmaf_rn(b1.x, w1.x, g1); g1 = __fmaf_rn(b1.y, w1.y, g1);
+    g1 = __fmaf_rn(b1.z, w1.z, g1); g1 = __fmaf_rn(b1.w, w1.w, g1);
+}
+
+__device__ __forceinline__ void gate_bf16(float &g0, float &g1, const uint8_t *xs, int pc, int t0,
+                                          const __nv_bfloat16 *wsg)
+{
+    const uint4 w = __ldg(reinterpret_cast<const uint4 *>(wsg));
+    const uint4 a = *reinterpret_cast<const uint4 *>(xs + t0 * 128 + 16 * (pc ^ sw8(t0)));
+    const uint4 c = *reinterpret_cast<const uint4 *>(xs + (t0 + 4) * 128 + 16 * (pc ^ sw8(t0 + 4)));
+    const uint32_t wa[4] = {w.x, w.y, w.z, w.w}, xa[4] = {a.x, a.y, a.z, a.w}, xc[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        g0 = __fmaf_rn(bf16lo(xa[q]), bf16lo(wa[q]), g0);
+        g0 = __fmaf_rn(bf16hi(xa[q]), bf16hi(wa[q]), g0);
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        g1 = __fmaf_rn(bf16lo(xc[q]), bf16lo(wa[q]), g1);
+        g1 = __fmaf_rn(bf16hi(xc[q]), bf16hi(wa[q]), g1);
     }
 }
 
@@ -310,19 +355,25 @@ constexpr int PT_THREADS = (PT_WARPS + 4) * 32;
 constexpr int PT_REGS_COMPUTE = 232, PT_REGS_PRODUCER = 40;
 static_assert(2 * 128 * PT_REGS_COMPUTE + 128 * PT_REGS_PRODUCER <= PT_THREADS * 168, "register split");
 
-template <typename InT>
+// GATE: also the shared gate (bi_router_gate_topk): the warps of every
+// item of the first expert tile run w_sg's chains for the tile's tokens from
+// the staged X rows; the gate's 8 partials per half go through the same
+// lower tree levels into a.gpart[g][M], and the selection kernel adds the
+// two halves.
+template <typename InT, bool GATE>
 __global__ void __launch_bounds__(PT_THREADS, 1)
 router_proj_persist_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
                            PersistArgs a)
 {
     pdl_trigger();   // dependents may launch now; each waits before reading our outputs
-    using Cfg = PersistCfg<InT>;
+    using Cfg = PersistCfg<InT, GATE>;
     constexpr int NST = Cfg::NST;
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[NST];    // stage landed (TMA bytes)
     __shared__ __align__(8) uint64_t empty_bar[NST];   // the 8 compute warps are done with the stage
     uint8_t *smem = smem_align1024(smem_raw);
     float *tree = reinterpret_cast<float *>(smem + NST * Cfg::STAGE);
+    float *gtree = reinterpret_cast<float *>(smem + NST * Cfg::STAGE + Cfg::TREE);   // GATE only
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, tg = lane & 3, eg = lane >> 2;
     const int b = blockIdx.x, G = gridDim.x, ns = a.ns;
@@ -396,12 +447,16 @@ router_proj_persist_kernel(const __grid_constant__ CUtensorMap tmx, const __grid
         *my_flag = ~done;      // left over, and happens to match: not this call's
 
     float acc[16][8];
+    float gacc0 = 0.0f, gacc1 = 0.0f;      // GATE: this lane's two tokens' chains
+    const int gt0 = tg + 8 * eg;            // GATE: the first of them (the second is gt0 + 4)
+    int gbuf = 0;                           // GATE: the gate tree's buffer (alternates)
     int slot = 0;
     uint32_t phase = 0;
     // the slabs [s_begin, s_end) of `item` into acc
     auto run = [&](int item, int s_begin, int s_end) {
         const int g = item & 1, tile = item >> 1;
         const bool live = tg < a.M - (tile / a.n_et) * PT_M;   // some of this lane's tokens exist
+        const bool gitem = GATE && tile % a.n_et == 0;
         for (int s = s_begin; s < s_end; ++s) {
             mbar_wait(&full_bar[slot], phase, a.err, 0x14);
             if (live && kSlab * s + kBlk * (8 * g + warp) < a.H) {
@@ -411,6 +466,15 @@ router_proj_persist_kernel(const __grid_constant__ CUtensorMap tmx, const __grid
                     pblock_f32(acc, st + bx * Cfg::XBOX, st + Cfg::XOP + bx * Cfg::WBOX, pc, tg, eg);
                 else
                     pblock_bf16(acc, st + bx * Cfg::XBOX, st + Cfg::XOP + bx * Cfg::WBOX, pc, tg, eg);
+                if (GATE && gitem) {
+                    const int hw = kSlab * s + kBlk * (8 * g + warp);
+                    if constexpr (sizeof(InT) == 4)
+                        gate_f32(gacc0, gacc1, st + bx * Cfg::XBOX, pc, gt0,
+                                 static_cast<const float *>(a.w_sg) + hw);
+                    else
+                        gate_bf16(gacc0, gacc1, st + bx * Cfg::XBOX, pc, gt0,
+                                  static_cast<const __nv_bfloat16 *>(a.w_sg) + hw);
+                }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty_bar[slot]);
@@ -425,12 +489,37 @@ router_proj_persist_kernel(const __grid_constant__ CUtensorMap tmx, const __grid
         for (int j = 0; j < 16; ++j)
 #pragma unroll
             for (int i = 0; i < 8; ++i) acc[j][i] = 0.0f;
+        gacc0 = 0.0f;
+        gacc1 = 0.0f;
     };
     // the item's group sums for its half of the partitions
     auto finish = [&](int item) {
         const int g = item & 1, tile = item >> 1;
         const int m0 = (tile / a.n_et) * PT_M, e0 = (tile % a.n_et) * PT_E;
         float *part = a.part + (size_t)g * a.M * a.E;
+        if (GATE && tile % a.n_et == 0) {
+            // the gate's 8 partials of every token meet in shared memory, and
+            // warp 0 adds them by the three lower levels of the pairwise tree.
+            // The buffers alternate: a buffer is written again only after
+            // every warp has passed the next gate tree's barrier, which warp 0
+            // reaches after its reads of this one.
+            float *gb = gtree + gbuf * (PT_WARPS * PT_M);
+            gb[warp * PT_M + gt0] = gacc0;
+            gb[warp * PT_M + gt0 + 4] = gacc1;
+            named_sync(1, PT_WARPS * 32);
+            if (warp == 0) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int t = lane + 32 * h;
+                    float p[PT_WARPS];
+#pragma unroll
+                    for (int w = 0; w < PT_WARPS; ++w) p[w] = gb[w * PT_M + t];
+                    const float s = ((p[0] + p[1]) + (p[2] + p[3])) + ((p[4] + p[5]) + (p[6] + p[7]));
+                    if (m0 + t < a.M) a.gpart[(size_t)g * a.M + m0 + t] = s;
+                }
+            }
+            gbuf ^= 1;
+        }
         switch (warp) {
         case 0: tree_and_store<0>(acc, tree, lane, part, a.M, a.E, m0, e0, tg, eg); break;
         case 1: tree_and_store<1>(acc, tree, lane, part, a.M, a.E, m0, e0, tg, eg); break;
@@ -452,6 +541,11 @@ router_proj_persist_kernel(const __grid_constant__ CUtensorMap tmx, const __grid
         for (int j = 0; j < 16; ++j)
 #pragma unroll
             for (int i = 0; i < 8; ++i) st_evict_first(ho + (j * 8 + i) * 32 + lane, acc[j][i], pol);
+        if (GATE && (last >> 1) % a.n_et == 0) {
+            float *gho = a.ghandoff + ((size_t)b * PT_WARPS + warp) * 64;
+            st_evict_first(gho + lane, gacc0, pol);
+            st_evict_first(gho + 32 + lane, gacc1, pol);
+        }
         __threadfence();
         __syncwarp();
         if (lane == 0) st_release(my_flag, done);
@@ -479,6 +573,12 @@ router_proj_persist_kernel(const __grid_constant__ CUtensorMap tmx, const __grid
         for (int j = 0; j < 16; ++j)
 #pragma unroll
             for (int i = 0; i < 8; ++i) acc[j][i] = __ldcg(ho + (j * 8 + i) * 32 + lane);
+        const bool gcont = GATE && (first >> 1) % a.n_et == 0;
+        const float *gho = a.ghandoff + ((size_t)(b - 1) * PT_WARPS + warp) * 64;
+        if (gcont) {
+            gacc0 = __ldcg(gho + lane);
+            gacc1 = __ldcg(gho + 32 + lane);
+        }
         run(first, sa, ns);
         finish(first);
         // every value read from the hand-off has been used by now: drop its
@@ -488,6 +588,8 @@ router_proj_persist_kernel(const __grid_constant__ CUtensorMap tmx, const __grid
 #pragma unroll
             for (int r = 0; r < PT_VALS / 32; ++r)
                 asm volatile("discard.global.L2 [%0], 128;" ::"l"(ho + (r * 32 + lane) * 32) : "memory");
+            if (gcont && lane < 2)
+                asm volatile("discard.global.L2 [%0], 128;" ::"l"(gho + 32 * lane) : "memory");
         }
     }
 }
@@ -496,31 +598,32 @@ router_proj_persist_kernel(const __grid_constant__ CUtensorMap tmx, const __grid
 
 size_t persist_workspace_bytes(long long M, long long E)
 {
-    return kPersistGroupSumsOffset + (size_t)(2 * M * E) * sizeof(float);
+    return kPersistGroupSumsOffset + (size_t)(2 * M * E + 2 * M) * sizeof(float);
 }
 
 namespace {
 // One block (12 warps, about 225 KB of shared memory) per SM
 // is what the kernel is built for; ask the runtime once per device.
-template <typename InT>
+constexpr int persist_kid(bool f32in, bool gate) { return KID_ROUTER_PERSIST + (f32in ? 0 : 1) + (gate ? 2 : 0); }
+
+template <typename InT, bool GATE>
 bool persist_fits(Device *d)
 {
-    std::atomic<int> &f = d->persist_fits[sizeof(InT) == 4 ? 0 : 1];
+    std::atomic<int> &f = d->persist_fits[(sizeof(InT) == 4 ? 0 : 1) + (GATE ? 2 : 0)];
     int v = f.load(std::memory_order_acquire);
     if (v >= 0) return v == 1;
-    auto kern = router_proj_persist_kernel<InT>;
+    auto kern = router_proj_persist_kernel<InT, GATE>;
     int blocks = 0;
-    const bool ok = set_smem_once(d, KID_ROUTER_PERSIST + (sizeof(InT) == 4 ? 0 : 1), kern,
-                                  PersistCfg<InT>::SMEM) == BI_OK &&
+    const bool ok = set_smem_once(d, persist_kid(sizeof(InT) == 4, GATE), kern, PersistCfg<InT, GATE>::SMEM) == BI_OK &&
                     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kern, PT_THREADS,
-                                                                  PersistCfg<InT>::SMEM) == cudaSuccess &&
+                                                                  PersistCfg<InT, GATE>::SMEM) == cudaSuccess &&
                     blocks >= 1;
     f.store(ok ? 1 : 0, std::memory_order_release);
     return ok;
 }
 }  // namespace
 
-PersistPlan persist_plan(Device *d, int M, int E, bool f32in)
+PersistPlan persist_plan(Device *d, int M, int E, bool f32in, bool gate)
 {
     PersistPlan p = {};
     const long long n_mt = (M + PT_M - 1) / PT_M, n_et = (E + PT_E - 1) / PT_E;
@@ -530,7 +633,9 @@ PersistPlan persist_plan(Device *d, int M, int E, bool f32in)
     // a continuation never fall in the same item), and the group sums must
     // fit the cap of the split plans
     if (n_items < kPersistMinItems || n_items < G || 8ll * M * E > kPersistSumsMax) return p;
-    if (!(f32in ? persist_fits<float>(d) : persist_fits<__nv_bfloat16>(d))) return p;
+    const bool fits = f32in ? (gate ? persist_fits<float, true>(d) : persist_fits<float, false>(d))
+                            : (gate ? persist_fits<__nv_bfloat16, true>(d) : persist_fits<__nv_bfloat16, false>(d));
+    if (!fits) return p;
     p.ok = true;
     p.G = G;
     p.n_et = (int)n_et;
@@ -538,13 +643,13 @@ PersistPlan persist_plan(Device *d, int M, int E, bool f32in)
     return p;
 }
 
-template <typename InT>
-bi_status launch_persist_t(Device *d, const PersistPlan &p, const void *x, const void *w, int M, int E, int H,
-                           void *workspace, cudaStream_t s)
+template <typename InT, bool GATE>
+bi_status launch_persist_t(Device *d, const PersistPlan &p, const void *x, const void *w, const void *w_sg, int M,
+                           int E, int H, void *workspace, cudaStream_t s)
 {
-    using Cfg = PersistCfg<InT>;
-    auto kern = router_proj_persist_kernel<InT>;
-    bi_status st = set_smem_once(d, KID_ROUTER_PERSIST + (sizeof(InT) == 4 ? 0 : 1), kern, Cfg::SMEM);
+    using Cfg = PersistCfg<InT, GATE>;
+    auto kern = router_proj_persist_kernel<InT, GATE>;
+    bi_status st = set_smem_once(d, persist_kid(sizeof(InT) == 4, GATE), kern, Cfg::SMEM);
     if (st != BI_OK) return st;
     const CUtensorMapDataType dt = sizeof(InT) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const uint64_t strides[1] = {(uint64_t)H * sizeof(InT)};
@@ -570,15 +675,21 @@ bi_status launch_persist_t(Device *d, const PersistPlan &p, const void *x, const
     a.epoch = reinterpret_cast<unsigned int *>(ws);
     a.flags = reinterpret_cast<unsigned int *>(ws + kPersistFlagsOffset);
     a.handoff = reinterpret_cast<float *>(ws + kPersistHandoffOffset);
+    a.w_sg = w_sg;
+    a.gpart = reinterpret_cast<float *>(ws + kPersistGroupSumsOffset + (size_t)2 * M * E * sizeof(float));
+    a.ghandoff = reinterpret_cast<float *>(ws + kPersistGateHandoffOffset);
     a.err = d->err;
     return launch_pdl(kern, dim3(p.G), dim3(PT_THREADS), (size_t)Cfg::SMEM, s, tmx, tmw, a);
 }
 
-bi_status launch_persist(Device *d, const PersistPlan &p, bool f32in, const void *x, const void *w, int M, int E,
-                         int H, void *workspace, cudaStream_t s)
+bi_status launch_persist(Device *d, const PersistPlan &p, bool f32in, const void *x, const void *w,
+                         const void *w_sg, int M, int E, int H, void *workspace, cudaStream_t s)
 {
-    return f32in ? launch_persist_t<float>(d, p, x, w, M, E, H, workspace, s)
-                 : launch_persist_t<__nv_bfloat16>(d, p, x, w, M, E, H, workspace, s);
+    if (w_sg)
+        return f32in ? launch_persist_t<float, true>(d, p, x, w, w_sg, M, E, H, workspace, s)
+                     : launch_persist_t<__nv_bfloat16, true>(d, p, x, w, w_sg, M, E, H, workspace, s);
+    return f32in ? launch_persist_t<float, false>(d, p, x, w, nullptr, M, E, H, workspace, s)
+                 : launch_persist_t<__nv_bfloat16, false>(d, p, x, w, nullptr, M, E, H, workspace, s);
 }
 
 }  // namespace bi

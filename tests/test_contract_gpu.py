@@ -114,7 +114,9 @@ def test_shared_gate_dot_is_the_contract(bi, M, H):
 # and read the gate rows from device memory directly
 FUSED = [(1, 2048, 256, 8, "f32"), (20, 264, 96, 5, "f32"), (100, 2048, 256, 8, "f32"), (1300, 2048, 256, 8, "f32"),
          (5, 2048, 512, 10, "bf16"), (700, 2048, 256, 8, "bf16"), (4096, 2048, 256, 8, "f32"),
-         (70, 4096, 64, 4, "f32"), (203, 6000, 64, 4, "bf16")]
+         (70, 4096, 64, 4, "f32"), (203, 6000, 64, 4, "bf16"),
+         # the persistent projection with the gate: ragged M, E and H, bf16
+         (2500, 2056, 96, 5, "bf16"), (2432, 264, 128, 6, "f32")]
 
 
 @pytest.mark.parametrize("M,H,E,k,dt", FUSED)
@@ -138,7 +140,8 @@ def test_router_gate_fused_is_the_two_calls(bi, M, H, E, k, dt):
     assert bi.bi_get_last_device_error() == 0
     for f in ("logits", "ids", "weights", "margin", "margin_ulps"):
         assert fused[f].cpu().numpy().tobytes() == plain[f].cpu().numpy().tobytes(), f
-    rows = np.arange(M) if M <= 1300 else np.array([0, 5, 3647, 3648, 4095])
+    rows = np.arange(M) if M <= 1300 else np.array(sorted({r for r in (0, 5, 63, 64, M // 2, 3647, 3648, M - 65,
+                                                                       M - 64, M - 1) if r < M}))
     want = contract.router_logits(X[rows], w[None, :])[:, 0]
     assert gu.host(fused["gate_dot"])[rows].view(np.uint32).tobytes() == want.view(np.uint32).tobytes()
     if dt == "f32":
