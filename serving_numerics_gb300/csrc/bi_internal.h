@@ -147,27 +147,29 @@ bi_status router_cluster_call(Device *d, const ClusterPlan &p, const void *x, co
 
 // The persistent projection for large batches (csrc/bi_router_persist.cu).
 // Workspace layout of that plan: the call epoch (one word), the hand-off
-// flags (8 words per CTA), the hand-off accumulators (128 KB per CTA), the
+// flags (16 words per CTA), the hand-off accumulators (128 KB per CTA), the
 // shared gate's hand-off (2 KB per CTA), then the two halves' group sums
 // [2][M][E] and the gate's [2][M], read by the selection kernel.
 constexpr int kPersistMaxCtas = 160;        // CTAs at most (one per SM)
 constexpr int kPersistMinItems = 128;       // below this many items the split plans are used
 constexpr long long kPersistSumsMax = 64ll << 20;
+constexpr int kPersistFlagsPerCta = 16;     // 8 compute warps, 2 gate warps, spare
 constexpr size_t kPersistFlagsOffset = 256;
-constexpr size_t kPersistHandoffOffset = 8192;
+constexpr size_t kPersistHandoffOffset = 16384;
 constexpr size_t kPersistGateHandoffOffset = kPersistHandoffOffset + (size_t)kPersistMaxCtas * 8 * 128 * 32 * 4;
 constexpr size_t kPersistGroupSumsOffset = kPersistGateHandoffOffset + (size_t)kPersistMaxCtas * 8 * 2 * 32 * 4;
-static_assert(kPersistFlagsOffset + (size_t)kPersistMaxCtas * 8 * 4 <= kPersistHandoffOffset, "flag words");
+static_assert(kPersistFlagsOffset + (size_t)kPersistMaxCtas * kPersistFlagsPerCta * 4 <= kPersistHandoffOffset,
+              "flag words");
 
 struct PersistArgs {
     int M, E, H, n_et, ns, n_items;
     float *part;              // group sums [2][M][E]
     unsigned int *epoch;      // advanced by the selection kernel of each call
-    unsigned int *flags;      // [G][8]
+    unsigned int *flags;      // [G][kPersistFlagsPerCta]
     float *handoff;           // [G][8][128][32]
     const void *w_sg;         // the shared gate's row (NULL: no gate)
     float *gpart;             // the gate's group sums [2][M]
-    float *ghandoff;          // [G][8][2][32]
+    float *ghandoff;          // [G][2 gate warps][8 partitions][32]
     unsigned int *err;
 };
 

@@ -58,10 +58,10 @@ struct PersistCfg {
     static constexpr int XBOX = PT_M * P, WBOX = PT_E * P;
     static constexpr int XOP = XBOX * NB, WOP = WBOX * NB;
     static constexpr int STAGE = XOP + WOP;        // 32 KB (f32), 16 KB (bf16)
-    static constexpr int NST = ((GATE ? 128 : 160) * 1024) / STAGE;
+    static constexpr int NST = (160 * 1024) / STAGE;
     static constexpr int TREE = 4 * PT_SLOT * 4;   // 8 warps x 64 partials: 64 KB
-    static constexpr int GTREE = GATE ? 2 * PT_WARPS * PT_M * 4 : 0;   // gate partials, two buffers: 4 KB
-    static constexpr int SMEM = NST * STAGE + TREE + GTREE + 1024;
+    static constexpr int WSG = PT_WARPS * kBlk * ES;   // GATE: w_sg's slice of a step (the half's 8 blocks)
+    static constexpr int SMEM = NST * STAGE + TREE + (GATE ? NST * WSG : 0) + 1024;
 };
 
 // 16-byte chunk `ch` of row r of a 128-byte-swizzled box sits at
@@ -135,47 +135,42 @@ __device__ __forceinline__ void pblock_bf16(float (&acc)[16][8], const uint8_t *
     }
 }
 
-// The shared gate's chains for this step: lane (tg, eg) owns tokens
-// t0 = tg + 8 eg and t0 + 4 of the tile, the warp's partition block of the
-// slab (the same staged X rows the logits use) against w_sg's 8 values
-// there, one FMA each in increasing h (the router's contract, w_sg being one
-// more gate row).
-__device__ __forceinline__ void gate_f32(float &g0, float &g1, const uint8_t *xs, int pc, int t0,
-                                         const float *wsg)
+// The shared gate (GATE): lane L of gate warp q owns token row t = 32 q + L
+// of the tile and runs w_sg's chains of the half's 8 partitions through the
+// same staged rows, one FMA each in increasing h (the router's contract,
+// w_sg being one more gate row); w_sg's slice of the step (wsl) is staged
+// with the step.  One row a lane keeps the shared loads free
+// of bank conflicts; the tree over the 8 partitions then needs no exchange.
+template <typename Cfg, typename InT>
+__device__ __forceinline__ void gate_rows_step(float (&gp)[8], const uint8_t *st, int t, int s, int g,
+                                               const uint8_t *wsl, int H)
 {
-    const float4 w0 = __ldg(reinterpret_cast<const float4 *>(wsg));
-    const float4 w1 = __ldg(reinterpret_cast<const float4 *>(wsg + 4));
-    const int t1 = t0 + 4;
-    const float4 a0 = *reinterpret_cast<const float4 *>(xs + t0 * 128 + 16 * ((2 * pc) ^ sw8(t0)));
-    const float4 a1 = *reinterpret_cast<const float4 *>(xs + t0 * 128 + 16 * ((2 * pc + 1) ^ sw8(t0)));
-    const float4 b0 = *reinterpret_cast<const float4 *>(xs + t1 * 128 + 16 * ((2 * pc) ^ sw8(t1)));
-    const float4 b1 = *reinterpret_cast<const float4 *>(xs + t1 * 128 + 16 * ((2 * pc + 1) ^ sw8(t1)));
-    g0 = __fmaf_rn(a0.x, w0.x, g0); g0 = __fmaf_rn(a0.y, w0.y, g0);
-    g0 = __fmaf_rn(a0.z, w0.z, g0); g0 = __fmaf_rn(a0.w, w0.w, g0);
-    g0 = __fmaf_rn(a1.x, w1.x, g0); g0 = __fmaf_rn(a1.y, w1.y, g0);
-    g0 = __fmaf_rn(a1.z, w1.z, g0); g0 = __fmaf_rn(a1.w, w1.w, g0);
-    g1 = __fmaf_rn(b0.x, w0.x, g1); g1 = __fmaf_rn(b0.y, w0.y, g1);
-    g1 = __fmaf_rn(b0.z, w0.z, g1); g1 = __fmaf_rn(b0.w, w0.w, g1);
-    g1 = __fmaf_rn(b1.x, w1.x, g1); g1 = __fmaf_rn(b1.y, w1.y, g1);
-    g1 = __fmaf_rn(b1.z, w1.z, g1); g1 = __fmaf_rn(b1.w, w1.w, g1);
-}
-
-__device__ __forceinline__ void gate_bf16(float &g0, float &g1, const uint8_t *xs, int pc, int t0,
-                                          const __nv_bfloat16 *wsg)
-{
-    const uint4 w = __ldg(reinterpret_cast<const uint4 *>(wsg));
-    const uint4 a = *reinterpret_cast<const uint4 *>(xs + t0 * 128 + 16 * (pc ^ sw8(t0)));
-    const uint4 c = *reinterpret_cast<const uint4 *>(xs + (t0 + 4) * 128 + 16 * (pc ^ sw8(t0 + 4)));
-    const uint32_t wa[4] = {w.x, w.y, w.z, w.w}, xa[4] = {a.x, a.y, a.z, a.w}, xc[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        g0 = __fmaf_rn(bf16lo(xa[q]), bf16lo(wa[q]), g0);
-        g0 = __fmaf_rn(bf16hi(xa[q]), bf16hi(wa[q]), g0);
-    }
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        g1 = __fmaf_rn(bf16lo(xc[q]), bf16lo(wa[q]), g1);
-        g1 = __fmaf_rn(bf16hi(xc[q]), bf16hi(wa[q]), g1);
+    for (int p = 0; p < PT_WARPS; ++p) {
+        const int hw = kSlab * s + kBlk * (8 * g + p);
+        if (hw < H) {
+            const uint8_t *xs = st + (p / Cfg::PB) * Cfg::XBOX + t * 128;
+            const int pc = p % Cfg::PB;
+            float c = gp[p];
+            if constexpr (sizeof(InT) == 4) {
+                const float4 w0 = *reinterpret_cast<const float4 *>(wsl + p * 32);
+                const float4 w1 = *reinterpret_cast<const float4 *>(wsl + p * 32 + 16);
+                const float4 a0 = *reinterpret_cast<const float4 *>(xs + 16 * ((2 * pc) ^ sw8(t)));
+                const float4 a1 = *reinterpret_cast<const float4 *>(xs + 16 * ((2 * pc + 1) ^ sw8(t)));
+                c = __fmaf_rn(a0.x, w0.x, c); c = __fmaf_rn(a0.y, w0.y, c);
+                c = __fmaf_rn(a0.z, w0.z, c); c = __fmaf_rn(a0.w, w0.w, c);
+                c = __fmaf_rn(a1.x, w1.x, c); c = __fmaf_rn(a1.y, w1.y, c);
+                c = __fmaf_rn(a1.z, w1.z, c); c = __fmaf_rn(a1.w, w1.w, c);
+            } else {
+                const uint4 w = *reinterpret_cast<const uint4 *>(wsl + p * 16);
+                const uint4 x = *reinterpret_cast<const uint4 *>(xs + 16 * (pc ^ sw8(t)));
+                c = __fmaf_rn(bf16lo(x.x), bf16lo(w.x), c); c = __fmaf_rn(bf16hi(x.x), bf16hi(w.x), c);
+                c = __fmaf_rn(bf16lo(x.y), bf16lo(w.y), c); c = __fmaf_rn(bf16hi(x.y), bf16hi(w.y), c);
+                c = __fmaf_rn(bf16lo(x.z), bf16lo(w.z), c); c = __fmaf_rn(bf16hi(x.z), bf16hi(w.z), c);
+                c = __fmaf_rn(bf16lo(x.w), bf16lo(w.w), c); c = __fmaf_rn(bf16hi(x.w), bf16hi(w.w), c);
+            }
+            gp[p] = c;
+        }
     }
 }
 
@@ -323,18 +318,25 @@ struct Cursor {
 // The boxes of one step (item, slab) into stage `st` (which: 1 = gate rows,
 // 2 = token rows, 3 = both; expect: arm the barrier with the step's bytes).
 // A box that starts past H is not loaded: its partition has no data there.
+// With `wsl` (the gate's kernel, items of the first expert tile), w_sg's
+// slice of the step goes there too: the half's 8 blocks, cut at H.
 template <typename Cfg>
 __device__ __forceinline__ void load_boxes(uint8_t *st, uint64_t *bar, const CUtensorMap *tmx, const CUtensorMap *tmw,
-                                           int item, int slab, const PersistArgs &a, int which, bool expect)
+                                           int item, int slab, const PersistArgs &a, int which, bool expect,
+                                           uint8_t *wsl = nullptr)
 {
     const int g = item & 1, tile = item >> 1;
     const int m0 = (tile / a.n_et) * PT_M, e0 = (tile % a.n_et) * PT_E;
+    const int hs = kSlab * slab + kBlk * 8 * g;                                // the slice's first h
+    const bool gate = wsl != nullptr && tile % a.n_et == 0 && hs < a.H && (which & 1);
+    const uint32_t wsg_bytes = gate ? (uint32_t)((a.H - hs < 8 * kBlk ? a.H - hs : 8 * kBlk) * Cfg::ES) : 0u;
     if (expect) {
         int nvalid = 0;
 #pragma unroll
         for (int bx = 0; bx < Cfg::NB; ++bx) nvalid += (kSlab * slab + kBlk * (8 * g + bx * Cfg::PB) < a.H) ? 1 : 0;
-        mbar_arrive_expect_tx(bar, (uint32_t)(nvalid * (Cfg::XBOX + Cfg::WBOX)));
+        mbar_arrive_expect_tx(bar, (uint32_t)(nvalid * (Cfg::XBOX + Cfg::WBOX)) + wsg_bytes);
     }
+    if (gate) bulk_load(wsl, static_cast<const uint8_t *>(a.w_sg) + (size_t)hs * Cfg::ES, wsg_bytes, bar);
 #pragma unroll
     for (int bx = 0; bx < Cfg::NB; ++bx) {
         const int h0 = kSlab * slab + kBlk * (8 * g + bx * Cfg::PB);
@@ -347,19 +349,21 @@ __device__ __forceinline__ void load_boxes(uint8_t *st, uint64_t *bar, const CUt
 
 // Register split: the block is launched as three warpgroups at 168
 // registers a thread (12 warps x 32 x 168 = 64,512); the two compute
-// warpgroups raise theirs to 232 and the producer warpgroup lowers its to 40
-// (2 x 128 x 232 + 128 x 40 = 64,512: the same total, so the raise never
+// warpgroups raise theirs to 224 and the producer warpgroup (the TMA
+// producer and the gate warps) lowers its to 56
+// (2 x 128 x 224 + 128 x 56 = 64,512: the same total, so the raise never
 // waits on registers nobody releases).  Each SM sub-partition has a quarter
 // of the register file, so a ninth warp at full width would not fit.
 constexpr int PT_THREADS = (PT_WARPS + 4) * 32;
-constexpr int PT_REGS_COMPUTE = 232, PT_REGS_PRODUCER = 40;
+constexpr int PT_REGS_COMPUTE = 224, PT_REGS_PRODUCER = 56;
 static_assert(2 * 128 * PT_REGS_COMPUTE + 128 * PT_REGS_PRODUCER <= PT_THREADS * 168, "register split");
 
-// GATE: also the shared gate (bi_router_gate_topk): the warps of every
-// item of the first expert tile run w_sg's chains for the tile's tokens from
-// the staged X rows; the gate's 8 partials per half go through the same
-// lower tree levels into a.gpart[g][M], and the selection kernel adds the
-// two halves.
+// GATE: also the shared gate (bi_router_gate_topk), on two warps of the
+// producer warpgroup: on every item of the first expert tile they run w_sg's
+// chains for the tile's 64 token rows from the same staged stages, add each
+// half's 8 partials by the lower tree levels into a.gpart[g][M], and the
+// selection kernel adds the two halves.  (Run on the compute warps instead,
+// the gate's few extra loads and FMAs cost those warps' main loop about 5 %.)
 template <typename InT, bool GATE>
 __global__ void __launch_bounds__(PT_THREADS, 1)
 router_proj_persist_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
@@ -368,12 +372,13 @@ router_proj_persist_kernel(const __grid_constant__ CUtensorMap tmx, const __grid
     pdl_trigger();   // dependents may launch now; each waits before reading our outputs
     using Cfg = PersistCfg<InT, GATE>;
     constexpr int NST = Cfg::NST;
+    constexpr int RELEASERS = PT_WARPS + (GATE ? 2 : 0);   // warps that read every stage
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[NST];    // stage landed (TMA bytes)
-    __shared__ __align__(8) uint64_t empty_bar[NST];   // the 8 compute warps are done with the stage
+    __shared__ __align__(8) uint64_t empty_bar[NST];   // every warp that reads stages is done with it
     uint8_t *smem = smem_align1024(smem_raw);
     float *tree = reinterpret_cast<float *>(smem + NST * Cfg::STAGE);
-    float *gtree = reinterpret_cast<float *>(smem + NST * Cfg::STAGE + Cfg::TREE);   // GATE only
+    uint8_t *wsg_ring = smem + NST * Cfg::STAGE + Cfg::TREE;    // GATE: w_sg's slice of each stage
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, tg = lane & 3, eg = lane >> 2;
     const int b = blockIdx.x, G = gridDim.x, ns = a.ns;
@@ -395,16 +400,30 @@ router_proj_persist_kernel(const __grid_constant__ CUtensorMap tmx, const __grid
 #pragma unroll
         for (int s = 0; s < NST; ++s) {
             mbar_init(&full_bar[s], 1);
-            mbar_init(&empty_bar[s], PT_WARPS);
+            mbar_init(&empty_bar[s], RELEASERS);
         }
         mbar_init_fence();
     }
     __syncthreads();
 
+    // the waits on a hand-off flag (bounded; the flag of the previous CTA)
+    auto wait_flag = [&](const unsigned int *fl, unsigned int done, unsigned int where) {
+        if (ld_acquire(fl) == done) return;
+        const uint64_t t0 = global_ns();
+        while (ld_acquire(fl) != done) {
+            if (load_volatile(a.err) != 0u) return;
+            if (global_ns() - t0 > kWaitLimitNs) {
+                report_error(a.err, 5u, where);
+                return;
+            }
+            __nanosleep(256);
+        }
+    };
+
     if (warp >= PT_WARPS) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(PT_REGS_PRODUCER));
         // the producer: one thread walks the steps in order, each into the
-        // next ring slot once the compute warps have released it
+        // next ring slot once the stage's readers have released it
         if (warp == PT_WARPS && lane == 0) {
             Cursor c;
             c.start(h_len, last, f0, f1, first, sa, ns);
@@ -415,7 +434,8 @@ router_proj_persist_kernel(const __grid_constant__ CUtensorMap tmx, const __grid
             for (int t = 0; t < npro; ++t) {
                 pro_item[t] = c.item;
                 pro_slab[t] = c.slab;
-                load_boxes<Cfg>(smem + t * Cfg::STAGE, &full_bar[t], &tmx, &tmw, c.item, c.slab, a, 1, true);
+                load_boxes<Cfg>(smem + t * Cfg::STAGE, &full_bar[t], &tmx, &tmw, c.item, c.slab, a, 1, true,
+                                GATE ? wsg_ring + t * Cfg::WSG : nullptr);
                 c.advance(f0, f1, first, sa, ns);
             }
             pdl_wait();
@@ -425,12 +445,86 @@ router_proj_persist_kernel(const __grid_constant__ CUtensorMap tmx, const __grid
             uint32_t parity = 0;        // of the release that step t waits for: round t / NST - 1
             for (int t = npro; t < T; ++t) {
                 mbar_wait(&empty_bar[slot], parity, a.err, 0x16);
-                load_boxes<Cfg>(smem + slot * Cfg::STAGE, &full_bar[slot], &tmx, &tmw, c.item, c.slab, a, 3, true);
+                load_boxes<Cfg>(smem + slot * Cfg::STAGE, &full_bar[slot], &tmx, &tmw, c.item, c.slab, a, 3, true,
+                                GATE ? wsg_ring + slot * Cfg::WSG : nullptr);
                 c.advance(f0, f1, first, sa, ns);
                 if (++slot == NST) {
                     slot = 0;
                     parity ^= 1u;
                 }
+            }
+        } else if (GATE && (warp == PT_WARPS + 1 || warp == PT_WARPS + 2)) {
+            // the shared gate: lane L of gate warp q owns token row 32 q + L
+            // of the tile and all 8 partition chains of the half for it, on
+            // the items of the first expert tile; it reads every stage, so it
+            // releases every stage
+            const int q = warp - PT_WARPS - 1, t = 32 * q + lane;
+            pdl_wait();
+            const unsigned int done = head_done(load_volatile(a.epoch));
+            unsigned int *my_flag = a.flags + (size_t)b * kPersistFlagsPerCta + PT_WARPS + q;
+            if (h_len > 0 && lane == 0 && load_volatile(my_flag) == done) *my_flag = ~done;
+            float gp[PT_WARPS];
+            int slot = 0;
+            uint32_t phase = 0;
+            auto run_g = [&](int item, int s_begin, int s_end) {
+                const int g = item & 1, tile = item >> 1;
+                const bool gitem = tile % a.n_et == 0 && (tile / a.n_et) * PT_M + 32 * q < a.M;
+                // (a stage of a first-expert-tile item carries the w_sg slice
+                // whatever this warp's rows; rows past M only skip the work)
+                for (int s = s_begin; s < s_end; ++s) {
+                    mbar_wait(&full_bar[slot], phase, a.err, 0x17);
+                    if (gitem)
+                        gate_rows_step<Cfg, InT>(gp, smem + slot * Cfg::STAGE, t, s, g, wsg_ring + slot * Cfg::WSG, a.H);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty_bar[slot]);
+                    if (++slot == NST) {
+                        slot = 0;
+                        phase ^= 1u;
+                    }
+                }
+            };
+            auto zero_g = [&]() {
+#pragma unroll
+                for (int p = 0; p < PT_WARPS; ++p) gp[p] = 0.0f;
+            };
+            // levels 1-3 of the pairwise tree over the half's partitions
+            auto store_g = [&](int item) {
+                const int g = item & 1, tile = item >> 1;
+                const int m = (tile / a.n_et) * PT_M + t;
+                if (tile % a.n_et == 0 && m < a.M)
+                    a.gpart[(size_t)g * a.M + m] = ((gp[0] + gp[1]) + (gp[2] + gp[3])) + ((gp[4] + gp[5]) + (gp[6] + gp[7]));
+            };
+            float *gho = a.ghandoff + ((size_t)b * 2 + q) * (PT_WARPS * 32);
+            if (h_len > 0) {
+                zero_g();
+                run_g(last, 0, h_len);
+                if ((last >> 1) % a.n_et == 0) {
+                    const uint64_t pol = l2_evict_first_policy();
+#pragma unroll
+                    for (int p = 0; p < PT_WARPS; ++p) st_evict_first(gho + p * 32 + lane, gp[p], pol);
+                    __threadfence();
+                    __syncwarp();
+                    if (lane == 0) st_release(my_flag, done);
+                }
+            }
+            for (int it = f0; it < f1; ++it) {
+                zero_g();
+                run_g(it, 0, ns);
+                store_g(it);
+            }
+            if (sa > 0) {
+                const bool gcont = (first >> 1) % a.n_et == 0;
+                const float *gprev = a.ghandoff + ((size_t)(b - 1) * 2 + q) * (PT_WARPS * 32);
+                zero_g();
+                if (gcont) {
+                    wait_flag(a.flags + (size_t)(b - 1) * kPersistFlagsPerCta + PT_WARPS + q, done, 0x18);
+#pragma unroll
+                    for (int p = 0; p < PT_WARPS; ++p) gp[p] = __ldcg(gprev + p * 32 + lane);
+                }
+                run_g(first, sa, ns);
+                store_g(first);
+                if (gcont && (reinterpret_cast<uintptr_t>(gprev) & 127u) == 0 && lane < PT_WARPS)
+                    asm volatile("discard.global.L2 [%0], 128;" ::"l"(gprev + lane * 32) : "memory");
             }
         }
         return;
@@ -442,21 +536,17 @@ router_proj_persist_kernel(const __grid_constant__ CUtensorMap tmx, const __grid
     // the epoch of this call; a flag equal to head_done(epoch) marks a
     // finished head
     const unsigned int done = head_done(load_volatile(a.epoch));
-    unsigned int *my_flag = a.flags + (size_t)b * PT_WARPS + warp;
+    unsigned int *my_flag = a.flags + (size_t)b * kPersistFlagsPerCta + warp;
     if (h_len > 0 && lane == 0 && load_volatile(my_flag) == done)
         *my_flag = ~done;      // left over, and happens to match: not this call's
 
     float acc[16][8];
-    float gacc0 = 0.0f, gacc1 = 0.0f;      // GATE: this lane's two tokens' chains
-    const int gt0 = tg + 8 * eg;            // GATE: the first of them (the second is gt0 + 4)
-    int gbuf = 0;                           // GATE: the gate tree's buffer (alternates)
     int slot = 0;
     uint32_t phase = 0;
     // the slabs [s_begin, s_end) of `item` into acc
     auto run = [&](int item, int s_begin, int s_end) {
         const int g = item & 1, tile = item >> 1;
         const bool live = tg < a.M - (tile / a.n_et) * PT_M;   // some of this lane's tokens exist
-        const bool gitem = GATE && tile % a.n_et == 0;
         for (int s = s_begin; s < s_end; ++s) {
             mbar_wait(&full_bar[slot], phase, a.err, 0x14);
             if (live && kSlab * s + kBlk * (8 * g + warp) < a.H) {
@@ -466,15 +556,6 @@ router_proj_persist_kernel(const __grid_constant__ CUtensorMap tmx, const __grid
                     pblock_f32(acc, st + bx * Cfg::XBOX, st + Cfg::XOP + bx * Cfg::WBOX, pc, tg, eg);
                 else
                     pblock_bf16(acc, st + bx * Cfg::XBOX, st + Cfg::XOP + bx * Cfg::WBOX, pc, tg, eg);
-                if (GATE && gitem) {
-                    const int hw = kSlab * s + kBlk * (8 * g + warp);
-                    if constexpr (sizeof(InT) == 4)
-                        gate_f32(gacc0, gacc1, st + bx * Cfg::XBOX, pc, gt0,
-                                 static_cast<const float *>(a.w_sg) + hw);
-                    else
-                        gate_bf16(gacc0, gacc1, st + bx * Cfg::XBOX, pc, gt0,
-                                  static_cast<const __nv_bfloat16 *>(a.w_sg) + hw);
-                }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty_bar[slot]);
@@ -489,37 +570,12 @@ router_proj_persist_kernel(const __grid_constant__ CUtensorMap tmx, const __grid
         for (int j = 0; j < 16; ++j)
 #pragma unroll
             for (int i = 0; i < 8; ++i) acc[j][i] = 0.0f;
-        gacc0 = 0.0f;
-        gacc1 = 0.0f;
     };
     // the item's group sums for its half of the partitions
     auto finish = [&](int item) {
         const int g = item & 1, tile = item >> 1;
         const int m0 = (tile / a.n_et) * PT_M, e0 = (tile % a.n_et) * PT_E;
         float *part = a.part + (size_t)g * a.M * a.E;
-        if (GATE && tile % a.n_et == 0) {
-            // the gate's 8 partials of every token meet in shared memory, and
-            // warp 0 adds them by the three lower levels of the pairwise tree.
-            // The buffers alternate: a buffer is written again only after
-            // every warp has passed the next gate tree's barrier, which warp 0
-            // reaches after its reads of this one.
-            float *gb = gtree + gbuf * (PT_WARPS * PT_M);
-            gb[warp * PT_M + gt0] = gacc0;
-            gb[warp * PT_M + gt0 + 4] = gacc1;
-            named_sync(1, PT_WARPS * 32);
-            if (warp == 0) {
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int t = lane + 32 * h;
-                    float p[PT_WARPS];
-#pragma unroll
-                    for (int w = 0; w < PT_WARPS; ++w) p[w] = gb[w * PT_M + t];
-                    const float s = ((p[0] + p[1]) + (p[2] + p[3])) + ((p[4] + p[5]) + (p[6] + p[7]));
-                    if (m0 + t < a.M) a.gpart[(size_t)g * a.M + m0 + t] = s;
-                }
-            }
-            gbuf ^= 1;
-        }
         switch (warp) {
         case 0: tree_and_store<0>(acc, tree, lane, part, a.M, a.E, m0, e0, tg, eg); break;
         case 1: tree_and_store<1>(acc, tree, lane, part, a.M, a.E, m0, e0, tg, eg); break;
@@ -541,11 +597,6 @@ router_proj_persist_kernel(const __grid_constant__ CUtensorMap tmx, const __grid
         for (int j = 0; j < 16; ++j)
 #pragma unroll
             for (int i = 0; i < 8; ++i) st_evict_first(ho + (j * 8 + i) * 32 + lane, acc[j][i], pol);
-        if (GATE && (last >> 1) % a.n_et == 0) {
-            float *gho = a.ghandoff + ((size_t)b * PT_WARPS + warp) * 64;
-            st_evict_first(gho + lane, gacc0, pol);
-            st_evict_first(gho + 32 + lane, gacc1, pol);
-        }
         __threadfence();
         __syncwarp();
         if (lane == 0) st_release(my_flag, done);
@@ -556,29 +607,12 @@ router_proj_persist_kernel(const __grid_constant__ CUtensorMap tmx, const __grid
         finish(it);
     }
     if (sa > 0) {                        // the continuation of the previous CTA's head
-        const unsigned int *fl = a.flags + (size_t)(b - 1) * PT_WARPS + warp;
-        if (ld_acquire(fl) != done) {
-            const uint64_t t0 = global_ns();
-            while (ld_acquire(fl) != done) {
-                if (load_volatile(a.err) != 0u) break;
-                if (global_ns() - t0 > kWaitLimitNs) {
-                    report_error(a.err, 5u, 0x15);
-                    break;
-                }
-                __nanosleep(256);
-            }
-        }
+        wait_flag(a.flags + (size_t)(b - 1) * kPersistFlagsPerCta + warp, done, 0x15);
         const float *ho = a.handoff + ((size_t)(b - 1) * PT_WARPS + warp) * PT_SLOT;
 #pragma unroll
         for (int j = 0; j < 16; ++j)
 #pragma unroll
             for (int i = 0; i < 8; ++i) acc[j][i] = __ldcg(ho + (j * 8 + i) * 32 + lane);
-        const bool gcont = GATE && (first >> 1) % a.n_et == 0;
-        const float *gho = a.ghandoff + ((size_t)(b - 1) * PT_WARPS + warp) * 64;
-        if (gcont) {
-            gacc0 = __ldcg(gho + lane);
-            gacc1 = __ldcg(gho + 32 + lane);
-        }
         run(first, sa, ns);
         finish(first);
         // every value read from the hand-off has been used by now: drop its
@@ -588,8 +622,6 @@ router_proj_persist_kernel(const __grid_constant__ CUtensorMap tmx, const __grid
 #pragma unroll
             for (int r = 0; r < PT_VALS / 32; ++r)
                 asm volatile("discard.global.L2 [%0], 128;" ::"l"(ho + (r * 32 + lane) * 32) : "memory");
-            if (gcont && lane < 2)
-                asm volatile("discard.global.L2 [%0], 128;" ::"l"(gho + 32 * lane) : "memory");
         }
     }
 }

@@ -70,7 +70,7 @@ __device__ __forceinline__ void warp_select(float (&v)[EPLM], int lane, int epl,
         }
     }
 
-    float l0 = 0.0f, den = 0.0f, my_e = 0.0f, v_sel_min = 0.0f, v_rej_max = 0.0f;
+    float l0 = 0.0f, my_v = 0.0f, v_sel_min = 0.0f, v_rej_max = 0.0f;
     int my_id = 0;
     for (int r = 0; r <= k; ++r) {
         const uint32_t bk = key[0];
@@ -101,14 +101,17 @@ __device__ __forceinline__ void warp_select(float (&v)[EPLM], int lane, int epl,
             break;
         }
         if (r == 0) l0 = wv;
-        const float ex = expf(wv - l0);
-        den += ex;                           // rank order
-        if (lane == r) {
-            my_e = ex;
+        if (lane == r) {                     // lane r keeps rank r
+            my_v = wv;
             my_id = (int)win;
         }
         v_sel_min = wv;
     }
+    // softmax over the selected: each of lanes 0..k-1 takes its rank's
+    // exponential once; the denominator adds them in rank order
+    const float my_e = lane < k ? expf(my_v - l0) : 0.0f;
+    float den = 0.0f;
+    for (int r = 0; r < k; ++r) den += __shfl_sync(0xFFFFFFFFu, my_e, r);
     if (lane < k) {
         ids[m * k + lane] = my_id;
         if (weights) weights[m * k + lane] = my_e / den;

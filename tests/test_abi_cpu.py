@@ -85,10 +85,10 @@ def test_router_workspace_bytes(lib):
     assert lib.bi_router_workspace_bytes(129, 256) == 129 * 256 * 64
     assert lib.bi_router_workspace_bytes(960, 256) == 64 * 960 * 256   # 120 items: below the persistent plan
     # persistent plan (at least 128 items of 64 x 64 x 8 partitions): epoch
-    # and flags (8 KB), 128 KB of hand-off and 2 KB of gate hand-off per CTA
+    # and flags (16 KB), 128 KB of hand-off and 2 KB of gate hand-off per CTA
     # for at most 160 CTAs, then the two halves' group sums 8*M*E and the
     # gate's 8*M
-    fixed = 8192 + 160 * 128 * 1024 + 160 * 2048
+    fixed = 16384 + 160 * 128 * 1024 + 160 * 2048
     assert lib.bi_router_workspace_bytes(1024, 256) == fixed + 8 * 1024 * 256 + 8 * 1024
     assert lib.bi_router_workspace_bytes(4096, 256) == fixed + 8 * 4096 * 256 + 8 * 4096
     assert lib.bi_router_workspace_bytes(8192, 512) == fixed + 8 * 8192 * 512 + 8 * 8192
