@@ -40,10 +40,13 @@ def f32_restatement(X, w):
     return r, orc.round_bf16(y.astype(np.float64))
 
 
-# short, ragged and long rows, f32 and bf16
+# short, ragged and long rows, f32 and bf16; a block's share of rows staged
+# in several chunks (M = 8000: 53 rows a block, 27 at a time; H = 32768: one
+# 128 KB row at a time)
 @pytest.mark.parametrize("M,H,dt", [(1, 2048, "f32"), (37, 264, "f32"), (300, 2048, "f32"), (19, 8, "f32"),
                                     (50, 2048, "bf16"), (33, 1032, "bf16"), (2000, 3328, "f32"),
-                                    (45, 3336, "f32"), (1300, 6656, "bf16"), (21, 6664, "bf16")])
+                                    (45, 3336, "f32"), (1300, 6656, "bf16"), (21, 6664, "bf16"),
+                                    (8000, 2048, "f32"), (400, 32768, "f32"), (700, 32768, "bf16")])
 def test_rmsnorm_parity_and_order(bi, M, H, dt):
     X = synth.tokens(70, 0, M, M, H)
     w = (1.0 + 0.1 * synth.shared_gate_weights(70, M, H)).astype(np.float32)
