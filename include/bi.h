@@ -118,8 +118,15 @@ typedef struct CUstream_st *bi_stream;
  * experts and sends them, through distributed shared memory, to the block
  * that selects their token.  Larger batches run the projection as 32 x 64
  * tiles whose 16 partitions may be spread over several thread blocks; their
- * group sums meet in `workspace` and the selection kernel adds them.  The
- * library allocates nothing: the caller passes the workspace.
+ * group sums meet in `workspace` and the selection kernel adds them.  From
+ * one 64 x 64 x 8-partition item per SM on, a persistent kernel gives every
+ * SM the same number of steps: where that cuts an item between two blocks,
+ * the second continues the first's FMA chains from accumulators handed over
+ * in `workspace` (the same operations in the same order).  The library
+ * allocates nothing: the caller passes the workspace, and its contents
+ * before a call do not matter (no clearing is needed, before the first call
+ * or between calls: the hand-off flags carry a per-call epoch that the call
+ * itself advances).
  *   workspace        device buffer, 16-byte aligned, owned by the caller; may
  *                    be NULL when workspace_bytes is 0
  *   workspace_bytes  its size; must be at least bi_router_workspace_bytes(M, E)
@@ -147,10 +154,14 @@ BI_API bi_status bi_router_topk(const void *x, const void *w_gate, bi_dtype in_d
 /*
  * bi_router_workspace_bytes -- the workspace bi_router_topk and
  * bi_router_gate_topk need for M rows and E experts, on any GPU: 0 for
- * M <= 112 with E <= 512 (the one-launch cluster router); otherwise the
- * largest group-sum area any of the tiled plans may use, 8*M*E bytes while
- * that is at most 64 MiB, never less than min(64*M*E, 16 MiB) and never more
- * than 64 MiB.  Host-only: touches no GPU.  Returns 0 for M <= 0.
+ * M <= 112 with E <= 512 (the one-launch cluster router); where some GPU may
+ * take the persistent projection (at least 128 items of 64 x 64 x 8
+ * partitions, 8*M*E at most 64 MiB), 16 KB + 160 * 130 KB (epoch, hand-off
+ * flags and accumulators of up to 160 blocks) + 8*M*E + 8*M (the two halves'
+ * group sums of the logits and of the gate); otherwise the largest
+ * group-sum area any of the tiled plans may use, 8*M*E bytes while that is
+ * at most 64 MiB, never less than min(64*M*E, 16 MiB) and never more than
+ * 64 MiB.  Host-only: touches no GPU.  Returns 0 for M <= 0.
  */
 BI_API size_t bi_router_workspace_bytes(int32_t M, int32_t E);
 
