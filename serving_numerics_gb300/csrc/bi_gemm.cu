@@ -22,7 +22,9 @@
 //   warps 2..5  epilogue: tcgen05.ld of their 32-lane quarter, bf16 pack,
 //               16-byte global stores; releases the accumulator buffer
 // Double-buffered accumulators let the epilogue of tile t overlap the MMAs
-// of tile t+1.  Tiles can be cut along N into 2, 4 or 8 pieces (N = 128, 64
+// of tile t+1.  Tiles are numbered N-fastest, so the blocks running at once
+// spread over many B tiles instead of all reading the same few (same-box
+// timings: 90.4 against 92.7 us at M = 4096, 162 against 173 us at 8192).  Tiles can be cut along N into 2, 4 or 8 pieces (N = 128, 64
 // or 32 tensor-core steps) without changing any element's arithmetic: each
 // output element still gets the same 16-deep steps in the same K order.
 // Pieces serve two cases: when the tiles are more than one wave but do not
@@ -89,7 +91,7 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant_
             for (int item = blockIdx.x; item < num_items; item += gridDim.x) {
                 int piece;
                 const int tile = item_tile(item, n_full, lg_s, piece);
-                const int mt = tile % m_tiles, nt = tile / m_tiles;
+                const int mt = tile / n_tiles, nt = tile % n_tiles;
                 const int n0 = nt * BN + (piece > 0 ? piece * pn : 0);
                 for (int kb = 0; kb < kblocks; ++kb) {
                     mbar_wait(&empty_bar[s], ph ^ 1u, err, 0x21);
@@ -139,7 +141,7 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant_
         for (int item = blockIdx.x; item < num_items; item += gridDim.x, ++tc) {
             int piece;
             const int tile = item_tile(item, n_full, lg_s, piece);
-            const int mt = tile % m_tiles, nt = tile / m_tiles;
+            const int mt = tile / n_tiles, nt = tile % n_tiles;
             const int nbase = nt * BN + (piece > 0 ? piece * pn : 0), nchunks = piece < 0 ? BN / 32 : pn / 32;
             const uint32_t b = tc & 1u, tph = (tc >> 1) & 1u;
             mbar_wait(&tfull_bar[b], tph, err, 0x24);
