@@ -348,6 +348,65 @@ BI_API bi_status bi_rmsnorm(const void *x, const void *w, bi_dtype dtype, int32_
                      void *y_out, float *rstd_out, bi_stream s);
 
 /*
+ * bi_attention_prefill -- batch-invariant causal attention for one prefill
+ * call over ragged requests (bf16 in, bf16 out, f32 arithmetic):
+ *
+ *   request r: queries q[q_offsets[r] .. q_offsets[r+1]), keys and values
+ *   k, v[kv_offsets[r] .. kv_offsets[r+1]); its q_len queries are the last
+ *   q_len positions of its kv_len-token context (a cached prefix, if any,
+ *   comes first), and query i (position kv_len - q_len + i) attends to keys
+ *   0 .. that position of its own request:
+ *
+ *     o[i, h]   = sum_j softmax_j( scale * q[i, h] . k[j, h / g] ) v[j, h / g]
+ *     lse[i, h] = log sum_j exp( scale * q[i, h] . k[j, h / g] )
+ *
+ *   with g = n_heads / n_kv_heads query heads per key/value head.
+ *
+ * [P3] "The physics of the cascade": the softmax's exponential stretches a
+ * one-ULP difference in the scores and the product with V spreads it over
+ * every feature, so attention is the next operation on the cascade path
+ * that must give a row the same bits whatever the batch.
+ *
+ * Invariance contract: each query row walks its own context in blocks of 64
+ * keys at fixed positions (block b = keys 64b .. 64b+63), in increasing
+ * order, up to the block holding its own position.  Per block: the scores
+ * as f32 tensor-core dot products over the 128 dimensions in 16-deep steps,
+ * in increasing order; the running maximum m of scale*log2(e)*score; the
+ * weights p = bf16_rne(exp2f(score*scale*log2(e) - m)); the running sum
+ * l = fmaf(l, a, pairwise sum of the block's 64 weights) with
+ * a = exp2f(m_old - m); the block's P.V as f32 tensor-core sums over the
+ * block's keys in 16-deep steps, in increasing order; the running output
+ * acc = fmaf(acc, a, block P.V).  Finally o = bf16_rne(acc / l) and
+ * lse = (m + log2f(l)) * ln 2.  So a row's bits depend only on its own
+ * query, its position and its request's keys and values: not on the
+ * other requests, on how many of its request's queries are in the call (a
+ * cached prefix, a chunked prefill), or on which query tile it falls in.
+ *
+ *   q           [Tq, n_heads, 128] bf16, Tq = q_offsets[n_req]
+ *   k, v        [Tkv, n_kv_heads, 128] bf16, Tkv = kv_offsets[n_req]
+ *   n_req       requests, >= 0
+ *   q_offsets   HOST [n_req + 1] int32: 0, then running sums of q_len
+ *   kv_offsets  HOST [n_req + 1] int32: 0, then running sums of kv_len;
+ *               0 <= q_len <= kv_len for every request (a request with
+ *               q_len == 0 is skipped)
+ *   n_heads, n_kv_heads  >= 1, n_heads a multiple of n_kv_heads,
+ *               n_heads <= BI_ATTN_MAX_HEADS
+ *   head_dim    must be 128 (else BI_ERR_UNSUPPORTED_SHAPE)
+ *   scale       finite, > 0 (usually 1 / sqrt(head_dim))
+ *   o           [Tq, n_heads, 128] bf16 output
+ *   lse         [Tq, n_heads] f32 natural-log sum of exponentials, or NULL
+ * All inputs must be finite.  Key and value rows past a request's end but
+ * inside the tensors are read (they belong to the next request) and get
+ * weight zero.  Tq == 0 returns BI_OK.  Nothing is allocated; the offsets
+ * are read before the call returns.
+ */
+#define BI_ATTN_MAX_HEADS 256
+BI_API bi_status bi_attention_prefill(const void *q, const void *k, const void *v, int32_t n_req,
+                                      const int32_t *q_offsets, const int32_t *kv_offsets, int32_t n_heads,
+                                      int32_t n_kv_heads, int32_t head_dim, float scale, void *o, float *lse,
+                                      bi_stream s);
+
+/*
  * bi_moe_expert_gemm -- the grouped expert projection that consumes the
  * router's choice: every token-slot (m, j) is one row through its expert,
  *

@@ -17,6 +17,7 @@ BI_OK, BI_ERR_INVALID_ARG, BI_ERR_UNSUPPORTED_SHAPE, BI_ERR_MISALIGNED, BI_ERR_C
 BI_F32, BI_BF16 = 0, 1
 BI_MAX_E, BI_MAX_K, BI_MAX_H, BI_MAX_HASH_RANGES = 1024, 32, 32768, 256
 BI_NOALLOC_SCRATCH_BYTES = 1 << 20
+BI_ATTN_MAX_HEADS = 256
 FNV64_BASIS = 0xCBF29CE484222325
 
 # name -> (restype, argtypes), mirroring include/bi.h
@@ -43,6 +44,7 @@ SIGNATURES = {
     "bi_moe_workspace_bytes": (C.c_size_t, [_I32, _I32, _I32, _I32, _I32]),
     "bi_moe_expert_gemm": (C.c_int, [_P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, C.c_size_t, _P]),
     "bi_prefix_split": (C.c_int, [_P, _I32, _I32, _P, _P]),
+    "bi_attention_prefill": (C.c_int, [_P, _P, _P, _I32, _P, _P, _I32, _I32, _I32, C.c_float, _P, _P, _P]),
 }
 
 BI_TREE_PAIRWISE = 1
@@ -250,6 +252,38 @@ def moe_expert_gemm(X, ids, weights, W, stream=None, want_y=True, want_out=True,
     out = torch.empty((M, N), dtype=torch.bfloat16, device=X.device) if want_out else None
     bi_moe_expert_gemm(X, ids, weights if want_out else None, W, M, k, E, N, K, Y, out, base, n, stream=stream)
     return {"Y": Y, "out": out}
+
+
+def _host_i32(a):
+    """A ctypes int32 array holding the values of a host sequence."""
+    vals = [int(v) for v in a]
+    return (C.c_int32 * max(len(vals), 1))(*vals)
+
+
+def bi_attention_prefill(q, k, v, n_req, q_offsets, kv_offsets, n_heads, n_kv_heads, head_dim, scale, o_out,
+                         lse_out=None, stream=None, check=True):
+    """q_offsets and kv_offsets are host sequences of n_req + 1 ints."""
+    st = load().bi_attention_prefill(_ptr(q), _ptr(k), _ptr(v), n_req, _host_i32(q_offsets),
+                                     _host_i32(kv_offsets), n_heads, n_kv_heads, head_dim, C.c_float(scale),
+                                     _ptr(o_out), _ptr(lse_out), _stream(stream))
+    if check:
+        _check(st, "bi_attention_prefill")
+    return st
+
+
+def attention_prefill(q, k, v, q_offsets, kv_offsets, scale: float, stream=None, want_lse=True):
+    """Allocate outputs with torch and run bi_attention_prefill.  q [Tq,
+    n_heads, 128], k and v [Tkv, n_kv_heads, 128], all bfloat16; offsets
+    host sequences (0, running sums).  Returns (o bf16 [Tq, n_heads, 128],
+    lse f32 [Tq, n_heads] or None)."""
+    import torch
+    Tq, nh, D = q.shape
+    nkv = k.shape[1]
+    o = torch.empty((Tq, nh, D), dtype=torch.bfloat16, device=q.device)
+    lse = torch.empty((Tq, nh), dtype=torch.float32, device=q.device) if want_lse else None
+    bi_attention_prefill(q, k, v, len(q_offsets) - 1, q_offsets, kv_offsets, nh, nkv, D, scale, o, lse,
+                         stream=stream)
+    return o, lse
 
 
 def selftest_fma_rate(iters: int, sink, packed: bool = False, stream=None) -> float:

@@ -16,7 +16,7 @@ from __future__ import annotations
 import numpy as np
 
 # stream ids keep every (workload, layer, tensor) draw independent
-_S_X, _S_W, _S_WSG, _S_A, _S_B, _S_LEN, _S_MISC = range(7)
+_S_X, _S_W, _S_WSG, _S_A, _S_B, _S_LEN, _S_MISC, _S_ATTN = range(8)
 
 
 def rng(seed: int, *path: int) -> np.random.Generator:
@@ -103,6 +103,33 @@ def gemm_b(seed: int, N: int, K: int, layer: int = 0) -> np.ndarray:
 # ---------------------------------------------------------------- mixed prefill
 def request_lengths(seed: int = 0, n: int = 16, lo: int = 5, hi: int = 300) -> np.ndarray:
     return rng(seed, _S_LEN).integers(lo, hi + 1, n)
+
+
+# ---------------------------------------------------------------- attention
+# The prefill attention workload: 16 query heads sharing 2 key/value heads of
+# dimension 128 (16 x 128 = the hidden size 2048 above), 4096 query tokens
+# in 8 requests of mixed length, five of them behind a cached prefix.
+ATTN_HEADS, ATTN_KV_HEADS, ATTN_D = 16, 2, 128
+ATTN_Q_LENS = (1024, 768, 512, 512, 384, 384, 256, 256)
+ATTN_PREFIX = (0, 2048, 1024, 0, 3072, 512, 0, 1536)
+
+
+def attention_offsets(q_lens, prefix):
+    """(q_offsets, kv_offsets) of requests with q_lens queries after
+    prefix cached tokens each: 0, then running sums."""
+    q = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    kv = np.concatenate([[0], np.cumsum(np.asarray(q_lens) + np.asarray(prefix))]).astype(np.int32)
+    return q, kv
+
+
+def attention_inputs(seed: int, Tq: int, Tkv: int, heads: int, kv_heads: int, D: int = ATTN_D):
+    """q [Tq, heads, D], k and v [Tkv, kv_heads, D] as bf16 bit patterns of
+    standard normal draws."""
+    g = rng(seed, _S_ATTN)
+    q = to_bf16_bits(g.standard_normal((Tq, heads, D)).astype(np.float32))
+    k = to_bf16_bits(g.standard_normal((Tkv, kv_heads, D)).astype(np.float32))
+    v = to_bf16_bits(g.standard_normal((Tkv, kv_heads, D)).astype(np.float32))
+    return q, k, v
 
 
 # ---------------------------------------------------------------- device pools

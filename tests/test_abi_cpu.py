@@ -230,3 +230,31 @@ def test_router_plan_validation(lib):
     assert lib.bi_router_plan(-1, 256, C.byref(x), C.byref(x), C.byref(x)) == 1
     assert lib.bi_router_plan(16, 0, C.byref(x), C.byref(x), C.byref(x)) == 1
     assert lib.bi_router_plan(16, 256, None, C.byref(x), C.byref(x)) == 1
+
+
+def _attn(lib, q=FAKE, k=FAKE, v=FAKE, qo=(0, 4), ko=(0, 9), nh=4, nkv=2, D=128, scale=0.088, o=FAKE,
+          lse=None):
+    n = len(qo) - 1
+    qa = (C.c_int32 * len(qo))(*qo) if qo is not None else None
+    ka = (C.c_int32 * len(ko))(*ko) if ko is not None else None
+    return lib.bi_attention_prefill(q, k, v, n, qa, ka, nh, nkv, D, C.c_float(scale), o, lse, None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(nh=0), 1), (dict(nkv=0), 1), (dict(nh=6, nkv=4), 1), (dict(scale=0.0), 1), (dict(scale=-1.0), 1),
+    (dict(scale=float("inf")), 1), (dict(scale=float("nan")), 1), (dict(D=64), 2), (dict(D=256), 2),
+    (dict(nh=512, nkv=2), 2), (dict(qo=(1, 4), ko=(1, 9)), 1), (dict(qo=(0, 10), ko=(0, 9)), 1),
+    (dict(qo=(0, 4, 2), ko=(0, 9, 12)), 1), (dict(qo=(0, 4, 6), ko=(0, 9, 8)), 1),
+    (dict(q=None), 1), (dict(k=None), 1), (dict(v=None), 1), (dict(o=None), 1),
+    (dict(q=MIS), 3), (dict(k=MIS), 3), (dict(v=MIS), 3), (dict(o=MIS), 3), (dict(lse=FAKE + 2), 3),
+])
+def test_attention_validation(lib, kw, want):
+    assert _attn(lib, **kw) == want
+
+
+def test_attention_empty_calls_are_noops(lib):
+    """No requests, or requests without queries: BI_OK before any CUDA call."""
+    assert _attn(lib, q=None, k=None, v=None, o=None, qo=(0,), ko=(0,)) == 0
+    assert _attn(lib, q=None, k=None, v=None, o=None, qo=(0, 0, 0), ko=(0, 5, 7)) == 0
+    assert lib.bi_attention_prefill(None, None, None, 1, None, None, 4, 2, 128, C.c_float(0.1), None, None,
+                                    None) == 1
