@@ -14,38 +14,45 @@
 // keys 64b .. 64b+63 of the context), from block 0 up to the block holding
 // the row's own position, and does the same arithmetic on each block:
 //
-//   s_j   = q . k_j               f32, on the tensor cores: d = 0..127 as
-//                                 eight 16-deep steps in increasing order
-//   bm    = max over visible j of s_j           (exact: order-free)
-//   m'    = max(m, bm * c)        c = scale * log2(e), m the running maximum
-//   p_j   = bf16_rne(exp2f(fmaf(s_j, c, -m')))  visible j, else 0
-//   l'    = fmaf(l, a, pairwise sum of the 64 widened p_j), a = exp2f(m - m')
-//   O_b   = sum_j p_j v_j         f32, on the tensor cores: four 16-deep
-//                                 steps over the block's keys, in order
-//   acc'  = fmaf(acc, a, O_b)     per output column
+//   s_j  = q . k_j                 f32 on the tensor cores: the 128
+//                                  dimensions as eight 16-deep steps, in
+//                                  increasing order; invisible keys -> -inf
+//   t    = c * max_j s_j           c = scale * log2(e) (max: order-free)
+//   if t > m + 8:                  the reference maximum moves (always on
+//                                  the first block, where m = -inf)
+//       a = 2^(m - t);  l = l * a;  O = O * a  (in tensor memory);  m = t
+//   p_j  = 2^(fmaf(s_j, c, -m))    ex2.approx.ftz, <= 2^8
+//   l    = l + (pairwise sum of the 64 f32 p_j)
+//   O    = O + sum_j bf16_rne(p_j) v_j   f32 on the tensor cores: four
+//                                  16-deep steps over the block's keys in
+//                                  increasing order, added to O in place
 //
-// and finally o = bf16_rne(acc / l), lse = (m + log2f(l)) * ln(2).  A
-// block that holds no key the row can see changes nothing (a = 1, the p_j
-// are 0, O_b is a sum of zero products), so a row's bits are the same
+// and finally o = bf16_rne(O * (1/l)), lse = (m + log2f(l)) * ln(2).  The
+// reference maximum only moves when a block's maximum exceeds it by more
+// than 2^8 in the exponent, so the rescaling is rare after the first block;
+// whether it moves depends only on the row's own scores.  A block that holds
+// no key the row can see changes nothing (its maximum is -inf, its p_j are
+// 0, its products with V are zeros added to O), so a row's bits are the same
 // whichever query tile it falls in, whatever tile boundaries the batch, a
 // cached prefix or a chunked prefill put around it, and whatever else is in
-// the launch.  Which tile a row lands in, how many tiles run and in which
-// order never enter its arithmetic.
+// the launch.
 //
-// Structure (one CTA per query tile of 128 rows and one head, 192 threads):
-//   warp 0      TMA producer: the Q tile once (two 64-column boxes, 128-byte
-//               swizzle), then K and V of each key block into a ring of 4
-//               stages (32 KB each)
-//   warp 1      allocates 512 tensor-memory columns (two S buffers of
-//               128 x 64 f32, two O buffers of 128 x 128 f32); one lane
-//               issues S = Q K^T for block b+1 before O_b = P_b V_b, so the
-//               tensor cores compute the next scores while the softmax of
-//               the current block runs
-//   warps 2..5  one thread per query row: the softmax of block b (P_b as
-//               bf16 into shared memory in the swizzled K-major layout the
-//               next MMA reads), then the correction of block b-1 (O_{b-1}
-//               from tensor memory folded into registers), then the output
-// V is read by the PV product straight from its TMA box as an MN-major
+// Structure (one CTA per query tile of 128 rows and NT = 2 query heads that
+// share one key/value head -- or NT = 1 head when the heads per key/value
+// head are odd -- with 64 + 128 NT threads):
+//   warp 0      TMA producer: the NT Q tiles once (two 64-column boxes
+//               each, 128-byte swizzle), then K and V of each key block
+//               into a ring of stages (32 KB each), shared by the NT heads
+//   warp 1      allocates 256 NT tensor-memory columns (per head: two S
+//               buffers of 128 x 64 f32 and the O accumulator of 128 x 128
+//               f32); one lane issues S = Q K^T of block b for every head
+//               before P V of block b-1, so the tensor cores compute the
+//               next scores while the softmax of the current block runs
+//   warps 2..   one warpgroup per head, one thread per query row: the
+//               softmax of each block (P as bf16 into shared memory in the
+//               swizzled K-major layout the P V product reads), the rare
+//               rescaling of its O row, and the output
+// V is read by the P V product straight from its TMA box as an MN-major
 // operand (keys along K, head dimension contiguous), so V needs no
 // transpose.  Every wait on an mbarrier is bounded (about 2 s); on expiry
 // the kernel records BI_ERR_TIMEOUT in the device error word and carries on.
@@ -65,18 +72,26 @@ namespace {
 constexpr int AT_D = 128;                          // head dimension
 constexpr int AT_BQ = 128;                         // query rows per tile (tensor-memory lanes)
 constexpr int AT_BKV = 64;                         // keys per block
-constexpr int AT_STAGES = 4;
+constexpr float AT_TAU = 8.0f;                     // the reference maximum moves past this growth
 constexpr int AT_Q_BOX = AT_BQ * 64 * 2;           // 16 KB: 128 rows x 64 dims
 constexpr int AT_KV_BOX = AT_BKV * 64 * 2;         // 8 KB: 64 keys x 64 dims
 constexpr int AT_Q_BYTES = 2 * AT_Q_BOX;
 constexpr int AT_STAGE_BYTES = 4 * AT_KV_BOX;      // K (two boxes), then V (two boxes)
 constexpr int AT_P_BYTES = AT_BQ * AT_BKV * 2;     // 16 KB: 128 rows x 64 keys bf16
-constexpr int AT_SMEM = AT_Q_BYTES + AT_STAGES * AT_STAGE_BYTES + 2 * AT_P_BYTES + 1024;
-constexpr int AT_THREADS = 192;
+constexpr uint32_t AT_HEAD_COLS = 256;             // tensor-memory columns per head
 constexpr uint32_t AT_S_COL = 0;                   // S buffers: columns 0..63 and 64..127
-constexpr uint32_t AT_O_COL = 128;                 // O buffers: 128..255 and 256..383
-constexpr uint32_t AT_TMEM_COLS = 512;
-static_assert(AT_SMEM <= 227 * 1024, "shared memory");
+constexpr uint32_t AT_O_COL = 128;                 // O: 128..255
+
+template <int NT>
+struct AttnCfg {
+    static constexpr int STAGES = NT == 2 ? 3 : 4;
+    static constexpr int THREADS = 64 + 128 * NT;
+    static constexpr int KV_OFF = NT * AT_Q_BYTES;
+    static constexpr int P_OFF = KV_OFF + STAGES * AT_STAGE_BYTES;
+    static constexpr int SMEM = P_OFF + NT * 2 * AT_P_BYTES + 1024;
+    static constexpr uint32_t TMEM_COLS = AT_HEAD_COLS * NT;
+    static_assert(SMEM <= 227 * 1024, "shared memory");
+};
 
 // One query tile: up to 128 consecutive queries of one request.
 struct AttnTile {
@@ -120,22 +135,77 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                  : "memory");
 }
 
-__global__ void __launch_bounds__(AT_THREADS, 1)
+// 2^x by the multi-function unit (flushes subnormal results to zero; 2^-inf = 0)
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Two independent f32 fused multiply-adds (each rounded once) in one instruction.
+__device__ __forceinline__ void ffma2(float &d0, float &d1, float a0, float a1, float b0, float b1, float c0, float c1)
+{
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
+// 32 lanes x 32 consecutive f32 columns without waiting (pair with tmem_ld_wait).
+__device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t *r)
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// 32 lanes x 32 consecutive f32 columns from registers (thread t writes lane t).
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t *r)
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+template <int NT>
+__global__ void __launch_bounds__(AttnCfg<NT>::THREADS, 1)
 attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                     const __grid_constant__ CUtensorMap tmv, const __grid_constant__ AttnTable tab,
                     __nv_bfloat16 *__restrict__ O, float *__restrict__ lse, int n_heads, int group, float c,
                     unsigned int *err)
 {
+    using Cfg = AttnCfg<NT>;
+    constexpr int NS = Cfg::STAGES;
     pdl_trigger();
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t q_bar, kv_full[AT_STAGES], kv_empty[AT_STAGES], s_full[2], s_empty[2],
-        p_full[2], o_full[2], o_empty[2];
+    __shared__ __align__(8) uint64_t q_bar, kv_full[NS], kv_empty[NS], s_full[NT][2], s_empty[NT][2],
+        p_full[NT][2], o_done[NT][2];
     __shared__ uint32_t tmem_base_sh;
     uint8_t *smem = smem_align1024(smem_raw);
-    uint8_t *sq = smem, *skv = smem + AT_Q_BYTES, *sp = skv + AT_STAGES * AT_STAGE_BYTES;
+    uint8_t *sq = smem, *skv = smem + Cfg::KV_OFF, *sp = smem + Cfg::P_OFF;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int ti = blockIdx.x / n_heads, h = blockIdx.x % n_heads, hk = h / group;
+    const int pairs = n_heads / NT;
+    const int ti = blockIdx.x / pairs, h0 = (blockIdx.x % pairs) * NT, hk = h0 / group;
     const AttnTile tile = tab.t[ti];
     const int nb = attn_blocks(tile.pos0, tile.rows);
 
@@ -144,20 +214,21 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         prefetch_tmap(&tmk);
         prefetch_tmap(&tmv);
         mbar_init(&q_bar, 1);
-        for (int s = 0; s < AT_STAGES; ++s) {
+        for (int s = 0; s < NS; ++s) {
             mbar_init(&kv_full[s], 1);
             mbar_init(&kv_empty[s], 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&s_full[b], 1);
-            mbar_init(&s_empty[b], 4);
-            mbar_init(&p_full[b], 4);
-            mbar_init(&o_full[b], 1);
-            mbar_init(&o_empty[b], 4);
+        for (int t = 0; t < NT; ++t) {
+            for (int b = 0; b < 2; ++b) {
+                mbar_init(&s_full[t][b], 1);
+                mbar_init(&s_empty[t][b], 4);
+                mbar_init(&p_full[t][b], 4);
+                mbar_init(&o_done[t][b], 1);
+            }
         }
         mbar_init_fence();
     }
-    if (warp == 1) tmem_alloc(&tmem_base_sh, AT_TMEM_COLS);
+    if (warp == 1) tmem_alloc(&tmem_base_sh, Cfg::TMEM_COLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -167,12 +238,14 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
 
     if (warp == 0) {
         if (lane == 0) {   // TMA producer
-            mbar_arrive_expect_tx(&q_bar, (uint32_t)AT_Q_BYTES);
-            tma_load_3d(sq, &tmq, &q_bar, 0, h, tile.q0);
-            tma_load_3d(sq + AT_Q_BOX, &tmq, &q_bar, 64, h, tile.q0);
+            mbar_arrive_expect_tx(&q_bar, (uint32_t)(NT * AT_Q_BYTES));
+            for (int t = 0; t < NT; ++t) {
+                tma_load_3d(sq + t * AT_Q_BYTES, &tmq, &q_bar, 0, h0 + t, tile.q0);
+                tma_load_3d(sq + t * AT_Q_BYTES + AT_Q_BOX, &tmq, &q_bar, 64, h0 + t, tile.q0);
+            }
             for (int b = 0; b < nb; ++b) {
-                const int st = b % AT_STAGES;
-                const uint32_t ph = (uint32_t)(b / AT_STAGES) & 1u;
+                const int st = b % NS;
+                const uint32_t ph = (uint32_t)(b / NS) & 1u;
                 mbar_wait(&kv_empty[st], ph ^ 1u, err, 0x61);
                 uint8_t *dst = skv + st * AT_STAGE_BYTES;
                 const int key = tile.kv0 + b * AT_BKV;
@@ -185,145 +258,185 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         }
     } else if (warp == 1) {
         if (lane == 0) {   // MMA issuer
-            const uint32_t id_s = idesc_n(AT_BKV), id_o = idesc_n(AT_D) | (1u << 16);   // B of PV MN-major
+            const uint32_t id_s = idesc_n(AT_BKV), id_o = idesc_n(AT_D) | (1u << 16);   // B of P V MN-major
             mbar_wait(&q_bar, 0, err, 0x62);
             tc_fence_after();
-            const uint32_t qa = smem_u32(sq);
             for (int b = 0; b <= nb; ++b) {
-                if (b < nb) {   // S_b = Q K_b^T
-                    const int st = b % AT_STAGES;
+                if (b < nb) {   // S_b = Q K_b^T for every head
+                    const int st = b % NS;
                     const uint32_t sb = (uint32_t)b & 1u, use = ((uint32_t)b >> 1) & 1u;
-                    mbar_wait(&kv_full[st], (uint32_t)(b / AT_STAGES) & 1u, err, 0x63);
-                    mbar_wait(&s_empty[sb], use ^ 1u, err, 0x64);
-                    tc_fence_after();
+                    mbar_wait(&kv_full[st], (uint32_t)(b / NS) & 1u, err, 0x63);
                     const uint32_t ka = smem_u32(skv + st * AT_STAGE_BYTES);
-                    const uint32_t d = tmem_base + AT_S_COL + sb * AT_BKV;
 #pragma unroll
-                    for (int half = 0; half < 2; ++half)
+                    for (int t = 0; t < NT; ++t) {
+                        mbar_wait(&s_empty[t][sb], use ^ 1u, err, 0x64);
+                        tc_fence_after();
+                        const uint32_t qa = smem_u32(sq + t * AT_Q_BYTES);
+                        const uint32_t d = tmem_base + t * AT_HEAD_COLS + AT_S_COL + sb * AT_BKV;
 #pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            umma_bf16(d, sw128_desc(qa + half * AT_Q_BOX + k * 32),
-                                      sw128_desc(ka + half * AT_KV_BOX + k * 32), id_s, (half | k) != 0 ? 1u : 0u);
-                    umma_commit(&s_full[sb]);
+                        for (int half = 0; half < 2; ++half)
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                umma_bf16(d, sw128_desc(qa + half * AT_Q_BOX + k * 32),
+                                          sw128_desc(ka + half * AT_KV_BOX + k * 32), id_s,
+                                          (half | k) != 0 ? 1u : 0u);
+                        umma_commit(&s_full[t][sb]);
+                    }
                 }
-                if (b >= 1) {   // O_{b-1} = P_{b-1} V_{b-1}
-                    const int pb = b - 1, st = pb % AT_STAGES;
+                if (b >= 1) {   // O += P_{b-1} V_{b-1} for every head
+                    const int pb = b - 1, st = pb % NS;
                     const uint32_t ob = (uint32_t)pb & 1u, use = ((uint32_t)pb >> 1) & 1u;
-                    mbar_wait(&p_full[ob], use, err, 0x65);
-                    mbar_wait(&o_empty[ob], use ^ 1u, err, 0x66);
-                    tc_fence_after();
-                    const uint32_t pa = smem_u32(sp + ob * AT_P_BYTES);
                     const uint32_t va = smem_u32(skv + st * AT_STAGE_BYTES + 2 * AT_KV_BOX);
-                    const uint32_t d = tmem_base + AT_O_COL + ob * AT_D;
 #pragma unroll
-                    for (int k = 0; k < AT_BKV / 16; ++k)
-                        umma_bf16(d, sw128_desc(pa + k * 32), sw128_mn_desc(va + k * 2048), id_o, k != 0 ? 1u : 0u);
-                    umma_commit(&o_full[ob]);
+                    for (int t = 0; t < NT; ++t) {
+                        mbar_wait(&p_full[t][ob], use, err, 0x65);
+                        tc_fence_after();
+                        const uint32_t pa = smem_u32(sp + (t * 2 + ob) * AT_P_BYTES);
+                        const uint32_t d = tmem_base + t * AT_HEAD_COLS + AT_O_COL;
+#pragma unroll
+                        for (int k = 0; k < AT_BKV / 16; ++k)
+                            umma_bf16(d, sw128_desc(pa + k * 32), sw128_mn_desc(va + k * 2048), id_o,
+                                      (pb | k) != 0 ? 1u : 0u);
+                        umma_commit(&o_done[t][ob]);
+                    }
                     umma_commit(&kv_empty[st]);   // K and V of block pb no longer read
                 }
             }
         }
     } else {
-        // softmax and correction: warp w may read tensor-memory lanes 32*(w%4) .. +31
-        const int quad = warp & 3, row = quad * 32 + lane;
+        // softmax: warpgroup t = head h0 + t; warp w may read tensor-memory
+        // lanes 32*(w%4) .. +31
+        const int t = (warp - 2) >> 2, quad = warp & 3, row = quad * 32 + lane;
         const int pos = tile.pos0 + row;
-        const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-        float m = -INFINITY, l = 0.f, a_prev = 0.f;
-        float acc[AT_D];
-#pragma unroll
-        for (int i = 0; i < AT_D; ++i) acc[i] = 0.f;
-
-        auto correct = [&](int cb, float a) {
-            const uint32_t ob = (uint32_t)cb & 1u, use = ((uint32_t)cb >> 1) & 1u;
-            mbar_wait(&o_full[ob], use, err, 0x67);
+        const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + t * AT_HEAD_COLS;
+        float m = -INFINITY, l = 0.f;
+        // Until P V of block n is done.  Block n's completion is phase n/2
+        // of barrier n%2; every wait names the exact phase, and the caller
+        // has already seen block n-2 complete (the wait for the P buffer),
+        // so neither barrier is ever two phases from the one awaited.
+        auto wait_pv = [&](int n) {
+            mbar_wait(&o_done[t][n & 1], ((uint32_t)n >> 1) & 1u, err, 0x67);
             tc_fence_after();
-#pragma unroll
-            for (int ch = 0; ch < AT_D / 32; ++ch) {
-                uint32_t r[32];
-                tmem_ld32(tmem_base + lane_off + AT_O_COL + ob * AT_D + ch * 32, r);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) acc[ch * 32 + i] = fmaf(acc[ch * 32 + i], a, __uint_as_float(r[i]));
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&o_empty[ob]);
         };
 
 #pragma unroll 1
         for (int b = 0; b < nb; ++b) {
             const uint32_t sb = (uint32_t)b & 1u, use = ((uint32_t)b >> 1) & 1u;
-            mbar_wait(&s_full[sb], use, err, 0x68);
+            mbar_wait(&s_full[t][sb], use, err, 0x68);
             tc_fence_after();
-            uint32_t s[AT_BKV];
-            tmem_ld32(tmem_base + lane_off + AT_S_COL + sb * AT_BKV, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
-            tmem_ld32(tmem_base + lane_off + AT_S_COL + sb * AT_BKV + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+            float s[AT_BKV];
+            tmem_ld32_nowait(tbase + AT_S_COL + sb * AT_BKV, reinterpret_cast<uint32_t *>(&s[0]));
+            tmem_ld32_nowait(tbase + AT_S_COL + sb * AT_BKV + 32, reinterpret_cast<uint32_t *>(&s[32]));
+            tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&s_empty[sb]);
+            if (lane == 0) mbar_arrive(&s_empty[t][sb]);
 
-            const int nvis = pos - b * AT_BKV + 1;        // keys of this block the row sees (clamped below)
-            float bm = -INFINITY;
+            const int nvis = pos - b * AT_BKV + 1;       // keys of this block the row sees
+            if (nvis < AT_BKV) {
 #pragma unroll
-            for (int j = 0; j < AT_BKV; ++j)
-                if (j < nvis) bm = fmaxf(bm, __uint_as_float(s[j]));
-            const float m_new = fmaxf(m, bm * c);
-            const float mu = m_new == -INFINITY ? 0.f : m_new;
-            const float a = exp2f(m - mu);
-
-            // P_b as bf16, and the pairwise sum of the rounded values
-            uint32_t pk[AT_BKV / 2];
-#pragma unroll
-            for (int j = 0; j < AT_BKV; j += 2) {
-                const float p0 = j < nvis ? exp2f(fmaf(__uint_as_float(s[j]), c, -mu)) : 0.f;
-                const float p1 = j + 1 < nvis ? exp2f(fmaf(__uint_as_float(s[j + 1]), c, -mu)) : 0.f;
-                pk[j / 2] = pack_bf16x2(__float_as_uint(p0), __float_as_uint(p1));
+                for (int j = 0; j < AT_BKV; ++j)
+                    if (j >= nvis) s[j] = -INFINITY;
             }
-            float t[AT_BKV / 2];
+            float mx[AT_BKV / 2];
 #pragma unroll
-            for (int i = 0; i < AT_BKV / 2; ++i) t[i] = bf16lo(pk[i]) + bf16hi(pk[i]);
+            for (int i = 0; i < AT_BKV / 2; ++i) mx[i] = fmaxf(s[2 * i], s[2 * i + 1]);
 #pragma unroll
             for (int w = AT_BKV / 4; w >= 1; w >>= 1)
 #pragma unroll
-                for (int i = 0; i < w; ++i) t[i] = t[2 * i] + t[2 * i + 1];
-            l = fmaf(l, a, t[0]);
-            m = m_new;
+                for (int i = 0; i < w; ++i) mx[i] = fmaxf(mx[2 * i], mx[2 * i + 1]);
+            const float bmc = mx[0] * c;
+            const bool move = bmc > m + AT_TAU;
 
-            // P_b into shared memory: row `row`, 16-byte chunk q of the
-            // 128-byte row at chunk position q ^ (row % 8) (128-byte swizzle)
-            const uint32_t prow = smem_u32(sp + sb * AT_P_BYTES) + (uint32_t)row * 128u;
+            if (b >= 2) wait_pv(b - 2);                  // P buffer sb free again
+            if (__any_sync(0xFFFFFFFFu, move)) {
+                // The tensor-memory loads and stores are warp-wide (.sync.aligned):
+                // every lane of the warp takes them, a lane whose maximum stays
+                // with a = 1 (its O row is rewritten with the same bits).
+                if (b >= 1) wait_pv(b - 1);              // O holds every block before b
+                float a = 1.f;
+                if (move) {
+                    a = ex2(m - bmc);
+                    l *= a;
+                    m = bmc;
+                }
+                if (b >= 1) {
+#pragma unroll 1
+                    for (int ch = 0; ch < AT_D / 32; ++ch) {
+                        uint32_t r[32];
+                        tmem_ld32_nowait(tbase + AT_O_COL + ch * 32, r);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * a);
+                        tmem_st32(tbase + AT_O_COL + ch * 32, r);
+                    }
+                    tmem_st_wait();
+                }
+            }
+
+            // p_j, their pairwise sum (as pairs, then the pair's two halves),
+            // P_b as bf16 into shared memory
+            uint32_t pk[AT_BKV / 2];
+            float e[AT_BKV / 2], o[AT_BKV / 2];
+#pragma unroll
+            for (int i = 0; i < AT_BKV / 2; ++i) {
+                float x0, x1;
+                ffma2(x0, x1, s[2 * i], s[2 * i + 1], c, c, -m, -m);
+                e[i] = ex2(x0);
+                o[i] = ex2(x1);
+                pk[i] = pack_bf16x2(__float_as_uint(e[i]), __float_as_uint(o[i]));
+            }
+#pragma unroll
+            for (int w = AT_BKV / 4; w >= 1; w >>= 1)
+#pragma unroll
+                for (int i = 0; i < w; ++i)
+                    ffma2(e[i], o[i], e[2 * i], o[2 * i], 1.f, 1.f, e[2 * i + 1], o[2 * i + 1]);
+            l += e[0] + o[0];
+
+            const uint32_t prow = smem_u32(sp + (t * 2 + sb) * AT_P_BYTES) + (uint32_t)row * 128u;
 #pragma unroll
             for (int q = 0; q < 8; ++q)
                 st_shared_v4(prow + (uint32_t)((q ^ (row & 7)) << 4), pk[4 * q], pk[4 * q + 1], pk[4 * q + 2],
                              pk[4 * q + 3]);
             fence_proxy_async_smem();
+            tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&p_full[sb]);
-
-            if (b >= 1) correct(b - 1, a_prev);
-            a_prev = a;
+            if (lane == 0) mbar_arrive(&p_full[t][sb]);
         }
-        correct(nb - 1, a_prev);
 
-        if (row < tile.rows) {
-            const size_t orow = (size_t)(tile.q0 + row) * (size_t)n_heads + (size_t)h;
-            uint4 *dst = reinterpret_cast<uint4 *>(O + orow * AT_D);
+        wait_pv(nb - 1);
+        const float rl = __frcp_rn(l);
+        const bool store = row < tile.rows;
+        const size_t orow = (size_t)(tile.q0 + (store ? row : 0)) * (size_t)n_heads + (size_t)(h0 + t);
+        uint4 *dst = reinterpret_cast<uint4 *>(O + orow * AT_D);
+#pragma unroll 1
+        for (int ch = 0; ch < AT_D / 32; ++ch) {
+            uint32_t r[32];
+            tmem_ld32_nowait(tbase + AT_O_COL + ch * 32, r);
+            tmem_ld_wait();
+            if (store) {
 #pragma unroll
-            for (int g = 0; g < AT_D / 8; ++g) {
-                uint4 v;
-                v.x = pack_bf16x2(__float_as_uint(__fdiv_rn(acc[8 * g + 0], l)), __float_as_uint(__fdiv_rn(acc[8 * g + 1], l)));
-                v.y = pack_bf16x2(__float_as_uint(__fdiv_rn(acc[8 * g + 2], l)), __float_as_uint(__fdiv_rn(acc[8 * g + 3], l)));
-                v.z = pack_bf16x2(__float_as_uint(__fdiv_rn(acc[8 * g + 4], l)), __float_as_uint(__fdiv_rn(acc[8 * g + 5], l)));
-                v.w = pack_bf16x2(__float_as_uint(__fdiv_rn(acc[8 * g + 6], l)), __float_as_uint(__fdiv_rn(acc[8 * g + 7], l)));
-                dst[g] = v;
+                for (int g = 0; g < 4; ++g) {
+                    uint4 v;
+                    v.x = pack_bf16x2(__float_as_uint(__uint_as_float(r[8 * g + 0]) * rl),
+                                      __float_as_uint(__uint_as_float(r[8 * g + 1]) * rl));
+                    v.y = pack_bf16x2(__float_as_uint(__uint_as_float(r[8 * g + 2]) * rl),
+                                      __float_as_uint(__uint_as_float(r[8 * g + 3]) * rl));
+                    v.z = pack_bf16x2(__float_as_uint(__uint_as_float(r[8 * g + 4]) * rl),
+                                      __float_as_uint(__uint_as_float(r[8 * g + 5]) * rl));
+                    v.w = pack_bf16x2(__float_as_uint(__uint_as_float(r[8 * g + 6]) * rl),
+                                      __float_as_uint(__uint_as_float(r[8 * g + 7]) * rl));
+                    dst[ch * 4 + g] = v;
+                }
             }
-            if (lse) lse[orow] = (m + log2f(l)) * 0.693147180559945309f;
         }
+        if (store && lse) lse[orow] = (m + log2f(l)) * 0.693147180559945309f;
     }
 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem_base, AT_TMEM_COLS);
+    if (warp == 1) tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
 }
 
 }  // namespace
@@ -387,18 +500,24 @@ extern "C" bi_status bi_attention_prefill(const void *q, const void *k, const vo
                                strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) != BI_OK)
             return st;
     }
-    if ((st = set_smem_once(d, KID_ATTN, attn_prefill_kernel, AT_SMEM)) != BI_OK) return st;
-
+    const int group = n_heads / n_kv_heads;
+    const int NT = group % 2 == 0 ? 2 : 1;     // two heads of one key/value head per CTA where they pair up
     const float c = scale * 1.44269504088896340736f;
     static_assert(sizeof(AttnTable) <= 8192, "kernel parameter space");
-    AttnTable tab;
-    for (size_t first = 0; first < tiles.size(); first += kAttnMaxTiles) {
-        const int n = (int)std::min<size_t>(kAttnMaxTiles, tiles.size() - first);
-        std::copy(tiles.begin() + first, tiles.begin() + first + n, tab.t);
-        st = launch_pdl(attn_prefill_kernel, dim3((unsigned)(n * n_heads)), dim3(AT_THREADS), (size_t)AT_SMEM,
-                        reinterpret_cast<cudaStream_t>(s), tmq, tmk, tmv, tab, static_cast<__nv_bfloat16 *>(o),
-                        lse, (int)n_heads, (int)(n_heads / n_kv_heads), c, d->err);
-        if (st != BI_OK) return st;
-    }
-    return BI_OK;
+    auto launch = [&](auto kernel, int smem, int threads, int kid) -> bi_status {
+        bi_status e = set_smem_once(d, kid, kernel, smem);
+        if (e != BI_OK) return e;
+        AttnTable tab;
+        for (size_t first = 0; first < tiles.size(); first += kAttnMaxTiles) {
+            const int n = (int)std::min<size_t>(kAttnMaxTiles, tiles.size() - first);
+            std::copy(tiles.begin() + first, tiles.begin() + first + n, tab.t);
+            e = launch_pdl(kernel, dim3((unsigned)(n * (n_heads / NT))), dim3(threads), (size_t)smem,
+                           reinterpret_cast<cudaStream_t>(s), tmq, tmk, tmv, tab, static_cast<__nv_bfloat16 *>(o),
+                           lse, (int)n_heads, group, c, d->err);
+            if (e != BI_OK) return e;
+        }
+        return BI_OK;
+    };
+    if (NT == 2) return launch(attn_prefill_kernel<2>, AttnCfg<2>::SMEM, AttnCfg<2>::THREADS, KID_ATTN + 1);
+    return launch(attn_prefill_kernel<1>, AttnCfg<1>::SMEM, AttnCfg<1>::THREADS, KID_ATTN);
 }

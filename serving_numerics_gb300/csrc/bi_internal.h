@@ -119,7 +119,7 @@ enum : int {
     KID_ROUTER_CLUSTER = 64,        // 10 instantiations: 64..73
     KID_FLOOR = 74,
     KID_ROUTER_PERSIST = 75,        // 4 instantiations: 75..78
-    KID_ATTN = 79,
+    KID_ATTN = 79,                  // 2 instantiations: 79..80
 };
 
 // Batches of at most this many rows (and E <= kClusterMaxE) take the
