@@ -22,6 +22,7 @@ from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -62,7 +63,8 @@ NCU_TRAFFIC = {# in the layer sequence, caches as the preceding router call left
                "router_call": (35_846_144 + 17_865_216 + 32_512 + 398_080
                                + 35_930_112 + 19_748_608 + 32_256 + 282_368) // 2,
                # one launch with the caches flushed: the reads; its bf16 output stays in L2
-               "rmsnorm_kernel": 33_581_824 + 0}
+               "rmsnorm_kernel": 33_581_824 + 0,
+               "attn_prefill_kernel": None}
 
 
 def fp32_peak(torch, dev) -> dict:
@@ -408,6 +410,7 @@ def run_ours(args):
         xs = [synth.device_normal((M, H), seed * 100 + 200 + l, 1.0, torch.float32, dev) for l in range(LAYERS)]
         out["rmsnorm"] = rmsnorm_measure(bi, synth, torch, dev, hbm, xs)
         del xs
+        out["attention_prefill"] = attention_measure(bi, synth, torch, dev, bf16_burst)
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_seconds)
     out["digest"] = digest(out)
@@ -668,6 +671,10 @@ def digest(out) -> dict:
     for key in ("moe_expert_gemm", "rmsnorm"):
         if key in out:
             d[key] = {"us": round(out[key]["us_per_call"], 1), "frac_hbm": round(out[key]["roofline"]["frac"], 3)}
+    at = out.get("attention_prefill")
+    if at:
+        d["attention_prefill"] = {"us": round(at["us_per_call"], 1), "frac_bf16": round(at["roofline"]["frac"], 3),
+                                  "long_context_frac_bf16": round(at["long_context"]["frac"], 3)}
     return d
 
 
@@ -754,6 +761,71 @@ def rmsnorm_measure(bi, synth, torch, dev, hbm_gbs, Xs):
             "roofline": {"bound": "hbm", "achieved": byt / t / 1e9, "peak": hbm_gbs, "unit": "GB/s",
                          "frac": byt / t / 1e9 / hbm_gbs, "algorithmic_bytes": byt,
                          "traffic": NCU_TRAFFIC["rmsnorm_kernel"]}}
+
+
+def attention_flops(q_lens, prefix, heads: int, D: int = 128) -> float:
+    """Algorithmic FLOPs of causal attention: 4 D per (query, visible key,
+    head) -- q.k and p.v, two flops per multiply-add; masked keys count
+    nothing."""
+    pairs = sum(int(n) * int(p) + int(n) * (int(n) + 1) // 2 for n, p in zip(q_lens, prefix))
+    return 4.0 * D * heads * pairs
+
+
+def attention_measure(bi, synth, torch, dev, bf16_peak, reps=50):
+    """bi_attention_prefill alone on the prefill workload: 4096 queries in 8
+    requests (five behind cached prefixes of 512 to 3072 tokens), 16 query
+    heads over 2 key/value heads of dimension 128, bf16; eight input sets
+    rotated, timed back to back with events on the launching stream.  Plus
+    one long context (a 16384-token full prefill), where every SM stays busy
+    to the end.  Bound by the tensor cores (and the exponentials, which
+    match them one to one per score)."""
+    nh, nkv, D = synth.ATTN_HEADS, synth.ATTN_KV_HEADS, synth.ATTN_D
+    qo, ko = synth.attention_offsets(synth.ATTN_Q_LENS, synth.ATTN_PREFIX)
+    Tq, Tkv = int(qo[-1]), int(ko[-1])
+    qo_l, ko_l = [int(v) for v in qo], [int(v) for v in ko]
+    sets = [(synth.device_normal((Tq, nh, D), 83000 + i, 1.0, torch.bfloat16, dev),
+             synth.device_normal((Tkv, nkv, D), 83100 + i, 1.0, torch.bfloat16, dev),
+             synth.device_normal((Tkv, nkv, D), 83200 + i, 1.0, torch.bfloat16, dev)) for i in range(8)]
+    o = torch.empty((Tq, nh, D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((Tq, nh), dtype=torch.float32, device=dev)
+    scale = 1.0 / math.sqrt(D)
+
+    def timed(call, n):
+        for i in range(4):
+            call(i)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record()
+        for i in range(n):
+            call(i)
+        b.record()
+        torch.cuda.synchronize()
+        assert bi.bi_get_last_device_error() == 0
+        return a.elapsed_time(b) / 1e3 / n
+
+    t = timed(lambda i: bi.bi_attention_prefill(*sets[i % 8], len(qo_l) - 1, qo_l, ko_l, nh, nkv, D, scale, o,
+                                                lse), reps)
+    flop = attention_flops(synth.ATTN_Q_LENS, synth.ATTN_PREFIX, nh, D)
+    del sets
+    n = 16384
+    ql = [synth.device_normal((n, nh, D), 83300, 1.0, torch.bfloat16, dev),
+          synth.device_normal((n, nkv, D), 83301, 1.0, torch.bfloat16, dev),
+          synth.device_normal((n, nkv, D), 83302, 1.0, torch.bfloat16, dev)]
+    o2 = torch.empty((n, nh, D), dtype=torch.bfloat16, device=dev)
+    t2 = timed(lambda i: bi.bi_attention_prefill(*ql, 1, [0, n], [0, n], nh, nkv, D, scale, o2, None), 10)
+    flop2 = attention_flops([n], [0], nh, D)
+    tiles = sum((int(q) + 127) // 128 for q in synth.ATTN_Q_LENS)
+    return {"config": f"{Tq} queries in {len(qo_l) - 1} requests (q_len {list(synth.ATTN_Q_LENS)}, cached prefix "
+                      f"{list(synth.ATTN_PREFIX)}), {nh} query heads over {nkv} key/value heads, D={D}, bf16, "
+                      "causal, lse written",
+            "us_per_call": t * 1e6, "tflops": flop / t / 1e12, "algorithmic_flop": flop,
+            "launches_per_call": 1, "ctas": tiles * nh // 2,
+            "roofline": {"bound": "tensor", "achieved": flop / t / 1e12, "peak": bf16_peak, "unit": "TFLOP/s",
+                         "frac": flop / t / 1e12 / bf16_peak, "peak_kind": "bf16 burst, of measured",
+                         "traffic": NCU_TRAFFIC["attn_prefill_kernel"]},
+            "long_context": {"config": f"one request, {n}-token full prefill, {nh}/{nkv} heads, D={D}",
+                             "us_per_call": t2 * 1e6, "tflops": flop2 / t2 / 1e12,
+                             "frac": flop2 / t2 / 1e12 / bf16_peak}}
 
 
 def m_variant_context(bi, synth, torch, dev):
@@ -970,7 +1042,9 @@ def run_case(args):
     (the third call is the one to capture):
       router:M    bi_router_topk, F32, H=2048, E=256, top-8, all outputs
       gemm:M      bi_gemm_bf16, K = N = 4096
-      rmsnorm:M   bi_rmsnorm, f32 rows of H=2048 -> bf16"""
+      rmsnorm:M   bi_rmsnorm, f32 rows of H=2048 -> bf16
+      attn:N      bi_attention_prefill, one N-token full prefill (default 4096),
+                  16 query heads over 2 key/value heads, D=128"""
     import torch
 
     from serving_numerics_gb300 import binding as bi
@@ -994,6 +1068,14 @@ def run_case(args):
         w = (1.0 + 0.1 * synth.device_normal((H,), 90400, 1.0, torch.float32, dev)).contiguous()
         xs = [synth.device_normal((Mi, H), 90500 + i, 1.0, torch.float32, dev) for i in range(3)]
         calls = [lambda i=i: bi.rmsnorm(xs[i], w, 1e-6) for i in range(3)]
+    elif kind == "attn":
+        nh, nkv, D = synth.ATTN_HEADS, synth.ATTN_KV_HEADS, synth.ATTN_D
+        n = Mi if m else 4096
+        xs = [[synth.device_normal((n, h_, D), 90600 + 3 * i + j, 1.0, torch.bfloat16, dev)
+               for j, h_ in enumerate((nh, nkv, nkv))] for i in range(3)]
+        o = torch.empty((n, nh, D), dtype=torch.bfloat16, device=dev)
+        calls = [lambda i=i: bi.bi_attention_prefill(*xs[i], 1, [0, n], [0, n], nh, nkv, D, 1 / math.sqrt(D), o,
+                                                     None) for i in range(3)]
     else:
         raise SystemExit(f"unknown case {args.case}")
     torch.cuda.synchronize()
@@ -1019,7 +1101,7 @@ def main():
     ap.add_argument("--layers", type=int, default=LAYERS,
                     help="fewer layers for a small profiling case (the benchmark uses 40)")
     ap.add_argument("--case", default=None,
-                    help="router:M, gemm:M or rmsnorm:M: three calls of one operation, for profiling")
+                    help="router:M, gemm:M, rmsnorm:M or attn:N: three calls of one operation, for profiling")
     args = ap.parse_args()
     globals()["LAYERS"] = args.layers
     if args.case:

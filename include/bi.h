@@ -367,20 +367,22 @@ BI_API bi_status bi_rmsnorm(const void *x, const void *w, bi_dtype dtype, int32_
  * every feature, so attention is the next operation on the cascade path
  * that must give a row the same bits whatever the batch.
  *
- * Invariance contract: each query row walks its own context in blocks of 64
- * keys at fixed positions (block b = keys 64b .. 64b+63), in increasing
- * order, up to the block holding its own position.  Per block: the scores
- * as f32 tensor-core dot products over the 128 dimensions in 16-deep steps,
- * in increasing order; the running maximum m of scale*log2(e)*score; the
- * weights p = bf16_rne(exp2f(score*scale*log2(e) - m)); the running sum
- * l = fmaf(l, a, pairwise sum of the block's 64 weights) with
- * a = exp2f(m_old - m); the block's P.V as f32 tensor-core sums over the
- * block's keys in 16-deep steps, in increasing order; the running output
- * acc = fmaf(acc, a, block P.V).  Finally o = bf16_rne(acc / l) and
- * lse = (m + log2f(l)) * ln 2.  So a row's bits depend only on its own
- * query, its position and its request's keys and values: not on the
- * other requests, on how many of its request's queries are in the call (a
- * cached prefix, a chunked prefill), or on which query tile it falls in.
+ * Invariance contract: each query row walks its own context in blocks of
+ * 128 keys at fixed positions (block b = keys 128b .. 128b+127), in
+ * increasing order, up to the block holding its own position.  Per block:
+ * the scores s_j as f32 tensor-core dot products over the 128 dimensions in
+ * 16-deep steps, in increasing order (keys the row cannot see: -inf); with
+ * c = scale * log2(e) rounded to f32 and t = c * max_j s_j, when t exceeds
+ * the row's reference maximum m by more than 8 (always on the first block)
+ * the accumulators are rescaled by a = 2^(m - t) and m = t; then
+ * p_j = 2^fmaf(s_j, c, -m) (ex2.approx.ftz); l += E + D, where E and D are
+ * pairwise trees over the block's 64 even- and 64 odd-position f32 p_j; and
+ * O += sum_j bf16_rne(p_j) v_j as f32 tensor-core sums over the block's keys
+ * in 16-deep steps, in increasing order.  Finally o = bf16_rne(O * (1/l))
+ * and lse = (m + log2f(l)) * ln 2.  So a row's bits depend only on its own
+ * query, its position and its request's keys and values: not on the other
+ * requests, on how many of its request's queries are in the call (a cached
+ * prefix, a chunked prefill), or on which query tile it falls in.
  *
  *   q           [Tq, n_heads, 128] bf16, Tq = q_offsets[n_req]
  *   k, v        [Tkv, n_kv_heads, 128] bf16, Tkv = kv_offsets[n_req]

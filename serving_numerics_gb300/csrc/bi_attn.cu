@@ -10,9 +10,10 @@
 // batch-invariant engine rewrites.
 //
 // Invariance by construction.  Every query row walks the keys of its own
-// request in blocks of 64 at fixed absolute key positions (block b holds
-// keys 64b .. 64b+63 of the context), from block 0 up to the block holding
-// the row's own position, and does the same arithmetic on each block:
+// request in blocks of 128 at fixed absolute key positions (block b holds
+// keys 128b .. 128b+127 of the context), from block 0 up to the block
+// holding the row's own position, and does the same arithmetic on each
+// block:
 //
 //   s_j  = q . k_j                 f32 on the tensor cores: the 128
 //                                  dimensions as eight 16-deep steps, in
@@ -22,8 +23,9 @@
 //                                  the first block, where m = -inf)
 //       a = 2^(m - t);  l = l * a;  O = O * a  (in tensor memory);  m = t
 //   p_j  = 2^(fmaf(s_j, c, -m))    ex2.approx.ftz, <= 2^8
-//   l    = l + (pairwise sum of the 64 f32 p_j)
-//   O    = O + sum_j bf16_rne(p_j) v_j   f32 on the tensor cores: four
+//   l    = l + (E + D)             E, D: pairwise trees over the 64 even-
+//                                  and the 64 odd-position p_j of the block
+//   O    = O + sum_j bf16_rne(p_j) v_j   f32 on the tensor cores: eight
 //                                  16-deep steps over the block's keys in
 //                                  increasing order, added to O in place
 //
@@ -42,20 +44,26 @@
 // head are odd -- with 64 + 128 NT threads):
 //   warp 0      TMA producer: the NT Q tiles once (two 64-column boxes
 //               each, 128-byte swizzle), then K and V of each key block
-//               into a ring of stages (32 KB each), shared by the NT heads
-//   warp 1      allocates 256 NT tensor-memory columns (per head: two S
-//               buffers of 128 x 64 f32 and the O accumulator of 128 x 128
-//               f32); one lane issues S = Q K^T of block b for every head
-//               before P V of block b-1, so the tensor cores compute the
-//               next scores while the softmax of the current block runs
+//               into a ring of two 64 KB stages, shared by the NT heads
+//   warp 1      allocates 256 NT tensor-memory columns: per head the scores
+//               S (128 x 128 f32), whose first 64 columns then hold P as
+//               bf16 pairs, and the O accumulator (128 x 128 f32).  One lane
+//               issues, per head and block, O += P V (A = P read from tensor
+//               memory, B = V from shared memory) and then S = Q K^T of the
+//               next block into the same columns.  The two heads' softmaxes
+//               alternate with their tensor-core work, so while one head's
+//               softmax runs the tensor cores serve the other head.
 //   warps 2..   one warpgroup per head, one thread per query row: the
-//               softmax of each block (P as bf16 into shared memory in the
-//               swizzled K-major layout the P V product reads), the rare
-//               rescaling of its O row, and the output
+//               softmax of each block (P as bf16 into tensor memory), the
+//               rare rescaling of its O row, and the output
+// Shared memory carries only Q, K and V: P never leaves tensor memory, and
 // V is read by the P V product straight from its TMA box as an MN-major
-// operand (keys along K, head dimension contiguous), so V needs no
-// transpose.  Every wait on an mbarrier is bounded (about 2 s); on expiry
-// the kernel records BI_ERR_TIMEOUT in the device error word and carries on.
+// operand (keys along K, head dimension contiguous).  The next block's
+// S = Q K^T overwrites the columns that held this block's P: the tensor
+// core executes one thread's tcgen05.mma operations in issue order, and the
+// S product is issued after the P V product that reads them.  Every wait on
+// an mbarrier is bounded (about 2 s); on expiry the kernel records
+// BI_ERR_TIMEOUT in the device error word and carries on.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -71,24 +79,22 @@ namespace {
 
 constexpr int AT_D = 128;                          // head dimension
 constexpr int AT_BQ = 128;                         // query rows per tile (tensor-memory lanes)
-constexpr int AT_BKV = 64;                         // keys per block
+constexpr int AT_BKV = 128;                        // keys per block
 constexpr float AT_TAU = 8.0f;                     // the reference maximum moves past this growth
 constexpr int AT_Q_BOX = AT_BQ * 64 * 2;           // 16 KB: 128 rows x 64 dims
-constexpr int AT_KV_BOX = AT_BKV * 64 * 2;         // 8 KB: 64 keys x 64 dims
+constexpr int AT_KV_BOX = AT_BKV * 64 * 2;         // 16 KB: 128 keys x 64 dims
 constexpr int AT_Q_BYTES = 2 * AT_Q_BOX;
 constexpr int AT_STAGE_BYTES = 4 * AT_KV_BOX;      // K (two boxes), then V (two boxes)
-constexpr int AT_P_BYTES = AT_BQ * AT_BKV * 2;     // 16 KB: 128 rows x 64 keys bf16
+constexpr int AT_STAGES = 2;
 constexpr uint32_t AT_HEAD_COLS = 256;             // tensor-memory columns per head
-constexpr uint32_t AT_S_COL = 0;                   // S buffers: columns 0..63 and 64..127
+constexpr uint32_t AT_S_COL = 0;                   // S: columns 0..127; P (bf16 pairs): 0..63
 constexpr uint32_t AT_O_COL = 128;                 // O: 128..255
 
 template <int NT>
 struct AttnCfg {
-    static constexpr int STAGES = NT == 2 ? 3 : 4;
     static constexpr int THREADS = 64 + 128 * NT;
     static constexpr int KV_OFF = NT * AT_Q_BYTES;
-    static constexpr int P_OFF = KV_OFF + STAGES * AT_STAGE_BYTES;
-    static constexpr int SMEM = P_OFF + NT * 2 * AT_P_BYTES + 1024;
+    static constexpr int SMEM = KV_OFF + AT_STAGES * AT_STAGE_BYTES + 1024;
     static constexpr uint32_t TMEM_COLS = AT_HEAD_COLS * NT;
     static_assert(SMEM <= 227 * 1024, "shared memory");
 };
@@ -110,9 +116,9 @@ __host__ __device__ constexpr int attn_blocks(int pos0, int rows) { return (pos0
 // Shared-memory descriptor of an MN-major operand with the 128-byte swizzle
 // as TMA lays it out from [keys][64 dims] boxes: along N (the head
 // dimension) 64 contiguous elements per 128-byte row and the next 64 in the
-// next box (leading byte offset = one box, 8 KB); along K (keys) rows of
-// 128 bytes, 8-row atoms 1024 bytes apart (stride byte offset).  A 16-key
-// step of K adds two atoms (2048 bytes) to the start address.
+// next box (leading byte offset = one box); along K (keys) rows of 128
+// bytes, 8-row atoms 1024 bytes apart (stride byte offset).  A 16-key step
+// of K adds two atoms (2048 bytes) to the start address.
 __device__ __forceinline__ uint64_t sw128_mn_desc(uint32_t saddr)
 {
     uint64_t d = 0;
@@ -124,15 +130,17 @@ __device__ __forceinline__ uint64_t sw128_mn_desc(uint32_t saddr)
     return d;
 }
 
-__device__ __forceinline__ void fence_proxy_async_smem()
+// D (tensor memory) (+)= A (tensor memory, K-major: row i in lane i, 16-bit
+// elements packed two to a 32-bit column) . B (shared memory descriptor).
+__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate)
 {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
-{
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
-                 : "memory");
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
 }
 
 // 2^x by the multi-function unit (flushes subnormal results to zero; 2^-inf = 0)
@@ -170,7 +178,7 @@ __device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t *r)
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-// 32 lanes x 32 consecutive f32 columns from registers (thread t writes lane t).
+// 32 lanes x 32 consecutive 32-bit columns from registers (thread t writes lane t).
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t *r)
 {
     asm volatile(
@@ -194,14 +202,13 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                     unsigned int *err)
 {
     using Cfg = AttnCfg<NT>;
-    constexpr int NS = Cfg::STAGES;
+    constexpr int NS = AT_STAGES;
     pdl_trigger();
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t q_bar, kv_full[NS], kv_empty[NS], s_full[NT][2], s_empty[NT][2],
-        p_full[NT][2], o_done[NT][2];
+    __shared__ __align__(8) uint64_t q_bar, kv_full[NS], kv_empty[NS], s_full[NT], p_full[NT], o_done[NT];
     __shared__ uint32_t tmem_base_sh;
     uint8_t *smem = smem_align1024(smem_raw);
-    uint8_t *sq = smem, *skv = smem + Cfg::KV_OFF, *sp = smem + Cfg::P_OFF;
+    uint8_t *sq = smem, *skv = smem + Cfg::KV_OFF;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int pairs = n_heads / NT;
@@ -219,12 +226,9 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             mbar_init(&kv_empty[s], 1);
         }
         for (int t = 0; t < NT; ++t) {
-            for (int b = 0; b < 2; ++b) {
-                mbar_init(&s_full[t][b], 1);
-                mbar_init(&s_empty[t][b], 4);
-                mbar_init(&p_full[t][b], 4);
-                mbar_init(&o_done[t][b], 1);
-            }
+            mbar_init(&s_full[t], 1);
+            mbar_init(&p_full[t], 4);
+            mbar_init(&o_done[t], 1);
         }
         mbar_init_fence();
     }
@@ -258,102 +262,91 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         }
     } else if (warp == 1) {
         if (lane == 0) {   // MMA issuer
-            const uint32_t id_s = idesc_n(AT_BKV), id_o = idesc_n(AT_D) | (1u << 16);   // B of P V MN-major
+            // S: A = Q, B = K (both K-major, shared memory); O: A = P (tensor
+            // memory), B = V (MN-major, shared memory)
+            const uint32_t id_s = idesc_n(AT_BKV), id_o = idesc_n(AT_D) | (1u << 16);
+            auto issue_s = [&](int t, int st) {
+                const uint32_t qa = smem_u32(sq + t * AT_Q_BYTES), ka = smem_u32(skv + st * AT_STAGE_BYTES);
+                const uint32_t d = tmem_base + t * AT_HEAD_COLS + AT_S_COL;
+#pragma unroll
+                for (int half = 0; half < 2; ++half)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        umma_bf16(d, sw128_desc(qa + half * AT_Q_BOX + k * 32),
+                                  sw128_desc(ka + half * AT_KV_BOX + k * 32), id_s, (half | k) != 0 ? 1u : 0u);
+                umma_commit(&s_full[t]);
+            };
             mbar_wait(&q_bar, 0, err, 0x62);
+            mbar_wait(&kv_full[0], 0, err, 0x63);
             tc_fence_after();
-            for (int b = 0; b <= nb; ++b) {
-                if (b < nb) {   // S_b = Q K_b^T for every head
-                    const int st = b % NS;
-                    const uint32_t sb = (uint32_t)b & 1u, use = ((uint32_t)b >> 1) & 1u;
-                    mbar_wait(&kv_full[st], (uint32_t)(b / NS) & 1u, err, 0x63);
-                    const uint32_t ka = smem_u32(skv + st * AT_STAGE_BYTES);
+            for (int t = 0; t < NT; ++t) issue_s(t, 0);
+            for (int b = 0; b < nb; ++b) {
+                const int st = b % NS;
+                const uint32_t va = smem_u32(skv + st * AT_STAGE_BYTES + 2 * AT_KV_BOX);
 #pragma unroll
-                    for (int t = 0; t < NT; ++t) {
-                        mbar_wait(&s_empty[t][sb], use ^ 1u, err, 0x64);
-                        tc_fence_after();
-                        const uint32_t qa = smem_u32(sq + t * AT_Q_BYTES);
-                        const uint32_t d = tmem_base + t * AT_HEAD_COLS + AT_S_COL + sb * AT_BKV;
+                for (int t = 0; t < NT; ++t) {
+                    mbar_wait(&p_full[t], (uint32_t)b & 1u, err, 0x65);
+                    tc_fence_after();
+                    const uint32_t pa = tmem_base + t * AT_HEAD_COLS + AT_S_COL;
+                    const uint32_t d = tmem_base + t * AT_HEAD_COLS + AT_O_COL;
 #pragma unroll
-                        for (int half = 0; half < 2; ++half)
-#pragma unroll
-                            for (int k = 0; k < 4; ++k)
-                                umma_bf16(d, sw128_desc(qa + half * AT_Q_BOX + k * 32),
-                                          sw128_desc(ka + half * AT_KV_BOX + k * 32), id_s,
-                                          (half | k) != 0 ? 1u : 0u);
-                        umma_commit(&s_full[t][sb]);
+                    for (int k = 0; k < AT_BKV / 16; ++k)
+                        umma_bf16_ts(d, pa + k * 8, sw128_mn_desc(va + k * 2048), id_o, (b | k) != 0 ? 1u : 0u);
+                    umma_commit(&o_done[t]);
+                    if (t == NT - 1) umma_commit(&kv_empty[st]);   // K and V of block b no longer read
+                    if (b + 1 < nb) {   // the next block's scores, into the columns P V has just read
+                        if (t == 0) {
+                            mbar_wait(&kv_full[(b + 1) % NS], (uint32_t)((b + 1) / NS) & 1u, err, 0x63);
+                            tc_fence_after();
+                        }
+                        issue_s(t, (b + 1) % NS);
                     }
-                }
-                if (b >= 1) {   // O += P_{b-1} V_{b-1} for every head
-                    const int pb = b - 1, st = pb % NS;
-                    const uint32_t ob = (uint32_t)pb & 1u, use = ((uint32_t)pb >> 1) & 1u;
-                    const uint32_t va = smem_u32(skv + st * AT_STAGE_BYTES + 2 * AT_KV_BOX);
-#pragma unroll
-                    for (int t = 0; t < NT; ++t) {
-                        mbar_wait(&p_full[t][ob], use, err, 0x65);
-                        tc_fence_after();
-                        const uint32_t pa = smem_u32(sp + (t * 2 + ob) * AT_P_BYTES);
-                        const uint32_t d = tmem_base + t * AT_HEAD_COLS + AT_O_COL;
-#pragma unroll
-                        for (int k = 0; k < AT_BKV / 16; ++k)
-                            umma_bf16(d, sw128_desc(pa + k * 32), sw128_mn_desc(va + k * 2048), id_o,
-                                      (pb | k) != 0 ? 1u : 0u);
-                        umma_commit(&o_done[t][ob]);
-                    }
-                    umma_commit(&kv_empty[st]);   // K and V of block pb no longer read
                 }
             }
         }
     } else {
-        // softmax: warpgroup t = head h0 + t; warp w may read tensor-memory
+        // softmax: warpgroup t = head h0 + t; warp w may access tensor-memory
         // lanes 32*(w%4) .. +31
         const int t = (warp - 2) >> 2, quad = warp & 3, row = quad * 32 + lane;
         const int pos = tile.pos0 + row;
         const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + t * AT_HEAD_COLS;
         float m = -INFINITY, l = 0.f;
-        // Until P V of block n is done.  Block n's completion is phase n/2
-        // of barrier n%2; every wait names the exact phase, and the caller
-        // has already seen block n-2 complete (the wait for the P buffer),
-        // so neither barrier is ever two phases from the one awaited.
-        auto wait_pv = [&](int n) {
-            mbar_wait(&o_done[t][n & 1], ((uint32_t)n >> 1) & 1u, err, 0x67);
-            tc_fence_after();
-        };
 
 #pragma unroll 1
         for (int b = 0; b < nb; ++b) {
-            const uint32_t sb = (uint32_t)b & 1u, use = ((uint32_t)b >> 1) & 1u;
-            mbar_wait(&s_full[t][sb], use, err, 0x68);
+            mbar_wait(&s_full[t], (uint32_t)b & 1u, err, 0x68);
             tc_fence_after();
-            float s[AT_BKV];
-            tmem_ld32_nowait(tbase + AT_S_COL + sb * AT_BKV, reinterpret_cast<uint32_t *>(&s[0]));
-            tmem_ld32_nowait(tbase + AT_S_COL + sb * AT_BKV + 32, reinterpret_cast<uint32_t *>(&s[32]));
-            tmem_ld_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&s_empty[t][sb]);
-
+            // First pass over the scores, 64 columns at a time: the block
+            // maximum over the keys the row sees (eight chains; the maximum is
+            // exact in any order).
             const int nvis = pos - b * AT_BKV + 1;       // keys of this block the row sees
-            if (nvis < AT_BKV) {
+            float mx[8];
 #pragma unroll
-                for (int j = 0; j < AT_BKV; ++j)
-                    if (j >= nvis) s[j] = -INFINITY;
+            for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                float s[64];
+                tmem_ld32_nowait(tbase + AT_S_COL + half * 64, reinterpret_cast<uint32_t *>(&s[0]));
+                tmem_ld32_nowait(tbase + AT_S_COL + half * 64 + 32, reinterpret_cast<uint32_t *>(&s[32]));
+                tmem_ld_wait();
+                if (nvis < (half + 1) * 64) {
+#pragma unroll
+                    for (int j = 0; j < 64; ++j)
+                        if (half * 64 + j >= nvis) s[j] = -INFINITY;
+                }
+#pragma unroll
+                for (int j = 0; j < 64; ++j) mx[j & 7] = fmaxf(mx[j & 7], s[j]);
             }
-            float mx[AT_BKV / 2];
-#pragma unroll
-            for (int i = 0; i < AT_BKV / 2; ++i) mx[i] = fmaxf(s[2 * i], s[2 * i + 1]);
-#pragma unroll
-            for (int w = AT_BKV / 4; w >= 1; w >>= 1)
-#pragma unroll
-                for (int i = 0; i < w; ++i) mx[i] = fmaxf(mx[2 * i], mx[2 * i + 1]);
-            const float bmc = mx[0] * c;
+            const float bmc = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                    fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * c;
             const bool move = bmc > m + AT_TAU;
 
-            if (b >= 2) wait_pv(b - 2);                  // P buffer sb free again
+            // O holds blocks 0 .. b-1 here: the P V product of block b-1 was
+            // issued before this block's S.  The tensor-memory loads and
+            // stores are warp-wide (.sync.aligned): every lane of the warp
+            // takes them, a lane whose maximum stays with a = 1 (its O row is
+            // rewritten with the same bits).
             if (__any_sync(0xFFFFFFFFu, move)) {
-                // The tensor-memory loads and stores are warp-wide (.sync.aligned):
-                // every lane of the warp takes them, a lane whose maximum stays
-                // with a = 1 (its O row is rewritten with the same bits).
-                if (b >= 1) wait_pv(b - 1);              // O holds every block before b
                 float a = 1.f;
                 if (move) {
                     a = ex2(m - bmc);
@@ -361,6 +354,8 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                     m = bmc;
                 }
                 if (b >= 1) {
+                    mbar_wait(&o_done[t], (uint32_t)(b - 1) & 1u, err, 0x67);
+                    tc_fence_after();
 #pragma unroll 1
                     for (int ch = 0; ch < AT_D / 32; ++ch) {
                         uint32_t r[32];
@@ -370,41 +365,58 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                         for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * a);
                         tmem_st32(tbase + AT_O_COL + ch * 32, r);
                     }
-                    tmem_st_wait();
                 }
             }
 
-            // p_j, their pairwise sum (as pairs, then the pair's two halves),
-            // P_b as bf16 into shared memory
-            uint32_t pk[AT_BKV / 2];
-            float e[AT_BKV / 2], o[AT_BKV / 2];
+            // Second pass, 64 keys at a time: p_j as bf16 pairs (the P
+            // operand, written over score columns already read: keys 64h ..
+            // 64h+63 go to columns 32h .. 32h+31) and l.  l adds two pairwise
+            // trees, over the block's even- and odd-position p_j, each built
+            // leaf by leaf from the pairs (p_2i, p_2i+1) (a subtree is closed
+            // as soon as its sibling is complete); the two halves' 32-leaf
+            // subtrees meet at the root.
+            float re[2], ro[2];
 #pragma unroll
-            for (int i = 0; i < AT_BKV / 2; ++i) {
-                float x0, x1;
-                ffma2(x0, x1, s[2 * i], s[2 * i + 1], c, c, -m, -m);
-                e[i] = ex2(x0);
-                o[i] = ex2(x1);
-                pk[i] = pack_bf16x2(__float_as_uint(e[i]), __float_as_uint(o[i]));
+            for (int half = 0; half < 2; ++half) {
+                float s[64];
+                tmem_ld32_nowait(tbase + AT_S_COL + half * 64, reinterpret_cast<uint32_t *>(&s[0]));
+                tmem_ld32_nowait(tbase + AT_S_COL + half * 64 + 32, reinterpret_cast<uint32_t *>(&s[32]));
+                tmem_ld_wait();
+                if (nvis < (half + 1) * 64) {
+#pragma unroll
+                    for (int j = 0; j < 64; ++j)
+                        if (half * 64 + j >= nvis) s[j] = -INFINITY;
+                }
+                uint32_t pk[32];
+                float te[6], to[6];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    float x0, x1;
+                    ffma2(x0, x1, s[2 * i], s[2 * i + 1], c, c, -m, -m);
+                    float e = ex2(x0), o = ex2(x1);
+                    pk[i] = pack_bf16x2(__float_as_uint(e), __float_as_uint(o));
+                    int lv = 0;
+#pragma unroll
+                    for (; lv < 5 && ((i >> lv) & 1); ++lv) ffma2(e, o, te[lv], to[lv], 1.f, 1.f, e, o);
+                    te[lv] = e;
+                    to[lv] = o;
+                }
+                re[half] = te[5];
+                ro[half] = to[5];
+                tmem_st32(tbase + AT_S_COL + half * 32, pk);
             }
-#pragma unroll
-            for (int w = AT_BKV / 4; w >= 1; w >>= 1)
-#pragma unroll
-                for (int i = 0; i < w; ++i)
-                    ffma2(e[i], o[i], e[2 * i], o[2 * i], 1.f, 1.f, e[2 * i + 1], o[2 * i + 1]);
-            l += e[0] + o[0];
+            float se, so;
+            ffma2(se, so, re[0], ro[0], 1.f, 1.f, re[1], ro[1]);
+            l += se + so;
 
-            const uint32_t prow = smem_u32(sp + (t * 2 + sb) * AT_P_BYTES) + (uint32_t)row * 128u;
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-                st_shared_v4(prow + (uint32_t)((q ^ (row & 7)) << 4), pk[4 * q], pk[4 * q + 1], pk[4 * q + 2],
-                             pk[4 * q + 3]);
-            fence_proxy_async_smem();
+            tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&p_full[t][sb]);
+            if (lane == 0) mbar_arrive(&p_full[t]);
         }
 
-        wait_pv(nb - 1);
+        mbar_wait(&o_done[t], (uint32_t)(nb - 1) & 1u, err, 0x67);
+        tc_fence_after();
         const float rl = __frcp_rn(l);
         const bool store = row < tile.rows;
         const size_t orow = (size_t)(tile.q0 + (store ? row : 0)) * (size_t)n_heads + (size_t)(h0 + t);
