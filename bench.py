@@ -64,7 +64,9 @@ NCU_TRAFFIC = {# in the layer sequence, caches as the preceding router call left
                                + 35_930_112 + 19_748_608 + 32_256 + 282_368) // 2,
                # one launch with the caches flushed: the reads; its bf16 output stays in L2
                "rmsnorm_kernel": 33_581_824 + 0,
-               "attn_prefill_kernel": None}
+               # the mixed prefill batch, one launch with the caches flushed: Q, K, V read; the
+               # output stays in L2
+               "attn_prefill_kernel": 29_407_232 + 0}
 
 
 def fp32_peak(torch, dev) -> dict:
@@ -1044,7 +1046,8 @@ def run_case(args):
       gemm:M      bi_gemm_bf16, K = N = 4096
       rmsnorm:M   bi_rmsnorm, f32 rows of H=2048 -> bf16
       attn:N      bi_attention_prefill, one N-token full prefill (default 4096),
-                  16 query heads over 2 key/value heads, D=128"""
+                  16 query heads over 2 key/value heads, D=128
+      attnmix     bi_attention_prefill on the benchmark's mixed prefill batch"""
     import torch
 
     from serving_numerics_gb300 import binding as bi
@@ -1076,6 +1079,17 @@ def run_case(args):
         o = torch.empty((n, nh, D), dtype=torch.bfloat16, device=dev)
         calls = [lambda i=i: bi.bi_attention_prefill(*xs[i], 1, [0, n], [0, n], nh, nkv, D, 1 / math.sqrt(D), o,
                                                      None) for i in range(3)]
+    elif kind == "attnmix":
+        nh, nkv, D = synth.ATTN_HEADS, synth.ATTN_KV_HEADS, synth.ATTN_D
+        qo, ko = synth.attention_offsets(synth.ATTN_Q_LENS, synth.ATTN_PREFIX)
+        qo_l, ko_l = [int(v) for v in qo], [int(v) for v in ko]
+        xs = [[synth.device_normal((qo_l[-1], nh, D), 90700 + 3 * i, 1.0, torch.bfloat16, dev),
+               synth.device_normal((ko_l[-1], nkv, D), 90701 + 3 * i, 1.0, torch.bfloat16, dev),
+               synth.device_normal((ko_l[-1], nkv, D), 90702 + 3 * i, 1.0, torch.bfloat16, dev)] for i in range(3)]
+        o = torch.empty((qo_l[-1], nh, D), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((qo_l[-1], nh), dtype=torch.float32, device=dev)
+        calls = [lambda i=i: bi.bi_attention_prefill(*xs[i], len(qo_l) - 1, qo_l, ko_l, nh, nkv, D,
+                                                     1 / math.sqrt(D), o, lse) for i in range(3)]
     else:
         raise SystemExit(f"unknown case {args.case}")
     torch.cuda.synchronize()
@@ -1101,7 +1115,7 @@ def main():
     ap.add_argument("--layers", type=int, default=LAYERS,
                     help="fewer layers for a small profiling case (the benchmark uses 40)")
     ap.add_argument("--case", default=None,
-                    help="router:M, gemm:M, rmsnorm:M or attn:N: three calls of one operation, for profiling")
+                    help="router:M, gemm:M, rmsnorm:M, attn:N or attnmix: three calls of one operation, for profiling")
     args = ap.parse_args()
     globals()["LAYERS"] = args.layers
     if args.case:
