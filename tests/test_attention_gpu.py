@@ -260,3 +260,22 @@ def test_rejects_bad_calls_on_device(bi):
         bi.BI_ERR_INVALID_ARG
     torch.cuda.synchronize()
     assert bi.bi_get_last_device_error() == 0
+
+
+def test_one_head_and_two_head_ctas_give_the_same_bytes(bi):
+    """In the prefill workload the longest tiles (request 4: 384 queries
+    behind 3072 cached tokens) run one head per CTA and the shorter ones two
+    heads per CTA (a tile runs alone only where pairing would leave its chain
+    far above an SM's average work); called alone, a request's tiles all run
+    one head per CTA.  Request 1 (768 queries behind 2048 cached tokens, paired
+    inside the batch) and request 4 alone must give their rows inside the batch
+    byte for byte."""
+    nh, nkv = synth.ATTN_HEADS, synth.ATTN_KV_HEADS
+    qo, ko = synth.attention_offsets(synth.ATTN_Q_LENS, synth.ATTN_PREFIX)
+    Q, K, V = synth.attention_inputs(17, int(qo[-1]), int(ko[-1]), nh, nkv)
+    o, lse = _run(bi, Q, K, V, qo, ko, nh, nkv)
+    for r in (1, 4, 7):
+        a, b, c, d = qo[r], qo[r + 1], ko[r], ko[r + 1]
+        ro, rl = _run(bi, Q[a:b], K[c:d], V[c:d], [0, b - a], [0, d - c], nh, nkv)
+        assert np.array_equal(o[a:b], ro), r
+        assert np.array_equal(lse[a:b].view(np.uint32), rl.view(np.uint32)), r
