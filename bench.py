@@ -779,8 +779,9 @@ def attention_measure(bi, synth, torch, dev, bf16_peak, reps=50):
     heads over 2 key/value heads of dimension 128, bf16; eight input sets
     rotated, timed back to back with events on the launching stream.  Plus
     one long context (a 16384-token full prefill), where every SM stays busy
-    to the end.  Bound by the tensor cores (and the exponentials, which
-    match them one to one per score)."""
+    to the end, and one request's prefix-cache hit (128 queries behind 32768
+    cached tokens), which fills only 16 SMs.  Bound by the tensor cores (and
+    the exponentials, which match them one to one per score)."""
     nh, nkv, D = synth.ATTN_HEADS, synth.ATTN_KV_HEADS, synth.ATTN_D
     qo, ko = synth.attention_offsets(synth.ATTN_Q_LENS, synth.ATTN_PREFIX)
     Tq, Tkv = int(qo[-1]), int(ko[-1])
@@ -816,6 +817,16 @@ def attention_measure(bi, synth, torch, dev, bf16_peak, reps=50):
     o2 = torch.empty((n, nh, D), dtype=torch.bfloat16, device=dev)
     t2 = timed(lambda i: bi.bi_attention_prefill(*ql, 1, [0, n], [0, n], nh, nkv, D, scale, o2, None), 10)
     flop2 = attention_flops([n], [0], nh, D)
+    del ql, o2
+    # a prefix-cache hit of one request: 128 new queries behind 32768 cached
+    # tokens (one query tile: 16 CTAs, one head each)
+    pre, nq = 32768, 128
+    hq = [synth.device_normal((nq, nh, D), 83400, 1.0, torch.bfloat16, dev),
+          synth.device_normal((pre + nq, nkv, D), 83401, 1.0, torch.bfloat16, dev),
+          synth.device_normal((pre + nq, nkv, D), 83402, 1.0, torch.bfloat16, dev)]
+    o3 = torch.empty((nq, nh, D), dtype=torch.bfloat16, device=dev)
+    t3 = timed(lambda i: bi.bi_attention_prefill(*hq, 1, [0, nq], [0, pre + nq], nh, nkv, D, scale, o3, None), 10)
+    flop3 = attention_flops([nq], [pre], nh, D)
     tiles = sum((int(q) + 127) // 128 for q in synth.ATTN_Q_LENS)
     return {"config": f"{Tq} queries in {len(qo_l) - 1} requests (q_len {list(synth.ATTN_Q_LENS)}, cached prefix "
                       f"{list(synth.ATTN_PREFIX)}), {nh} query heads over {nkv} key/value heads, D={D}, bf16, "
@@ -827,7 +838,11 @@ def attention_measure(bi, synth, torch, dev, bf16_peak, reps=50):
                          "traffic": NCU_TRAFFIC["attn_prefill_kernel"]},
             "long_context": {"config": f"one request, {n}-token full prefill, {nh}/{nkv} heads, D={D}",
                              "us_per_call": t2 * 1e6, "tflops": flop2 / t2 / 1e12,
-                             "frac": flop2 / t2 / 1e12 / bf16_peak}}
+                             "frac": flop2 / t2 / 1e12 / bf16_peak},
+            "cache_hit_one_request": {"config": f"one request, {nq} queries behind {pre} cached tokens, "
+                                                f"{nh}/{nkv} heads, D={D}: one query tile, {nh} CTAs",
+                                      "us_per_call": t3 * 1e6, "tflops": flop3 / t3 / 1e12,
+                                      "frac": flop3 / t3 / 1e12 / bf16_peak}}
 
 
 def m_variant_context(bi, synth, torch, dev):

@@ -41,9 +41,8 @@
 //
 // Structure (one CTA per query tile of 128 rows and NT = 2 query heads that
 // share one key/value head -- or NT = 1 head when the heads per key/value
-// head are odd -- with 64 + 128 NT threads; the longest tiles of a call, the
-// first n_single of its table, take one head per CTA when pairing would
-// leave their chains far above an SM's average work):
+// head are odd, or when a call is small enough that one CTA per tile and
+// head still leaves SMs free -- with 64 + 128 NT threads):
 //   warp 0      TMA producer: the NT Q tiles once (two 64-column boxes
 //               each, 128-byte swizzle), then K and V of each key block
 //               into a ring of two 64 KB stages, shared by the NT heads
@@ -200,8 +199,8 @@ template <int NT>
 __global__ void __launch_bounds__(AttnCfg<NT>::THREADS, 1)
 attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                     const __grid_constant__ CUtensorMap tmv, const __grid_constant__ AttnTable tab,
-                    __nv_bfloat16 *__restrict__ O, float *__restrict__ lse, int n_heads, int group, int n_single,
-                    float c, unsigned int *err)
+                    __nv_bfloat16 *__restrict__ O, float *__restrict__ lse, int n_heads, int group, float c,
+                    unsigned int *err)
 {
     using Cfg = AttnCfg<NT>;
     constexpr int NS = AT_STAGES;
@@ -213,21 +212,8 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     uint8_t *sq = smem, *skv = smem + Cfg::KV_OFF;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // CTAs [0, n_single * n_heads) take the first n_single tiles one head
-    // each; the rest take the other tiles NT heads at a time
     const int pairs = n_heads / NT;
-    int ti, h0, nh;
-    if ((int)blockIdx.x < n_single * n_heads) {
-        ti = blockIdx.x / n_heads;
-        h0 = blockIdx.x % n_heads;
-        nh = 1;
-    } else {
-        const int j = blockIdx.x - n_single * n_heads;
-        ti = n_single + j / pairs;
-        h0 = (j % pairs) * NT;
-        nh = NT;
-    }
-    const int hk = h0 / group;
+    const int ti = blockIdx.x / pairs, h0 = (blockIdx.x % pairs) * NT, hk = h0 / group;
     const AttnTile tile = tab.t[ti];
     const int nb = attn_blocks(tile.pos0, tile.rows);
 
@@ -257,8 +243,8 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
 
     if (warp == 0) {
         if (lane == 0) {   // TMA producer
-            mbar_arrive_expect_tx(&q_bar, (uint32_t)(nh * AT_Q_BYTES));
-            for (int t = 0; t < nh; ++t) {
+            mbar_arrive_expect_tx(&q_bar, (uint32_t)(NT * AT_Q_BYTES));
+            for (int t = 0; t < NT; ++t) {
                 tma_load_3d(sq + t * AT_Q_BYTES, &tmq, &q_bar, 0, h0 + t, tile.q0);
                 tma_load_3d(sq + t * AT_Q_BYTES + AT_Q_BOX, &tmq, &q_bar, 64, h0 + t, tile.q0);
             }
@@ -294,13 +280,12 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             mbar_wait(&q_bar, 0, err, 0x62);
             mbar_wait(&kv_full[0], 0, err, 0x63);
             tc_fence_after();
-            for (int t = 0; t < nh; ++t) issue_s(t, 0);
+            for (int t = 0; t < NT; ++t) issue_s(t, 0);
             for (int b = 0; b < nb; ++b) {
                 const int st = b % NS;
                 const uint32_t va = smem_u32(skv + st * AT_STAGE_BYTES + 2 * AT_KV_BOX);
 #pragma unroll
                 for (int t = 0; t < NT; ++t) {
-                    if (t >= nh) break;
                     mbar_wait(&p_full[t], (uint32_t)b & 1u, err, 0x65);
                     tc_fence_after();
                     const uint32_t pa = tmem_base + t * AT_HEAD_COLS + AT_S_COL;
@@ -309,7 +294,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                     for (int k = 0; k < AT_BKV / 16; ++k)
                         umma_bf16_ts(d, pa + k * 8, sw128_mn_desc(va + k * 2048), id_o, (b | k) != 0 ? 1u : 0u);
                     umma_commit(&o_done[t]);
-                    if (t == nh - 1) umma_commit(&kv_empty[st]);   // K and V of block b no longer read
+                    if (t == NT - 1) umma_commit(&kv_empty[st]);   // K and V of block b no longer read
                     if (b + 1 < nb) {   // the next block's scores, into the columns P V has just read
                         if (t == 0) {
                             mbar_wait(&kv_full[(b + 1) % NS], (uint32_t)((b + 1) / NS) & 1u, err, 0x63);
@@ -320,10 +305,9 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                 }
             }
         }
-    } else if (((warp - 2) >> 2) < nh) {
-        // softmax: warpgroup t = head h0 + t (a CTA with one head leaves its
-        // second warpgroup idle); warp w may access tensor-memory lanes
-        // 32*(w%4) .. +31
+    } else {
+        // softmax: warpgroup t = head h0 + t; warp w may access tensor-memory
+        // lanes 32*(w%4) .. +31
         const int t = (warp - 2) >> 2, quad = warp & 3, row = quad * 32 + lane;
         const int pos = tile.pos0 + row;
         const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + t * AT_HEAD_COLS;
@@ -530,20 +514,11 @@ extern "C" bi_status bi_attention_prefill(const void *q, const void *k, const vo
             return st;
     }
     const int group = n_heads / n_kv_heads;
-    const int NT = group % 2 == 0 ? 2 : 1;     // two heads of one key/value head per CTA where they pair up
-    // A CTA runs its tile's key blocks one after another, so the longest
-    // tile bounds the call.  Where pairing heads would leave a tile's chain
-    // well above the average work of an SM, the longest tiles (they sort
-    // first) run one head per CTA: twice the CTAs, each with a shorter chain.
-    // The per-head arithmetic is the same either way.
-    int n_single = 0;
-    if (NT == 2) {
-        double work = 0;
-        for (const AttnTile &t : tiles) work += (double)attn_blocks(t.pos0, t.rows) * (n_heads / 2);
-        const double avg = work / d->sm_count;
-        while (n_single < (int)tiles.size() && attn_blocks(tiles[n_single].pos0, tiles[n_single].rows) > 1.2 * avg)
-            ++n_single;
-    }
+    // Two heads of one key/value head per CTA where they pair up, so that one
+    // head's softmax overlaps the other's tensor-core work; but a call whose
+    // tiles fit the SMs one head per CTA runs that way (twice the CTAs, each
+    // chain a little shorter).  The per-head arithmetic is the same code.
+    const int NT = (group % 2 == 0 && (long long)tiles.size() * n_heads > d->sm_count) ? 2 : 1;
     const float c = scale * 1.44269504088896340736f;
     static_assert(sizeof(AttnTable) <= 8192, "kernel parameter space");
     auto launch = [&](auto kernel, int smem, int threads, int kid) -> bi_status {
@@ -552,12 +527,10 @@ extern "C" bi_status bi_attention_prefill(const void *q, const void *k, const vo
         AttnTable tab;
         for (size_t first = 0; first < tiles.size(); first += kAttnMaxTiles) {
             const int n = (int)std::min<size_t>(kAttnMaxTiles, tiles.size() - first);
-            const int ns = std::max(0, std::min(n, n_single - (int)first));
             std::copy(tiles.begin() + first, tiles.begin() + first + n, tab.t);
-            const long long ctas = (long long)ns * n_heads + (long long)(n - ns) * (n_heads / NT);
-            e = launch_pdl(kernel, dim3((unsigned)ctas), dim3(threads), (size_t)smem,
+            e = launch_pdl(kernel, dim3((unsigned)(n * (n_heads / NT))), dim3(threads), (size_t)smem,
                            reinterpret_cast<cudaStream_t>(s), tmq, tmk, tmv, tab, static_cast<__nv_bfloat16 *>(o),
-                           lse, (int)n_heads, group, ns, c, d->err);
+                           lse, (int)n_heads, group, c, d->err);
             if (e != BI_OK) return e;
         }
         return BI_OK;

@@ -81,8 +81,9 @@ def _check_parity(bi, q_lens, kv_lens, nh, nkv, seed, scale=SCALE):
 # (q_lens, kv_lens, heads, kv heads): a single key; one query after a long
 # prefix; a full 128-row tile; several tiles with a ragged tail behind a
 # prefix that is not a multiple of 64; an empty request; MHA, GQA 2:1, 3:1
-# and 4:1, MQA (two heads per CTA where the heads per key/value head are
-# even, one otherwise)
+# and 4:1, MQA.  A call whose query tiles times heads fit the 152 SMs of a
+# GB300 runs one head per CTA; the last two cases have more (11 tiles x 16
+# heads, 7 x 32) and run two heads of a key/value head per CTA.
 CASES = [
     ((1, 17, 128, 200, 0, 64), (1, 100, 128, 700, 5, 128), 4, 2),
     ((300,), (300,), 2, 2),
@@ -90,6 +91,8 @@ CASES = [
     ((1, 1, 1), (1, 64, 65), 4, 1),
     ((130, 129, 63), (130, 1153, 200), 4, 4),
     ((100, 50), (300, 50), 6, 2),
+    ((700, 600), (1500, 600), 16, 2),
+    ((300, 250, 200), (800, 250, 200), 32, 4),
 ]
 
 
@@ -98,12 +101,14 @@ def test_attention_parity(bi, q_lens, kv_lens, nh, nkv):
     _check_parity(bi, q_lens, kv_lens, nh, nkv, seed=len(q_lens) * 31 + nh)
 
 
-@pytest.mark.parametrize("nh,nkv", [(2, 1), (3, 3)])
-def test_attention_parity_other_scale(bi, nh, nkv):
+@pytest.mark.parametrize("q_lens,kv_lens,nh,nkv", [((150, 40), (400, 40), 2, 1), ((150, 40), (400, 40), 3, 3),
+                                                    ((300, 250, 200), (800, 250, 200), 32, 4)])
+def test_attention_parity_other_scale(bi, q_lens, kv_lens, nh, nkv):
     """A larger scale (peakier softmax: exponent gaps of tens), so that the
     rows' reference maxima move after the first block and O is rescaled in
-    place, for warps where only some rows move; two heads per CTA and one."""
-    _check_parity(bi, (150, 40), (400, 40), nh, nkv, seed=7, scale=0.5)
+    place, for warps where only some rows move; one head per CTA (the first
+    two) and two (the last: 7 tiles x 32 heads exceed the SMs)."""
+    _check_parity(bi, q_lens, kv_lens, nh, nkv, seed=7, scale=0.5)
 
 
 def _context(seed, n, nh=4, nkv=2):
@@ -263,13 +268,10 @@ def test_rejects_bad_calls_on_device(bi):
 
 
 def test_one_head_and_two_head_ctas_give_the_same_bytes(bi):
-    """In the prefill workload the longest tiles (request 4: 384 queries
-    behind 3072 cached tokens) run one head per CTA and the shorter ones two
-    heads per CTA (a tile runs alone only where pairing would leave its chain
-    far above an SM's average work); called alone, a request's tiles all run
-    one head per CTA.  Request 1 (768 queries behind 2048 cached tokens, paired
-    inside the batch) and request 4 alone must give their rows inside the batch
-    byte for byte."""
+    """The prefill workload (32 query tiles x 16 heads, more than the SMs)
+    runs two heads per CTA; a request of it called alone (a few tiles) runs
+    one head per CTA.  Requests 1, 4 and 7 alone must give their rows inside
+    the batch byte for byte."""
     nh, nkv = synth.ATTN_HEADS, synth.ATTN_KV_HEADS
     qo, ko = synth.attention_offsets(synth.ATTN_Q_LENS, synth.ATTN_PREFIX)
     Q, K, V = synth.attention_inputs(17, int(qo[-1]), int(ko[-1]), nh, nkv)
