@@ -281,3 +281,34 @@ def test_one_head_and_two_head_ctas_give_the_same_bytes(bi):
         ro, rl = _run(bi, Q[a:b], K[c:d], V[c:d], [0, b - a], [0, d - c], nh, nkv)
         assert np.array_equal(o[a:b], ro), r
         assert np.array_equal(lse[a:b].view(np.uint32), rl.view(np.uint32)), r
+
+
+def test_max_heads_and_long_context(bi):
+    """The largest shapes the call accepts, checked where the oracle can
+    afford it: BI_ATTN_MAX_HEADS (256) query heads over 32 key/value heads on
+    a small ragged batch, against the oracle element by element; and one
+    65536-token context (16 over 2 heads, 512 query tiles: one full table of
+    a launch) on sampled rows against the oracle run one query at a time,
+    with its last 100 queries asked again after the cached prefix."""
+    from oracle import attention as oatt
+    assert bi.BI_ATTN_MAX_HEADS == 256
+    _check_parity(bi, (130, 7), (300, 7), 256, 32, seed=21)
+
+    n, nh, nkv = 65536, 16, 2
+    Q, K, V = synth.attention_inputs(22, n, n, nh, nkv)
+    o, lse = _run(bi, Q, K, V, [0, n], [0, n], nh, nkv)
+    got = gu_bf16_to_f64(o)
+    assert np.isfinite(got).all() and np.isfinite(lse).all()
+    g = nh // nkv
+    for i in (0, 1, 127, 128, 16383, 16384, 40000, n - 1):
+        for h in (0, 5, 8, 15):                      # both key/value heads; one head at a time
+            hk = h // g
+            ref_o, ref_l = oatt.attention_prefill(Q[i:i + 1, h:h + 1], K[:i + 1, hk:hk + 1], V[:i + 1, hk:hk + 1],
+                                                  [0, 1], [0, i + 1], SCALE)
+            vmax = np.abs(gu_bf16_to_f64(V[:i + 1, hk])).max()
+            tol = 1.05 * 2.0 ** -8 * vmax + 2.0 ** -8 * np.abs(ref_o[0, 0])
+            assert (np.abs(got[i, h] - ref_o[0, 0]) <= tol).all(), (i, h)
+            assert abs(lse[i, h] - ref_l[0, 0]) <= 2.0 ** -8 + 1e-5 * abs(ref_l[0, 0]), (i, h)
+    suf, suf_l = _run(bi, Q[n - 100:], K, V, [0, 100], [0, n], nh, nkv)
+    assert np.array_equal(suf, o[n - 100:])
+    assert np.array_equal(suf_l.view(np.uint32), lse[n - 100:].view(np.uint32))
