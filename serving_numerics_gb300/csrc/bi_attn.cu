@@ -91,13 +91,21 @@ constexpr uint32_t AT_HEAD_COLS = 256;             // tensor-memory columns per 
 constexpr uint32_t AT_S_COL = 0;                   // S: columns 0..127; P (bf16 pairs): 0..63
 constexpr uint32_t AT_O_COL = 128;                 // O: 128..255
 
+// Warp roles: warpgroup t (warps 4t .. 4t+3) is head t's softmax; then the
+// TMA producer warp and the MMA warp.  With two heads the block has a third,
+// whole warpgroup (producer, MMA, two idle warps) so that setmaxnreg can move
+// registers from it to the two softmax warpgroups: launched at 168 a thread,
+// 200 for the softmax, 96 for the rest.
+constexpr int AT_REGS_SOFTMAX = 200, AT_REGS_OTHER = 96;
 template <int NT>
 struct AttnCfg {
-    static constexpr int THREADS = 64 + 128 * NT;
+    static constexpr int PRODUCER_WARP = 4 * NT, MMA_WARP = 4 * NT + 1;
+    static constexpr int THREADS = NT == 2 ? 384 : 192;
     static constexpr int KV_OFF = NT * AT_Q_BYTES;
     static constexpr int SMEM = KV_OFF + AT_STAGES * AT_STAGE_BYTES + 1024;
     static constexpr uint32_t TMEM_COLS = AT_HEAD_COLS * NT;
     static_assert(SMEM <= 227 * 1024, "shared memory");
+    static_assert(NT == 1 || 2 * 128 * AT_REGS_SOFTMAX + 128 * AT_REGS_OTHER <= THREADS * 168, "register split");
 };
 
 // One query tile: up to 128 consecutive queries of one request.
@@ -233,82 +241,88 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         }
         mbar_init_fence();
     }
-    if (warp == 1) tmem_alloc(&tmem_base_sh, Cfg::TMEM_COLS);
+    if (warp == Cfg::MMA_WARP) tmem_alloc(&tmem_base_sh, Cfg::TMEM_COLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = tmem_base_sh;
 
-    pdl_wait();
-
-    if (warp == 0) {
-        if (lane == 0) {   // TMA producer
-            mbar_arrive_expect_tx(&q_bar, (uint32_t)(NT * AT_Q_BYTES));
-            for (int t = 0; t < NT; ++t) {
-                tma_load_3d(sq + t * AT_Q_BYTES, &tmq, &q_bar, 0, h0 + t, tile.q0);
-                tma_load_3d(sq + t * AT_Q_BYTES + AT_Q_BOX, &tmq, &q_bar, 64, h0 + t, tile.q0);
-            }
-            for (int b = 0; b < nb; ++b) {
-                const int st = b % NS;
-                const uint32_t ph = (uint32_t)(b / NS) & 1u;
-                mbar_wait(&kv_empty[st], ph ^ 1u, err, 0x61);
-                uint8_t *dst = skv + st * AT_STAGE_BYTES;
-                const int key = tile.kv0 + b * AT_BKV;
-                mbar_arrive_expect_tx(&kv_full[st], (uint32_t)AT_STAGE_BYTES);
-                tma_load_3d(dst, &tmk, &kv_full[st], 0, hk, key);
-                tma_load_3d(dst + AT_KV_BOX, &tmk, &kv_full[st], 64, hk, key);
-                tma_load_3d(dst + 2 * AT_KV_BOX, &tmv, &kv_full[st], 0, hk, key);
-                tma_load_3d(dst + 3 * AT_KV_BOX, &tmv, &kv_full[st], 64, hk, key);
-            }
-        }
-    } else if (warp == 1) {
-        if (lane == 0) {   // MMA issuer
-            // S: A = Q, B = K (both K-major, shared memory); O: A = P (tensor
-            // memory), B = V (MN-major, shared memory)
-            const uint32_t id_s = idesc_n(AT_BKV), id_o = idesc_n(AT_D) | (1u << 16);
-            auto issue_s = [&](int t, int st) {
-                const uint32_t qa = smem_u32(sq + t * AT_Q_BYTES), ka = smem_u32(skv + st * AT_STAGE_BYTES);
-                const uint32_t d = tmem_base + t * AT_HEAD_COLS + AT_S_COL;
-#pragma unroll
-                for (int half = 0; half < 2; ++half)
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        umma_bf16(d, sw128_desc(qa + half * AT_Q_BOX + k * 32),
-                                  sw128_desc(ka + half * AT_KV_BOX + k * 32), id_s, (half | k) != 0 ? 1u : 0u);
-                umma_commit(&s_full[t]);
-            };
-            mbar_wait(&q_bar, 0, err, 0x62);
-            mbar_wait(&kv_full[0], 0, err, 0x63);
-            tc_fence_after();
-            for (int t = 0; t < NT; ++t) issue_s(t, 0);
-            for (int b = 0; b < nb; ++b) {
-                const int st = b % NS;
-                const uint32_t va = smem_u32(skv + st * AT_STAGE_BYTES + 2 * AT_KV_BOX);
-#pragma unroll
+    // each role under its own register budget: ptxas allocates a region after
+    // setmaxnreg to that count
+    if (warp >= Cfg::PRODUCER_WARP) {
+        if constexpr (NT == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(AT_REGS_OTHER));
+        pdl_wait();
+        if (warp == Cfg::PRODUCER_WARP) {
+            if (lane == 0) {   // TMA producer
+                mbar_arrive_expect_tx(&q_bar, (uint32_t)(NT * AT_Q_BYTES));
                 for (int t = 0; t < NT; ++t) {
-                    mbar_wait(&p_full[t], (uint32_t)b & 1u, err, 0x65);
-                    tc_fence_after();
-                    const uint32_t pa = tmem_base + t * AT_HEAD_COLS + AT_S_COL;
-                    const uint32_t d = tmem_base + t * AT_HEAD_COLS + AT_O_COL;
-#pragma unroll
-                    for (int k = 0; k < AT_BKV / 16; ++k)
-                        umma_bf16_ts(d, pa + k * 8, sw128_mn_desc(va + k * 2048), id_o, (b | k) != 0 ? 1u : 0u);
-                    umma_commit(&o_done[t]);
-                    if (t == NT - 1) umma_commit(&kv_empty[st]);   // K and V of block b no longer read
-                    if (b + 1 < nb) {   // the next block's scores, into the columns P V has just read
-                        if (t == 0) {
-                            mbar_wait(&kv_full[(b + 1) % NS], (uint32_t)((b + 1) / NS) & 1u, err, 0x63);
-                            tc_fence_after();
+                    tma_load_3d(sq + t * AT_Q_BYTES, &tmq, &q_bar, 0, h0 + t, tile.q0);
+                    tma_load_3d(sq + t * AT_Q_BYTES + AT_Q_BOX, &tmq, &q_bar, 64, h0 + t, tile.q0);
+                }
+                for (int b = 0; b < nb; ++b) {
+                    const int st = b % NS;
+                    const uint32_t ph = (uint32_t)(b / NS) & 1u;
+                    mbar_wait(&kv_empty[st], ph ^ 1u, err, 0x61);
+                    uint8_t *dst = skv + st * AT_STAGE_BYTES;
+                    const int key = tile.kv0 + b * AT_BKV;
+                    mbar_arrive_expect_tx(&kv_full[st], (uint32_t)AT_STAGE_BYTES);
+                    tma_load_3d(dst, &tmk, &kv_full[st], 0, hk, key);
+                    tma_load_3d(dst + AT_KV_BOX, &tmk, &kv_full[st], 64, hk, key);
+                    tma_load_3d(dst + 2 * AT_KV_BOX, &tmv, &kv_full[st], 0, hk, key);
+                    tma_load_3d(dst + 3 * AT_KV_BOX, &tmv, &kv_full[st], 64, hk, key);
+                }
+            }
+        } else if (warp == Cfg::MMA_WARP) {
+            if (lane == 0) {   // MMA issuer
+                // S: A = Q, B = K (both K-major, shared memory); O: A = P (tensor
+                // memory), B = V (MN-major, shared memory)
+                const uint32_t id_s = idesc_n(AT_BKV), id_o = idesc_n(AT_D) | (1u << 16);
+                auto issue_s = [&](int t, int st) {
+                    const uint32_t qa = smem_u32(sq + t * AT_Q_BYTES), ka = smem_u32(skv + st * AT_STAGE_BYTES);
+                    const uint32_t d = tmem_base + t * AT_HEAD_COLS + AT_S_COL;
+    #pragma unroll
+                    for (int half = 0; half < 2; ++half)
+    #pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            umma_bf16(d, sw128_desc(qa + half * AT_Q_BOX + k * 32),
+                                      sw128_desc(ka + half * AT_KV_BOX + k * 32), id_s, (half | k) != 0 ? 1u : 0u);
+                    umma_commit(&s_full[t]);
+                };
+                mbar_wait(&q_bar, 0, err, 0x62);
+                mbar_wait(&kv_full[0], 0, err, 0x63);
+                tc_fence_after();
+                for (int t = 0; t < NT; ++t) issue_s(t, 0);
+                for (int b = 0; b < nb; ++b) {
+                    const int st = b % NS;
+                    const uint32_t va = smem_u32(skv + st * AT_STAGE_BYTES + 2 * AT_KV_BOX);
+    #pragma unroll
+                    for (int t = 0; t < NT; ++t) {
+                        mbar_wait(&p_full[t], (uint32_t)b & 1u, err, 0x65);
+                        tc_fence_after();
+                        const uint32_t pa = tmem_base + t * AT_HEAD_COLS + AT_S_COL;
+                        const uint32_t d = tmem_base + t * AT_HEAD_COLS + AT_O_COL;
+    #pragma unroll
+                        for (int k = 0; k < AT_BKV / 16; ++k)
+                            umma_bf16_ts(d, pa + k * 8, sw128_mn_desc(va + k * 2048), id_o, (b | k) != 0 ? 1u : 0u);
+                        umma_commit(&o_done[t]);
+                        if (t == NT - 1) umma_commit(&kv_empty[st]);   // K and V of block b no longer read
+                        if (b + 1 < nb) {   // the next block's scores, into the columns P V has just read
+                            if (t == 0) {
+                                mbar_wait(&kv_full[(b + 1) % NS], (uint32_t)((b + 1) / NS) & 1u, err, 0x63);
+                                tc_fence_after();
+                            }
+                            issue_s(t, (b + 1) % NS);
                         }
-                        issue_s(t, (b + 1) % NS);
                     }
                 }
             }
         }
     } else {
+        if constexpr (NT == 2) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(AT_REGS_SOFTMAX));
+        pdl_wait();
         // softmax: warpgroup t = head h0 + t; warp w may access tensor-memory
         // lanes 32*(w%4) .. +31
-        const int t = (warp - 2) >> 2, quad = warp & 3, row = quad * 32 + lane;
+        const int t = warp >> 2, quad = warp & 3, row = quad * 32 + lane;
         const int pos = tile.pos0 + row;
         const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + t * AT_HEAD_COLS;
         float m = -INFINITY, l = 0.f;
@@ -317,27 +331,25 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         for (int b = 0; b < nb; ++b) {
             mbar_wait(&s_full[t], (uint32_t)b & 1u, err, 0x68);
             tc_fence_after();
-            // First pass over the scores, 64 columns at a time: the block
-            // maximum over the keys the row sees (eight chains; the maximum is
-            // exact in any order).
+            // The block's 128 scores (one tensor-memory wait), the keys the row
+            // cannot see set to -inf, and the block maximum (eight chains; the
+            // maximum is exact in any order).
             const int nvis = pos - b * AT_BKV + 1;       // keys of this block the row sees
+            float s[AT_BKV];
+#pragma unroll
+            for (int ch = 0; ch < AT_BKV / 32; ++ch)
+                tmem_ld32_nowait(tbase + AT_S_COL + ch * 32, reinterpret_cast<uint32_t *>(&s[ch * 32]));
+            tmem_ld_wait();
+            if (nvis < AT_BKV) {
+#pragma unroll
+                for (int j = 0; j < AT_BKV; ++j)
+                    if (j >= nvis) s[j] = -INFINITY;
+            }
             float mx[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
+            for (int i = 0; i < 8; ++i) mx[i] = s[i];
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                float s[64];
-                tmem_ld32_nowait(tbase + AT_S_COL + half * 64, reinterpret_cast<uint32_t *>(&s[0]));
-                tmem_ld32_nowait(tbase + AT_S_COL + half * 64 + 32, reinterpret_cast<uint32_t *>(&s[32]));
-                tmem_ld_wait();
-                if (nvis < (half + 1) * 64) {
-#pragma unroll
-                    for (int j = 0; j < 64; ++j)
-                        if (half * 64 + j >= nvis) s[j] = -INFINITY;
-                }
-#pragma unroll
-                for (int j = 0; j < 64; ++j) mx[j & 7] = fmaxf(mx[j & 7], s[j]);
-            }
+            for (int j = 8; j < AT_BKV; ++j) mx[j & 7] = fmaxf(mx[j & 7], s[j]);
             const float bmc = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                     fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * c;
             const bool move = bmc > m + AT_TAU;
@@ -369,8 +381,8 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                 }
             }
 
-            // Second pass, 64 keys at a time: p_j as bf16 pairs (the P
-            // operand, written over score columns already read: keys 64h ..
+            // p_j as bf16 pairs, 64 keys at a time (the P operand, written over
+            // the score columns, all of them already in registers: keys 64h ..
             // 64h+63 go to columns 32h .. 32h+31) and l.  l adds two pairwise
             // trees, over the block's even- and odd-position p_j, each built
             // leaf by leaf from the pairs (p_2i, p_2i+1) (a subtree is closed
@@ -379,21 +391,12 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             float re[2], ro[2];
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
-                float s[64];
-                tmem_ld32_nowait(tbase + AT_S_COL + half * 64, reinterpret_cast<uint32_t *>(&s[0]));
-                tmem_ld32_nowait(tbase + AT_S_COL + half * 64 + 32, reinterpret_cast<uint32_t *>(&s[32]));
-                tmem_ld_wait();
-                if (nvis < (half + 1) * 64) {
-#pragma unroll
-                    for (int j = 0; j < 64; ++j)
-                        if (half * 64 + j >= nvis) s[j] = -INFINITY;
-                }
                 uint32_t pk[32];
                 float te[6], to[6];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     float x0, x1;
-                    ffma2(x0, x1, s[2 * i], s[2 * i + 1], c, c, -m, -m);
+                    ffma2(x0, x1, s[half * 64 + 2 * i], s[half * 64 + 2 * i + 1], c, c, -m, -m);
                     float e = ex2(x0), o = ex2(x1);
                     pk[i] = pack_bf16x2(__float_as_uint(e), __float_as_uint(o));
                     int lv = 0;
@@ -449,7 +452,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+    if (warp == Cfg::MMA_WARP) tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
 }
 
 }  // namespace
