@@ -39,24 +39,24 @@
 // cached prefix or a chunked prefill put around it, and whatever else is in
 // the launch.
 //
-// Structure (one CTA per query tile of 128 rows and NT = 2 query heads that
-// share one key/value head -- or NT = 1 head when the heads per key/value
-// head are odd, or when a call is small enough that one CTA per tile and
-// head still leaves SMs free -- with 64 + 128 NT threads):
-//   warp 0      TMA producer: the NT Q tiles once (two 64-column boxes
-//               each, 128-byte swizzle), then K and V of each key block
-//               into a ring of two 64 KB stages, shared by the NT heads
-//   warp 1      allocates 256 NT tensor-memory columns: per head the scores
-//               S (128 x 128 f32), whose first 64 columns then hold P as
-//               bf16 pairs, and the O accumulator (128 x 128 f32).  One lane
-//               issues, per head and block, O += P V (A = P read from tensor
-//               memory, B = V from shared memory) and then S = Q K^T of the
-//               next block into the same columns.  The two heads' softmaxes
-//               alternate with their tensor-core work, so while one head's
-//               softmax runs the tensor cores serve the other head.
-//   warps 2..   one warpgroup per head, one thread per query row: the
-//               softmax of each block (P as bf16 into tensor memory), the
-//               rare rescaling of its O row, and the output
+// Structure: one CTA per query tile of 128 rows and NT query heads of one
+// key/value head.  Warpgroup t (warps 4t .. 4t+3) is head t's softmax, one
+// thread per query row; after them a TMA producer warp (the NT Q tiles once,
+// then K and V of each key block into a ring of 64 KB stages, shared by the
+// heads) and an MMA warp, whose one lane issues S = Q K^T and O += P V (A = P
+// read from tensor memory, B = V from shared memory):
+//   NT = 2   (the call bound by its total work; the heads per key/value head
+//            even): 384 threads, a third warpgroup of producer, MMA and two
+//            idle warps giving registers to the softmax warpgroups through
+//            setmaxnreg.  Per head one S buffer; per block O += P V and then
+//            the next block's S into the same columns, head after head, so
+//            each head's softmax runs while the tensor cores serve the
+//            other head.
+//   NT = 1   (the call bound by its longest tile, or an odd group): 192
+//            threads, two S buffers: S of block b+2 goes into the buffer
+//            block b's P leaves, so the scores of block b+1 are ready while
+//            block b's softmax runs, and a tile's chain of blocks runs in
+//            about 0.55 of the time two paired heads take.
 // Shared memory carries only Q, K and V: P never leaves tensor memory, and
 // V is read by the P V product straight from its TMA box as an MN-major
 // operand (keys along K, head dimension contiguous).  The next block's
@@ -86,10 +86,6 @@ constexpr int AT_Q_BOX = AT_BQ * 64 * 2;           // 16 KB: 128 rows x 64 dims
 constexpr int AT_KV_BOX = AT_BKV * 64 * 2;         // 16 KB: 128 keys x 64 dims
 constexpr int AT_Q_BYTES = 2 * AT_Q_BOX;
 constexpr int AT_STAGE_BYTES = 4 * AT_KV_BOX;      // K (two boxes), then V (two boxes)
-constexpr int AT_STAGES = 2;
-constexpr uint32_t AT_HEAD_COLS = 256;             // tensor-memory columns per head
-constexpr uint32_t AT_S_COL = 0;                   // S: columns 0..127; P (bf16 pairs): 0..63
-constexpr uint32_t AT_O_COL = 128;                 // O: 128..255
 
 // Warp roles: warpgroup t (warps 4t .. 4t+3) is head t's softmax; then the
 // TMA producer warp and the MMA warp.  With two heads the block has a third,
@@ -97,13 +93,20 @@ constexpr uint32_t AT_O_COL = 128;                 // O: 128..255
 // registers from it to the two softmax warpgroups: launched at 168 a thread,
 // 200 for the softmax, 96 for the rest.
 constexpr int AT_REGS_SOFTMAX = 200, AT_REGS_OTHER = 96;
+// Tensor memory (512 columns either way; S is 128 x 128 f32, P its first 64
+// columns as bf16 pairs, O 128 x 128 f32):
+//   NT = 2: head t's S at columns 256t .. 256t+127, its O at 256t+128 ..
+//   NT = 1: two S buffers at 0 and 128 (block b in buffer b % 2), O at 256
 template <int NT>
 struct AttnCfg {
     static constexpr int PRODUCER_WARP = 4 * NT, MMA_WARP = 4 * NT + 1;
     static constexpr int THREADS = NT == 2 ? 384 : 192;
+    static constexpr int STAGES = NT == 2 ? 2 : 3;       // K/V blocks in flight
     static constexpr int KV_OFF = NT * AT_Q_BYTES;
-    static constexpr int SMEM = KV_OFF + AT_STAGES * AT_STAGE_BYTES + 1024;
-    static constexpr uint32_t TMEM_COLS = AT_HEAD_COLS * NT;
+    static constexpr int SMEM = KV_OFF + STAGES * AT_STAGE_BYTES + 1024;
+    static constexpr uint32_t TMEM_COLS = 512;
+    __device__ static constexpr uint32_t s_col(int t, int buf) { return NT == 2 ? 256u * t : 128u * buf; }
+    __device__ static constexpr uint32_t o_col(int t) { return NT == 2 ? 256u * t + 128u : 256u; }
     static_assert(SMEM <= 227 * 1024, "shared memory");
     static_assert(NT == 1 || 2 * 128 * AT_REGS_SOFTMAX + 128 * AT_REGS_OTHER <= THREADS * 168, "register split");
 };
@@ -211,10 +214,10 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                     unsigned int *err)
 {
     using Cfg = AttnCfg<NT>;
-    constexpr int NS = AT_STAGES;
+    constexpr int NS = Cfg::STAGES;
     pdl_trigger();
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t q_bar, kv_full[NS], kv_empty[NS], s_full[NT], p_full[NT], o_done[NT];
+    __shared__ __align__(8) uint64_t q_bar, kv_full[NS], kv_empty[NS], s_full[2], p_full[NT], o_done[NT];
     __shared__ uint32_t tmem_base_sh;
     uint8_t *smem = smem_align1024(smem_raw);
     uint8_t *sq = smem, *skv = smem + Cfg::KV_OFF;
@@ -234,8 +237,8 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             mbar_init(&kv_full[s], 1);
             mbar_init(&kv_empty[s], 1);
         }
+        for (int t = 0; t < 2; ++t) mbar_init(&s_full[t], 1);    // per head (NT = 2) or per S buffer (NT = 1)
         for (int t = 0; t < NT; ++t) {
-            mbar_init(&s_full[t], 1);
             mbar_init(&p_full[t], 4);
             mbar_init(&o_done[t], 1);
         }
@@ -277,41 +280,72 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                 // S: A = Q, B = K (both K-major, shared memory); O: A = P (tensor
                 // memory), B = V (MN-major, shared memory)
                 const uint32_t id_s = idesc_n(AT_BKV), id_o = idesc_n(AT_D) | (1u << 16);
-                auto issue_s = [&](int t, int st) {
+                // S into head t's columns (NT = 2) or into buffer buf (NT = 1)
+                auto issue_s = [&](int t, int buf, int st, uint64_t *bar) {
                     const uint32_t qa = smem_u32(sq + t * AT_Q_BYTES), ka = smem_u32(skv + st * AT_STAGE_BYTES);
-                    const uint32_t d = tmem_base + t * AT_HEAD_COLS + AT_S_COL;
-    #pragma unroll
+                    const uint32_t d = tmem_base + Cfg::s_col(t, buf);
+#pragma unroll
                     for (int half = 0; half < 2; ++half)
-    #pragma unroll
+#pragma unroll
                         for (int k = 0; k < 4; ++k)
                             umma_bf16(d, sw128_desc(qa + half * AT_Q_BOX + k * 32),
                                       sw128_desc(ka + half * AT_KV_BOX + k * 32), id_s, (half | k) != 0 ? 1u : 0u);
-                    umma_commit(&s_full[t]);
+                    umma_commit(bar);
+                };
+                // O += P V for block b of head t, P read from the columns S of block b left
+                auto issue_pv = [&](int t, int b, int buf, int st) {
+                    const uint32_t va = smem_u32(skv + st * AT_STAGE_BYTES + 2 * AT_KV_BOX);
+                    const uint32_t pa = tmem_base + Cfg::s_col(t, buf);
+                    const uint32_t d = tmem_base + Cfg::o_col(t);
+#pragma unroll
+                    for (int k = 0; k < AT_BKV / 16; ++k)
+                        umma_bf16_ts(d, pa + k * 8, sw128_mn_desc(va + k * 2048), id_o, (b | k) != 0 ? 1u : 0u);
+                };
+                auto wait_kv = [&](int b) {
+                    mbar_wait(&kv_full[b % NS], (uint32_t)(b / NS) & 1u, err, 0x63);
+                    tc_fence_after();
                 };
                 mbar_wait(&q_bar, 0, err, 0x62);
-                mbar_wait(&kv_full[0], 0, err, 0x63);
-                tc_fence_after();
-                for (int t = 0; t < NT; ++t) issue_s(t, 0);
-                for (int b = 0; b < nb; ++b) {
-                    const int st = b % NS;
-                    const uint32_t va = smem_u32(skv + st * AT_STAGE_BYTES + 2 * AT_KV_BOX);
-    #pragma unroll
-                    for (int t = 0; t < NT; ++t) {
-                        mbar_wait(&p_full[t], (uint32_t)b & 1u, err, 0x65);
-                        tc_fence_after();
-                        const uint32_t pa = tmem_base + t * AT_HEAD_COLS + AT_S_COL;
-                        const uint32_t d = tmem_base + t * AT_HEAD_COLS + AT_O_COL;
-    #pragma unroll
-                        for (int k = 0; k < AT_BKV / 16; ++k)
-                            umma_bf16_ts(d, pa + k * 8, sw128_mn_desc(va + k * 2048), id_o, (b | k) != 0 ? 1u : 0u);
-                        umma_commit(&o_done[t]);
-                        if (t == NT - 1) umma_commit(&kv_empty[st]);   // K and V of block b no longer read
-                        if (b + 1 < nb) {   // the next block's scores, into the columns P V has just read
-                            if (t == 0) {
-                                mbar_wait(&kv_full[(b + 1) % NS], (uint32_t)((b + 1) / NS) & 1u, err, 0x63);
-                                tc_fence_after();
+                if constexpr (NT == 2) {
+                    // per block: O += P V, then the next block's S into the same
+                    // columns, head 0 then head 1 (each head's softmax overlaps
+                    // the other head's products)
+                    wait_kv(0);
+                    for (int t = 0; t < NT; ++t) issue_s(t, 0, 0, &s_full[t]);
+                    for (int b = 0; b < nb; ++b) {
+#pragma unroll
+                        for (int t = 0; t < NT; ++t) {
+                            mbar_wait(&p_full[t], (uint32_t)b & 1u, err, 0x65);
+                            tc_fence_after();
+                            issue_pv(t, b, 0, b % NS);
+                            umma_commit(&o_done[t]);
+                            if (t == NT - 1) umma_commit(&kv_empty[b % NS]);   // K and V of block b no longer read
+                            if (b + 1 < nb) {   // the next block's scores, into the columns P V has just read
+                                if (t == 0) wait_kv(b + 1);
+                                issue_s(t, 0, (b + 1) % NS, &s_full[t]);
                             }
-                            issue_s(t, (b + 1) % NS);
+                        }
+                    }
+                } else {
+                    // two S buffers: S of blocks 0 and 1 first; then per block b,
+                    // O += P_b V_b and S of block b+2 into the buffer P_b was in,
+                    // so the scores of block b+1 are ready while block b's
+                    // softmax runs
+                    wait_kv(0);
+                    issue_s(0, 0, 0, &s_full[0]);
+                    if (nb > 1) {
+                        wait_kv(1);
+                        issue_s(0, 1, 1, &s_full[1]);
+                    }
+                    for (int b = 0; b < nb; ++b) {
+                        mbar_wait(&p_full[0], (uint32_t)b & 1u, err, 0x65);
+                        tc_fence_after();
+                        issue_pv(0, b, b & 1, b % NS);
+                        umma_commit(&o_done[0]);
+                        umma_commit(&kv_empty[b % NS]);
+                        if (b + 2 < nb) {
+                            wait_kv(b + 2);
+                            issue_s(0, b & 1, (b + 2) % NS, &s_full[b & 1]);
                         }
                     }
                 }
@@ -324,12 +358,16 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         // lanes 32*(w%4) .. +31
         const int t = warp >> 2, quad = warp & 3, row = quad * 32 + lane;
         const int pos = tile.pos0 + row;
-        const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + t * AT_HEAD_COLS;
+        const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16);
+        const uint32_t ocol = Cfg::o_col(t);
         float m = -INFINITY, l = 0.f;
 
 #pragma unroll 1
         for (int b = 0; b < nb; ++b) {
-            mbar_wait(&s_full[t], (uint32_t)b & 1u, err, 0x68);
+            // block b's scores: head t's columns (NT = 2), buffer b % 2 (NT = 1)
+            const int sb = NT == 2 ? t : (b & 1);
+            const uint32_t scol = Cfg::s_col(t, b & 1);
+            mbar_wait(&s_full[sb], NT == 2 ? ((uint32_t)b & 1u) : (((uint32_t)b >> 1) & 1u), err, 0x68);
             tc_fence_after();
             // The block's 128 scores (one tensor-memory wait), the keys the row
             // cannot see set to -inf, and the block maximum (eight chains; the
@@ -338,7 +376,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             float s[AT_BKV];
 #pragma unroll
             for (int ch = 0; ch < AT_BKV / 32; ++ch)
-                tmem_ld32_nowait(tbase + AT_S_COL + ch * 32, reinterpret_cast<uint32_t *>(&s[ch * 32]));
+                tmem_ld32_nowait(tbase + scol + ch * 32, reinterpret_cast<uint32_t *>(&s[ch * 32]));
             tmem_ld_wait();
             if (nvis < AT_BKV) {
 #pragma unroll
@@ -354,11 +392,12 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                                     fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * c;
             const bool move = bmc > m + AT_TAU;
 
-            // O holds blocks 0 .. b-1 here: the P V product of block b-1 was
-            // issued before this block's S.  The tensor-memory loads and
-            // stores are warp-wide (.sync.aligned): every lane of the warp
-            // takes them, a lane whose maximum stays with a = 1 (its O row is
-            // rewritten with the same bits).
+            // Before O is rescaled it must hold blocks 0 .. b-1: wait for block
+            // b-1's P V product (phase b-1 of o_done; block b-2's is complete,
+            // since this block's S was issued after it).  The tensor-memory
+            // loads and stores are warp-wide (.sync.aligned): every lane of the
+            // warp takes them, a lane whose maximum stays with a = 1 (its O row
+            // is rewritten with the same bits).
             if (__any_sync(0xFFFFFFFFu, move)) {
                 float a = 1.f;
                 if (move) {
@@ -372,11 +411,11 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
 #pragma unroll 1
                     for (int ch = 0; ch < AT_D / 32; ++ch) {
                         uint32_t r[32];
-                        tmem_ld32_nowait(tbase + AT_O_COL + ch * 32, r);
+                        tmem_ld32_nowait(tbase + ocol + ch * 32, r);
                         tmem_ld_wait();
 #pragma unroll
                         for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * a);
-                        tmem_st32(tbase + AT_O_COL + ch * 32, r);
+                        tmem_st32(tbase + ocol + ch * 32, r);
                     }
                 }
             }
@@ -407,7 +446,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                 }
                 re[half] = te[5];
                 ro[half] = to[5];
-                tmem_st32(tbase + AT_S_COL + half * 32, pk);
+                tmem_st32(tbase + scol + half * 32, pk);
             }
             float se, so;
             ffma2(se, so, re[0], ro[0], 1.f, 1.f, re[1], ro[1]);
@@ -428,7 +467,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
 #pragma unroll 1
         for (int ch = 0; ch < AT_D / 32; ++ch) {
             uint32_t r[32];
-            tmem_ld32_nowait(tbase + AT_O_COL + ch * 32, r);
+            tmem_ld32_nowait(tbase + ocol + ch * 32, r);
             tmem_ld_wait();
             if (store) {
 #pragma unroll
@@ -517,11 +556,19 @@ extern "C" bi_status bi_attention_prefill(const void *q, const void *k, const vo
             return st;
     }
     const int group = n_heads / n_kv_heads;
-    // Two heads of one key/value head per CTA where they pair up, so that one
-    // head's softmax overlaps the other's tensor-core work; but a call whose
-    // tiles fit the SMs one head per CTA runs that way (twice the CTAs, each
-    // chain a little shorter).  The per-head arithmetic is the same code.
-    const int NT = (group % 2 == 0 && (long long)tiles.size() * n_heads > d->sm_count) ? 2 : 1;
+    // Two heads of one key/value head per CTA share the K/V ring and keep the
+    // tensor cores busiest, which wins where the call is bound by the
+    // average work of an SM; one head per CTA (two score buffers) runs a
+    // tile's chain of blocks in about 0.55 of the time, which wins where the
+    // longest tile bounds the call.  The per-head arithmetic is the same
+    // either way.
+    int NT = 1;
+    if (group % 2 == 0) {
+        long long work = 0;                        // key blocks x head pairs
+        for (const AttnTile &t : tiles) work += (long long)attn_blocks(t.pos0, t.rows) * (n_heads / 2);
+        const long long longest = attn_blocks(tiles[0].pos0, tiles[0].rows);
+        if (longest * d->sm_count * 5 <= work * 6) NT = 2;
+    }
     const float c = scale * 1.44269504088896340736f;
     static_assert(sizeof(AttnTable) <= 8192, "kernel parameter space");
     auto launch = [&](auto kernel, int smem, int threads, int kid) -> bi_status {

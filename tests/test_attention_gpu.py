@@ -81,9 +81,9 @@ def _check_parity(bi, q_lens, kv_lens, nh, nkv, seed, scale=SCALE):
 # (q_lens, kv_lens, heads, kv heads): a single key; one query after a long
 # prefix; a full 128-row tile; several tiles with a ragged tail behind a
 # prefix that is not a multiple of 64; an empty request; MHA, GQA 2:1, 3:1
-# and 4:1, MQA.  A call whose query tiles times heads fit the 152 SMs of a
-# GB300 runs one head per CTA; the last two cases have more (11 tiles x 16
-# heads, 7 x 32) and run two heads of a key/value head per CTA.
+# and 4:1, MQA.  A call bound by its longest tile (all the small ones)
+# runs one head per CTA; the last two, bound by their total work on a
+# 152-SM GB300, run two heads of a key/value head per CTA.
 CASES = [
     ((1, 17, 128, 200, 0, 64), (1, 100, 128, 700, 5, 128), 4, 2),
     ((300,), (300,), 2, 2),
@@ -91,8 +91,8 @@ CASES = [
     ((1, 1, 1), (1, 64, 65), 4, 1),
     ((130, 129, 63), (130, 1153, 200), 4, 4),
     ((100, 50), (300, 50), 6, 2),
-    ((700, 600), (1500, 600), 16, 2),
-    ((300, 250, 200), (800, 250, 200), 32, 4),
+    ((1000, 1024, 900, 1100), (1000, 1500, 900, 1300), 16, 2),
+    ((700, 600, 650), (1500, 600, 900), 32, 2),
 ]
 
 
@@ -102,12 +102,12 @@ def test_attention_parity(bi, q_lens, kv_lens, nh, nkv):
 
 
 @pytest.mark.parametrize("q_lens,kv_lens,nh,nkv", [((150, 40), (400, 40), 2, 1), ((150, 40), (400, 40), 3, 3),
-                                                    ((300, 250, 200), (800, 250, 200), 32, 4)])
+                                                    ((1024,) * 4, (1024,) * 4, 32, 4)])
 def test_attention_parity_other_scale(bi, q_lens, kv_lens, nh, nkv):
     """A larger scale (peakier softmax: exponent gaps of tens), so that the
     rows' reference maxima move after the first block and O is rescaled in
     place, for warps where only some rows move; one head per CTA (the first
-    two) and two (the last: 7 tiles x 32 heads exceed the SMs)."""
+    two) and two (the last, bound by its total work)."""
     _check_parity(bi, q_lens, kv_lens, nh, nkv, seed=7, scale=0.5)
 
 
@@ -268,19 +268,17 @@ def test_rejects_bad_calls_on_device(bi):
 
 
 def test_one_head_and_two_head_ctas_give_the_same_bytes(bi):
-    """The prefill workload (32 query tiles x 16 heads, more than the SMs)
-    runs two heads per CTA; a request of it called alone (a few tiles) runs
-    one head per CTA.  Requests 1, 4 and 7 alone must give their rows inside
-    the batch byte for byte."""
-    nh, nkv = synth.ATTN_HEADS, synth.ATTN_KV_HEADS
-    qo, ko = synth.attention_offsets(synth.ATTN_Q_LENS, synth.ATTN_PREFIX)
-    Q, K, V = synth.attention_inputs(17, int(qo[-1]), int(ko[-1]), nh, nkv)
-    o, lse = _run(bi, Q, K, V, qo, ko, nh, nkv)
-    for r in (1, 4, 7):
-        a, b, c, d = qo[r], qo[r + 1], ko[r], ko[r + 1]
-        ro, rl = _run(bi, Q[a:b], K[c:d], V[c:d], [0, b - a], [0, d - c], nh, nkv)
-        assert np.array_equal(o[a:b], ro), r
-        assert np.array_equal(lse[a:b].view(np.uint32), rl.view(np.uint32)), r
+    """A 4096-token full prefill (32 tiles x 16 heads, bound by its total
+    work) runs two heads of a key/value head per CTA; its last 128 queries,
+    a chunk in the middle and its first 300 queries asked alone run one head
+    per CTA (each bound by its longest tile).  Same rows, same bytes."""
+    n, nh, nkv = 4096, 16, 2
+    Q, K, V = synth.attention_inputs(17, n, n, nh, nkv)
+    o, lse = _run(bi, Q, K, V, [0, n], [0, n], nh, nkv)
+    for a, b in ((n - 128, n), (1000, 1300), (0, 300)):
+        ro, rl = _run(bi, Q[a:b], K[:b], V[:b], [0, b - a], [0, b], nh, nkv)
+        assert np.array_equal(o[a:b], ro), (a, b)
+        assert np.array_equal(lse[a:b].view(np.uint32), rl.view(np.uint32)), (a, b)
 
 
 def test_max_heads_and_long_context(bi):
