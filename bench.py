@@ -64,9 +64,9 @@ NCU_TRAFFIC = {# in the layer sequence, caches as the preceding router call left
                                + 35_930_112 + 19_748_608 + 32_256 + 282_368) // 2,
                # one launch with the caches flushed: the reads; its bf16 output stays in L2
                "rmsnorm_kernel": 33_581_824 + 0,
-               # the mixed prefill batch, one launch with the caches flushed: Q, K, V read; the
-               # output stays in L2
-               "attn_prefill_kernel": 29_407_232 + 0}
+               # the mixed prefill batch (the one-head kernel), one launch with the caches flushed:
+               # Q, K, V read; the output stays in L2
+               "attn_prefill_kernel": 29_400_320 + 3_072}
 
 
 def fp32_peak(torch, dev) -> dict:
