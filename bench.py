@@ -815,9 +815,11 @@ def attention_measure(bi, synth, torch, dev, bf16_peak, reps=50):
           synth.device_normal((n, nkv, D), 83301, 1.0, torch.bfloat16, dev),
           synth.device_normal((n, nkv, D), 83302, 1.0, torch.bfloat16, dev)]
     o2 = torch.empty((n, nh, D), dtype=torch.bfloat16, device=dev)
-    t2 = timed(lambda i: bi.bi_attention_prefill(*ql, 1, [0, n], [0, n], nh, nkv, D, scale, o2, None), 10)
+    ws2 = bi.attention_workspace([0, n], [0, n], nh, dev)
+    t2 = timed(lambda i: bi.bi_attention_prefill(*ql, 1, [0, n], [0, n], nh, nkv, D, scale, o2, None, workspace=ws2),
+               10)
     flop2 = attention_flops([n], [0], nh, D)
-    del ql, o2
+    del ql, o2, ws2
     # a prefix-cache hit of one request: 128 new queries behind 32768 cached
     # tokens (one query tile: 16 CTAs, one head each)
     pre, nq = 32768, 128
@@ -825,7 +827,9 @@ def attention_measure(bi, synth, torch, dev, bf16_peak, reps=50):
           synth.device_normal((pre + nq, nkv, D), 83401, 1.0, torch.bfloat16, dev),
           synth.device_normal((pre + nq, nkv, D), 83402, 1.0, torch.bfloat16, dev)]
     o3 = torch.empty((nq, nh, D), dtype=torch.bfloat16, device=dev)
-    t3 = timed(lambda i: bi.bi_attention_prefill(*hq, 1, [0, nq], [0, pre + nq], nh, nkv, D, scale, o3, None), 10)
+    ws3 = bi.attention_workspace([0, nq], [0, pre + nq], nh, dev)
+    t3 = timed(lambda i: bi.bi_attention_prefill(*hq, 1, [0, nq], [0, pre + nq], nh, nkv, D, scale, o3, None,
+                                                 workspace=ws3), 10)
     flop3 = attention_flops([nq], [pre], nh, D)
     tiles = sum((int(q) + 127) // 128 for q in synth.ATTN_Q_LENS)
     return {"config": f"{Tq} queries in {len(qo_l) - 1} requests (q_len {list(synth.ATTN_Q_LENS)}, cached prefix "

@@ -379,10 +379,18 @@ BI_API bi_status bi_rmsnorm(const void *x, const void *w, bi_dtype dtype, int32_
  * pairwise trees over the block's 64 even- and 64 odd-position f32 p_j; and
  * O += sum_j bf16_rne(p_j) v_j as f32 tensor-core sums over the block's keys
  * in 16-deep steps, in increasing order.  Finally o = bf16_rne(O * (1/l))
- * and lse = (m + log2f(l)) * ln 2.  So a row's bits depend only on its own
- * query, its position and its request's keys and values: not on the other
- * requests, on how many of its request's queries are in the call (a cached
- * prefix, a chunked prefill), or on which query tile it falls in.
+ * and lse = (m + log2f(l)) * ln 2.  Keys come in chunks of 8192 (64
+ * blocks) at fixed positions: a row whose position is below 8192 is exactly
+ * the above; a later row's chunks c = 0 .. pos/8192 each run the above from
+ * a fresh state (m = -inf, l = 0, O = 0), giving (m_c, l_c, O_c), which are
+ * merged in chunk order: (M, L, N) = (m_0, l_0, O_0), then for c >= 1 with
+ * M' = max(M, m_c), a = 2^(M - M') and b = 2^(m_c - M') (each exactly 1
+ * where its maximum is M'), L = fmaf(L, a, l_c b), N = fmaf(N, a, O_c b),
+ * M = M' (products rounded once); o = bf16_rne(N * (1/L)), lse =
+ * (M + log2f(L)) * ln 2.  So a row's bits depend only on its own query, its
+ * position and its request's keys and values: not on the other requests,
+ * on how many of its request's queries are in the call (a cached prefix, a
+ * chunked prefill), or on which query tile it falls in.
  *
  *   q           [Tq, n_heads, 128] bf16, Tq = q_offsets[n_req]
  *   k, v        [Tkv, n_kv_heads, 128] bf16, Tkv = kv_offsets[n_req]
@@ -397,16 +405,25 @@ BI_API bi_status bi_rmsnorm(const void *x, const void *w, bi_dtype dtype, int32_
  *   scale       finite, > 0 (usually 1 / sqrt(head_dim))
  *   o           [Tq, n_heads, 128] bf16 output
  *   lse         [Tq, n_heads] f32 natural-log sum of exponentials, or NULL
+ *   workspace, workspace_bytes  caller-owned device buffer, 256-byte
+ *               aligned, at least bi_attention_workspace_bytes(n_req,
+ *               q_offsets, kv_offsets, n_heads) bytes: the chunks' partials of
+ *               the query tiles whose context runs past 8192 keys (0 bytes,
+ *               and NULL allowed, when none does); its contents do not
+ *               matter; nothing is allocated by the call.
+ *               Two calls that could overlap on the GPU must not share it.
  * All inputs must be finite.  Key and value rows past a request's end but
  * inside the tensors are read (they belong to the next request) and get
- * weight zero.  Tq == 0 returns BI_OK.  Nothing is allocated; the offsets
- * are read before the call returns.
+ * weight zero.  Tq == 0 returns BI_OK.  The offsets are read before the
+ * call returns.
  */
 #define BI_ATTN_MAX_HEADS 256
+BI_API size_t bi_attention_workspace_bytes(int32_t n_req, const int32_t *q_offsets, const int32_t *kv_offsets,
+                                          int32_t n_heads);
 BI_API bi_status bi_attention_prefill(const void *q, const void *k, const void *v, int32_t n_req,
                                       const int32_t *q_offsets, const int32_t *kv_offsets, int32_t n_heads,
                                       int32_t n_kv_heads, int32_t head_dim, float scale, void *o, float *lse,
-                                      bi_stream s);
+                                      void *workspace, size_t workspace_bytes, bi_stream s);
 
 /*
  * bi_moe_expert_gemm -- the grouped expert projection that consumes the

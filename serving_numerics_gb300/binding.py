@@ -44,7 +44,9 @@ SIGNATURES = {
     "bi_moe_workspace_bytes": (C.c_size_t, [_I32, _I32, _I32, _I32, _I32]),
     "bi_moe_expert_gemm": (C.c_int, [_P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, C.c_size_t, _P]),
     "bi_prefix_split": (C.c_int, [_P, _I32, _I32, _P, _P]),
-    "bi_attention_prefill": (C.c_int, [_P, _P, _P, _I32, _P, _P, _I32, _I32, _I32, C.c_float, _P, _P, _P]),
+    "bi_attention_prefill": (C.c_int, [_P, _P, _P, _I32, _P, _P, _I32, _I32, _I32, C.c_float, _P, _P, _P,
+                                       C.c_size_t, _P]),
+    "bi_attention_workspace_bytes": (C.c_size_t, [_I32, _P, _P, _I32]),
 }
 
 BI_TREE_PAIRWISE = 1
@@ -261,28 +263,46 @@ def _host_i32(a):
 
 
 def bi_attention_prefill(q, k, v, n_req, q_offsets, kv_offsets, n_heads, n_kv_heads, head_dim, scale, o_out,
-                         lse_out=None, stream=None, check=True):
-    """q_offsets and kv_offsets are host sequences of n_req + 1 ints."""
+                         lse_out=None, workspace=None, stream=None, check=True):
+    """q_offsets and kv_offsets are host sequences of n_req + 1 ints;
+    workspace a torch tensor (its whole storage), a (pointer, bytes) pair or
+    None (enough when no context runs past 8192 keys)."""
+    wp, wn = _workspace(workspace)
     st = load().bi_attention_prefill(_ptr(q), _ptr(k), _ptr(v), n_req, _host_i32(q_offsets),
                                      _host_i32(kv_offsets), n_heads, n_kv_heads, head_dim, C.c_float(scale),
-                                     _ptr(o_out), _ptr(lse_out), _stream(stream))
+                                     _ptr(o_out), _ptr(lse_out), wp, wn, _stream(stream))
     if check:
         _check(st, "bi_attention_prefill")
     return st
 
 
-def attention_prefill(q, k, v, q_offsets, kv_offsets, scale: float, stream=None, want_lse=True):
-    """Allocate outputs with torch and run bi_attention_prefill.  q [Tq,
-    n_heads, 128], k and v [Tkv, n_kv_heads, 128], all bfloat16; offsets
-    host sequences (0, running sums).  Returns (o bf16 [Tq, n_heads, 128],
-    lse f32 [Tq, n_heads] or None)."""
+def attention_workspace_bytes(q_offsets, kv_offsets, n_heads: int) -> int:
+    return int(load().bi_attention_workspace_bytes(len(q_offsets) - 1, _host_i32(q_offsets), _host_i32(kv_offsets),
+                                                   n_heads))
+
+
+def attention_workspace(q_offsets, kv_offsets, n_heads: int, device="cuda"):
+    """A caller-owned workspace for bi_attention_prefill (torch uint8 tensor,
+    or None when the call needs none)."""
+    import torch
+    n = attention_workspace_bytes(q_offsets, kv_offsets, n_heads)
+    return torch.empty(n, dtype=torch.uint8, device=device) if n else None
+
+
+def attention_prefill(q, k, v, q_offsets, kv_offsets, scale: float, stream=None, want_lse=True, workspace=None):
+    """Allocate outputs (and the workspace, unless given) with torch and run
+    bi_attention_prefill.  q [Tq, n_heads, 128], k and v [Tkv, n_kv_heads,
+    128], all bfloat16; offsets host sequences (0, running sums).  Returns
+    (o bf16 [Tq, n_heads, 128], lse f32 [Tq, n_heads] or None)."""
     import torch
     Tq, nh, D = q.shape
     nkv = k.shape[1]
     o = torch.empty((Tq, nh, D), dtype=torch.bfloat16, device=q.device)
     lse = torch.empty((Tq, nh), dtype=torch.float32, device=q.device) if want_lse else None
+    if workspace is None:
+        workspace = attention_workspace(q_offsets, kv_offsets, nh, q.device)
     bi_attention_prefill(q, k, v, len(q_offsets) - 1, q_offsets, kv_offsets, nh, nkv, D, scale, o, lse,
-                         stream=stream)
+                         workspace=workspace, stream=stream)
     return o, lse
 
 

@@ -111,19 +111,52 @@ struct AttnCfg {
     static_assert(NT == 1 || 2 * 128 * AT_REGS_SOFTMAX + 128 * AT_REGS_OTHER <= THREADS * 168, "register split");
 };
 
-// One query tile: up to 128 consecutive queries of one request.
+// Keys are cut into chunks of 64 blocks (8192 keys) at fixed positions.  A
+// row whose context fits the first chunk is computed in one pass; a longer
+// row's chunks are computed from fresh softmax states, each into a partial
+// (m, l, O), and merged in chunk order (merge_chunk below).
+constexpr int AT_CHUNK_BLOCKS = 64;
+constexpr int AT_CHUNK_KEYS = AT_CHUNK_BLOCKS * AT_BKV;
+constexpr int AT_PART_STRIDE = 132;                // floats per partial row: O[128], m, l, two spare
+
+// One work entry: key blocks [kb0, kb1) of a query tile (up to 128
+// consecutive queries of one request) -- the whole tile, or one chunk of it.
 struct AttnTile {
     int q0;     // token index of the tile's first query in q and o
     int kv0;    // token index of the request's first key in k and v
     int pos0;   // context position of the tile's first query
     int rows;   // queries in the tile (1..128)
+    int kb0;    // first key block (a multiple of AT_CHUNK_BLOCKS)
+    int kb1;    // one past the last key block
+    int part;   // the tile's scratch slot (mode 0, tiles past the first chunk), chunk's partial slot (mode 1), or -1
+    int mode;   // 0: one CTA walks the tile, merging chunk by chunk; 1: one chunk, its partial for the merge kernel
 };
-constexpr int kAttnMaxTiles = 512;                 // tiles per launch (8 KB of kernel parameters)
+constexpr int kAttnMaxTiles = 256;                 // entries per launch (8 KB of kernel parameters)
 struct AttnTable {
     AttnTile t[kAttnMaxTiles];
 };
 
 __host__ __device__ constexpr int attn_blocks(int pos0, int rows) { return (pos0 + rows - 1) / AT_BKV + 1; }
+
+// Merge of a row's chunk c >= 1 (m, l, O) into its running state (M, L, N)
+// (which starts as chunk 0's (m, l, O) unchanged): with M' = max(M, m),
+// a = 2^(M - M') and b = 2^(m - M') (each exactly 1 where its maximum is
+// M'), L = fmaf(L, a, l b) and N_d = fmaf(N_d, a, O_d b), every product
+// rounded once.
+__device__ __forceinline__ float ex2_merge(float x) { float y; asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x)); return y; }
+struct MergeWeights {
+    float a, b;
+};
+__device__ __forceinline__ MergeWeights merge_weights(float &M, float &L, float m, float l)
+{
+    const float Mn = fmaxf(M, m);
+    MergeWeights w;
+    w.a = M == Mn ? 1.f : ex2_merge(M - Mn);
+    w.b = m == Mn ? 1.f : ex2_merge(m - Mn);
+    L = fmaf(L, w.a, __fmul_rn(l, w.b));
+    M = Mn;
+    return w;
+}
 
 // Shared-memory descriptor of an MN-major operand with the 128-byte swizzle
 // as TMA lays it out from [keys][64 dims] boxes: along N (the head
@@ -206,18 +239,81 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t *r)
 
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// Chunk c of a row ends (its block's P V products done).  A row with keys
+// in chunk c:
+//   c == 0 and its context ends there: o from O (o = O / l)
+//   mode 0: chunk 0 starts its merged state (N = O in its scratch row, M = m,
+//           L = l); a later chunk merges into it (merge_weights), finishing
+//           the row in its last chunk
+//   mode 1: chunk c's (O, m, l) into the partial slot
+// Returns the merged (M, L).  Kept out of line: it runs once a chunk, and
+// inlined its registers would weigh on the block loop.  Every lane of the
+// warp calls it (the tensor-memory loads are warp-wide).
+__device__ __noinline__ float2 attn_chunk_end(int c, float m, float l, float M, float L, uint32_t otaddr, int lc,
+                                              bool valid, int mode, uint4 *dst, float4 *srow, float *lse_elem)
+{
+    const bool seq = mode == 0, has = valid && lc >= c;
+    const bool direct = has && c == 0 && lc == 0;
+    const bool merge = seq && has && c >= 1;
+    const bool merged_out = merge && c == lc;
+    const bool keep = (seq && has && lc > c) || (!seq && has && lc >= 1);
+    MergeWeights w = {1.f, 0.f};
+    if (merge) w = merge_weights(M, L, m, l);
+    else if (seq && has && c == 0 && lc >= 1) { M = m; L = l; }
+    const float rl = direct ? __frcp_rn(l) : (merged_out ? __frcp_rn(L) : 0.f);
+#pragma unroll 1
+    for (int ch = 0; ch < AT_D / 32; ++ch) {             // columns 32 ch .. 32 ch + 31
+        uint32_t r[32];
+        tmem_ld32_nowait(otaddr + ch * 32, r);
+        tmem_ld_wait();
+        float x[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(r[i]);
+        if (merge) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 n4 = srow[ch * 8 + i];
+                x[4 * i] = fmaf(n4.x, w.a, __fmul_rn(x[4 * i], w.b));
+                x[4 * i + 1] = fmaf(n4.y, w.a, __fmul_rn(x[4 * i + 1], w.b));
+                x[4 * i + 2] = fmaf(n4.z, w.a, __fmul_rn(x[4 * i + 2], w.b));
+                x[4 * i + 3] = fmaf(n4.w, w.a, __fmul_rn(x[4 * i + 3], w.b));
+            }
+        }
+        if (direct || merged_out) {
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                uint4 v;
+                v.x = pack_bf16x2(__float_as_uint(x[8 * g + 0] * rl), __float_as_uint(x[8 * g + 1] * rl));
+                v.y = pack_bf16x2(__float_as_uint(x[8 * g + 2] * rl), __float_as_uint(x[8 * g + 3] * rl));
+                v.z = pack_bf16x2(__float_as_uint(x[8 * g + 4] * rl), __float_as_uint(x[8 * g + 5] * rl));
+                v.w = pack_bf16x2(__float_as_uint(x[8 * g + 6] * rl), __float_as_uint(x[8 * g + 7] * rl));
+                dst[ch * 4 + g] = v;
+            }
+        }
+        if (keep) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                srow[ch * 8 + i] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+        }
+    }
+    if (lse_elem && direct) *lse_elem = (m + log2f(l)) * 0.693147180559945309f;
+    if (lse_elem && merged_out) *lse_elem = (M + log2f(L)) * 0.693147180559945309f;
+    if (!seq && has && lc >= 1) srow[AT_D / 4] = make_float4(m, l, 0.f, 0.f);
+    return make_float2(M, L);
+}
+
 template <int NT>
 __global__ void __launch_bounds__(AttnCfg<NT>::THREADS, 1)
 attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                     const __grid_constant__ CUtensorMap tmv, const __grid_constant__ AttnTable tab,
-                    __nv_bfloat16 *__restrict__ O, float *__restrict__ lse, int n_heads, int group, float c,
-                    unsigned int *err)
+                    __nv_bfloat16 *__restrict__ O, float *__restrict__ lse, float *__restrict__ part, int n_heads,
+                    int group, float c, unsigned int *err)
 {
     using Cfg = AttnCfg<NT>;
     constexpr int NS = Cfg::STAGES;
     pdl_trigger();
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t q_bar, kv_full[NS], kv_empty[NS], s_full[2], p_full[NT], o_done[NT];
+    __shared__ __align__(8) uint64_t q_bar, kv_full[NS], kv_empty[NS], s_full[2], p_full[NT], o_done[NT][2];
     __shared__ uint32_t tmem_base_sh;
     uint8_t *smem = smem_align1024(smem_raw);
     uint8_t *sq = smem, *skv = smem + Cfg::KV_OFF;
@@ -226,7 +322,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     const int pairs = n_heads / NT;
     const int ti = blockIdx.x / pairs, h0 = (blockIdx.x % pairs) * NT, hk = h0 / group;
     const AttnTile tile = tab.t[ti];
-    const int nb = attn_blocks(tile.pos0, tile.rows);
+    const int kb0 = tile.kb0, nb = tile.kb1 - tile.kb0;   // this CTA's key blocks: kb0 + 0 .. nb-1
 
     if (threadIdx.x == 0) {
         prefetch_tmap(&tmq);
@@ -240,7 +336,8 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         for (int t = 0; t < 2; ++t) mbar_init(&s_full[t], 1);    // per head (NT = 2) or per S buffer (NT = 1)
         for (int t = 0; t < NT; ++t) {
             mbar_init(&p_full[t], 4);
-            mbar_init(&o_done[t], 1);
+            mbar_init(&o_done[t][0], 1);   // P V of even blocks
+            mbar_init(&o_done[t][1], 1);   // of odd blocks
         }
         mbar_init_fence();
     }
@@ -267,7 +364,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                     const uint32_t ph = (uint32_t)(b / NS) & 1u;
                     mbar_wait(&kv_empty[st], ph ^ 1u, err, 0x61);
                     uint8_t *dst = skv + st * AT_STAGE_BYTES;
-                    const int key = tile.kv0 + b * AT_BKV;
+                    const int key = tile.kv0 + (kb0 + b) * AT_BKV;
                     mbar_arrive_expect_tx(&kv_full[st], (uint32_t)AT_STAGE_BYTES);
                     tma_load_3d(dst, &tmk, &kv_full[st], 0, hk, key);
                     tma_load_3d(dst + AT_KV_BOX, &tmk, &kv_full[st], 64, hk, key);
@@ -299,7 +396,8 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                     const uint32_t d = tmem_base + Cfg::o_col(t);
 #pragma unroll
                     for (int k = 0; k < AT_BKV / 16; ++k)
-                        umma_bf16_ts(d, pa + k * 8, sw128_mn_desc(va + k * 2048), id_o, (b | k) != 0 ? 1u : 0u);
+                        umma_bf16_ts(d, pa + k * 8, sw128_mn_desc(va + k * 2048), id_o,
+                                     ((kb0 + b) % AT_CHUNK_BLOCKS | k) != 0 ? 1u : 0u);   // O restarts with every chunk
                 };
                 auto wait_kv = [&](int b) {
                     mbar_wait(&kv_full[b % NS], (uint32_t)(b / NS) & 1u, err, 0x63);
@@ -318,7 +416,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                             mbar_wait(&p_full[t], (uint32_t)b & 1u, err, 0x65);
                             tc_fence_after();
                             issue_pv(t, b, 0, b % NS);
-                            umma_commit(&o_done[t]);
+                            umma_commit(&o_done[t][b & 1]);
                             if (t == NT - 1) umma_commit(&kv_empty[b % NS]);   // K and V of block b no longer read
                             if (b + 1 < nb) {   // the next block's scores, into the columns P V has just read
                                 if (t == 0) wait_kv(b + 1);
@@ -341,7 +439,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                         mbar_wait(&p_full[0], (uint32_t)b & 1u, err, 0x65);
                         tc_fence_after();
                         issue_pv(0, b, b & 1, b % NS);
-                        umma_commit(&o_done[0]);
+                        umma_commit(&o_done[0][b & 1]);
                         umma_commit(&kv_empty[b % NS]);
                         if (b + 2 < nb) {
                             wait_kv(b + 2);
@@ -360,19 +458,82 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         const int pos = tile.pos0 + row;
         const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16);
         const uint32_t ocol = Cfg::o_col(t);
-        float m = -INFINITY, l = 0.f;
+        float m = -INFINITY, l = 0.f;   // the current chunk's reference maximum and sum
+        float M = 0.f, L = 0.f;         // a row past the first chunk: its merged state (mode 0)
 
+        // P V of this CTA's block n done: block n's completion is phase n/2
+        // of barrier n%2; the caller has already seen the scores of a later
+        // block, so the product of block n-2 is complete and neither barrier
+        // is ever two phases from the one awaited.
+        auto wait_pv = [&](int n) {
+            mbar_wait(&o_done[t][n & 1], ((uint32_t)n >> 1) & 1u, err, 0x67);
+            tc_fence_after();
+        };
+        const int lc = pos / AT_CHUNK_KEYS;             // the row's last chunk
+        const bool valid = row < tile.rows;
+        const size_t orow = (size_t)(tile.q0 + (valid ? row : 0)) * (size_t)n_heads + (size_t)(h0 + t);
+        uint4 *dst = reinterpret_cast<uint4 *>(O + orow * AT_D);
+        float4 *srow = tile.part >= 0 ? reinterpret_cast<float4 *>(
+                           part + (((size_t)tile.part * n_heads + (h0 + t)) * AT_BQ + row) * AT_PART_STRIDE)
+                                      : nullptr;
+
+        auto chunk_end = [&](int c, int bl) {
+            wait_pv(bl);
+            const float2 ML = attn_chunk_end(c, m, l, M, L, tbase + ocol, lc, valid, tile.mode, dst, srow,
+                                             lse ? lse + orow : nullptr);
+            M = ML.x;
+            L = ML.y;
+        };
+
+        // blocks 0 .. nb-1, then b == nb closes the last chunk (one call site
+        // of chunk_end keeps the loop's code small)
 #pragma unroll 1
-        for (int b = 0; b < nb; ++b) {
+        for (int b = 0;; ++b) {
             // block b's scores: head t's columns (NT = 2), buffer b % 2 (NT = 1)
             const int sb = NT == 2 ? t : (b & 1);
             const uint32_t scol = Cfg::s_col(t, b & 1);
-            mbar_wait(&s_full[sb], NT == 2 ? ((uint32_t)b & 1u) : (((uint32_t)b >> 1) & 1u), err, 0x68);
-            tc_fence_after();
+            if (b < nb) {
+                mbar_wait(&s_full[sb], NT == 2 ? ((uint32_t)b & 1u) : (((uint32_t)b >> 1) & 1u), err, 0x68);
+                tc_fence_after();
+            }
+            const bool chunk_start = (kb0 + b) % AT_CHUNK_BLOCKS == 0;
+            if (b == nb && tile.part < 0) {             // a tile within the first chunk: o = O / l
+                wait_pv(b - 1);
+                const float rl = __frcp_rn(l);
+#pragma unroll 1
+                for (int ch = 0; ch < AT_D / 32; ++ch) {
+                    uint32_t r[32];
+                    tmem_ld32_nowait(tbase + ocol + ch * 32, r);
+                    tmem_ld_wait();
+                    if (valid) {
+#pragma unroll
+                        for (int g = 0; g < 4; ++g) {
+                            uint4 v;
+                            v.x = pack_bf16x2(__float_as_uint(__uint_as_float(r[8 * g + 0]) * rl),
+                                              __float_as_uint(__uint_as_float(r[8 * g + 1]) * rl));
+                            v.y = pack_bf16x2(__float_as_uint(__uint_as_float(r[8 * g + 2]) * rl),
+                                              __float_as_uint(__uint_as_float(r[8 * g + 3]) * rl));
+                            v.z = pack_bf16x2(__float_as_uint(__uint_as_float(r[8 * g + 4]) * rl),
+                                              __float_as_uint(__uint_as_float(r[8 * g + 5]) * rl));
+                            v.w = pack_bf16x2(__float_as_uint(__uint_as_float(r[8 * g + 6]) * rl),
+                                              __float_as_uint(__uint_as_float(r[8 * g + 7]) * rl));
+                            dst[ch * 4 + g] = v;
+                        }
+                    }
+                }
+                if (valid && lse) lse[orow] = (m + log2f(l)) * 0.693147180559945309f;
+                break;
+            }
+            if (b == nb || (b > 0 && chunk_start)) {    // a chunk ends with block b-1
+                chunk_end((kb0 + b - 1) / AT_CHUNK_BLOCKS, b - 1);
+                if (b == nb) break;
+                m = -INFINITY;
+                l = 0.f;
+            }
             // The block's 128 scores (one tensor-memory wait), the keys the row
             // cannot see set to -inf, and the block maximum (eight chains; the
             // maximum is exact in any order).
-            const int nvis = pos - b * AT_BKV + 1;       // keys of this block the row sees
+            const int nvis = pos - (kb0 + b) * AT_BKV + 1;   // keys of this block the row sees
             float s[AT_BKV];
 #pragma unroll
             for (int ch = 0; ch < AT_BKV / 32; ++ch)
@@ -392,12 +553,12 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                                     fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * c;
             const bool move = bmc > m + AT_TAU;
 
-            // Before O is rescaled it must hold blocks 0 .. b-1: wait for block
-            // b-1's P V product (phase b-1 of o_done; block b-2's is complete,
-            // since this block's S was issued after it).  The tensor-memory
-            // loads and stores are warp-wide (.sync.aligned): every lane of the
-            // warp takes them, a lane whose maximum stays with a = 1 (its O row
-            // is rewritten with the same bits).
+            // Before O is rescaled it must hold the chunk's blocks before b:
+            // wait for block b-1's P V product (at a chunk's first block O is
+            // about to restart, so there is nothing to rescale).  The
+            // tensor-memory loads and stores are warp-wide (.sync.aligned):
+            // every lane of the warp takes them, a lane whose maximum stays
+            // with a = 1 (its O row is rewritten with the same bits).
             if (__any_sync(0xFFFFFFFFu, move)) {
                 float a = 1.f;
                 if (move) {
@@ -405,9 +566,8 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                     l *= a;
                     m = bmc;
                 }
-                if (b >= 1) {
-                    mbar_wait(&o_done[t], (uint32_t)(b - 1) & 1u, err, 0x67);
-                    tc_fence_after();
+                if (!chunk_start) {                      // a new chunk's O starts from zero
+                    wait_pv(b - 1);
 #pragma unroll 1
                     for (int ch = 0; ch < AT_D / 32; ++ch) {
                         uint32_t r[32];
@@ -457,35 +617,6 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             __syncwarp();
             if (lane == 0) mbar_arrive(&p_full[t]);
         }
-
-        mbar_wait(&o_done[t], (uint32_t)(nb - 1) & 1u, err, 0x67);
-        tc_fence_after();
-        const float rl = __frcp_rn(l);
-        const bool store = row < tile.rows;
-        const size_t orow = (size_t)(tile.q0 + (store ? row : 0)) * (size_t)n_heads + (size_t)(h0 + t);
-        uint4 *dst = reinterpret_cast<uint4 *>(O + orow * AT_D);
-#pragma unroll 1
-        for (int ch = 0; ch < AT_D / 32; ++ch) {
-            uint32_t r[32];
-            tmem_ld32_nowait(tbase + ocol + ch * 32, r);
-            tmem_ld_wait();
-            if (store) {
-#pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    uint4 v;
-                    v.x = pack_bf16x2(__float_as_uint(__uint_as_float(r[8 * g + 0]) * rl),
-                                      __float_as_uint(__uint_as_float(r[8 * g + 1]) * rl));
-                    v.y = pack_bf16x2(__float_as_uint(__uint_as_float(r[8 * g + 2]) * rl),
-                                      __float_as_uint(__uint_as_float(r[8 * g + 3]) * rl));
-                    v.z = pack_bf16x2(__float_as_uint(__uint_as_float(r[8 * g + 4]) * rl),
-                                      __float_as_uint(__uint_as_float(r[8 * g + 5]) * rl));
-                    v.w = pack_bf16x2(__float_as_uint(__uint_as_float(r[8 * g + 6]) * rl),
-                                      __float_as_uint(__uint_as_float(r[8 * g + 7]) * rl));
-                    dst[ch * 4 + g] = v;
-                }
-            }
-        }
-        if (store && lse) lse[orow] = (m + log2f(l)) * 0.693147180559945309f;
     }
 
     tc_fence_before();
@@ -494,50 +625,183 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     if (warp == Cfg::MMA_WARP) tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
 }
 
+// The rows of split tiles whose context runs past the first chunk: merge
+// their chunks' partials in chunk order (merge_weights), then o and lse as
+// in one pass.  One warp per (tile, head, row), four columns a lane.
+struct AttnSplit {
+    int q0, pos0, rows, slot0;   // the tile's first query, its position and rows; chunk c's partial slot = slot0 + c
+};
+constexpr int kAttnMaxSplits = 512;
+struct AttnSplitTable {
+    AttnSplit t[kAttnMaxSplits];
+};
+
+__global__ void __launch_bounds__(256)
+attn_combine_kernel(const __grid_constant__ AttnSplitTable tab, int n_split, const float *__restrict__ part,
+                    __nv_bfloat16 *__restrict__ O, float *__restrict__ lse, int n_heads)
+{
+    pdl_trigger();
+    pdl_wait();
+    const int lane = threadIdx.x & 31;
+    const long long w = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const long long per_split = (long long)n_heads * AT_BQ;
+    if (w >= (long long)n_split * per_split) return;
+    const AttnSplit sp = tab.t[w / per_split];
+    const int h = (int)((w % per_split) / AT_BQ), row = (int)(w % AT_BQ);
+    if (row >= sp.rows) return;
+    const int pos = sp.pos0 + row, lc = pos / AT_CHUNK_KEYS;
+    if (lc == 0) return;                               // finished by its chunk-0 CTA
+    auto prow = [&](int ck) {
+        return part + (((size_t)(sp.slot0 + ck) * n_heads + h) * AT_BQ + row) * AT_PART_STRIDE;
+    };
+    const float *p0 = prow(0);
+    float M = p0[AT_D], L = p0[AT_D + 1];
+    float4 N = reinterpret_cast<const float4 *>(p0)[lane];
+    for (int ck = 1; ck <= lc; ++ck) {
+        const float *pc = prow(ck);
+        const MergeWeights mw = merge_weights(M, L, pc[AT_D], pc[AT_D + 1]);
+        const float4 Oc = reinterpret_cast<const float4 *>(pc)[lane];
+        N.x = fmaf(N.x, mw.a, __fmul_rn(Oc.x, mw.b));
+        N.y = fmaf(N.y, mw.a, __fmul_rn(Oc.y, mw.b));
+        N.z = fmaf(N.z, mw.a, __fmul_rn(Oc.z, mw.b));
+        N.w = fmaf(N.w, mw.a, __fmul_rn(Oc.w, mw.b));
+    }
+    const float rl = __frcp_rn(L);
+    const size_t orow = (size_t)(sp.q0 + row) * (size_t)n_heads + (size_t)h;
+    uint2 v;
+    v.x = pack_bf16x2(__float_as_uint(N.x * rl), __float_as_uint(N.y * rl));
+    v.y = pack_bf16x2(__float_as_uint(N.z * rl), __float_as_uint(N.w * rl));
+    reinterpret_cast<uint2 *>(O + orow * AT_D)[lane] = v;
+    if (lane == 0 && lse) lse[orow] = (M + log2f(L)) * 0.693147180559945309f;
+}
+
 }  // namespace
 }  // namespace bi
 
 using namespace bi;
 
+// The work of one call.  A query tile whose context ends within the first
+// chunk is one entry.  A longer tile is either one entry whose CTA walks its
+// chunks in turn, merging each into the tile's scratch slot (mode 0: the
+// call is bound by its total work), or an entry per chunk, each leaving its
+// partial in a slot for the merge kernel (mode 1: the call is bound by its
+// longest tile, and the chunks of a long tile then run on other SMs at the
+// same time).  The arithmetic, and so every bit of the result, is the same.
+// Longest entries first: the CTAs that run longest start first.
+struct AttnPlan {
+    std::vector<AttnTile> entries;
+    std::vector<AttnSplit> splits;
+    long long slots = 0;
+};
+
+// Workspace: the slots, [slot][head][row][AT_PART_STRIDE] f32 (the split
+// plan's count bounds the other's).
+static size_t attn_workspace_size(const AttnPlan &pl, int n_heads)
+{
+    return (size_t)pl.slots * (size_t)n_heads * AT_BQ * AT_PART_STRIDE * sizeof(float);
+}
+
+static bool attn_plan(int n_req, const int32_t *q_offsets, const int32_t *kv_offsets, bool split, AttnPlan &pl)
+{
+    for (int r = 0; r < n_req; ++r) {
+        const int ql = q_offsets[r + 1] - q_offsets[r], kl = kv_offsets[r + 1] - kv_offsets[r];
+        for (int t0 = 0; t0 < ql; t0 += AT_BQ) {
+            const int rows = std::min(AT_BQ, ql - t0), pos0 = kl - ql + t0;
+            const int nb = attn_blocks(pos0, rows);
+            if (nb <= AT_CHUNK_BLOCKS) {
+                pl.entries.push_back({q_offsets[r] + t0, kv_offsets[r], pos0, rows, 0, nb, -1, 0});
+                continue;
+            }
+            const int nch = (nb + AT_CHUNK_BLOCKS - 1) / AT_CHUNK_BLOCKS;
+            if (pl.slots + nch > INT32_MAX) return false;
+            if (!split) {
+                pl.entries.push_back({q_offsets[r] + t0, kv_offsets[r], pos0, rows, 0, nb, (int)pl.slots, 0});
+                pl.slots += 1;
+                continue;
+            }
+            pl.splits.push_back({q_offsets[r] + t0, pos0, rows, (int)pl.slots});
+            for (int ck = 0; ck < nch; ++ck)
+                pl.entries.push_back({q_offsets[r] + t0, kv_offsets[r], pos0, rows, ck * AT_CHUNK_BLOCKS,
+                                      std::min(nb, (ck + 1) * AT_CHUNK_BLOCKS), (int)pl.slots + ck, 1});
+            pl.slots += nch;
+        }
+    }
+    std::stable_sort(pl.entries.begin(), pl.entries.end(),
+                     [](const AttnTile &x, const AttnTile &y) { return x.kb1 - x.kb0 > y.kb1 - y.kb0; });
+    return true;
+}
+
+// Whether a call is bound by its longest tile: the tile's key blocks times
+// the SMs against 1.2 times the call's key blocks times head pairs.
+static bool attn_longest_bound(long long longest, long long work_pairs, int sm_count)
+{
+    return longest * sm_count * 5 > work_pairs * 6;
+}
+
+static bi_status attn_check_offsets(int32_t n_req, const int32_t *q_offsets, const int32_t *kv_offsets)
+{
+    if (n_req > 0 && (!q_offsets || !kv_offsets)) return BI_ERR_INVALID_ARG;
+    if (n_req == 0) return BI_OK;
+    if (q_offsets[0] != 0 || kv_offsets[0] != 0) return BI_ERR_INVALID_ARG;
+    for (int r = 0; r < n_req; ++r) {
+        const int64_t ql = (int64_t)q_offsets[r + 1] - q_offsets[r], kl = (int64_t)kv_offsets[r + 1] - kv_offsets[r];
+        if (ql < 0 || kl < 0 || ql > kl) return BI_ERR_INVALID_ARG;
+    }
+    return BI_OK;
+}
+
+extern "C" size_t bi_attention_workspace_bytes(int32_t n_req, const int32_t *q_offsets, const int32_t *kv_offsets,
+                                              int32_t n_heads)
+{
+    if (n_req < 0 || n_heads <= 0 || attn_check_offsets(n_req, q_offsets, kv_offsets) != BI_OK) return 0;
+    AttnPlan pl;
+    if (!attn_plan(n_req, q_offsets, kv_offsets, true, pl)) return 0;
+    return attn_workspace_size(pl, n_heads);
+}
+
 extern "C" bi_status bi_attention_prefill(const void *q, const void *k, const void *v, int32_t n_req,
                                           const int32_t *q_offsets, const int32_t *kv_offsets, int32_t n_heads,
                                           int32_t n_kv_heads, int32_t head_dim, float scale, void *o, float *lse,
-                                          bi_stream s)
+                                          void *workspace, size_t workspace_bytes, bi_stream s)
 {
     if (n_req < 0 || n_heads <= 0 || n_kv_heads <= 0) return BI_ERR_INVALID_ARG;
-    if (n_req > 0 && (!q_offsets || !kv_offsets)) return BI_ERR_INVALID_ARG;
     if (!(scale > 0.f) || !std::isfinite(scale)) return BI_ERR_INVALID_ARG;
     if (n_heads % n_kv_heads != 0) return BI_ERR_INVALID_ARG;
     if (head_dim != AT_D) return BI_ERR_UNSUPPORTED_SHAPE;
     if (n_heads > BI_ATTN_MAX_HEADS) return BI_ERR_UNSUPPORTED_SHAPE;
+    bi_status st = attn_check_offsets(n_req, q_offsets, kv_offsets);
+    if (st != BI_OK) return st;
     if (n_req == 0) return BI_OK;
-    if (q_offsets[0] != 0 || kv_offsets[0] != 0) return BI_ERR_INVALID_ARG;
-    for (int r = 0; r < n_req; ++r) {
-        const int32_t ql = q_offsets[r + 1] - q_offsets[r], kl = kv_offsets[r + 1] - kv_offsets[r];
-        if (ql < 0 || kl < 0 || ql > kl) return BI_ERR_INVALID_ARG;
-    }
     const int64_t Tq = q_offsets[n_req], Tkv = kv_offsets[n_req];
     if (Tq == 0) return BI_OK;
     if (!q || !k || !v || !o) return BI_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return BI_ERR_MISALIGNED;
     if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return BI_ERR_MISALIGNED;
 
-    Device *d = nullptr;
-    bi_status st = current_device(&d);
-    if (st != BI_OK) return st;
+    AttnPlan bound;                                    // the workspace the caller was told to provide
+    if (!attn_plan(n_req, q_offsets, kv_offsets, true, bound)) return BI_ERR_UNSUPPORTED_SHAPE;
+    const size_t need = attn_workspace_size(bound, n_heads);
+    if (need > 0) {
+        if (!workspace || workspace_bytes < need) return BI_ERR_INVALID_ARG;
+        if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return BI_ERR_MISALIGNED;
+    }
 
-    // The query tiles, longest (most key blocks) first so that the CTAs
-    // that take longest start first; the order changes no result.
-    std::vector<AttnTile> tiles;
+    Device *d = nullptr;
+    if ((st = current_device(&d)) != BI_OK) return st;
+    // split long tiles into chunk CTAs where the call is bound by its longest tile
+    long long work = 0, longest = 0;
     for (int r = 0; r < n_req; ++r) {
         const int ql = q_offsets[r + 1] - q_offsets[r], kl = kv_offsets[r + 1] - kv_offsets[r];
-        for (int t0 = 0; t0 < ql; t0 += AT_BQ)
-            tiles.push_back({q_offsets[r] + t0, kv_offsets[r], kl - ql + t0, std::min(AT_BQ, ql - t0)});
+        for (int t0 = 0; t0 < ql; t0 += AT_BQ) {
+            const long long nb = attn_blocks(kl - ql + t0, std::min(AT_BQ, ql - t0));
+            work += nb * std::max(1, n_heads / 2);
+            longest = std::max(longest, nb);
+        }
     }
-    std::stable_sort(tiles.begin(), tiles.end(), [](const AttnTile &x, const AttnTile &y) {
-        return attn_blocks(x.pos0, x.rows) > attn_blocks(y.pos0, y.rows);
-    });
-
+    AttnPlan pl;
+    if (!attn_plan(n_req, q_offsets, kv_offsets, attn_longest_bound(longest, work, d->sm_count), pl))
+        return BI_ERR_UNSUPPORTED_SHAPE;
+    const std::vector<AttnTile> &tiles = pl.entries;
     alignas(64) CUtensorMap tmq, tmk, tmv;
     {
         const uint64_t dims[3] = {(uint64_t)AT_D, (uint64_t)n_heads, (uint64_t)Tq};
@@ -565,9 +829,9 @@ extern "C" bi_status bi_attention_prefill(const void *q, const void *k, const vo
     int NT = 1;
     if (group % 2 == 0) {
         long long work = 0;                        // key blocks x head pairs
-        for (const AttnTile &t : tiles) work += (long long)attn_blocks(t.pos0, t.rows) * (n_heads / 2);
-        const long long longest = attn_blocks(tiles[0].pos0, tiles[0].rows);
-        if (longest * d->sm_count * 5 <= work * 6) NT = 2;
+        for (const AttnTile &t : tiles) work += (long long)(t.kb1 - t.kb0) * (n_heads / 2);
+        const long long longest = tiles[0].kb1 - tiles[0].kb0;
+        if (!attn_longest_bound(longest, work, d->sm_count)) NT = 2;
     }
     const float c = scale * 1.44269504088896340736f;
     static_assert(sizeof(AttnTable) <= 8192, "kernel parameter space");
@@ -580,11 +844,24 @@ extern "C" bi_status bi_attention_prefill(const void *q, const void *k, const vo
             std::copy(tiles.begin() + first, tiles.begin() + first + n, tab.t);
             e = launch_pdl(kernel, dim3((unsigned)(n * (n_heads / NT))), dim3(threads), (size_t)smem,
                            reinterpret_cast<cudaStream_t>(s), tmq, tmk, tmv, tab, static_cast<__nv_bfloat16 *>(o),
-                           lse, (int)n_heads, group, c, d->err);
+                           lse, static_cast<float *>(workspace), (int)n_heads, group, c, d->err);
             if (e != BI_OK) return e;
         }
         return BI_OK;
     };
-    if (NT == 2) return launch(attn_prefill_kernel<2>, AttnCfg<2>::SMEM, AttnCfg<2>::THREADS, KID_ATTN + 1);
-    return launch(attn_prefill_kernel<1>, AttnCfg<1>::SMEM, AttnCfg<1>::THREADS, KID_ATTN);
+    st = NT == 2 ? launch(attn_prefill_kernel<2>, AttnCfg<2>::SMEM, AttnCfg<2>::THREADS, KID_ATTN + 1)
+                 : launch(attn_prefill_kernel<1>, AttnCfg<1>::SMEM, AttnCfg<1>::THREADS, KID_ATTN);
+    if (st != BI_OK || pl.splits.empty()) return st;
+    if ((st = set_smem_once(d, KID_ATTN + 2, attn_combine_kernel, 0)) != BI_OK) return st;
+    AttnSplitTable stab;
+    for (size_t first = 0; first < pl.splits.size(); first += kAttnMaxSplits) {
+        const int n = (int)std::min<size_t>(kAttnMaxSplits, pl.splits.size() - first);
+        std::copy(pl.splits.begin() + first, pl.splits.begin() + first + n, stab.t);
+        const long long warps = (long long)n * n_heads * AT_BQ;
+        st = launch_pdl(attn_combine_kernel, dim3((unsigned)((warps + 7) / 8)), dim3(256), 0,
+                        reinterpret_cast<cudaStream_t>(s), stab, n, static_cast<const float *>(workspace),
+                        static_cast<__nv_bfloat16 *>(o), lse, (int)n_heads);
+        if (st != BI_OK) return st;
+    }
+    return BI_OK;
 }

@@ -233,11 +233,11 @@ def test_router_plan_validation(lib):
 
 
 def _attn(lib, q=FAKE, k=FAKE, v=FAKE, qo=(0, 4), ko=(0, 9), nh=4, nkv=2, D=128, scale=0.088, o=FAKE,
-          lse=None):
+          lse=None, ws=None, wsb=0):
     n = len(qo) - 1
     qa = (C.c_int32 * len(qo))(*qo) if qo is not None else None
     ka = (C.c_int32 * len(ko))(*ko) if ko is not None else None
-    return lib.bi_attention_prefill(q, k, v, n, qa, ka, nh, nkv, D, C.c_float(scale), o, lse, None)
+    return lib.bi_attention_prefill(q, k, v, n, qa, ka, nh, nkv, D, C.c_float(scale), o, lse, ws, wsb, None)
 
 
 @pytest.mark.parametrize("kw,want", [
@@ -257,4 +257,32 @@ def test_attention_empty_calls_are_noops(lib):
     assert _attn(lib, q=None, k=None, v=None, o=None, qo=(0,), ko=(0,)) == 0
     assert _attn(lib, q=None, k=None, v=None, o=None, qo=(0, 0, 0), ko=(0, 5, 7)) == 0
     assert lib.bi_attention_prefill(None, None, None, 1, None, None, 4, 2, 128, C.c_float(0.1), None, None,
-                                    None) == 1
+                                    None, 0, None) == 1
+
+
+def _wsb(lib, qo, ko, nh):
+    return lib.bi_attention_workspace_bytes(len(qo) - 1, (C.c_int32 * len(qo))(*qo), (C.c_int32 * len(ko))(*ko), nh)
+
+
+def test_attention_workspace_bytes(lib):
+    """Contexts within 8192 keys need none; past it, one partial slot per
+    8192-key chunk of each query tile that reaches beyond, of 128 rows x
+    132 floats per head."""
+    slot = 128 * 132 * 4
+    cnt = lambda splits, nh: 0
+    assert _wsb(lib, (0, 4096), (0, 4096), 16) == 0
+    assert _wsb(lib, (0, 128), (0, 8192), 16) == 0                    # positions 8064..8191: one chunk
+    assert _wsb(lib, (0, 128), (0, 8193), 16) == 2 * 16 * slot + cnt(1, 16)   # position 8192 opens chunk 1
+    assert _wsb(lib, (0, 128, 256), (0, 32896, 65792), 4) == (5 + 5) * 4 * slot + cnt(2, 4)   # 257 blocks each
+    assert _wsb(lib, (0, 128, 256), (0, 32896, 33024), 4) == 5 * 4 * slot + cnt(1, 4)         # the second fits
+    assert _wsb(lib, (0, 4), (0, 3), 4) == 0                           # invalid offsets: 0
+    assert _wsb(lib, (1, 4), (1, 9), 4) == 0
+
+
+def test_attention_rejects_a_small_workspace(lib):
+    qo, ko = (0, 128), (0, 20000)
+    n = _wsb(lib, qo, ko, 4)
+    assert n > 0
+    assert _attn(lib, qo=qo, ko=ko, ws=None, wsb=0) == 1
+    assert _attn(lib, qo=qo, ko=ko, ws=FAKE, wsb=n - 1) == 1
+    assert _attn(lib, qo=qo, ko=ko, ws=MIS, wsb=n) == 3

@@ -310,3 +310,80 @@ def test_max_heads_and_long_context(bi):
     suf, suf_l = _run(bi, Q[n - 100:], K, V, [0, 100], [0, n], nh, nkv)
     assert np.array_equal(suf, o[n - 100:])
     assert np.array_equal(suf_l.view(np.uint32), lse[n - 100:].view(np.uint32))
+
+
+def _oracle_rows(Q, K, V, rows_pos, heads, g, scale=SCALE):
+    """The oracle one query and head at a time: rows_pos = [(row in Q, position)]."""
+    from oracle import attention as oatt
+    out = {}
+    for r, p in rows_pos:
+        for h in heads:
+            hk = h // g
+            ro, rl = oatt.attention_prefill(Q[r:r + 1, h:h + 1], K[:p + 1, hk:hk + 1], V[:p + 1, hk:hk + 1],
+                                            [0, 1], [0, p + 1], scale)
+            vmax = np.abs(gu_bf16_to_f64(V[:p + 1, hk])).max()
+            out[(r, h)] = (ro[0, 0], rl[0, 0], vmax)
+    return out
+
+
+def _check_rows(o, lse, ref):
+    got = gu_bf16_to_f64(o)
+    for (r, h), (ro, rl, vmax) in ref.items():
+        tol = 1.05 * 2.0 ** -8 * vmax + 2.0 ** -8 * np.abs(ro)
+        assert (np.abs(got[r, h] - ro) <= tol).all(), (r, h)
+        assert abs(lse[r, h] - rl) <= 2.0 ** -8 + 1e-5 * abs(rl), (r, h)
+
+
+def test_chunked_context_parity_and_invariance(bi):
+    """Past 8192 keys a row's context is computed in 8192-key chunks merged
+    in order.  An 8300-token context: rows just below and above the chunk
+    boundary against the oracle; the full prefill, two suffixes (one whose
+    tile straddles the boundary, one entirely past it) and a prefill chunked
+    across the boundary give the same bytes."""
+    n, nh, nkv = 8300, 4, 2
+    Q, K, V = _context(31, n, nh, nkv)
+    full, full_l = _run(bi, Q, K, V, [0, n], [0, n], nh, nkv)
+    rows = [0, 8063, 8064, 8191, 8192, 8193, 8255, 8256, n - 1]
+    _check_rows(full, full_l, _oracle_rows(Q, K, V, [(r, r) for r in rows], range(nh), nh // nkv))
+    for ql in (150, 50):
+        o, lse = _run(bi, Q[n - ql:], K, V, [0, ql], [0, n], nh, nkv)
+        assert np.array_equal(o, full[n - ql:]), ql
+        assert np.array_equal(lse.view(np.uint32), full_l[n - ql:].view(np.uint32)), ql
+    parts = []
+    for a, b in ((0, 8100), (8100, 8200), (8200, n)):
+        o, _ = _run(bi, Q[a:b], K[:b], V[:b], [0, b - a], [0, b], nh, nkv)
+        parts.append(o)
+    assert np.array_equal(np.concatenate(parts), full)
+
+
+def test_long_prefix_cache_hit(bi):
+    """One request's prefix-cache hit: 128 queries behind 20000 cached tokens
+    (three chunks, 16 query heads over 2), against the oracle on sampled rows
+    and heads, and the same rows inside a batch with a short request."""
+    nh, nkv = 16, 2
+    pre, nq = 20000, 128
+    Q, K, V = synth.attention_inputs(32, nq, pre + nq, nh, nkv)
+    o, lse = _run(bi, Q, K, V, [0, nq], [0, pre + nq], nh, nkv)
+    ref = _oracle_rows(Q, K, V, [(r, pre + r) for r in (0, 1, 63, 127)], (0, 7, 8, 15), nh // nkv)
+    _check_rows(o, lse, ref)
+    Qs, Ks, Vs = synth.attention_inputs(33, 40, 300, nh, nkv)
+    ob, lb = _run(bi, np.concatenate([Qs, Q]), np.concatenate([Ks, K]), np.concatenate([Vs, V]),
+                  [0, 40, 40 + nq], [0, 300, 300 + pre + nq], nh, nkv)
+    assert np.array_equal(ob[40:], o)
+    assert np.array_equal(lb[40:].view(np.uint32), lse.view(np.uint32))
+
+
+def test_walked_and_split_chunks_give_the_same_bytes(bi):
+    """A 16384-token prefill (bound by its total work) walks each long tile's
+    chunks in one CTA, merging as it goes; its last 200 queries asked alone
+    (bound by their longest tile) run each chunk in its own CTA and merge
+    them in a second kernel.  Same rows, same bytes; rows on both sides of
+    the chunk boundary against the oracle."""
+    n, nh, nkv = 16384, 16, 2
+    Q, K, V = synth.attention_inputs(34, n, n, nh, nkv)
+    o, lse = _run(bi, Q, K, V, [0, n], [0, n], nh, nkv)
+    so, sl = _run(bi, Q[n - 200:], K, V, [0, 200], [0, n], nh, nkv)
+    assert np.array_equal(so, o[n - 200:])
+    assert np.array_equal(sl.view(np.uint32), lse[n - 200:].view(np.uint32))
+    ref = _oracle_rows(Q, K, V, [(r, r) for r in (8191, 8192, 12000, n - 1)], (0, 9), nh // nkv)
+    _check_rows(o, lse, ref)
