@@ -66,7 +66,7 @@ NCU_TRAFFIC = {# in the layer sequence, caches as the preceding router call left
                "rmsnorm_kernel": 33_581_824 + 0,
                # the mixed prefill batch (the one-head kernel), one launch with the caches flushed:
                # Q, K, V read; the output stays in L2
-               "attn_prefill_kernel": 29_400_320 + 3_072}
+               "attn_prefill_kernel": 29_408_256 + 2_304}
 
 
 def fp32_peak(torch, dev) -> dict:
