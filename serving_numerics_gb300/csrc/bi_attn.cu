@@ -39,6 +39,13 @@
 // cached prefix or a chunked prefill put around it, and whatever else is in
 // the launch.
 //
+// Keys also come in chunks of 8192 (64 blocks) at fixed positions.  A row
+// below position 8192 is exactly the above; a later row runs the above on
+// each of its chunks c = 0 .. pos/8192 from a fresh state, giving (m_c, l_c,
+// O_c), and these are merged in chunk order (merge_weights).  The chunk
+// boundaries depend on the position alone, so the bits still do not depend
+// on the batch, while one tile's chunks can run on several SMs at once.
+//
 // Structure: one CTA per query tile of 128 rows and NT query heads of one
 // key/value head.  Warpgroup t (warps 4t .. 4t+3) is head t's softmax, one
 // thread per query row; after them a TMA producer warp (the NT Q tiles once,
@@ -114,7 +121,7 @@ struct AttnCfg {
 // Keys are cut into chunks of 64 blocks (8192 keys) at fixed positions.  A
 // row whose context fits the first chunk is computed in one pass; a longer
 // row's chunks are computed from fresh softmax states, each into a partial
-// (m, l, O), and merged in chunk order (merge_chunk below).
+// (m, l, O), and merged in chunk order (merge_weights below).
 constexpr int AT_CHUNK_BLOCKS = 64;
 constexpr int AT_CHUNK_KEYS = AT_CHUNK_BLOCKS * AT_BKV;
 constexpr int AT_PART_STRIDE = 132;                // floats per partial row: O[128], m, l, two spare
@@ -138,25 +145,6 @@ struct AttnTable {
 
 __host__ __device__ constexpr int attn_blocks(int pos0, int rows) { return (pos0 + rows - 1) / AT_BKV + 1; }
 
-// Merge of a row's chunk c >= 1 (m, l, O) into its running state (M, L, N)
-// (which starts as chunk 0's (m, l, O) unchanged): with M' = max(M, m),
-// a = 2^(M - M') and b = 2^(m - M') (each exactly 1 where its maximum is
-// M'), L = fmaf(L, a, l b) and N_d = fmaf(N_d, a, O_d b), every product
-// rounded once.
-__device__ __forceinline__ float ex2_merge(float x) { float y; asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x)); return y; }
-struct MergeWeights {
-    float a, b;
-};
-__device__ __forceinline__ MergeWeights merge_weights(float &M, float &L, float m, float l)
-{
-    const float Mn = fmaxf(M, m);
-    MergeWeights w;
-    w.a = M == Mn ? 1.f : ex2_merge(M - Mn);
-    w.b = m == Mn ? 1.f : ex2_merge(m - Mn);
-    L = fmaf(L, w.a, __fmul_rn(l, w.b));
-    M = Mn;
-    return w;
-}
 
 // Shared-memory descriptor of an MN-major operand with the 128-byte swizzle
 // as TMA lays it out from [keys][64 dims] boxes: along N (the head
@@ -194,6 +182,25 @@ __device__ __forceinline__ float ex2(float x)
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// Merge of a row's chunk c >= 1 (m, l, O) into its running state (M, L, N)
+// (which starts as chunk 0's (m, l, O) unchanged): with M' = max(M, m),
+// a = 2^(M - M') and b = 2^(m - M') (each exactly 1 where its maximum is
+// M'), L = fmaf(L, a, l b) and N_d = fmaf(N_d, a, O_d b), every product
+// rounded once.
+struct MergeWeights {
+    float a, b;
+};
+__device__ __forceinline__ MergeWeights merge_weights(float &M, float &L, float m, float l)
+{
+    const float Mn = fmaxf(M, m);
+    MergeWeights w;
+    w.a = M == Mn ? 1.f : ex2(M - Mn);
+    w.b = m == Mn ? 1.f : ex2(m - Mn);
+    L = fmaf(L, w.a, __fmul_rn(l, w.b));
+    M = Mn;
+    return w;
 }
 
 // Two independent f32 fused multiply-adds (each rounded once) in one instruction.
