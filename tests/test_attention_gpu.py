@@ -387,3 +387,22 @@ def test_walked_and_split_chunks_give_the_same_bytes(bi):
     assert np.array_equal(sl.view(np.uint32), lse[n - 200:].view(np.uint32))
     ref = _oracle_rows(Q, K, V, [(r, r) for r in (8191, 8192, 12000, n - 1)], (0, 9), nh // nkv)
     _check_rows(o, lse, ref)
+
+
+def test_walked_tile_across_the_chunk_boundary(bi):
+    """A call bound by its total work (5000 queries behind 5000 cached
+    tokens, 40 tiles x 8 head pairs) walks its long tiles; tile 24 holds
+    positions 8072..8199, across the first chunk boundary, so its rows finish
+    at two different chunk ends of one walk.  The same rows asked alone (a
+    few tiles: chunk CTAs and the merge kernel) give the same bytes; rows on
+    both sides of position 8192 against the oracle."""
+    nh, nkv = 16, 2
+    ql, kl = 5000, 10000
+    Q, K, V = synth.attention_inputs(35, ql, kl, nh, nkv)
+    o, lse = _run(bi, Q, K, V, [0, ql], [0, kl], nh, nkv)
+    a, b = 3000, 3250                                # positions 8000 .. 8249
+    so, sl = _run(bi, Q[a:b], K[:kl - ql + b], V[:kl - ql + b], [0, b - a], [0, kl - ql + b], nh, nkv)
+    assert np.array_equal(so, o[a:b])
+    assert np.array_equal(sl.view(np.uint32), lse[a:b].view(np.uint32))
+    rows = [(r, kl - ql + r) for r in (3191, 3192, 3199, 3200)]     # positions 8191, 8192, 8199, 8200
+    _check_rows(o, lse, _oracle_rows(Q, K, V, rows, (0, 15), nh // nkv))
