@@ -32,8 +32,14 @@
  *  - Arguments are validated on the host before anything is launched; an
  *    invalid call returns an error and leaves every output untouched.
  *  - A launch failure reported by the runtime returns BI_ERR_CUDA.  Faults
- *    detected on the device (a bounded wait that ran out) set a sticky
- *    device word read by bi_get_last_device_error().
+ *    detected on the device (a bounded wait that ran out, an expert id out
+ *    of range) set a sticky device word read by bi_get_last_device_error();
+ *    the first report stands until it is read.  After a wait has run out,
+ *    every kernel's later waits give up at once, each block still lets its
+ *    own bulk copies and tensor-core operations finish before it frees its
+ *    tensor memory and exits, and the outputs of calls made before the word
+ *    is read are unspecified; the context stays usable.  An id out of range
+ *    affects only the slots that hold it.
  *  - There is no CPU fallback: an unsupported shape is an error.
  *  - Data-pointer alignment: 16 bytes.  Layouts are row-major.
  *  - bf16 means IEEE binary32 with the low 16 bits dropped (bfloat16).

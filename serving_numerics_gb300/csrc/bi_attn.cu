@@ -320,7 +320,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     constexpr int NS = Cfg::STAGES;
     pdl_trigger();
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t q_bar, kv_full[NS], kv_empty[NS], s_full[2], p_full[NT], o_done[NT][2];
+    __shared__ __align__(8) uint64_t q_bar, kv_full[NS], kv_empty[NS], s_full[2], p_full[NT], o_done[NT][2], drain_bar;
     __shared__ uint32_t tmem_base_sh;
     uint8_t *smem = smem_align1024(smem_raw);
     uint8_t *sq = smem, *skv = smem + Cfg::KV_OFF;
@@ -346,6 +346,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             mbar_init(&o_done[t][0], 1);   // P V of even blocks
             mbar_init(&o_done[t][1], 1);   // of odd blocks
         }
+        mbar_init(&drain_bar, 1);
         mbar_init_fence();
     }
     if (warp == Cfg::MMA_WARP) tmem_alloc(&tmem_base_sh, Cfg::TMEM_COLS);
@@ -353,6 +354,8 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = tmem_base_sh;
+    bool ok = true;        // every wait of this thread completed
+    int issued = 0;        // the producer's K/V blocks issued
 
     // each role under its own register budget: ptxas allocates a region after
     // setmaxnreg to that count
@@ -366,10 +369,14 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                     tma_load_3d(sq + t * AT_Q_BYTES, &tmq, &q_bar, 0, h0 + t, tile.q0);
                     tma_load_3d(sq + t * AT_Q_BYTES + AT_Q_BOX, &tmq, &q_bar, 64, h0 + t, tile.q0);
                 }
-                for (int b = 0; b < nb; ++b) {
+                for (int b = 0; b < nb; ++b, ++issued) {
                     const int st = b % NS;
                     const uint32_t ph = (uint32_t)(b / NS) & 1u;
-                    mbar_wait(&kv_empty[st], ph ^ 1u, err, 0x61);
+                    // after a wait has given up, nothing more is issued
+                    if (!mbar_wait(&kv_empty[st], ph ^ 1u, err, 0x61) || !ring_slot_free(kv_full, NS, b)) {
+                        ok = false;
+                        break;
+                    }
                     uint8_t *dst = skv + st * AT_STAGE_BYTES;
                     const int key = tile.kv0 + (kb0 + b) * AT_BKV;
                     mbar_arrive_expect_tx(&kv_full[st], (uint32_t)AT_STAGE_BYTES);
@@ -407,10 +414,10 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                                      ((kb0 + b) % AT_CHUNK_BLOCKS | k) != 0 ? 1u : 0u);   // O restarts with every chunk
                 };
                 auto wait_kv = [&](int b) {
-                    mbar_wait(&kv_full[b % NS], (uint32_t)(b / NS) & 1u, err, 0x63);
+                    ok &= mbar_wait(&kv_full[b % NS], (uint32_t)(b / NS) & 1u, err, 0x63);
                     tc_fence_after();
                 };
-                mbar_wait(&q_bar, 0, err, 0x62);
+                ok &= mbar_wait(&q_bar, 0, err, 0x62);
                 if constexpr (NT == 2) {
                     // per block: O += P V, then the next block's S into the same
                     // columns, head 0 then head 1 (each head's softmax overlaps
@@ -420,7 +427,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                     for (int b = 0; b < nb; ++b) {
 #pragma unroll
                         for (int t = 0; t < NT; ++t) {
-                            mbar_wait(&p_full[t], (uint32_t)b & 1u, err, 0x65);
+                            ok &= mbar_wait(&p_full[t], (uint32_t)b & 1u, err, 0x65);
                             tc_fence_after();
                             issue_pv(t, b, 0, b % NS);
                             umma_commit(&o_done[t][b & 1]);
@@ -443,7 +450,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                         issue_s(0, 1, 1, &s_full[1]);
                     }
                     for (int b = 0; b < nb; ++b) {
-                        mbar_wait(&p_full[0], (uint32_t)b & 1u, err, 0x65);
+                        ok &= mbar_wait(&p_full[0], (uint32_t)b & 1u, err, 0x65);
                         tc_fence_after();
                         issue_pv(0, b, b & 1, b % NS);
                         umma_commit(&o_done[0][b & 1]);
@@ -473,7 +480,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         // block, so the product of block n-2 is complete and neither barrier
         // is ever two phases from the one awaited.
         auto wait_pv = [&](int n) {
-            mbar_wait(&o_done[t][n & 1], ((uint32_t)n >> 1) & 1u, err, 0x67);
+            ok &= mbar_wait(&o_done[t][n & 1], ((uint32_t)n >> 1) & 1u, err, 0x67);
             tc_fence_after();
         };
         const int lc = pos / AT_CHUNK_KEYS;             // the row's last chunk
@@ -500,7 +507,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             const int sb = NT == 2 ? t : (b & 1);
             const uint32_t scol = Cfg::s_col(t, b & 1);
             if (b < nb) {
-                mbar_wait(&s_full[sb], NT == 2 ? ((uint32_t)b & 1u) : (((uint32_t)b >> 1) & 1u), err, 0x68);
+                ok &= mbar_wait(&s_full[sb], NT == 2 ? ((uint32_t)b & 1u) : (((uint32_t)b >> 1) & 1u), err, 0x68);
                 tc_fence_after();
             }
             const bool chunk_start = (kb0 + b) % AT_CHUNK_BLOCKS == 0;
@@ -627,8 +634,16 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     }
 
     tc_fence_before();
-    __syncthreads();
+    const bool failed = __syncthreads_or(!ok) != 0;
     tc_fence_after();
+    if (failed) {   // a wait gave up: this block's copies and products finish before it leaves
+        if (warp == Cfg::PRODUCER_WARP && lane == 0) {
+            mbar_drain(&q_bar, 0);
+            drain_ring(kv_full, NS, issued);
+        }
+        if (warp == Cfg::MMA_WARP && lane == 0) umma_drain(&drain_bar);
+        __syncwarp();
+    }
     if (warp == Cfg::MMA_WARP) tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
 }
 

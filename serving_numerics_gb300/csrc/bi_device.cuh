@@ -6,7 +6,10 @@
 
 namespace bi {
 
-// error word layout: low byte = bi_status, next bytes = where it happened
+// error word layout: low byte = bi_status, next bytes = where it happened;
+// the first report stands until the host reads the word
+constexpr unsigned int kErrTimeout = 5u;   // BI_ERR_TIMEOUT: a bounded wait ran out
+
 __device__ __forceinline__ void report_error(unsigned int *err, unsigned int code, unsigned int where)
 {
     atomicCAS(err, 0u, code | (where << 8));
@@ -82,9 +85,11 @@ __device__ __forceinline__ unsigned int load_volatile(const unsigned int *p)
 // Wait for the phase with the given parity to complete, for at most about
 // two seconds.  On expiry: record BI_ERR_TIMEOUT (code 5) with `where` and
 // return false; the caller carries on so that no thread is left waiting.
-// Once any wait has given up (the error word is set), every later wait
-// that is not already satisfied gives up at once, so a broken pipeline
-// drains in milliseconds instead of two seconds per wait.
+// Once any wait has given up (the error word holds a timeout), every later
+// wait that is not already satisfied gives up at once, so a broken pipeline
+// drains in milliseconds instead of two seconds per wait.  Other reports (an
+// expert id out of range) leave the waits alone: the rest of the work in
+// flight still completes correctly.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 __device__ __forceinline__ bool mbar_wait_limit(uint64_t *bar, uint32_t parity, unsigned int *err,
@@ -96,9 +101,9 @@ __device__ __forceinline__ bool mbar_wait_limit(uint64_t *bar, uint32_t parity, 
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(addr, parity)) return true;
         if ((i & 255u) == 0) {
-            if (load_volatile(err) != 0u) return false;
+            if ((load_volatile(err) & 0xFFu) == kErrTimeout) return false;
             if (global_ns() - t0 > limit_ns) {
-                report_error(err, 5u, where);
+                report_error(err, kErrTimeout, where);
                 return false;
             }
         }
@@ -109,6 +114,55 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsign
                                           unsigned int where)
 {
     return mbar_wait_limit(bar, parity, err, where, kWaitLimitNs);
+}
+
+// Has the phase with this parity completed?  One test, no waiting.
+__device__ __forceinline__ bool mbar_done(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// After a wait has given up, a block still lets the bulk copies it issued
+// land (and its tensor-core products finish) before it exits or frees
+// tensor memory: no copy may still be writing the shared memory of a block
+// that has gone.  This wait ignores the error word and ends after at most
+// about 0.1 s.
+constexpr uint64_t kDrainLimitNs = 100000000ull;
+
+__device__ __forceinline__ bool mbar_drain(uint64_t *bar, uint32_t parity)
+{
+    const uint32_t addr = smem_u32(bar);
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 0;; ++i) {
+        if (mbar_try_wait(addr, parity)) return true;
+        if ((i & 255u) == 255u && global_ns() - t0 > kDrainLimitNs) return false;
+    }
+}
+
+// A ring of `stages` slots filled in order: step j goes into slot
+// j % stages and completes phase j / stages of that slot's full barrier.
+// A producer issues step j only once step j - stages has landed
+// (ring_slot_free), so a slot's barrier is never more than one phase behind
+// the last step issued into it, and drain_ring can wait for exactly those
+// steps.  In a pipeline whose waits all completed the test always passes:
+// the slot was released by readers that had waited for that step.
+__device__ __forceinline__ bool ring_slot_free(uint64_t *full, int stages, int j)
+{
+    return j < stages || mbar_done(&full[j % stages], (uint32_t)(j / stages - 1) & 1u);
+}
+
+__device__ __forceinline__ void drain_ring(uint64_t *full, int stages, int issued)
+{
+    for (int j = issued > stages ? issued - stages : 0; j < issued; ++j)
+        mbar_drain(&full[j % stages], (uint32_t)(j / stages) & 1u);
 }
 
 // 3-D tiled TMA load into shared memory, completing on `bar`.

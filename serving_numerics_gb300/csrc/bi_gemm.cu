@@ -52,7 +52,7 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant_
 {
     pdl_trigger();   // dependents may launch now; each waits before reading our outputs
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t full_bar[STAGES], empty_bar[STAGES], tfull_bar[2], tempty_bar[2];
+    __shared__ __align__(8) uint64_t full_bar[STAGES], empty_bar[STAGES], tfull_bar[2], tempty_bar[2], drain_bar;
     __shared__ uint32_t tmem_base_sh;
     uint8_t *smem = smem_align1024(smem_raw);
 
@@ -75,6 +75,7 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant_
             mbar_init(&tfull_bar[b], 1);
             mbar_init(&tempty_bar[b], 4);
         }
+        mbar_init(&drain_bar, 1);
         mbar_init_fence();
     }
     if (warp == 1) tmem_alloc(&tmem_base_sh, TMEM_COLS);
@@ -85,16 +86,22 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant_
 
     pdl_wait();
 
+    bool ok = true;        // every wait of this thread completed
+    int issued = 0;        // the producer's ring steps (K blocks) issued
     if (warp == 0) {
         if (lane == 0) {   // TMA producer
             uint32_t s = 0, ph = 0;          // ring slot and its phase parity, advanced per K block
-            for (int item = blockIdx.x; item < num_items; item += gridDim.x) {
+            for (int item = blockIdx.x; ok && item < num_items; item += gridDim.x) {
                 int piece;
                 const int tile = item_tile(item, n_full, lg_s, piece);
                 const int mt = tile / n_tiles, nt = tile % n_tiles;
                 const int n0 = nt * BN + (piece > 0 ? piece * pn : 0);
-                for (int kb = 0; kb < kblocks; ++kb) {
-                    mbar_wait(&empty_bar[s], ph ^ 1u, err, 0x21);
+                for (int kb = 0; kb < kblocks; ++kb, ++issued) {
+                    // after a wait has given up, nothing more is issued
+                    if (!mbar_wait(&empty_bar[s], ph ^ 1u, err, 0x21) || !ring_slot_free(full_bar, STAGES, issued)) {
+                        ok = false;
+                        break;
+                    }
                     uint8_t *st = smem + s * STAGE_BYTES;
                     mbar_arrive_expect_tx(&full_bar[s], (uint32_t)a_bytes + (piece < 0 ? B_BYTES : (B_BYTES >> lg_s)));
                     tma_load_2d(st, &tma, &full_bar[s], kb * BK, mt * BM);
@@ -112,11 +119,11 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant_
             for (int item = blockIdx.x; item < num_items; item += gridDim.x, ++tc) {
                 const uint32_t idesc = item < n_full ? IDESC : idesc_n(pn);
                 const uint32_t b = tc & 1u, tph = (tc >> 1) & 1u;
-                mbar_wait(&tempty_bar[b], tph ^ 1u, err, 0x22);
+                ok &= mbar_wait(&tempty_bar[b], tph ^ 1u, err, 0x22);
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + b * ACC_COLS;
                 for (int kb = 0; kb < kblocks; ++kb) {
-                    mbar_wait(&full_bar[s], ph, err, 0x23);
+                    ok &= mbar_wait(&full_bar[s], ph, err, 0x23);
                     tc_fence_after();
                     const uint32_t a_addr = smem_u32(smem + s * STAGE_BYTES);
                     const uint32_t b_addr = a_addr + a_bytes;
@@ -144,7 +151,7 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant_
             const int mt = tile / n_tiles, nt = tile % n_tiles;
             const int nbase = nt * BN + (piece > 0 ? piece * pn : 0), nchunks = piece < 0 ? BN / 32 : pn / 32;
             const uint32_t b = tc & 1u, tph = (tc >> 1) & 1u;
-            mbar_wait(&tfull_bar[b], tph, err, 0x24);
+            ok &= mbar_wait(&tfull_bar[b], tph, err, 0x24);
             tc_fence_after();
             const int m = mt * BM + row;
             __nv_bfloat16 *crow = C + (size_t)(m < M ? m : 0) * (size_t)ldc;
@@ -174,8 +181,13 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant_
     }
 
     tc_fence_before();
-    __syncthreads();
+    const bool failed = __syncthreads_or(!ok) != 0;
     tc_fence_after();
+    if (failed) {   // a wait gave up: this block's copies and products finish before it leaves
+        if (warp == 0 && lane == 0) drain_ring(full_bar, STAGES, issued);
+        if (warp == 1 && lane == 0) umma_drain(&drain_bar);
+        __syncwarp();
+    }
     if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
 }
 

@@ -217,7 +217,7 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__
 {
     pdl_trigger();
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t full_bar[STAGES], empty_bar[STAGES], tfull_bar[2], tempty_bar[2];
+    __shared__ __align__(8) uint64_t full_bar[STAGES], empty_bar[STAGES], tfull_bar[2], tempty_bar[2], drain_bar;
     __shared__ uint32_t tmem_base_sh;
     uint8_t *smem = smem_align1024(smem_raw);
 
@@ -235,6 +235,7 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__
             mbar_init(&tfull_bar[b], 1);
             mbar_init(&tempty_bar[b], 4);
         }
+        mbar_init(&drain_bar, 1);
         mbar_init_fence();
     }
     if (warp == 1) tmem_alloc(&tmem_base_sh, TMEM_COLS);
@@ -246,15 +247,20 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__
     pdl_wait();
     const int num_items = *ntiles_p * n_tiles;
 
+    bool ok = true;        // every wait of this thread completed
+    uint32_t it = 0;       // the producer's ring steps issued
     if (warp == 0) {
         if (lane == 0) {   // TMA producer
-            uint32_t it = 0;
-            for (int item = blockIdx.x; item < num_items; item += gridDim.x) {
+            for (int item = blockIdx.x; ok && item < num_items; item += gridDim.x) {
                 const int mt = item / n_tiles, nt = item % n_tiles;
                 const int row0 = tile_row0[mt], e = tile_expert[mt];
                 for (int kb = 0; kb < kblocks; ++kb, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
-                    mbar_wait(&empty_bar[s], ph ^ 1u, err, 0x51);
+                    // after a wait has given up, nothing more is issued
+                    if (!mbar_wait(&empty_bar[s], ph ^ 1u, err, 0x51) || !ring_slot_free(full_bar, STAGES, (int)it)) {
+                        ok = false;
+                        break;
+                    }
                     uint8_t *st = smem + s * STAGE_BYTES;
                     mbar_arrive_expect_tx(&full_bar[s], STAGE_BYTES);
                     tma_load_2d(st, &tma, &full_bar[s], kb * BK, row0);
@@ -264,15 +270,15 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__
         }
     } else if (warp == 1) {
         if (lane == 0) {   // MMA issuer
-            uint32_t it = 0, tc = 0;
+            uint32_t rit = 0, tc = 0;
             for (int item = blockIdx.x; item < num_items; item += gridDim.x, ++tc) {
                 const uint32_t b = tc & 1u, tph = (tc >> 1) & 1u;
-                mbar_wait(&tempty_bar[b], tph ^ 1u, err, 0x52);
+                ok &= mbar_wait(&tempty_bar[b], tph ^ 1u, err, 0x52);
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + b * ACC_COLS;
-                for (int kb = 0; kb < kblocks; ++kb, ++it) {
-                    const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
-                    mbar_wait(&full_bar[s], ph, err, 0x53);
+                for (int kb = 0; kb < kblocks; ++kb, ++rit) {
+                    const uint32_t s = rit % STAGES, ph = (rit / STAGES) & 1u;
+                    ok &= mbar_wait(&full_bar[s], ph, err, 0x53);
                     tc_fence_after();
                     const uint32_t a_addr = smem_u32(smem + s * STAGE_BYTES);
                     const uint32_t b_addr = a_addr + A_BYTES;
@@ -295,7 +301,7 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__
             const int mt = item / n_tiles, nt = item % n_tiles;
             const int src = row_src[tile_row0[mt] + row];      // -1: a padding row
             const uint32_t b = tc & 1u, tph = (tc >> 1) & 1u;
-            mbar_wait(&tfull_bar[b], tph, err, 0x54);
+            ok &= mbar_wait(&tfull_bar[b], tph, err, 0x54);
             tc_fence_after();
             __nv_bfloat16 *yrow = Y + (int64_t)(src >= 0 ? src : 0) * N;
 #pragma unroll 1
@@ -324,8 +330,13 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__
     }
 
     tc_fence_before();
-    __syncthreads();
+    const bool failed = __syncthreads_or(!ok) != 0;
     tc_fence_after();
+    if (failed) {   // a wait gave up: this block's copies and products finish before it leaves
+        if (warp == 0 && lane == 0) drain_ring(full_bar, STAGES, (int)it);
+        if (warp == 1 && lane == 0) umma_drain(&drain_bar);
+        __syncwarp();
+    }
     if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
 }
 

@@ -91,11 +91,14 @@ rmsnorm_kernel(const InT *__restrict__ x, const InT *__restrict__ w, int M, int 
         bulk_load(smem, w, row_bytes, &w_bar);
     }
     pdl_wait();
-    if (stage_w) mbar_wait(&w_bar, 0, err, 0x30);
+    bool ok = true;        // every wait of this thread completed
+    if (stage_w) ok &= mbar_wait(&w_bar, 0, err, 0x30);
 
+    // every block has rows: the grid is cut so that m_begin < m_end
     uint32_t parity = 0;
-    for (int c0 = m_begin; c0 < m_end; c0 += chunk, parity ^= 1u) {
-        const int nrows = min(chunk, m_end - c0);
+    int nrows = 0;
+    for (int c0 = m_begin;; c0 += chunk, parity ^= 1u) {
+        nrows = min(chunk, m_end - c0);
         if (tid == 0) {
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the previous chunk's reads first
             for (int r = 0; r < nrows; ++r) {
@@ -105,7 +108,7 @@ rmsnorm_kernel(const InT *__restrict__ x, const InT *__restrict__ w, int M, int 
         }
         if (r_loc < nrows) {
             const int m = c0 + r_loc;
-            mbar_wait(&row_bar[r_loc], parity, err, 0x31);
+            ok &= mbar_wait(&row_bar[r_loc], parity, err, 0x31);
             const InT *xr = reinterpret_cast<const InT *>(rows + (size_t)r_loc * row_bytes);
             float acc = 0.0f;
             for (int s0 = 0; s0 < ns; ++s0) {
@@ -139,7 +142,14 @@ rmsnorm_kernel(const InT *__restrict__ x, const InT *__restrict__ w, int M, int 
                 }
             }
         }
-        if (c0 + chunk < m_end) __syncthreads();       // every staged row read before the next chunk's copies
+        // the last chunk; else every staged row is read before the next
+        // chunk's copies, and after a wait that gave up none is issued
+        if (c0 + chunk >= m_end || __syncthreads_or(!ok)) break;
+    }
+    // a wait gave up: the rows still landing finish before the block exits
+    if (__syncthreads_or(!ok) && tid == 0) {
+        for (int r = 0; r < nrows; ++r) mbar_drain(&row_bar[r], parity);
+        if (stage_w) mbar_drain(&w_bar, 0);
     }
 }
 

@@ -164,6 +164,8 @@ router_proj_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[NST];
     __shared__ int released[NST];          // warps done with the slot's current slab
+    __shared__ int last_step[NST];         // the last slab issued into each slot
+    __shared__ int ring_stop;              // set once a refill was skipped: nothing more is issued
     uint8_t *smem = smem_align1024(smem_raw);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -179,7 +181,9 @@ router_proj_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
         for (int s = 0; s < NST; ++s) {
             mbar_init(&full_bar[s], 1);
             released[s] = 0;
+            last_step[s] = s < ns ? s : -1;
         }
+        ring_stop = 0;
         mbar_init_fence();
     }
     __syncthreads();
@@ -240,10 +244,11 @@ router_proj_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
 
     // a warp whose four token rows are all past M has nothing to compute
     const bool live = tg < M - m0;
+    bool ok = true;        // every wait of this thread completed
     int slot = 0;
     uint32_t phase = 0;
     for (int s = 0; s < ns; ++s) {
-        mbar_wait(&full_bar[slot], phase, err, 0x11);
+        ok &= mbar_wait(&full_bar[slot], phase, err, 0x11);
         if (live && kSlab * s + kBlk * (q0 + warp) < H) {
             const uint8_t *st = smem + slot * Cfg::STAGE_BYTES;
             const int bx = warp / Cfg::PB, pc = warp % Cfg::PB;
@@ -261,8 +266,16 @@ router_proj_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
             if (atomicAdd(&released[slot], 1) == NPL - 1) {
                 released[slot] = 0;
                 if (s + NST < ns) {
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    issue(s + NST, slot);
+                    // slab s must have landed (always so unless a wait gave
+                    // up; then this and every later refill is skipped)
+                    volatile int *stop = &ring_stop;
+                    if (*stop == 0 && ring_slot_free(full_bar, NST, s + NST)) {
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                        issue(s + NST, slot);
+                        last_step[slot] = s + NST;
+                    } else {
+                        *stop = 1;
+                    }
                 }
             }
         }
@@ -271,7 +284,14 @@ router_proj_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constan
             phase ^= 1u;
         }
     }
-    __syncthreads();                                       // every warp is done with the ring
+    if (__syncthreads_or(!ok)) {                           // every warp is done with the ring
+        // a wait gave up: the slabs still landing finish before the ring's
+        // memory is reused
+        if (tid == 0)
+            for (int sl = 0; sl < NST; ++sl)
+                if (last_step[sl] >= 0) mbar_drain(&full_bar[sl], (uint32_t)(last_step[sl] / NST) & 1u);
+        __syncthreads();
+    }
 
     // partition tree: every warp parks its 64 partial sums (value v of lane L
     // at part[(warp * 64 + v) * 33 + L], padded rows); after one barrier each
@@ -524,7 +544,9 @@ router_select_kernel(const float *__restrict__ part, int C, int m_split, void *l
     if (GATE) {
         float g = 0.0f;
         if (staged) {
-            mbar_wait(&gate_bar, 0, gate.err, 0x40);
+            // warp 0 outlives the copies: after a wait that gave up it
+            // still lets them land
+            if (!mbar_wait(&gate_bar, 0, gate.err, 0x40) && warp == 0) mbar_drain(&gate_bar, 0);
             if (lane < 16) {
                 const uint8_t *xr = gate_rows + warp * row_bytes, *wr = gate_rows + kSelWarps * row_bytes;
                 g = gate.bf16 ? gate_partition(reinterpret_cast<const __nv_bfloat16 *>(xr),

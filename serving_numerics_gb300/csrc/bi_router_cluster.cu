@@ -250,26 +250,31 @@ router_cluster_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_cons
         }
     };
 
+    bool ok = true;          // every wait of this thread completed
+    int issued = nst;        // slabs issued (by thread 0)
     if (ns <= NST) {
         // the ring holds all of H: every stage is waited for up front, and
         // the loop has no waits in it, so that the loads of one slab can be
         // scheduled under the arithmetic of the previous one
-        for (int s = 0; s < ns; ++s) mbar_wait(&full_bar[s], 0, a.err, 0x1C);
+        for (int s = 0; s < ns; ++s) ok &= mbar_wait(&full_bar[s], 0, a.err, 0x1C);
 #pragma unroll 2
         for (int s = 0; s < ns; ++s) slab(s, s);
     } else {
         int slot = 0;
         uint32_t phase = 0;
         for (int s = 0; s < ns; ++s) {
-            mbar_wait(&full_bar[slot], phase, a.err, 0x1C);
+            ok &= mbar_wait(&full_bar[slot], phase, a.err, 0x1C);
             slab(s, slot);
             if (s + NST < ns) {          // refill the slot once every warp is done with it
                 __syncthreads();
-                if (tid == 0) {
+                // slabs are issued in order while each slot's previous slab
+                // has landed (always so unless a wait gave up)
+                if (tid == 0 && issued == s + NST && ring_slot_free(full_bar, NST, s + NST)) {
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     mbar_arrive_expect_tx(&full_bar[slot], stage_tx(s + NST));
                     issue_w(s + NST, slot);
                     issue_x(s + NST, slot);
+                    ++issued;
                 }
             }
             if (++slot == NST) {
@@ -278,6 +283,9 @@ router_cluster_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_cons
             }
         }
     }
+    // thread 0 waited for every slab it issued; if one of those waits gave
+    // up, the slabs still landing finish before the block goes on
+    if (tid == 0 && !ok) drain_ring(full_bar, NST, issued);
 
     // the pairwise tree over the 16 partitions of every (expert, token), then
     // the block's logits (in the logit dtype's values) into its own tile

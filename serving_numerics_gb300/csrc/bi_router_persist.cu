@@ -411,9 +411,9 @@ router_proj_persist_kernel(const __grid_constant__ CUtensorMap tmx, const __grid
         if (ld_acquire(fl) == done) return;
         const uint64_t t0 = global_ns();
         while (ld_acquire(fl) != done) {
-            if (load_volatile(a.err) != 0u) return;
+            if ((load_volatile(a.err) & 0xFFu) == kErrTimeout) return;
             if (global_ns() - t0 > kWaitLimitNs) {
-                report_error(a.err, 5u, where);
+                report_error(a.err, kErrTimeout, where);
                 return;
             }
             __nanosleep(256);
@@ -443,8 +443,10 @@ router_proj_persist_kernel(const __grid_constant__ CUtensorMap tmx, const __grid
                 load_boxes<Cfg>(smem + t * Cfg::STAGE, &full_bar[t], &tmx, &tmw, pro_item[t], pro_slab[t], a, 2, false);
             int slot = 0;
             uint32_t parity = 0;        // of the release that step t waits for: round t / NST - 1
-            for (int t = npro; t < T; ++t) {
-                mbar_wait(&empty_bar[slot], parity, a.err, 0x16);
+            int t = npro;               // steps issued
+            for (; t < T; ++t) {
+                // after a wait has given up, nothing more is issued
+                if (!mbar_wait(&empty_bar[slot], parity, a.err, 0x16) || !ring_slot_free(full_bar, NST, t)) break;
                 load_boxes<Cfg>(smem + slot * Cfg::STAGE, &full_bar[slot], &tmx, &tmw, c.item, c.slab, a, 3, true,
                                 GATE ? wsg_ring + slot * Cfg::WSG : nullptr);
                 c.advance(f0, f1, first, sa, ns);
@@ -453,6 +455,10 @@ router_proj_persist_kernel(const __grid_constant__ CUtensorMap tmx, const __grid
                     parity ^= 1u;
                 }
             }
+            // the block outlives its copies: the producer stays until the
+            // last steps it issued have landed (the readers wait for them
+            // too, so this costs nothing unless a wait gave up)
+            drain_ring(full_bar, NST, t);
         } else if (GATE && (warp == PT_WARPS + 1 || warp == PT_WARPS + 2)) {
             // the shared gate: lane L of gate warp q owns token row 32 q + L
             // of the tile and all 8 partition chains of the half for it, on

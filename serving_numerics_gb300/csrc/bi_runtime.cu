@@ -10,6 +10,8 @@
 
 namespace bi {
 
+static_assert(kErrTimeout == (unsigned int)BI_ERR_TIMEOUT, "the device code of a wait that ran out");
+
 // Sticky error word: a kernel that gives up a bounded wait records
 // (status | where << 8) here; bi_get_last_device_error() reads and clears it.
 __device__ unsigned int g_device_error;

@@ -95,6 +95,14 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar)
                  : "memory");
 }
 
+// After a wait has given up: every tcgen05 operation this thread issued is
+// complete (bounded) before the block frees its tensor memory.
+__device__ __forceinline__ void umma_drain(uint64_t *bar)
+{
+    umma_commit(bar);
+    mbar_drain(bar, 0);
+}
+
 // 32 lanes x 32 consecutive f32 columns: thread t gets row (lane) t.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
 {
