@@ -354,8 +354,6 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = tmem_base_sh;
-    bool ok = true;        // every wait of this thread completed
-    int issued = 0;        // the producer's K/V blocks issued
 
     // each role under its own register budget: ptxas allocates a region after
     // setmaxnreg to that count
@@ -369,14 +367,15 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                     tma_load_3d(sq + t * AT_Q_BYTES, &tmq, &q_bar, 0, h0 + t, tile.q0);
                     tma_load_3d(sq + t * AT_Q_BYTES + AT_Q_BOX, &tmq, &q_bar, 64, h0 + t, tile.q0);
                 }
-                for (int b = 0; b < nb; ++b, ++issued) {
-                    const int st = b % NS;
+                // a stage is released only by the MMA thread, after it saw
+                // the stage full (it stops at its first wait that gives up),
+                // so a stage is never refilled before its last load landed;
+                // after a wait has given up nothing more is issued
+                int issued = 0;
+                for (; issued < nb; ++issued) {
+                    const int b = issued, st = b % NS;
                     const uint32_t ph = (uint32_t)(b / NS) & 1u;
-                    // after a wait has given up, nothing more is issued
-                    if (!mbar_wait(&kv_empty[st], ph ^ 1u, err, 0x61) || !ring_slot_free(kv_full, NS, b)) {
-                        ok = false;
-                        break;
-                    }
+                    if (!mbar_wait(&kv_empty[st], ph ^ 1u, err, 0x61)) break;
                     uint8_t *dst = skv + st * AT_STAGE_BYTES;
                     const int key = tile.kv0 + (kb0 + b) * AT_BKV;
                     mbar_arrive_expect_tx(&kv_full[st], (uint32_t)AT_STAGE_BYTES);
@@ -385,6 +384,10 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                     tma_load_3d(dst + 2 * AT_KV_BOX, &tmv, &kv_full[st], 0, hk, key);
                     tma_load_3d(dst + 3 * AT_KV_BOX, &tmv, &kv_full[st], 64, hk, key);
                 }
+                // the block outlives its copies (free in a healthy pipeline:
+                // the MMA thread waits for the same loads)
+                mbar_drain(&q_bar, 0);
+                drain_ring(kv_full, NS, issued);
             }
         } else if (warp == Cfg::MMA_WARP) {
             if (lane == 0) {   // MMA issuer
@@ -413,27 +416,31 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                         umma_bf16_ts(d, pa + k * 8, sw128_mn_desc(va + k * 2048), id_o,
                                      ((kb0 + b) % AT_CHUNK_BLOCKS | k) != 0 ? 1u : 0u);   // O restarts with every chunk
                 };
-                auto wait_kv = [&](int b) {
-                    ok &= mbar_wait(&kv_full[b % NS], (uint32_t)(b / NS) & 1u, err, 0x63);
+                // every wait that completes is followed by a fence; the
+                // thread stops at the first one that gives up (it then
+                // issues and releases nothing more)
+                auto wait = [&](uint64_t *bar, uint32_t parity, unsigned int where) {
+                    const bool done = mbar_wait(bar, parity, err, where);
                     tc_fence_after();
+                    return done;
                 };
-                ok &= mbar_wait(&q_bar, 0, err, 0x62);
+                auto wait_kv = [&](int b) { return wait(&kv_full[b % NS], (uint32_t)(b / NS) & 1u, 0x63); };
+                bool run = wait(&q_bar, 0, 0x62) && wait_kv(0);
                 if constexpr (NT == 2) {
                     // per block: O += P V, then the next block's S into the same
                     // columns, head 0 then head 1 (each head's softmax overlaps
                     // the other head's products)
-                    wait_kv(0);
-                    for (int t = 0; t < NT; ++t) issue_s(t, 0, 0, &s_full[t]);
-                    for (int b = 0; b < nb; ++b) {
+                    if (run)
+                        for (int t = 0; t < NT; ++t) issue_s(t, 0, 0, &s_full[t]);
+                    for (int b = 0; run && b < nb; ++b) {
 #pragma unroll
                         for (int t = 0; t < NT; ++t) {
-                            ok &= mbar_wait(&p_full[t], (uint32_t)b & 1u, err, 0x65);
-                            tc_fence_after();
+                            if (!(run = wait(&p_full[t], (uint32_t)b & 1u, 0x65))) break;
                             issue_pv(t, b, 0, b % NS);
                             umma_commit(&o_done[t][b & 1]);
                             if (t == NT - 1) umma_commit(&kv_empty[b % NS]);   // K and V of block b no longer read
                             if (b + 1 < nb) {   // the next block's scores, into the columns P V has just read
-                                if (t == 0) wait_kv(b + 1);
+                                if (t == 0 && !(run = wait_kv(b + 1))) break;
                                 issue_s(t, 0, (b + 1) % NS, &s_full[t]);
                             }
                         }
@@ -443,24 +450,23 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                     // O += P_b V_b and S of block b+2 into the buffer P_b was in,
                     // so the scores of block b+1 are ready while block b's
                     // softmax runs
-                    wait_kv(0);
-                    issue_s(0, 0, 0, &s_full[0]);
-                    if (nb > 1) {
-                        wait_kv(1);
-                        issue_s(0, 1, 1, &s_full[1]);
-                    }
-                    for (int b = 0; b < nb; ++b) {
-                        ok &= mbar_wait(&p_full[0], (uint32_t)b & 1u, err, 0x65);
-                        tc_fence_after();
+                    if (run) issue_s(0, 0, 0, &s_full[0]);
+                    if (run && nb > 1 && (run = wait_kv(1))) issue_s(0, 1, 1, &s_full[1]);
+                    for (int b = 0; run && b < nb; ++b) {
+                        if (!(run = wait(&p_full[0], (uint32_t)b & 1u, 0x65))) break;
                         issue_pv(0, b, b & 1, b % NS);
                         umma_commit(&o_done[0][b & 1]);
                         umma_commit(&kv_empty[b % NS]);
                         if (b + 2 < nb) {
-                            wait_kv(b + 2);
+                            if (!(run = wait_kv(b + 2))) break;
                             issue_s(0, b & 1, (b + 2) % NS, &s_full[b & 1]);
                         }
                     }
                 }
+                // every product issued is complete before the tensor memory is
+                // freed (free in a healthy pipeline: the softmax waits for the
+                // last of them)
+                umma_drain(&drain_bar);
             }
         }
     } else {
@@ -480,7 +486,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         // block, so the product of block n-2 is complete and neither barrier
         // is ever two phases from the one awaited.
         auto wait_pv = [&](int n) {
-            ok &= mbar_wait(&o_done[t][n & 1], ((uint32_t)n >> 1) & 1u, err, 0x67);
+            mbar_wait(&o_done[t][n & 1], ((uint32_t)n >> 1) & 1u, err, 0x67);
             tc_fence_after();
         };
         const int lc = pos / AT_CHUNK_KEYS;             // the row's last chunk
@@ -507,7 +513,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             const int sb = NT == 2 ? t : (b & 1);
             const uint32_t scol = Cfg::s_col(t, b & 1);
             if (b < nb) {
-                ok &= mbar_wait(&s_full[sb], NT == 2 ? ((uint32_t)b & 1u) : (((uint32_t)b >> 1) & 1u), err, 0x68);
+                mbar_wait(&s_full[sb], NT == 2 ? ((uint32_t)b & 1u) : (((uint32_t)b >> 1) & 1u), err, 0x68);
                 tc_fence_after();
             }
             const bool chunk_start = (kb0 + b) % AT_CHUNK_BLOCKS == 0;
@@ -634,16 +640,8 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     }
 
     tc_fence_before();
-    const bool failed = __syncthreads_or(!ok) != 0;
+    __syncthreads();
     tc_fence_after();
-    if (failed) {   // a wait gave up: this block's copies and products finish before it leaves
-        if (warp == Cfg::PRODUCER_WARP && lane == 0) {
-            mbar_drain(&q_bar, 0);
-            drain_ring(kv_full, NS, issued);
-        }
-        if (warp == Cfg::MMA_WARP && lane == 0) umma_drain(&drain_bar);
-        __syncwarp();
-    }
     if (warp == Cfg::MMA_WARP) tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
 }
 

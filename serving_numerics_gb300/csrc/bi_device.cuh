@@ -149,11 +149,14 @@ __device__ __forceinline__ bool mbar_drain(uint64_t *bar, uint32_t parity)
 
 // A ring of `stages` slots filled in order: step j goes into slot
 // j % stages and completes phase j / stages of that slot's full barrier.
-// A producer issues step j only once step j - stages has landed
-// (ring_slot_free), so a slot's barrier is never more than one phase behind
-// the last step issued into it, and drain_ring can wait for exactly those
-// steps.  In a pipeline whose waits all completed the test always passes:
-// the slot was released by readers that had waited for that step.
+// A producer issues step j only once step j - stages has landed, so a
+// slot's barrier is never more than one phase behind the last step issued
+// into it, and drain_ring can wait for exactly those steps.  Where the one
+// reader that releases a slot stops at its first wait that gives up (the
+// MMA thread of the tensor-core kernels), every release follows a completed
+// wait and that holds by itself; where readers carry on after a wait gave
+// up, the producer tests it (ring_slot_free), a test that always passes in
+// a pipeline whose waits all completed.
 __device__ __forceinline__ bool ring_slot_free(uint64_t *full, int stages, int j)
 {
     return j < stages || mbar_done(&full[j % stages], (uint32_t)(j / stages - 1) & 1u);

@@ -86,22 +86,22 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant_
 
     pdl_wait();
 
-    bool ok = true;        // every wait of this thread completed
-    int issued = 0;        // the producer's ring steps (K blocks) issued
     if (warp == 0) {
         if (lane == 0) {   // TMA producer
+            // a stage is released only by the MMA thread, after it saw the
+            // stage full (it stops at its first wait that gives up), so a
+            // stage is never refilled before its last load landed; after a
+            // wait has given up nothing more is issued
             uint32_t s = 0, ph = 0;          // ring slot and its phase parity, advanced per K block
-            for (int item = blockIdx.x; ok && item < num_items; item += gridDim.x) {
+            int issued = 0;                  // ring steps issued
+            bool run = true;
+            for (int item = blockIdx.x; run && item < num_items; item += gridDim.x) {
                 int piece;
                 const int tile = item_tile(item, n_full, lg_s, piece);
                 const int mt = tile / n_tiles, nt = tile % n_tiles;
                 const int n0 = nt * BN + (piece > 0 ? piece * pn : 0);
                 for (int kb = 0; kb < kblocks; ++kb, ++issued) {
-                    // after a wait has given up, nothing more is issued
-                    if (!mbar_wait(&empty_bar[s], ph ^ 1u, err, 0x21) || !ring_slot_free(full_bar, STAGES, issued)) {
-                        ok = false;
-                        break;
-                    }
+                    if (!(run = mbar_wait(&empty_bar[s], ph ^ 1u, err, 0x21))) break;
                     uint8_t *st = smem + s * STAGE_BYTES;
                     mbar_arrive_expect_tx(&full_bar[s], (uint32_t)a_bytes + (piece < 0 ? B_BYTES : (B_BYTES >> lg_s)));
                     tma_load_2d(st, &tma, &full_bar[s], kb * BK, mt * BM);
@@ -112,18 +112,24 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant_
                     }
                 }
             }
+            // the block outlives its copies (free in a healthy pipeline: the
+            // MMA thread waits for the same loads)
+            drain_ring(full_bar, STAGES, issued);
         }
     } else if (warp == 1) {
         if (lane == 0) {   // MMA issuer
+            // stops at its first wait that gives up: it then issues and
+            // releases nothing more
             uint32_t s = 0, ph = 0, tc = 0;
-            for (int item = blockIdx.x; item < num_items; item += gridDim.x, ++tc) {
+            bool run = true;
+            for (int item = blockIdx.x; run && item < num_items; item += gridDim.x, ++tc) {
                 const uint32_t idesc = item < n_full ? IDESC : idesc_n(pn);
                 const uint32_t b = tc & 1u, tph = (tc >> 1) & 1u;
-                ok &= mbar_wait(&tempty_bar[b], tph ^ 1u, err, 0x22);
+                if (!(run = mbar_wait(&tempty_bar[b], tph ^ 1u, err, 0x22))) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + b * ACC_COLS;
                 for (int kb = 0; kb < kblocks; ++kb) {
-                    ok &= mbar_wait(&full_bar[s], ph, err, 0x23);
+                    if (!(run = mbar_wait(&full_bar[s], ph, err, 0x23))) break;
                     tc_fence_after();
                     const uint32_t a_addr = smem_u32(smem + s * STAGE_BYTES);
                     const uint32_t b_addr = a_addr + a_bytes;
@@ -137,8 +143,13 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant_
                         ph ^= 1u;
                     }
                 }
+                if (!run) break;
                 umma_commit(&tfull_bar[b]);           // accumulator ready for the epilogue
             }
+            // every product issued is complete before the tensor memory is
+            // freed (free in a healthy pipeline: the epilogue waits for the
+            // last of them)
+            umma_drain(&drain_bar);
         }
     } else {
         // epilogue: warp w may read tensor-memory lanes 32*(w%4) .. +31
@@ -151,7 +162,7 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant_
             const int mt = tile / n_tiles, nt = tile % n_tiles;
             const int nbase = nt * BN + (piece > 0 ? piece * pn : 0), nchunks = piece < 0 ? BN / 32 : pn / 32;
             const uint32_t b = tc & 1u, tph = (tc >> 1) & 1u;
-            ok &= mbar_wait(&tfull_bar[b], tph, err, 0x24);
+            mbar_wait(&tfull_bar[b], tph, err, 0x24);
             tc_fence_after();
             const int m = mt * BM + row;
             __nv_bfloat16 *crow = C + (size_t)(m < M ? m : 0) * (size_t)ldc;
@@ -181,13 +192,8 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant_
     }
 
     tc_fence_before();
-    const bool failed = __syncthreads_or(!ok) != 0;
+    __syncthreads();
     tc_fence_after();
-    if (failed) {   // a wait gave up: this block's copies and products finish before it leaves
-        if (warp == 0 && lane == 0) drain_ring(full_bar, STAGES, issued);
-        if (warp == 1 && lane == 0) umma_drain(&drain_bar);
-        __syncwarp();
-    }
     if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
 }
 

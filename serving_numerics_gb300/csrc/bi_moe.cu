@@ -247,38 +247,44 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__
     pdl_wait();
     const int num_items = *ntiles_p * n_tiles;
 
-    bool ok = true;        // every wait of this thread completed
-    uint32_t it = 0;       // the producer's ring steps issued
     if (warp == 0) {
         if (lane == 0) {   // TMA producer
-            for (int item = blockIdx.x; ok && item < num_items; item += gridDim.x) {
+            // a stage is released only by the MMA thread, after it saw the
+            // stage full (it stops at its first wait that gives up), so a
+            // stage is never refilled before its last load landed; after a
+            // wait has given up nothing more is issued
+            uint32_t it = 0;                 // ring steps issued
+            bool run = true;
+            for (int item = blockIdx.x; run && item < num_items; item += gridDim.x) {
                 const int mt = item / n_tiles, nt = item % n_tiles;
                 const int row0 = tile_row0[mt], e = tile_expert[mt];
                 for (int kb = 0; kb < kblocks; ++kb, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
-                    // after a wait has given up, nothing more is issued
-                    if (!mbar_wait(&empty_bar[s], ph ^ 1u, err, 0x51) || !ring_slot_free(full_bar, STAGES, (int)it)) {
-                        ok = false;
-                        break;
-                    }
+                    if (!(run = mbar_wait(&empty_bar[s], ph ^ 1u, err, 0x51))) break;
                     uint8_t *st = smem + s * STAGE_BYTES;
                     mbar_arrive_expect_tx(&full_bar[s], STAGE_BYTES);
                     tma_load_2d(st, &tma, &full_bar[s], kb * BK, row0);
                     tma_load_3d(st + A_BYTES, &tmw, &full_bar[s], kb * BK, nt * BN, e);
                 }
             }
+            // the block outlives its copies (free in a healthy pipeline: the
+            // MMA thread waits for the same loads)
+            drain_ring(full_bar, STAGES, (int)it);
         }
     } else if (warp == 1) {
         if (lane == 0) {   // MMA issuer
-            uint32_t rit = 0, tc = 0;
-            for (int item = blockIdx.x; item < num_items; item += gridDim.x, ++tc) {
+            // stops at its first wait that gives up: it then issues and
+            // releases nothing more
+            uint32_t it = 0, tc = 0;
+            bool run = true;
+            for (int item = blockIdx.x; run && item < num_items; item += gridDim.x, ++tc) {
                 const uint32_t b = tc & 1u, tph = (tc >> 1) & 1u;
-                ok &= mbar_wait(&tempty_bar[b], tph ^ 1u, err, 0x52);
+                if (!(run = mbar_wait(&tempty_bar[b], tph ^ 1u, err, 0x52))) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + b * ACC_COLS;
-                for (int kb = 0; kb < kblocks; ++kb, ++rit) {
-                    const uint32_t s = rit % STAGES, ph = (rit / STAGES) & 1u;
-                    ok &= mbar_wait(&full_bar[s], ph, err, 0x53);
+                for (int kb = 0; kb < kblocks; ++kb, ++it) {
+                    const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+                    if (!(run = mbar_wait(&full_bar[s], ph, err, 0x53))) break;
                     tc_fence_after();
                     const uint32_t a_addr = smem_u32(smem + s * STAGE_BYTES);
                     const uint32_t b_addr = a_addr + A_BYTES;
@@ -288,8 +294,13 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__
                                   IDESC, (kb | kk) != 0 ? 1u : 0u);
                     umma_commit(&empty_bar[s]);
                 }
+                if (!run) break;
                 umma_commit(&tfull_bar[b]);
             }
+            // every product issued is complete before the tensor memory is
+            // freed (free in a healthy pipeline: the epilogue waits for the
+            // last of them)
+            umma_drain(&drain_bar);
         }
     } else {
         // epilogue: warp w reads tensor-memory lanes 32*(w%4) .. +31; row r
@@ -301,7 +312,7 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__
             const int mt = item / n_tiles, nt = item % n_tiles;
             const int src = row_src[tile_row0[mt] + row];      // -1: a padding row
             const uint32_t b = tc & 1u, tph = (tc >> 1) & 1u;
-            ok &= mbar_wait(&tfull_bar[b], tph, err, 0x54);
+            mbar_wait(&tfull_bar[b], tph, err, 0x54);
             tc_fence_after();
             __nv_bfloat16 *yrow = Y + (int64_t)(src >= 0 ? src : 0) * N;
 #pragma unroll 1
@@ -330,13 +341,8 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__
     }
 
     tc_fence_before();
-    const bool failed = __syncthreads_or(!ok) != 0;
+    __syncthreads();
     tc_fence_after();
-    if (failed) {   // a wait gave up: this block's copies and products finish before it leaves
-        if (warp == 0 && lane == 0) drain_ring(full_bar, STAGES, (int)it);
-        if (warp == 1 && lane == 0) umma_drain(&drain_bar);
-        __syncwarp();
-    }
     if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
 }
 
