@@ -71,7 +71,9 @@
 // core executes one thread's tcgen05.mma operations in issue order, and the
 // S product is issued after the P V product that reads them.  Every wait on
 // an mbarrier is bounded (about 2 s); on expiry the kernel records
-// BI_ERR_TIMEOUT in the device error word and carries on.
+// BI_ERR_TIMEOUT in the device error word, the producer and MMA threads
+// issue nothing more and wait (bounded) for their own copies and products,
+// the softmax warps carry on, and the block frees its tensor memory.
 #include <cuda_bf16.h>
 
 #include <algorithm>

@@ -84,7 +84,8 @@ __device__ __forceinline__ unsigned int load_volatile(const unsigned int *p)
 
 // Wait for the phase with the given parity to complete, for at most about
 // two seconds.  On expiry: record BI_ERR_TIMEOUT (code 5) with `where` and
-// return false; the caller carries on so that no thread is left waiting.
+// return false; no thread is left waiting (what the caller does next is its
+// kernel's failure path: carry on, or stop issuing and drain).
 // Once any wait has given up (the error word holds a timeout), every later
 // wait that is not already satisfied gives up at once, so a broken pipeline
 // drains in milliseconds instead of two seconds per wait.  Other reports (an

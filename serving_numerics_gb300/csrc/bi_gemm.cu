@@ -32,9 +32,11 @@
 // it takes about half the time of a full wave; and when there are fewer
 // tiles than SMs (small M: one 128-row tile holds up to 128 tokens), every
 // tile is cut into the most pieces that still fit one per SM, so that
-// 8 times as many SMs stream the weight matrix.  Every wait on an mbarrier is bounded (about 2 s); on
-// expiry the kernel records BI_ERR_TIMEOUT in the device error word and
-// carries on.
+// 8 times as many SMs stream the weight matrix.  Every wait on an mbarrier
+// is bounded (about 2 s); on expiry the kernel records BI_ERR_TIMEOUT in the
+// device error word, the producer and MMA threads issue nothing more and
+// wait (bounded) for their own copies and products, the epilogue carries
+// on, and the block frees its tensor memory.
 #include <cuda_bf16.h>
 
 #include "bi_device.cuh"
