@@ -5,7 +5,6 @@ computed here with integers; relabelling the experts leaves every slot's
 output unchanged; the combine has closed forms for one slot, dyadic weights
 and a zero weight."""
 import numpy as np
-import pytest
 
 from oracle import moe
 from oracle import oracle as orc
